@@ -1,0 +1,193 @@
+"""CPU oracle for absorbed MLA decode (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py``
+may import this package.  The product path (the CUDA library and its Python binding)
+never imports it and never falls back to it.
+
+The arithmetic lives in ``mla_oracle.c`` (plain C, IEEE double, two-pass softmax);
+this module compiles it with gcc on first use and marshals numpy arrays through
+ctypes.  It shares no code with the CUDA library.
+
+Functions follow these passages (page title, section):
+
+* ``decode_dense`` / ``attend_f64``: "MLA 在极长上下文下的显存带宽突围" (run-time
+  matrix absorption: score = q~ c^T + q^R k_R^T over the 576-wide cache entry) and
+  "MLA & DSA 推理性能优化指南" §1.1 (absorbed path computes in the latent space).
+* ``decode_sparse``: same guide §1.2 / §4.2 (attend over the top-k selected tokens).
+* ``decode_fp8`` / ``e4m3_to_float``: same guide §5.3 (FP8 latent cache).  The format
+  (e4m3 "fn", one fp32 scale per 128 channels) is this library's reading; the pages
+  name only "FP8".
+* ``combine``: merge of split-KV partial results through their log-sum-exp, the
+  "Fused Reduction" the operator survey ("MLA 最佳算子全景调研" §3) pairs with
+  weight-absorbed decode.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mla_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "libmla_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+D_LATENT = 512
+D_ROPE = 64
+D_ENTRY = 576
+PAGE_ROWS = 64
+FP8_RECORD_BYTES = 656
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/libmla_oracle.so`` (gcc, -O2)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            I64 = ctypes.c_int64
+            D = ctypes.c_double
+            lib.mla_oracle_attend_f64.argtypes = [I, I64, P, P, P, P, D, P, P]
+            lib.mla_oracle_attend_f64.restype = None
+            lib.mla_oracle_combine_f64.argtypes = [I, I, P, P, P, P]
+            lib.mla_oracle_combine_f64.restype = None
+            lib.mla_oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+            lib.mla_oracle_e4m3_to_double.restype = D
+            lib.mla_oracle_default_threads.argtypes = []
+            lib.mla_oracle_default_threads.restype = I
+            common = [I, I, P, P, P, I64, P, I, P]
+            lib.mla_oracle_decode_dense.argtypes = common + [D, P, P, I]
+            lib.mla_oracle_decode_dense.restype = I
+            lib.mla_oracle_decode_fp8.argtypes = common + [D, P, P, I]
+            lib.mla_oracle_decode_fp8.restype = I
+            lib.mla_oracle_decode_sparse.argtypes = common + [P, I, D, P, P, I]
+            lib.mla_oracle_decode_sparse.restype = I
+            _lib = lib
+    return _lib
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+def default_threads() -> int:
+    return int(_load().mla_oracle_default_threads())
+
+
+def e4m3_to_float(code: int) -> float:
+    """Value of one e4m3 "fn" code (bias 7, no infinities, 0x7F/0xFF NaN)."""
+    return float(_load().mla_oracle_e4m3_to_double(int(code) & 0xFF))
+
+
+def attend_f64(q_nope, q_rope, C, Kr, scale):
+    """Definition of absorbed decode for one request in double precision.
+
+    q_nope [H,512], q_rope [H,64], C [N,512], Kr [N,64] (float64) -> out [H,512], lse [H].
+    """
+    lib = _load()
+    qn, pqn = _c(q_nope, np.float64)
+    qr, pqr = _c(q_rope, np.float64)
+    c, pc = _c(C, np.float64)
+    k, pk = _c(Kr, np.float64)
+    H = qn.shape[0]
+    N = c.shape[0]
+    assert qn.shape == (H, D_LATENT) and qr.shape == (H, D_ROPE)
+    assert c.shape == (N, D_LATENT) and k.shape == (N, D_ROPE)
+    out = np.zeros((H, D_LATENT), np.float64)
+    lse = np.zeros((H,), np.float64)
+    lib.mla_oracle_attend_f64(H, N, pqn, pqr, pc, pk, float(scale),
+                              out.ctypes.data_as(ctypes.c_void_p),
+                              lse.ctypes.data_as(ctypes.c_void_p))
+    return out, lse
+
+
+def combine(outs, lses):
+    """Merge S partial results of one head: outs [S,D], lses [S] -> out [D], lse."""
+    lib = _load()
+    o, po = _c(outs, np.float64)
+    l, pl = _c(lses, np.float64)
+    S, D = o.shape
+    out = np.zeros((D,), np.float64)
+    lse = np.zeros((1,), np.float64)
+    lib.mla_oracle_combine_f64(S, D, po, pl, out.ctypes.data_as(ctypes.c_void_p),
+                               lse.ctypes.data_as(ctypes.c_void_p))
+    return out, float(lse[0])
+
+
+def _bits16(a):
+    """bf16 storage (torch.bfloat16 tensor or uint16/int16 numpy array) -> uint16 numpy."""
+    if hasattr(a, "detach"):
+        import torch
+        a = a.detach().cpu().contiguous().view(torch.int16).numpy()
+    return np.ascontiguousarray(a).view(np.uint16)
+
+
+def _np(a, dtype):
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().contiguous().numpy()
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _run(fn_name, q_nope, q_rope, cache, block_table, seq_lens, scale, nthreads,
+         extra=(), cache_kind="bf16"):
+    lib = _load()
+    qn = _bits16(q_nope)
+    qr = _bits16(q_rope)
+    B, H, _ = qn.shape
+    if cache_kind == "bf16":
+        cb = _bits16(cache)
+        num_pages = cb.shape[0]
+    else:
+        cb = _np(cache, np.uint8)
+        num_pages = cb.shape[0]
+    bt = _np(block_table, np.int32)
+    sl = _np(seq_lens, np.int32)
+    assert bt.shape[0] == B and sl.shape == (B,)
+    out = np.zeros((B, H, D_LATENT), np.float64)
+    lse = np.zeros((B, H), np.float64)
+    P = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    args = [B, H, P(qn), P(qr), P(cb), num_pages, P(bt), bt.shape[1], P(sl)]
+    args += list(extra)
+    args += [float(scale), P(out), P(lse), int(nthreads)]
+    rc = getattr(lib, fn_name)(*args)
+    if rc != 0:
+        raise ValueError(f"{fn_name}: a page or token reference is out of range")
+    return out, lse
+
+
+def decode_dense(q_nope, q_rope, cache, block_table, seq_lens, scale, nthreads=0):
+    """Dense decode over the paged bf16 cache [num_pages,64,576] -> (out [B,H,512], lse [B,H])."""
+    return _run("mla_oracle_decode_dense", q_nope, q_rope, cache, block_table, seq_lens,
+                scale, nthreads)
+
+
+def decode_fp8(q_nope, q_rope, cache, block_table, seq_lens, scale, nthreads=0):
+    """Dense decode over the paged FP8 cache [num_pages,64,656] (bytes)."""
+    return _run("mla_oracle_decode_fp8", q_nope, q_rope, cache, block_table, seq_lens,
+                scale, nthreads, cache_kind="fp8")
+
+
+def decode_sparse(q_nope, q_rope, cache, block_table, seq_lens, indices, scale, nthreads=0):
+    """Token-sparse decode: indices [B,topk] int32 logical positions, -1 = padding."""
+    idx = _np(indices, np.int32)
+    P = idx.ctypes.data_as(ctypes.c_void_p)
+    return _run("mla_oracle_decode_sparse", q_nope, q_rope, cache, block_table, seq_lens,
+                scale, nthreads, extra=(P, idx.shape[1]))

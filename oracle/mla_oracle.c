@@ -1,0 +1,312 @@
+/*
+ * Plain, slow CPU oracle for absorbed (MQA-mode) Multi-head Latent Attention decode.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's CPU
+ * baseline leg may load this code.  It shares nothing with the CUDA library: no
+ * header, no helper, no table.  Every value is decoded from its stored bits and all
+ * arithmetic is done in IEEE double.  The softmax is the textbook two-pass form
+ * (maximum first, then the sum of exponentials); there is no blocking, no online
+ * rescaling and no fusion.
+ *
+ * What it computes, for one request with query heads h and the token list N:
+ *
+ *   s_t       = scale * ( q~[h] . c[t]  +  q_R[h] . k_R[t] )             t in N
+ *   m         = max_t s_t,       l = sum_t exp(s_t - m)
+ *   out[h, :] = (1 / l) * sum_t exp(s_t - m) * c[t, :]
+ *   lse[h]    = m + ln(l)
+ *
+ * Sources (page title, section):
+ *  - "MLA 在极长上下文下的显存带宽突围：128K 场景下的算子访存深度解析", section
+ *    "运行期矩阵吸收" (run-time matrix absorption): the absorbed query q~ = q^C W^UK and the
+ *    score q~ (c^KV)^T + q^R (k^R)^T, read against a 576-wide cache entry (512 latent +
+ *    64 decoupled-RoPE key).  The "+" between the two terms is lost in the extracted
+ *    text; the guide below and the two-term form of the cache entry fix it.
+ *  - "MLA & DSA 推理性能优化指南", §1.1 (absorbed path: W_UK folded into the query,
+ *    attention computed in latent space, only c_t^KV and the 64-d RoPE key cached) and
+ *    §4.1 (decode reads (d_c + d_rope) values per token).  The output stays in the
+ *    512-d latent space; W^UV is applied afterwards, outside this operation.
+ *  - Same guide, §4.2: the token-sparse (DSA) decode attends over the selected top-k
+ *    tokens only.
+ *  - Same guide, §5.3: the FP8 latent cache.  The pages do not fix the FP8 format; this
+ *    oracle reads e4m3 "fn" (bias 7, no infinities, S.1111.111 is NaN) with one fp32
+ *    scale per 128 latent channels, x = e4m3(code) * scale.
+ *
+ * Readings where the pages are silent: the scale multiplies the raw score before the
+ * exponential; lse is the natural log of the normaliser of the scaled scores; an empty
+ * token list gives out = 0 and lse = -inf; a sparse index of -1 is padding and is
+ * skipped; a repeated index is attended once per occurrence.
+ *
+ * Paged cache addressing: logical token t of request b lives in physical page
+ * block_table[b][t / 64] at row t % 64.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#define D_LATENT 512
+#define D_ROPE 64
+#define D_ENTRY 576
+#define PAGE_ROWS 64
+#define FP8_RECORD_BYTES 656 /* 512 e4m3 codes, 4 fp32 scales, 64 bf16 RoPE values */
+
+/* bfloat16: the upper 16 bits of an IEEE binary32. */
+static double bf16_bits_to_double(uint16_t bits) {
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* e4m3 "fn": 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; no infinities;
+ * exponent 1111 with mantissa 111 is NaN; exponent 0000 is subnormal. */
+double mla_oracle_e4m3_to_double(uint8_t code) {
+    int sign = (code >> 7) & 1;
+    int e = (code >> 3) & 0xF;
+    int m = code & 0x7;
+    double v;
+    if (e == 0xF && m == 0x7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, 1 - 7);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+static double f32_bits_to_double(const uint8_t *p) {
+    float f;
+    memcpy(&f, p, sizeof f);
+    return (double)f;
+}
+
+/* The definition above, for one request and all its heads, over N gathered tokens.
+ * qn[H*512], qr[H*64], C[N*512], Kr[N*64] -> out[H*512], lse[H]. */
+void mla_oracle_attend_f64(int H, int64_t N, const double *qn, const double *qr,
+                           const double *C, const double *Kr, double scale, double *out,
+                           double *lse) {
+    double *s = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    for (int h = 0; h < H; ++h) {
+        double *o = out + (size_t)h * D_LATENT;
+        for (int c = 0; c < D_LATENT; ++c) o[c] = 0.0;
+        if (N == 0) {
+            lse[h] = -INFINITY;
+            continue;
+        }
+        /* pass 1: scores and their maximum */
+        double m = -INFINITY;
+        for (int64_t t = 0; t < N; ++t) {
+            double dot = 0.0;
+            for (int c = 0; c < D_LATENT; ++c)
+                dot += qn[(size_t)h * D_LATENT + c] * C[(size_t)t * D_LATENT + c];
+            for (int r = 0; r < D_ROPE; ++r)
+                dot += qr[(size_t)h * D_ROPE + r] * Kr[(size_t)t * D_ROPE + r];
+            s[t] = scale * dot;
+            if (s[t] > m) m = s[t];
+        }
+        /* pass 2: normaliser and weighted sum of latents */
+        double l = 0.0;
+        for (int64_t t = 0; t < N; ++t) {
+            double w = exp(s[t] - m);
+            l += w;
+            for (int c = 0; c < D_LATENT; ++c) o[c] += w * C[(size_t)t * D_LATENT + c];
+        }
+        for (int c = 0; c < D_LATENT; ++c) o[c] /= l;
+        lse[h] = m + log(l);
+    }
+    free(s);
+}
+
+/* Merge of per-chunk results of one head: lse = ln sum_i exp(lse_i),
+ * out = sum_i exp(lse_i - lse) out_i.  Chunks with lse_i = -inf hold no tokens. */
+void mla_oracle_combine_f64(int S, int D, const double *outs, const double *lses,
+                            double *out, double *lse) {
+    double m = -INFINITY;
+    for (int i = 0; i < S; ++i)
+        if (lses[i] > m) m = lses[i];
+    for (int c = 0; c < D; ++c) out[c] = 0.0;
+    if (m == -INFINITY) {
+        *lse = -INFINITY;
+        return;
+    }
+    double z = 0.0;
+    for (int i = 0; i < S; ++i) z += exp(lses[i] - m);
+    double L = m + log(z);
+    for (int i = 0; i < S; ++i) {
+        double w = exp(lses[i] - L);
+        for (int c = 0; c < D; ++c) out[c] += w * outs[(size_t)i * D + c];
+    }
+    *lse = L;
+}
+
+/* ---------------------------------------------------------------------------------
+ * Paged front ends.  They gather the request's token rows into double arrays and call
+ * mla_oracle_attend_f64.  Work is spread over requests with plain pthreads.
+ * -------------------------------------------------------------------------------*/
+
+enum { CACHE_BF16 = 0, CACHE_FP8 = 1 };
+
+typedef struct {
+    int kind; /* CACHE_BF16 or CACHE_FP8 */
+    int B, H;
+    const uint16_t *q_nope, *q_rope;
+    const void *cache;
+    int64_t num_pages;
+    const int32_t *block_table;
+    int max_pages;
+    const int32_t *seq_lens;
+    const int32_t *indices; /* NULL: dense (tokens 0..L-1) */
+    int topk;
+    double scale;
+    double *out, *lse;
+    int next_b; /* shared work counter */
+    pthread_mutex_t mu;
+    int error;
+} job_t;
+
+/* Decodes logical token t of request b into c[512], kr[64].  Returns 0 or -1. */
+static int load_token(const job_t *J, int b, int64_t t, double *c, double *kr) {
+    if (t < 0 || t >= J->seq_lens[b]) return -1;
+    int64_t lp = t / PAGE_ROWS;
+    if (lp >= J->max_pages) return -1;
+    int64_t page = J->block_table[(size_t)b * J->max_pages + lp];
+    if (page < 0 || page >= J->num_pages) return -1;
+    int64_t row = page * PAGE_ROWS + t % PAGE_ROWS;
+    if (J->kind == CACHE_BF16) {
+        const uint16_t *e = (const uint16_t *)J->cache + (size_t)row * D_ENTRY;
+        for (int i = 0; i < D_LATENT; ++i) c[i] = bf16_bits_to_double(e[i]);
+        for (int i = 0; i < D_ROPE; ++i) kr[i] = bf16_bits_to_double(e[D_LATENT + i]);
+    } else {
+        const uint8_t *e = (const uint8_t *)J->cache + (size_t)row * FP8_RECORD_BYTES;
+        double sc[4];
+        for (int g = 0; g < 4; ++g) sc[g] = f32_bits_to_double(e + 512 + 4 * g);
+        for (int i = 0; i < D_LATENT; ++i)
+            c[i] = mla_oracle_e4m3_to_double(e[i]) * sc[i / 128];
+        const uint8_t *rp = e + 528;
+        for (int i = 0; i < D_ROPE; ++i) {
+            uint16_t bits = (uint16_t)(rp[2 * i] | (rp[2 * i + 1] << 8));
+            kr[i] = bf16_bits_to_double(bits);
+        }
+    }
+    return 0;
+}
+
+static int do_request(job_t *J, int b) {
+    int H = J->H;
+    int64_t N = 0;
+    if (J->indices) {
+        for (int j = 0; j < J->topk; ++j)
+            if (J->indices[(size_t)b * J->topk + j] >= 0) ++N;
+    } else {
+        N = J->seq_lens[b];
+    }
+    double *qn = (double *)malloc(sizeof(double) * (size_t)H * D_LATENT);
+    double *qr = (double *)malloc(sizeof(double) * (size_t)H * D_ROPE);
+    double *C = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1) * D_LATENT);
+    double *Kr = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1) * D_ROPE);
+    int rc = 0;
+    for (int i = 0; i < H * D_LATENT; ++i)
+        qn[i] = bf16_bits_to_double(J->q_nope[(size_t)b * H * D_LATENT + i]);
+    for (int i = 0; i < H * D_ROPE; ++i)
+        qr[i] = bf16_bits_to_double(J->q_rope[(size_t)b * H * D_ROPE + i]);
+    int64_t n = 0;
+    if (J->indices) {
+        for (int j = 0; j < J->topk && rc == 0; ++j) {
+            int32_t t = J->indices[(size_t)b * J->topk + j];
+            if (t == -1) continue;
+            if (t < -1) { rc = -1; break; }
+            rc = load_token(J, b, t, C + (size_t)n * D_LATENT, Kr + (size_t)n * D_ROPE);
+            ++n;
+        }
+    } else {
+        for (int64_t t = 0; t < N && rc == 0; ++t, ++n)
+            rc = load_token(J, b, t, C + (size_t)t * D_LATENT, Kr + (size_t)t * D_ROPE);
+    }
+    if (rc == 0)
+        mla_oracle_attend_f64(H, N, qn, qr, C, Kr, J->scale,
+                              J->out + (size_t)b * H * D_LATENT, J->lse + (size_t)b * H);
+    free(qn); free(qr); free(C); free(Kr);
+    return rc;
+}
+
+static void *worker(void *arg) {
+    job_t *J = (job_t *)arg;
+    for (;;) {
+        pthread_mutex_lock(&J->mu);
+        int b = J->next_b++;
+        pthread_mutex_unlock(&J->mu);
+        if (b >= J->B) break;
+        if (do_request(J, b) != 0) {
+            pthread_mutex_lock(&J->mu);
+            J->error = 1;
+            pthread_mutex_unlock(&J->mu);
+        }
+    }
+    return NULL;
+}
+
+static int run_jobs(job_t *J, int nthreads) {
+    if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > J->B) nthreads = J->B > 0 ? J->B : 1;
+    pthread_mutex_init(&J->mu, NULL);
+    J->next_b = 0;
+    J->error = 0;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    for (int i = 0; i < nthreads; ++i) pthread_create(&th[i], NULL, worker, J);
+    for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&J->mu);
+    return J->error ? -1 : 0;
+}
+
+/* Number of worker threads this library would use for nthreads <= 0. */
+int mla_oracle_default_threads(void) { return (int)sysconf(_SC_NPROCESSORS_ONLN); }
+
+/* Dense decode over a paged bf16 cache [num_pages][64][576].  Returns 0, or -1 if a
+ * page or token reference falls outside the given arrays. */
+int mla_oracle_decode_dense(int B, int H, const uint16_t *q_nope, const uint16_t *q_rope,
+                            const uint16_t *cache, int64_t num_pages,
+                            const int32_t *block_table, int max_pages,
+                            const int32_t *seq_lens, double scale, double *out,
+                            double *lse, int nthreads) {
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.kind = CACHE_BF16; J.B = B; J.H = H; J.q_nope = q_nope; J.q_rope = q_rope;
+    J.cache = cache; J.num_pages = num_pages; J.block_table = block_table;
+    J.max_pages = max_pages; J.seq_lens = seq_lens; J.scale = scale; J.out = out; J.lse = lse;
+    return run_jobs(&J, nthreads);
+}
+
+/* Dense decode over a paged FP8 cache: page = 64 records of 656 bytes
+ * (512 e4m3 latent codes | 4 little-endian fp32 scales | 64 bf16 RoPE values). */
+int mla_oracle_decode_fp8(int B, int H, const uint16_t *q_nope, const uint16_t *q_rope,
+                          const uint8_t *cache, int64_t num_pages,
+                          const int32_t *block_table, int max_pages,
+                          const int32_t *seq_lens, double scale, double *out, double *lse,
+                          int nthreads) {
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.kind = CACHE_FP8; J.B = B; J.H = H; J.q_nope = q_nope; J.q_rope = q_rope;
+    J.cache = cache; J.num_pages = num_pages; J.block_table = block_table;
+    J.max_pages = max_pages; J.seq_lens = seq_lens; J.scale = scale; J.out = out; J.lse = lse;
+    return run_jobs(&J, nthreads);
+}
+
+/* Token-sparse decode: request b attends over the logical positions
+ * indices[b][0..topk) that are >= 0 (each occurrence counts once); -1 is padding.
+ * An index outside [-1, seq_lens[b]) makes the call return -1. */
+int mla_oracle_decode_sparse(int B, int H, const uint16_t *q_nope, const uint16_t *q_rope,
+                             const uint16_t *cache, int64_t num_pages,
+                             const int32_t *block_table, int max_pages,
+                             const int32_t *seq_lens, const int32_t *indices, int topk,
+                             double scale, double *out, double *lse, int nthreads) {
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.kind = CACHE_BF16; J.B = B; J.H = H; J.q_nope = q_nope; J.q_rope = q_rope;
+    J.cache = cache; J.num_pages = num_pages; J.block_table = block_table;
+    J.max_pages = max_pages; J.seq_lens = seq_lens; J.indices = indices; J.topk = topk;
+    J.scale = scale; J.out = out; J.lse = lse;
+    return run_jobs(&J, nthreads);
+}

@@ -1,0 +1,324 @@
+"""Pins for the CPU oracle: each test checks it against something other than itself.
+
+The pages print no worked attention example, so the oracle is pinned by closed-form
+algebra (the absorption identity of "MLA 在极长上下文下的显存带宽突围", run-time matrix
+absorption), textbook special cases, a library decoder for the FP8 format, brute force on
+tiny inputs, and structural invariants (split + merge, sparse with every index = dense).
+Each pin is chosen so that a plausible slip in the oracle (a dropped RoPE term, a wrong
+scale, a transposed operand, an off-by-one page row, a wrong FP8 scale group) fails it.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mla_latent_kv_17_gb300 import inputs
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+SCALE = 1.0 / math.sqrt(192.0)
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# --------------------------------------------------------------------------------------
+# absorbed == non-absorbed (closed-form algebra; P4 run-time matrix absorption, P1 §1.1)
+# --------------------------------------------------------------------------------------
+@pytest.mark.parametrize("H,N", [(1, 1), (3, 7), (8, 129)])
+def test_absorbed_equals_nonabsorbed(H, N):
+    r = _rng(100 + H * N)
+    d_h = 128
+    qC = r.standard_normal((H, d_h))
+    qR = r.standard_normal((H, 64))
+    W_UK = r.standard_normal((H, d_h, 512)) / math.sqrt(512)
+    W_UV = r.standard_normal((H, d_h, 512)) / math.sqrt(512)
+    C = r.standard_normal((N, 512))
+    KR = r.standard_normal((N, 64))
+
+    # Non-absorbed (MHA mode): decompress per-head keys/values, standard attention with
+    # the 192-wide key [K_h | k_R] and query [q^C_h | q^R_h].
+    ref_out = np.zeros((H, d_h))
+    ref_lse = np.zeros(H)
+    for h in range(H):
+        K = C @ W_UK[h].T               # [N, 128]
+        V = C @ W_UV[h].T               # [N, 128]
+        s = (K @ qC[h] + KR @ qR[h]) * SCALE
+        m = s.max()
+        p = np.exp(s - m)
+        ref_out[h] = (p / p.sum()) @ V
+        ref_lse[h] = m + math.log(p.sum())
+
+    # Absorbed: q~ = q^C W^UK, attend in latent space, project the latent output with W^UV.
+    q_abs = np.stack([qC[h] @ W_UK[h] for h in range(H)])      # [H, 512]
+    out_lat, lse = oracle.attend_f64(q_abs, qR, C, KR, SCALE)
+    proj = np.stack([W_UV[h] @ out_lat[h] for h in range(H)])
+    np.testing.assert_allclose(proj, ref_out, rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, rtol=1e-12, atol=1e-12)
+
+
+def test_rope_term_and_scale_matter():
+    """Changing only k_R or only the scale must change the result (guards dropped terms)."""
+    r = _rng(5)
+    q, qr = r.standard_normal((2, 512)), r.standard_normal((2, 64))
+    C, K = r.standard_normal((9, 512)), r.standard_normal((9, 64))
+    o1, l1 = oracle.attend_f64(q, qr, C, K, SCALE)
+    o2, l2 = oracle.attend_f64(q, qr, C, K * 2.0, SCALE)
+    o3, l3 = oracle.attend_f64(q, qr, C, K, SCALE * 0.5)
+    assert np.abs(o1 - o2).max() > 1e-3 and np.abs(l1 - l2).max() > 1e-3
+    assert np.abs(o1 - o3).max() > 1e-3
+
+
+# --------------------------------------------------------------------------------------
+# Textbook special cases
+# --------------------------------------------------------------------------------------
+def test_weights_sum_to_one():
+    r = _rng(1)
+    v = r.standard_normal(512)
+    C = np.tile(v, (37, 1))
+    out, _ = oracle.attend_f64(r.standard_normal((4, 512)) * 3, r.standard_normal((4, 64)), C,
+                               r.standard_normal((37, 64)), SCALE)
+    np.testing.assert_allclose(out, np.tile(v, (4, 1)), rtol=1e-12, atol=1e-12)
+
+
+def test_output_in_convex_hull():
+    r = _rng(2)
+    C = r.standard_normal((50, 512))
+    out, _ = oracle.attend_f64(r.standard_normal((6, 512)) * 4, r.standard_normal((6, 64)), C,
+                               r.standard_normal((50, 64)), SCALE)
+    assert np.all(out <= C.max(axis=0) + 1e-12) and np.all(out >= C.min(axis=0) - 1e-12)
+
+
+def test_single_token():
+    r = _rng(3)
+    q, qr = r.standard_normal((5, 512)), r.standard_normal((5, 64))
+    C, K = r.standard_normal((1, 512)), r.standard_normal((1, 64))
+    out, lse = oracle.attend_f64(q, qr, C, K, SCALE)
+    np.testing.assert_array_equal(out, np.tile(C[0], (5, 1)))
+    s0 = np.array([SCALE * (np.dot(q[h], C[0]) + np.dot(qr[h], K[0])) for h in range(5)])
+    np.testing.assert_allclose(lse, s0, rtol=1e-13, atol=1e-13)
+
+
+def test_zero_query_gives_mean_and_log_n():
+    r = _rng(4)
+    N = 77
+    C = r.standard_normal((N, 512))
+    out, lse = oracle.attend_f64(np.zeros((3, 512)), np.zeros((3, 64)), C,
+                                 r.standard_normal((N, 64)), SCALE)
+    np.testing.assert_allclose(out, np.tile(C.mean(axis=0), (3, 1)), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse, np.full(3, math.log(N)), rtol=1e-14)
+
+
+def test_empty_token_list():
+    out, lse = oracle.attend_f64(np.ones((2, 512)), np.ones((2, 64)), np.zeros((0, 512)),
+                                 np.zeros((0, 64)), SCALE)
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
+def test_bruteforce_tiny_paged():
+    """Pure-Python softmax without the max shift, gathering rows through the block table."""
+    for seed, (B, H, lens) in enumerate([(1, 1, [1]), (2, 3, [5, 8]), (2, 4, [8, 3])]):
+        c = inputs.make_case(B, H, lens, seed=seed, extra_pages=3)
+        c.cache[:] = c.cache.float().clamp(-2, 2).to(torch.bfloat16)  # tiny case: no NaN tail
+        out, lse = oracle.decode_dense(c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens,
+                                       SCALE)
+        qn, qr = c.q_nope.double().numpy(), c.q_rope.double().numpy()
+        cache = c.cache.double().numpy()
+        bt = c.block_table.numpy()
+        for b in range(B):
+            for h in range(H):
+                ws, acc = [], [0.0] * 512
+                for t in range(lens[b]):
+                    row = cache[bt[b, t // 64], t % 64]
+                    s = sum(qn[b, h, i] * row[i] for i in range(512))
+                    s += sum(qr[b, h, i] * row[512 + i] for i in range(64))
+                    ws.append(math.exp(SCALE * s))
+                z = sum(ws)
+                for t in range(lens[b]):
+                    row = cache[bt[b, t // 64], t % 64]
+                    for i in range(512):
+                        acc[i] += ws[t] / z * row[i]
+                np.testing.assert_allclose(out[b, h], acc, rtol=1e-10, atol=1e-12)
+                assert abs(lse[b, h] - math.log(z)) < 1e-10
+
+
+def test_one_hot_reads_the_mapped_row():
+    """Row r of physical page p holds the code (p, r); a dominant score on one token makes
+    the output equal that row, so the output names the row the oracle read."""
+    B, H = 2, 2
+    lens = [130, 70]
+    c = inputs.make_case(B, H, lens, seed=9, extra_pages=5)
+    P = c.cache.shape[0]
+    cache = torch.zeros((P, 64, 576), dtype=torch.float32)
+    for p in range(P):
+        for r in range(64):
+            cache[p, r, 0] = p
+            cache[p, r, 1] = r
+    qn = torch.zeros((B, H, 512))
+    qr = torch.zeros((B, H, 64))
+    targets = [[0, 129], [69, 3]]
+    cache[:, :, 512:] = 0
+    for b in range(B):
+        for h in range(H):
+            t = targets[b][h]
+            p = int(c.block_table[b, t // 64])
+            cache[p, t % 64, 512 + 8 * h + b] = 1.0   # unique marker key for (b, h)
+            qr[b, h, 8 * h + b] = 1000.0   # exp(-1000) underflows to 0 in double
+    out, lse = oracle.decode_dense(qn.to(torch.bfloat16), qr.to(torch.bfloat16),
+                                   cache.to(torch.bfloat16), c.block_table, c.seq_lens, 1.0)
+    for b in range(B):
+        for h in range(H):
+            t = targets[b][h]
+            assert out[b, h, 0] == int(c.block_table[b, t // 64])
+            assert out[b, h, 1] == t % 64
+
+
+# --------------------------------------------------------------------------------------
+# Structural invariants: split + merge, sparse with all indices, duplicates
+# --------------------------------------------------------------------------------------
+def _dense_case(B=2, H=4, lens=(200, 131), seed=11):
+    return inputs.make_case(B, H, list(lens), seed=seed, extra_pages=2)
+
+
+def test_sparse_all_indices_equals_dense():
+    c = _dense_case()
+    topk = int(c.seq_lens.max())
+    idx = torch.full((c.B, topk), -1, dtype=torch.int32)
+    perm_idx = idx.clone()
+    g = torch.Generator().manual_seed(0)
+    for b, L in enumerate(c.seq_lens.tolist()):
+        idx[b, :L] = torch.arange(L)
+        perm_idx[b, :L] = torch.randperm(L, generator=g).to(torch.int32)
+    d_out, d_lse = oracle.decode_dense(c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens, SCALE)
+    for ix in (idx, perm_idx):
+        s_out, s_lse = oracle.decode_sparse(c.q_nope, c.q_rope, c.cache, c.block_table,
+                                            c.seq_lens, ix, SCALE)
+        np.testing.assert_allclose(s_out, d_out, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(s_lse, d_lse, rtol=1e-13, atol=1e-13)
+
+
+def test_split_and_merge_equals_single_pass():
+    c = _dense_case(B=1, H=3, lens=(300,))
+    L = 300
+    d_out, d_lse = oracle.decode_dense(c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens, SCALE)
+    for cuts in ([0, 1, 2, 300], [0, 64, 128, 192, 256, 300], [0, 150, 300], [0, 299, 300]):
+        parts_o, parts_l = [], []
+        for a, e in zip(cuts[:-1], cuts[1:]):
+            ix = torch.full((1, L), -1, dtype=torch.int32)
+            ix[0, :e - a] = torch.arange(a, e)
+            o, l = oracle.decode_sparse(c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens,
+                                        ix, SCALE)
+            parts_o.append(o[0])
+            parts_l.append(l[0])
+        po, pl = np.stack(parts_o), np.stack(parts_l)   # [S, H, 512], [S, H]
+        for h in range(3):
+            o, l = oracle.combine(po[:, h], pl[:, h])
+            np.testing.assert_allclose(o, d_out[0, h], rtol=1e-11, atol=1e-13)
+            assert abs(l - d_lse[0, h]) < 1e-12
+
+
+def test_combine_empty_chunks():
+    o, l = oracle.combine(np.zeros((3, 8)), np.full(3, -np.inf))
+    assert np.all(o == 0) and l == -np.inf
+    x = np.arange(8.0)
+    o, l = oracle.combine(np.stack([x, np.zeros(8)]), np.array([0.5, -np.inf]))
+    np.testing.assert_array_equal(o, x)
+    assert l == 0.5
+
+
+def test_sparse_duplicate_counts_twice_and_padding_skipped():
+    c = _dense_case(B=1, H=2, lens=(40,))
+    ix = torch.tensor([[5, 5, -1, 17, -1]], dtype=torch.int32)
+    out, lse = oracle.decode_sparse(c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens, ix,
+                                    SCALE)
+    cache = c.cache.double().numpy()
+    rows = [cache[int(c.block_table[0, t // 64]), t % 64] for t in (5, 5, 17)]
+    C = np.stack([r[:512] for r in rows])
+    K = np.stack([r[512:] for r in rows])
+    ref_o, ref_l = oracle.attend_f64(c.q_nope[0].double().numpy(), c.q_rope[0].double().numpy(),
+                                     C, K, SCALE)
+    np.testing.assert_allclose(out[0], ref_o, rtol=1e-13)
+    np.testing.assert_allclose(lse[0], ref_l, rtol=1e-13)
+
+
+def test_all_padding_and_zero_length():
+    c = inputs.make_case(2, 2, [0, 10], seed=3)
+    out, lse = oracle.decode_dense(c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens, SCALE)
+    assert np.all(out[0] == 0) and np.all(np.isneginf(lse[0])) and np.all(np.isfinite(lse[1]))
+    ix = torch.full((2, 4), -1, dtype=torch.int32)
+    out, lse = oracle.decode_sparse(c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens, ix, SCALE)
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
+def test_nan_tail_rows_never_read():
+    c = inputs.make_case(3, 2, [1, 63, 65], seed=4)
+    assert torch.isnan(c.cache.float()).any()
+    out, lse = oracle.decode_dense(c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens, SCALE)
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+
+
+def test_out_of_range_index_rejected():
+    c = _dense_case(B=1, H=1, lens=(10,))
+    with pytest.raises(ValueError):
+        oracle.decode_sparse(c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens,
+                             torch.tensor([[10]], dtype=torch.int32), SCALE)
+    with pytest.raises(ValueError):
+        oracle.decode_sparse(c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens,
+                             torch.tensor([[-2]], dtype=torch.int32), SCALE)
+
+
+# --------------------------------------------------------------------------------------
+# FP8 latent cache
+# --------------------------------------------------------------------------------------
+def test_e4m3_decoder_against_library_and_format_constants():
+    lib = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double()
+    for code in range(256):
+        v = oracle.e4m3_to_float(code)
+        ref = float(lib[code])
+        if math.isnan(ref):
+            assert math.isnan(v)
+        else:
+            assert v == ref, (code, v, ref)
+    # OCP FP8 e4m3: max normal 448, min normal 2^-6, min subnormal 2^-9, 1.0 = 0x38.
+    assert oracle.e4m3_to_float(0x7E) == 448.0
+    assert oracle.e4m3_to_float(0x08) == 2.0 ** -6
+    assert oracle.e4m3_to_float(0x01) == 2.0 ** -9
+    assert oracle.e4m3_to_float(0x38) == 1.0 and oracle.e4m3_to_float(0xB8) == -1.0
+    assert math.isnan(oracle.e4m3_to_float(0x7F)) and math.isnan(oracle.e4m3_to_float(0xFF))
+
+
+def test_fp8_decode_equals_dense_on_dequantised_values():
+    B, H, lens = 2, 3, [97, 64]
+    c = inputs.make_case(B, H, lens, seed=21, kv_dtype="fp8", extra_pages=1)
+    out, lse = oracle.decode_fp8(c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens, SCALE)
+    rec = c.cache
+    codes = rec[..., :512].contiguous().view(torch.float8_e4m3fn).double()     # library decode
+    scales = rec[..., 512:528].contiguous().view(torch.float32).double()       # [P,64,4]
+    rope = rec[..., 528:656].contiguous().view(torch.bfloat16).double()
+    lat = codes * scales.repeat_interleave(128, dim=-1)
+    for b in range(B):
+        rows = [(int(c.block_table[b, t // 64]), t % 64) for t in range(lens[b])]
+        C = np.stack([lat[p, r].numpy() for p, r in rows])
+        K = np.stack([rope[p, r].numpy() for p, r in rows])
+        o, l = oracle.attend_f64(c.q_nope[b].double().numpy(), c.q_rope[b].double().numpy(), C, K,
+                                 SCALE)
+        np.testing.assert_allclose(out[b], o, rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(lse[b], l, rtol=1e-13)
+
+
+def test_fp8_quantisation_error_within_format_bound():
+    """e4m3 has 3 mantissa bits: |x - x_hat| <= 2^-4 |x| for normals, and the block scale
+    maps max|x| exactly onto 448."""
+    r = torch.randn((8, 64, 512))
+    rope = torch.randn((8, 64, 64))
+    rec = inputs.quantize_fp8_records(r, rope)
+    codes = rec[..., :512].contiguous().view(torch.float8_e4m3fn).float()
+    s = rec[..., 512:528].contiguous().view(torch.float32)
+    xh = codes * s.repeat_interleave(128, dim=-1)
+    err = (xh - r).abs()
+    sub = s.repeat_interleave(128, dim=-1) * 2.0 ** -6
+    assert torch.all(err <= 2.0 ** -4 * r.abs() + sub)
+    amax = r.reshape(8, 64, 4, 128).abs().amax(-1)
+    torch.testing.assert_close(s * 448.0, amax, rtol=1e-6, atol=0)

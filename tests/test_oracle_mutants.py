@@ -1,0 +1,88 @@
+"""The pins must be strong enough to catch plausible slips.
+
+Each mutant is a copy of the oracle's C source with one deliberate mistake (planted here,
+on the CPU, never in the product).  It is compiled to a temporary library and run through
+the same closed-form checks the oracle passes; every mutant must fail at least one.
+"""
+import ctypes
+import math
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "mla_oracle.c")
+SCALE = 1.0 / math.sqrt(192.0)
+
+MUTANTS = {
+    "drop_rope_term": ("dot += qr[(size_t)h * D_ROPE + r] * Kr[(size_t)t * D_ROPE + r];",
+                       "(void)r;"),
+    "scale_after_exp": ("s[t] = scale * dot;", "s[t] = dot;"),
+    "no_normalise": ("o[c] /= l;", "(void)0;"),
+    "lse_log2": ("lse[h] = m + log(l);", "lse[h] = m + log2(l);"),
+    "rope_in_output": ("for (int c = 0; c < D_LATENT; ++c) o[c] += w * C[(size_t)t * D_LATENT + c];",
+                       "for (int c = 0; c < D_LATENT; ++c) o[c] += w * (c < D_ROPE ? Kr[(size_t)t * D_ROPE + c] : C[(size_t)t * D_LATENT + c]);"),
+    "transposed_query": ("dot += qn[(size_t)h * D_LATENT + c] * C[(size_t)t * D_LATENT + c];",
+                         "dot += qn[(size_t)(c % H) * D_LATENT + (h * 7 + c) % D_LATENT] * C[(size_t)t * D_LATENT + c];"),
+}
+
+
+def _build(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert old in src, name
+    mut = tmp_path / f"{name}.c"
+    mut.write_text(src.replace(old, new))
+    so = tmp_path / f"lib{name}.so"
+    subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread", "-o",
+                           str(so), str(mut), "-lm"])
+    lib = ctypes.CDLL(str(so))
+    P, I, I64, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+    lib.mla_oracle_attend_f64.argtypes = [I, I64, P, P, P, P, D, P, P]
+    return lib
+
+
+def _attend(lib, qn, qr, C, K, scale):
+    H, N = qn.shape[0], C.shape[0]
+    out = np.zeros((H, 512))
+    lse = np.zeros(H)
+    arrs = [np.ascontiguousarray(a, dtype=np.float64) for a in (qn, qr, C, K)]
+    P = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    lib.mla_oracle_attend_f64(H, N, *[P(a) for a in arrs], scale, P(out), P(lse))
+    return out, lse
+
+
+def _pins_hold(att):
+    """The closed-form pins of test_oracle.py, as a yes/no over an attend function."""
+    r = np.random.default_rng(7)
+    H, N, d_h = 3, 11, 128
+    qC, qR = r.standard_normal((H, d_h)), r.standard_normal((H, 64))
+    W_UK = r.standard_normal((H, d_h, 512)) / math.sqrt(512)
+    W_UV = r.standard_normal((H, d_h, 512)) / math.sqrt(512)
+    C, KR = r.standard_normal((N, 512)), r.standard_normal((N, 64))
+    ok = True
+    q_abs = np.stack([qC[h] @ W_UK[h] for h in range(H)])
+    out, lse = att(q_abs, qR, C, KR, SCALE)
+    for h in range(H):
+        K, V = C @ W_UK[h].T, C @ W_UV[h].T
+        s = (K @ qC[h] + KR @ qR[h]) * SCALE
+        p = np.exp(s - s.max())
+        ok &= np.allclose(W_UV[h] @ out[h], (p / p.sum()) @ V, rtol=1e-9, atol=1e-12)
+        ok &= abs(lse[h] - (s.max() + math.log(p.sum()))) < 1e-12
+    out, lse = att(np.zeros((2, 512)), np.zeros((2, 64)), C, KR, SCALE)
+    ok &= np.allclose(out, np.tile(C.mean(0), (2, 1)), atol=1e-12)
+    ok &= np.allclose(lse, math.log(N), atol=1e-13)
+    return bool(ok)
+
+
+def test_real_oracle_passes_pins():
+    assert _pins_hold(oracle.attend_f64)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmp_path, name):
+    old, new = MUTANTS[name]
+    lib = _build(tmp_path, name, old, new)
+    assert not _pins_hold(lambda *a: _attend(lib, *a)), f"pins missed mutant {name}"
