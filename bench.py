@@ -1,0 +1,379 @@
+#!/usr/bin/env python
+"""Benchmark of absorbed MLA decode on GB300: prints ONE JSON line on rank 0.
+
+A step is one pass of the whole hot path over one batch: the split-KV plan from the
+device seq_lens, the decode kernel and the log-sum-exp merge of split partials
+(mla_decode_plan + mla_decode, or mla_decode_sparse).  Inputs are seeded synthetic data
+already resident in HBM when the timed region starts; L2 is flushed (a 2 x L2-size write)
+before every timed step and each step is timed with CUDA events on the launching stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+N > 1 runs under torch.distributed.run: every rank decodes its own full batch (requests are
+independent, no collective on the data path), value = all ranks' FLOPs / max rank time.
+--impl reference times the CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode TFLOPS & HBM GB/s (B=64,H=128,L≤8K) and % of roofline, 1×GB300"
+DEFAULT_WORKLOAD = "dsv3_dense_b64_h128_l1k_8k"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "mla_latent_kv_17_gb300", "csrc", "*"))):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(workload: str):
+    """DRAM bytes per decode call from the committed ncu summary, if it matches the source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    e = d.get(workload)
+    if not e or e.get("kernel_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_call")
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(parts)
+            except ValueError:
+                pass
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def oracle_sample_time(case, budget_s=15.0):
+    """Times the oracle on whole requests of `case` until ~budget_s of wall time is used;
+    returns (flops_done, seconds, threads, description)."""
+    import oracle
+    import torch
+    from mla_latent_kv_17_gb300 import metrics
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from oracle_ref import oracle_for
+
+    threads = oracle.default_threads()
+    toks = metrics.attended_tokens(case)
+    done_flops, spent, nreq = 0, 0.0, 0
+    b = 0
+    group = max(1, threads)
+    while b < case.B and spent < budget_s:
+        bs = list(range(b, min(case.B, b + group)))
+        t0 = time.perf_counter()
+        oracle_for(case, bs, None, nthreads=threads)
+        spent += time.perf_counter() - t0
+        done_flops += sum(toks[i] for i in bs) * 2 * 1088 * case.H
+        nreq += len(bs)
+        b += group
+    desc = f"{nreq} of {case.B} requests (all {case.H} heads), fp64 oracle, {threads} threads"
+    return done_flops, spent, threads, desc
+
+
+def run_reference(args, ws_n, rank):
+    if rank != 0:
+        return
+    import torch
+    from mla_latent_kv_17_gb300 import inputs
+    case = inputs.make_workload(args.workload, device="cpu")
+    per_step = []
+    flops_tot = 0
+    threads, desc = 0, ""
+    for i in range(args.warmup + args.steps):
+        f, s, threads, desc = oracle_sample_time(case, budget_s=args.ref_budget)
+        if i >= args.warmup:
+            per_step.append(s)
+            flops_tot += f
+    secs = sum(per_step)
+    val = flops_tot / secs / 1e12
+    line = {"metric": METRIC, "value": val, "unit": "TFLOP/s", "impl": "reference",
+            "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=8.0,
+                    help="seconds of oracle work per reference step")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    ws_n, rank, local = dist_env()
+    import torch
+    pg = None
+    if ws_n > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        pg = dist
+    if args.impl == "reference":
+        run_reference(args, ws_n, rank)
+        if pg:
+            pg.destroy_process_group()
+        return
+
+    from mla_latent_kv_17_gb300 import build as mbuild
+    mbuild.build()
+    from mla_latent_kv_17_gb300 import inputs, metrics, ops
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    case = inputs.make_workload(args.workload, device=dev)
+    alg = metrics.algorithmic(case)
+    sparse = case.indices is not None
+    topk = case.indices.shape[1] if sparse else 0
+    wsp = ops.Workspace(case.B, case.H, device=dev)
+    out = torch.empty((case.B, case.H, 512), dtype=torch.float32, device=dev)
+    lse = torch.empty((case.B, case.H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def decode_call():
+        if sparse:
+            ops.decode_sparse(wsp, case.q_nope, case.q_rope, case.cache, case.block_table,
+                              case.seq_lens, case.indices, case.scale, out, lse, stream)
+        else:
+            ops.decode(wsp, case.q_nope, case.q_rope, case.cache, case.block_table,
+                       case.seq_lens, case.scale, out, lse, stream)
+
+    def step():
+        ops.plan(wsp, None if sparse else case.seq_lens, topk=topk, stream=stream)
+        decode_call()
+
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20)
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    st = ops.status(wsp, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {ops.STATUS_NAMES.get(st, st)} during warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            ops.plan(wsp, None if sparse else case.seq_lens, topk=topk, stream=stream)
+            ev[i][1].record(stream)
+            decode_call()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    st = ops.status(wsp, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {ops.STATUS_NAMES.get(st, st)} in timed region")
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    tot_ms = sum(step_ms)
+    if pg:
+        t = torch.tensor([tot_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        tot_ms = float(t.item())
+    ms_per_step = tot_ms / args.steps
+    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+
+    # ---- end to end through the public API with host buffers -------------------------
+    pin = lambda t: t.cpu().pin_memory()
+    h_q_nope, h_q_rope = pin(case.q_nope), pin(case.q_rope)
+    h_bt, h_sl = pin(case.block_table), pin(case.seq_lens)
+    h_idx = pin(case.indices) if sparse else None
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    d_q_nope, d_q_rope = torch.empty_like(case.q_nope), torch.empty_like(case.q_rope)
+    d_bt, d_sl = torch.empty_like(case.block_table), torch.empty_like(case.seq_lens)
+    d_idx = torch.empty_like(case.indices) if sparse else None
+    h2d = sum(t.numel() * t.element_size() for t in (h_q_nope, h_q_rope, h_bt, h_sl)) + (
+        h_idx.numel() * 4 if sparse else 0)
+    d2h = h_out.numel() * 4 + h_lse.numel() * 4
+
+    def e2e_step():
+        d_q_nope.copy_(h_q_nope, non_blocking=True)
+        d_q_rope.copy_(h_q_rope, non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        d_sl.copy_(h_sl, non_blocking=True)
+        if sparse:
+            d_idx.copy_(h_idx, non_blocking=True)
+        ops.plan(wsp, None if sparse else d_sl, topk=topk, stream=stream)
+        if sparse:
+            ops.decode_sparse(wsp, d_q_nope, d_q_rope, case.cache, d_bt, d_sl, d_idx, case.scale,
+                              out, lse, stream)
+        else:
+            ops.decode(wsp, d_q_nope, d_q_rope, case.cache, d_bt, d_sl, case.scale, out, lse,
+                       stream)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        flush.fill_(2)
+        e2e_step()
+    torch.cuda.synchronize()
+    e_ms = []
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e_ms.append(a.elapsed_time(b))
+    e2e_ms = sum(e_ms) / len(e_ms)
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    pk, pk_kind = peaks()
+    tf = alg["flops"] / (ms_per_step * 1e-3) / 1e12 * ws_n
+    gbs = alg["bytes"] / (ms_per_step * 1e-3) / 1e9
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    bound = "hbm" if alg["ai"] < ridge else "tensor"
+    dec_s = dec_avg_ms * 1e-3
+    if bound == "hbm":
+        achieved, peak, unit = alg["bytes"] / dec_s / 1e9, pk["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = alg["flops"] / dec_s / 1e12, pk["bf16_tflops"], "TFLOP/s"
+    roof_s = metrics.roofline_seconds(alg["flops"], alg["bytes"], pk["bf16_tflops"], pk["hbm_gbs"])
+    line = {
+        "metric": METRIC, "value": tf, "unit": "TFLOP/s", "n_gpus": ws_n, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "B": case.B, "H": case.H,
+                   "tokens": alg["tokens"], "kv": case.kv_dtype,
+                   "l2": "flushed before every step (2x L2 write); step = plan + decode + merge",
+                   "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU"},
+        "hbm_gbs": gbs, "tflops_decode_call": alg["flops"] / dec_s / 1e12,
+        "pct_roofline": roof_s / (ms_per_step * 1e-3),
+        "roofline": {"kernel": "mla_decode call (decode kernel + split-KV merge)", "bound": bound,
+                     "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": dram_traffic(args.workload),
+                     "peak_source": pk_kind, "ai_flop_per_byte": alg["ai"],
+                     "alg_bytes_per_call": alg["bytes"], "alg_flops_per_call": alg["flops"],
+                     "call_ms": dec_avg_ms},
+        "e2e": {"value": alg["flops"] / (e2e_ms * 1e-3) / 1e12 * ws_n, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": t_wall,
+    }
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        f, s, threads, desc = oracle_sample_time(case, budget_s=12.0)
+        line["cpu_baseline"] = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": threads,
+                                "kind": "oracle", "sample": desc, "seconds": s}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

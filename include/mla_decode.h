@@ -1,0 +1,118 @@
+/*
+ * mla_decode.h — C ABI of the GB300 (sm_103a) absorbed Multi-head Latent Attention decode
+ * library (libmla_decode.so).
+ *
+ * The operation ("MLA 在极长上下文下的显存带宽突围", run-time matrix absorption;
+ * "MLA & DSA 推理性能优化指南" §1.1 and §4.1): every query step of request b has H heads.
+ * Head h carries an absorbed query q~ = q^C W^UK (512 values) and a decoupled-RoPE query
+ * q_R (64 values).  All heads attend over one shared paged cache whose per-token entry is
+ * the 512-d latent c_KV followed by the 64-d RoPE key k_R (576 values, 1152 B in bf16):
+ *
+ *     s_t      = softmax_scale * (q~ . c_t + q_R . k_R,t)
+ *     out[b,h] = sum_t softmax(s)_t * c_t             (512 fp32 values, still latent)
+ *     lse[b,h] = ln sum_t exp(s_t)                    (natural log of the scaled scores)
+ *
+ * W^UV is applied by the caller afterwards.  A request with no tokens gets out = 0 and
+ * lse = -inf.
+ *
+ * Memory: every pointer argument is caller-owned DEVICE memory unless stated otherwise.
+ * The library allocates nothing per call.  All calls are asynchronous on `stream`
+ * (a cudaStream_t; NULL means the legacy default stream) and return as soon as the work
+ * is enqueued.  Host-detectable argument errors are returned immediately and nothing is
+ * enqueued.  Errors that only the GPU can see (a page id outside [0, num_pages), a token
+ * index outside [-1, seq_len), a length beyond the block table, a pipeline wait that
+ * exceeded its iteration limit) are recorded in a status word inside the workspace; the
+ * offending access is skipped, nothing traps, and mla_decode_status() reports the code.
+ *
+ * Layouts (row-major, no padding):
+ *   q_nope        bf16  [B][H][512]     absorbed queries
+ *   q_rope        bf16  [B][H][64]      RoPE queries
+ *   cache (bf16)  bf16  [num_pages][64][576]   row = latent[512] | k_rope[64]
+ *   cache (fp8)   u8    [num_pages][64][656]   row = 512 e4m3 "fn" codes |
+ *                                              4 fp32 scales (channel block c/128) |
+ *                                              64 bf16 k_rope; latent = e4m3 * scale
+ *   block_table   int32 [B][max_pages]  physical page of logical page j of request b
+ *   seq_lens      int32 [B]             tokens of request b (0 allowed)
+ *   indices       int32 [B][topk]       sparse: logical positions in [0, seq_len), -1 pad
+ *   out           fp32  [B][H][512]
+ *   lse           fp32  [B][H]
+ * Token t of request b lives in page block_table[b][t / 64], row t % 64.  Rows of a
+ * request's last page at or beyond seq_len are never attended and may hold anything.
+ * Base pointers of q_nope, q_rope and cache must be 16-byte aligned.
+ */
+#ifndef MLA_DECODE_H
+#define MLA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1, /* null pointer, bad size or alignment, non-finite scale   */
+    MLA_ERR_UNSUPPORTED = 2, /* H > 128, no sm_103a device, ...                          */
+    MLA_ERR_WORKSPACE = 3,   /* workspace too small, or it does not hold a matching plan */
+    MLA_ERR_CUDA = 4,        /* a CUDA runtime call failed                               */
+    MLA_ERR_INDEX = 5,       /* device: page id, token index or length out of range      */
+    MLA_ERR_TIMEOUT = 6      /* device: a pipeline wait exceeded its iteration limit     */
+} mla_status;
+
+typedef enum { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
+
+/* Bytes of device workspace a plan for B requests of H heads needs on a GPU with
+ * `num_sms` SMs (pass 0 for the current device's count).  The workspace holds the plan,
+ * the split-KV partial results and the status word.  Returns 0 for invalid arguments. */
+size_t mla_decode_workspace_size(int B, int H, int num_sms);
+
+/* Split-KV planner ("Fused Reduction" of weight-absorbed decode, "MLA 最佳算子全景调研"
+ * §3; variable-length paged batches, same page §2).  Reads the device array seq_lens[B]
+ * on the GPU (no host synchronisation; capturable in a CUDA graph) and writes into
+ * `workspace` a list of (request, token range) work items balanced over the persistent
+ * decode workers, the number of splits of each request and where its partial results go.
+ * With topk > 0 the plan is for mla_decode_sparse: every request is planned over its
+ * topk index slots and seq_lens may be NULL.  The plan stays valid until seq_lens changes.
+ * num_sms: SMs the decode may use (0 = all SMs of the current device). */
+mla_status mla_decode_plan(const int32_t *seq_lens, int B, int H, int topk, int num_sms,
+                           void *workspace, size_t ws_bytes, void *stream);
+
+/* Dense decode over the paged cache with the plan in `workspace` (built by
+ * mla_decode_plan with topk = 0 for the same B, H and seq_lens).  Writes out and lse.
+ * kv_dtype selects the cache layout above.  softmax_scale must be finite. */
+mla_status mla_decode(const void *workspace, size_t ws_bytes, const void *q_nope,
+                      const void *q_rope, const void *cache, mla_kv_dtype kv_dtype,
+                      int64_t num_pages, const int32_t *block_table, int max_pages,
+                      const int32_t *seq_lens, int B, int H, float softmax_scale, float *out,
+                      float *lse, void *stream);
+
+/* Token-sparse (DSA top-k) decode ("MLA & DSA 推理性能优化指南" §1.2, §4.2): request b
+ * attends only over the logical positions indices[b][0..topk) that are >= 0; -1 is
+ * padding.  A repeated index is attended once per occurrence.  bf16 cache only.  Needs
+ * a plan built with the same topk. */
+mla_status mla_decode_sparse(const void *workspace, size_t ws_bytes, const void *q_nope,
+                             const void *q_rope, const void *cache, int64_t num_pages,
+                             const int32_t *block_table, int max_pages,
+                             const int32_t *seq_lens, const int32_t *indices, int topk, int B,
+                             int H, float softmax_scale, float *out, float *lse,
+                             void *stream);
+
+/* Synchronises `stream`, returns the first device-side error recorded in the workspace
+ * since the last call (MLA_OK if none) and clears it. */
+mla_status mla_decode_status(void *workspace, size_t ws_bytes, void *stream);
+
+/* Static description of a status code. */
+const char *mla_status_string(mla_status status);
+
+/* Host twin of mla_decode_plan for tests and tooling: plans from a HOST array
+ * seq_lens[B] (NULL with topk > 0) into a HOST buffer of mla_decode_workspace_size()
+ * bytes, producing exactly the bytes the device planner writes into the plan region.
+ * num_sms must be > 0. */
+mla_status mla_decode_plan_host(const int32_t *seq_lens, int B, int H, int topk,
+                                int num_sms, void *workspace_host, size_t ws_bytes);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_DECODE_H */

@@ -1,0 +1,237 @@
+// C ABI of libmla_decode: argument checks, the device planner, the split-KV merge kernel
+// and the launches of the decode kernels.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "mla_decode.h"
+
+namespace mla {
+namespace {
+
+// ---------------------------------------------------------------------------------
+// Device planner: one thread runs the same sequential planner as the host twin.
+// ---------------------------------------------------------------------------------
+__global__ void plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int num_units,
+                            unsigned char *ws) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) {
+        build_plan(seq_lens, B, H, topk, num_units, ws);
+        *reinterpret_cast<int *>(ws + ws_layout(B, H, num_units).status) = 0;
+    }
+}
+
+// ---------------------------------------------------------------------------------
+// Merge of split-KV partial results through their log-sum-exp:
+//   lse = ln sum_i exp(lse_i),  out = sum_i exp(lse_i - lse) * out_i.
+// One CTA per (request, head); requests with a single piece were written directly.
+// ---------------------------------------------------------------------------------
+constexpr int kCombineThreads = 128;
+
+__global__ void __launch_bounds__(kCombineThreads)
+combine_kernel(DecodeArgs a) {
+    if (!plan_matches(a)) return;
+    const unsigned char *ws = a.ws;
+    const int H = a.H;
+    float *out = a.out, *lse = a.lse;
+    const PlanHeader *hd = reinterpret_cast<const PlanHeader *>(ws);
+    const WsLayout L = ws_layout(hd->B, hd->H, hd->num_units);
+    const int b = blockIdx.x, h = blockIdx.y;
+    const int32_t n = reinterpret_cast<const int32_t *>(ws + L.num_splits)[b];
+    if (n <= 1) return;
+    const int32_t base = reinterpret_cast<const int32_t *>(ws + L.split_base)[b];
+    const float *plse = reinterpret_cast<const float *>(ws + L.part_lse);
+    const float *po = reinterpret_cast<const float *>(ws + L.part_o);
+    float m = -INFINITY;
+    for (int i = 0; i < n; ++i) m = fmaxf(m, plse[(int64_t)(base + i) * H + h]);
+    float z = 0.f;
+    if (m != -INFINITY)
+        for (int i = 0; i < n; ++i) z += exp2f((plse[(int64_t)(base + i) * H + h] - m) * kLog2e);
+    const float total = m == -INFINITY ? -INFINITY : m + logf(z);
+    float4 acc[1];
+    for (int d4 = threadIdx.x; d4 < kDLatent / 4; d4 += kCombineThreads) {
+        float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (m != -INFINITY) {
+            for (int i = 0; i < n; ++i) {
+                float w = exp2f((plse[(int64_t)(base + i) * H + h] - total) * kLog2e);
+                float4 v = reinterpret_cast<const float4 *>(po + ((int64_t)(base + i) * H + h) * kDLatent)[d4];
+                r.x = fmaf(w, v.x, r.x);
+                r.y = fmaf(w, v.y, r.y);
+                r.z = fmaf(w, v.z, r.z);
+                r.w = fmaf(w, v.w, r.w);
+            }
+        }
+        acc[0] = r;
+        reinterpret_cast<float4 *>(out + ((int64_t)b * H + h) * kDLatent)[d4] = acc[0];
+    }
+    if (threadIdx.x == 0) lse[(int64_t)b * H + h] = total;
+}
+
+int device_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+mla_status check_common(const void *ws, size_t ws_bytes, const void *q_nope, const void *q_rope,
+                        const void *cache, int64_t num_pages, const int32_t *block_table,
+                        int max_pages, const int32_t *seq_lens, int B, int H, float scale,
+                        const float *out, const float *lse) {
+    if (!ws || !q_nope || !q_rope || !cache || !block_table || !seq_lens || !out || !lse)
+        return MLA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || max_pages < 1 || num_pages < 1) return MLA_ERR_INVALID_ARG;
+    if (H > kMaxHeads) return MLA_ERR_UNSUPPORTED;
+    if (!isfinite(scale)) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(cache) || !aligned16(out))
+        return MLA_ERR_INVALID_ARG;
+    if (ws_bytes < ws_layout(B, H, 1).plan_end) return MLA_ERR_WORKSPACE;
+    return MLA_OK;
+}
+
+mla_status run_decode(const DecodeArgs &a, cudaStream_t stream) {
+    int sms = device_sm_count();
+    if (sms <= 0) return MLA_ERR_CUDA;
+    int units = num_units_for(sms);
+    if (launch_decode_simt(a, units, stream) != cudaSuccess) return MLA_ERR_CUDA;
+    dim3 cgrid(a.B, a.H);
+    combine_kernel<<<cgrid, kCombineThreads, 0, stream>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+    return MLA_OK;
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+size_t mla_decode_workspace_size(int B, int H, int num_sms) {
+    if (B < 1 || H < 1 || H > kMaxHeads || num_sms < 0) return 0;
+    if (num_sms == 0) num_sms = device_sm_count();
+    if (num_sms <= 0) return 0;
+    return ws_layout(B, H, num_units_for(num_sms)).total;
+}
+
+mla_status mla_decode_plan(const int32_t *seq_lens, int B, int H, int topk, int num_sms,
+                           void *workspace, size_t ws_bytes, void *stream) {
+    if (!workspace || B < 1 || H < 1 || topk < 0 || num_sms < 0) return MLA_ERR_INVALID_ARG;
+    if (H > kMaxHeads) return MLA_ERR_UNSUPPORTED;
+    if (topk == 0 && !seq_lens) return MLA_ERR_INVALID_ARG;
+    if (num_sms == 0) num_sms = device_sm_count();
+    if (num_sms <= 0) return MLA_ERR_CUDA;
+    const int units = num_units_for(num_sms);
+    if (ws_bytes < ws_layout(B, H, units).total) return MLA_ERR_WORKSPACE;
+    plan_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(seq_lens, B, H, topk, units,
+                                                    (unsigned char *)workspace);
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+mla_status mla_decode_plan_host(const int32_t *seq_lens, int B, int H, int topk, int num_sms,
+                                void *workspace_host, size_t ws_bytes) {
+    if (!workspace_host || B < 1 || H < 1 || topk < 0 || num_sms < 1) return MLA_ERR_INVALID_ARG;
+    if (H > kMaxHeads) return MLA_ERR_UNSUPPORTED;
+    if (topk == 0 && !seq_lens) return MLA_ERR_INVALID_ARG;
+    const int units = num_units_for(num_sms);
+    const WsLayout L = ws_layout(B, H, units);
+    if (ws_bytes < L.plan_end) return MLA_ERR_WORKSPACE;
+    build_plan(seq_lens, B, H, topk, units, (unsigned char *)workspace_host);
+    *reinterpret_cast<int *>((unsigned char *)workspace_host + L.status) = 0;
+    return MLA_OK;
+}
+
+mla_status mla_decode(const void *workspace, size_t ws_bytes, const void *q_nope,
+                      const void *q_rope, const void *cache, mla_kv_dtype kv_dtype,
+                      int64_t num_pages, const int32_t *block_table, int max_pages,
+                      const int32_t *seq_lens, int B, int H, float softmax_scale, float *out,
+                      float *lse, void *stream) {
+    mla_status st = check_common(workspace, ws_bytes, q_nope, q_rope, cache, num_pages,
+                                 block_table, max_pages, seq_lens, B, H, softmax_scale, out, lse);
+    if (st != MLA_OK) return st;
+    if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+    DecodeArgs a;
+    memset(&a, 0, sizeof a);
+    a.ws = (const unsigned char *)workspace;
+    a.status = (int *)((unsigned char *)workspace + ws_layout(B, H, 1).status);
+    a.q_nope = (const uint16_t *)q_nope;
+    a.q_rope = (const uint16_t *)q_rope;
+    a.cache = (const unsigned char *)cache;
+    a.num_pages = num_pages;
+    a.block_table = block_table;
+    a.max_pages = max_pages;
+    a.seq_lens = seq_lens;
+    a.indices = nullptr;
+    a.topk = 0;
+    a.B = B;
+    a.H = H;
+    a.scale_log2 = softmax_scale * kLog2e;
+    a.out = out;
+    a.lse = lse;
+    a.kv_fp8 = kv_dtype == MLA_KV_FP8_E4M3;
+    a.ws_bytes = ws_bytes;
+    return run_decode(a, (cudaStream_t)stream);
+}
+
+mla_status mla_decode_sparse(const void *workspace, size_t ws_bytes, const void *q_nope,
+                             const void *q_rope, const void *cache, int64_t num_pages,
+                             const int32_t *block_table, int max_pages,
+                             const int32_t *seq_lens, const int32_t *indices, int topk, int B,
+                             int H, float softmax_scale, float *out, float *lse,
+                             void *stream) {
+    mla_status st = check_common(workspace, ws_bytes, q_nope, q_rope, cache, num_pages,
+                                 block_table, max_pages, seq_lens, B, H, softmax_scale, out, lse);
+    if (st != MLA_OK) return st;
+    if (!indices || topk < 1) return MLA_ERR_INVALID_ARG;
+    DecodeArgs a;
+    memset(&a, 0, sizeof a);
+    a.ws = (const unsigned char *)workspace;
+    a.status = (int *)((unsigned char *)workspace + ws_layout(B, H, 1).status);
+    a.q_nope = (const uint16_t *)q_nope;
+    a.q_rope = (const uint16_t *)q_rope;
+    a.cache = (const unsigned char *)cache;
+    a.num_pages = num_pages;
+    a.block_table = block_table;
+    a.max_pages = max_pages;
+    a.seq_lens = seq_lens;
+    a.indices = indices;
+    a.topk = topk;
+    a.B = B;
+    a.H = H;
+    a.scale_log2 = softmax_scale * kLog2e;
+    a.out = out;
+    a.lse = lse;
+    a.kv_fp8 = 0;
+    a.ws_bytes = ws_bytes;
+    return run_decode(a, (cudaStream_t)stream);
+}
+
+mla_status mla_decode_status(void *workspace, size_t ws_bytes, void *stream) {
+    if (!workspace || ws_bytes < 256) return MLA_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
+    int *dev_status = (int *)((unsigned char *)workspace + ws_layout(1, 1, 1).status);
+    int host = 0;
+    if (cudaMemcpy(&host, dev_status, sizeof host, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    if (host != 0 && cudaMemset(dev_status, 0, sizeof(int)) != cudaSuccess) return MLA_ERR_CUDA;
+    return (mla_status)host;
+}
+
+const char *mla_status_string(mla_status s) {
+    switch (s) {
+        case MLA_OK: return "ok";
+        case MLA_ERR_INVALID_ARG: return "invalid argument";
+        case MLA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case MLA_ERR_WORKSPACE: return "workspace too small or holds no matching plan";
+        case MLA_ERR_CUDA: return "CUDA runtime error";
+        case MLA_ERR_INDEX: return "page id, token index or length out of range";
+        case MLA_ERR_TIMEOUT: return "pipeline wait exceeded its iteration limit";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

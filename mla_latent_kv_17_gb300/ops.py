@@ -1,0 +1,195 @@
+"""Python binding of libmla_decode (argument marshalling only).
+
+Every function here checks tensor dtypes/shapes, passes raw device pointers and sizes to
+the C ABI declared in ``include/mla_decode.h`` and raises on a non-OK status.  All
+computation happens in the library's CUDA kernels.  If the library has not been built,
+the first call raises; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libmla_decode.so")
+
+MLA_OK = 0
+STATUS_NAMES = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
+                3: "MLA_ERR_WORKSPACE", 4: "MLA_ERR_CUDA", 5: "MLA_ERR_INDEX",
+                6: "MLA_ERR_TIMEOUT"}
+KV_BF16, KV_FP8 = 0, 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MlaError(RuntimeError):
+    def __init__(self, fn, status, text):
+        super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)} ({text})")
+        self.status = status
+
+
+def lib():
+    """The loaded libmla_decode (ctypes.CDLL); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with `python -m mla_latent_kv_17_gb300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I, I64, F, SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                                ctypes.c_size_t)
+            L.mla_decode_workspace_size.argtypes = [I, I, I]
+            L.mla_decode_workspace_size.restype = SZ
+            L.mla_decode_plan.argtypes = [P, I, I, I, I, P, SZ, P]
+            L.mla_decode_plan.restype = I
+            L.mla_decode_plan_host.argtypes = [P, I, I, I, I, P, SZ]
+            L.mla_decode_plan_host.restype = I
+            L.mla_decode.argtypes = [P, SZ, P, P, P, I, I64, P, I, P, I, I, F, P, P, P]
+            L.mla_decode.restype = I
+            L.mla_decode_sparse.argtypes = [P, SZ, P, P, P, I64, P, I, P, P, I, I, I, F, P, P, P]
+            L.mla_decode_sparse.restype = I
+            L.mla_decode_status.argtypes = [P, SZ, P]
+            L.mla_decode_status.restype = I
+            L.mla_status_string.argtypes = [I]
+            L.mla_status_string.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def _check(fn, st):
+    if st != MLA_OK:
+        raise MlaError(fn, st, lib().mla_status_string(st).decode())
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def workspace_size(B: int, H: int, num_sms: int = 0) -> int:
+    n = lib().mla_decode_workspace_size(int(B), int(H), int(num_sms))
+    if n == 0:
+        raise MlaError("mla_decode_workspace_size", 1, "invalid arguments")
+    return int(n)
+
+
+class Workspace:
+    """Device workspace holding a plan, the split-KV partials and the status word."""
+
+    def __init__(self, B: int, H: int, num_sms: int = 0, device=None):
+        self.B, self.H = int(B), int(H)
+        self.nbytes = workspace_size(B, H, num_sms)
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8,
+                               device=device or torch.device("cuda", torch.cuda.current_device()))
+        self.topk = None
+
+    def ptr(self):
+        return _ptr(self.buf)
+
+
+def _i32(t, name):
+    if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    return t
+
+
+def plan(ws: Workspace, seq_lens=None, topk: int = 0, num_sms: int = 0, stream=None) -> Workspace:
+    """Build the split-KV plan for seq_lens (device int32 [B]) or for topk index slots."""
+    if seq_lens is not None:
+        _i32(seq_lens, "seq_lens")
+    st = lib().mla_decode_plan(_ptr(seq_lens), ws.B, ws.H, int(topk), int(num_sms), ws.ptr(),
+                               ws.nbytes, _stream(stream))
+    _check("mla_decode_plan", st)
+    ws.topk = int(topk)
+    return ws
+
+
+def _outputs(B, H, device, out, lse):
+    if out is None:
+        out = torch.empty((B, H, 512), dtype=torch.float32, device=device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=device)
+    if out.dtype != torch.float32 or out.shape != (B, H, 512) or not out.is_contiguous():
+        raise ValueError("out must be contiguous fp32 [B,H,512]")
+    if lse.dtype != torch.float32 or lse.shape != (B, H) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [B,H]")
+    return out, lse
+
+
+def _queries(q_nope, q_rope):
+    B, H, d = q_nope.shape
+    if d != 512 or q_nope.dtype != torch.bfloat16 or not q_nope.is_contiguous():
+        raise ValueError("q_nope must be contiguous bf16 [B,H,512]")
+    if q_rope.shape != (B, H, 64) or q_rope.dtype != torch.bfloat16 or not q_rope.is_contiguous():
+        raise ValueError("q_rope must be contiguous bf16 [B,H,64]")
+    return B, H
+
+
+def decode(ws: Workspace, q_nope, q_rope, cache, block_table, seq_lens, softmax_scale: float,
+           out=None, lse=None, stream=None):
+    """Dense decode; the cache is bf16 [P,64,576] or uint8 FP8 records [P,64,656]."""
+    B, H = _queries(q_nope, q_rope)
+    _i32(block_table, "block_table")
+    _i32(seq_lens, "seq_lens")
+    if cache.dtype == torch.bfloat16 and cache.shape[1:] == (64, 576):
+        kv = KV_BF16
+    elif cache.dtype == torch.uint8 and cache.shape[1:] == (64, 656):
+        kv = KV_FP8
+    else:
+        raise ValueError("cache must be bf16 [P,64,576] or uint8 [P,64,656]")
+    if not cache.is_contiguous():
+        raise ValueError("cache must be contiguous")
+    out, lse = _outputs(B, H, q_nope.device, out, lse)
+    st = lib().mla_decode(ws.ptr(), ws.nbytes, _ptr(q_nope), _ptr(q_rope), _ptr(cache), kv,
+                          cache.shape[0], _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                          B, H, float(softmax_scale), _ptr(out), _ptr(lse), _stream(stream))
+    _check("mla_decode", st)
+    return out, lse
+
+
+def decode_sparse(ws: Workspace, q_nope, q_rope, cache, block_table, seq_lens, indices,
+                  softmax_scale: float, out=None, lse=None, stream=None):
+    """Token-sparse decode over indices [B,topk] (int32, -1 = padding); bf16 cache."""
+    B, H = _queries(q_nope, q_rope)
+    _i32(block_table, "block_table")
+    _i32(seq_lens, "seq_lens")
+    _i32(indices, "indices")
+    if cache.dtype != torch.bfloat16 or cache.shape[1:] != (64, 576) or not cache.is_contiguous():
+        raise ValueError("cache must be contiguous bf16 [P,64,576]")
+    out, lse = _outputs(B, H, q_nope.device, out, lse)
+    st = lib().mla_decode_sparse(ws.ptr(), ws.nbytes, _ptr(q_nope), _ptr(q_rope), _ptr(cache),
+                                 cache.shape[0], _ptr(block_table), block_table.shape[1],
+                                 _ptr(seq_lens), _ptr(indices), indices.shape[1], B, H,
+                                 float(softmax_scale), _ptr(out), _ptr(lse), _stream(stream))
+    _check("mla_decode_sparse", st)
+    return out, lse
+
+
+def status(ws: Workspace, stream=None) -> int:
+    """Synchronise and return (and clear) the device-side status code of the workspace."""
+    return int(lib().mla_decode_status(ws.ptr(), ws.nbytes, _stream(stream)))
+
+
+def plan_host(seq_lens, B: int, H: int, topk: int = 0, num_sms: int = 148):
+    """Host twin of the planner: returns the plan bytes (numpy uint8) for host seq_lens."""
+    import numpy as np
+    n = lib().mla_decode_workspace_size(int(B), int(H), int(num_sms))
+    buf = np.zeros(n, dtype=np.uint8)
+    sl = None
+    if seq_lens is not None:
+        sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    st = lib().mla_decode_plan_host(
+        sl.ctypes.data_as(ctypes.c_void_p) if sl is not None else None, int(B), int(H),
+        int(topk), int(num_sms), buf.ctypes.data_as(ctypes.c_void_p), n)
+    _check("mla_decode_plan_host", st)
+    return buf

@@ -1,0 +1,238 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Tolerances (bf16 inputs, fp32 accumulation): |out - ref| <= 1e-2 + 1e-2 |ref| element by
+element and |lse - ref| <= 1e-3; page and index handling is checked bit-exactly.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from mla_latent_kv_17_gb300 import inputs, ops
+from oracle_ref import assert_close, oracle_for
+from planview import parse
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from mla_latent_kv_17_gb300 import build
+    build.build()
+    ops.lib()
+
+
+def run(case, num_sms=0, ws=None):
+    c = case
+    if ws is None:
+        ws = ops.Workspace(c.B, c.H, num_sms)
+    topk = c.indices.shape[1] if c.indices is not None else 0
+    ops.plan(ws, c.seq_lens if topk == 0 else None, topk=topk, num_sms=num_sms)
+    if c.indices is not None:
+        out, lse = ops.decode_sparse(ws, c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens,
+                                     c.indices, c.scale)
+    else:
+        out, lse = ops.decode(ws, c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens, c.scale)
+    st = ops.status(ws)
+    assert st == 0, ops.STATUS_NAMES.get(st, st)
+    return out, lse, ws
+
+
+def check(case, num_sms=0, what=""):
+    out, lse, _ = run(case, num_sms)
+    ref_out, ref_lse = oracle_for(case)
+    assert_close(out, lse, ref_out, ref_lse, what)
+    return out, lse
+
+
+def small(B, H, lens, seed, **kw):
+    return inputs.make_case(B, H, lens, seed=seed, extra_pages=3, **kw).to("cuda")
+
+
+# ------------------------------------------------------------------------------ dense
+def test_tiny_workload():
+    c = inputs.make_workload("tiny_dense_b1_h16_l256", device="cpu").to("cuda")
+    check(c, what="tiny")
+
+
+@pytest.mark.parametrize("H", [16, 64, 128])
+def test_dense_edge_lengths(H):
+    check(small(6, H, [1, 63, 64, 65, 127, 300], seed=H), what=f"H={H}")
+
+
+def test_dense_zero_length_request():
+    c = small(3, 32, [0, 77, 0], seed=5)
+    out, lse, _ = run(c)
+    assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
+    assert torch.all(out[2] == 0) and torch.all(torch.isneginf(lse[2]))
+    ref_out, ref_lse = oracle_for(c)
+    assert_close(out, lse, ref_out, ref_lse, "zero-length")
+
+
+@pytest.mark.parametrize("num_sms", [2, 4, 10])
+def test_dense_split_kv_and_combine(num_sms):
+    # few SMs force long requests into several pieces merged by the combine step
+    c = small(3, 128, [3000, 1000, 4097], seed=num_sms)
+    out, lse, ws = run(c, num_sms=num_sms)
+    p = parse(ws.buf.cpu().numpy(), c.B, c.H)
+    assert p["n_partials"] > 0
+    ref_out, ref_lse = oracle_for(c)
+    assert_close(out, lse, ref_out, ref_lse, f"split num_sms={num_sms}")
+
+
+def test_device_plan_equals_host_plan():
+    sl = inputs.workload_seq_lens("dsv3_dense_b64_h128_l1k_8k")
+    ws = ops.Workspace(64, 128)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ops.plan(ws, sl.cuda(), num_sms=sms)
+    torch.cuda.synchronize()
+    dev = ws.buf.cpu().numpy()
+    host = ops.plan_host(sl.numpy(), 64, 128, 0, sms)
+    end = parse(host, 64, 128)["plan_end"]
+    assert np.array_equal(dev[:128], host[:128]) and np.array_equal(dev[256:end], host[256:end])
+
+
+def test_large_query_scale_is_stable():
+    c = small(2, 128, [500, 129], seed=3, q_scale=8.0)   # very peaked softmax
+    check(c, what="peaked")
+
+
+def test_one_hot_page_mapping_bit_exact():
+    """Row r of physical page p holds (p, r) in latent channels 0 and 1.  Each (b, h) gets
+    its own marker channel k, set to 1 only in its target row, and a query of 1000 on k:
+    the softmax is exactly one-hot, so the output names the row the kernel read."""
+    B, H = 2, 128
+    lens = [300, 130]
+    c = inputs.make_case(B, H, lens, seed=11, extra_pages=7)
+    P = c.num_pages
+    cache = torch.zeros((P, 64, 576))
+    cache[:, :, 0] = torch.arange(P).view(P, 1).float()
+    cache[:, :, 1] = torch.arange(64).view(1, 64).float()
+    qn = torch.zeros((B, H, 512))
+    g = torch.Generator().manual_seed(1)
+    targets = torch.stack([torch.randint(0, L, (H,), generator=g) for L in lens])
+    for b in range(B):
+        for h in range(H):
+            t, k = int(targets[b, h]), 2 + b * H + h
+            cache[int(c.block_table[b, t // 64]), t % 64, k] = 1.0
+            qn[b, h, k] = 1000.0
+    c.cache = cache.to(torch.bfloat16)
+    c.q_nope = qn.to(torch.bfloat16)
+    c.q_rope = torch.zeros((B, H, 64), dtype=torch.bfloat16)
+    c.scale = 1.0
+    out, lse, _ = run(c.to("cuda"))
+    out = out.cpu()
+    for b in range(B):
+        for h in range(H):
+            t = int(targets[b, h])
+            assert out[b, h, 0].item() == float(c.block_table[b, t // 64]), (b, h)
+            assert out[b, h, 1].item() == float(t % 64), (b, h)
+            assert abs(lse[b, h].item() - 1000.0) <= 1e-3
+
+
+# ------------------------------------------------------------------------------ fp8
+def test_fp8_small():
+    c = small(4, 128, [1, 64, 65, 700], seed=8, kv_dtype="fp8")
+    check(c, what="fp8")
+
+
+def test_fp8_split():
+    c = small(2, 64, [2500, 3000], seed=9, kv_dtype="fp8")
+    check(c, num_sms=4, what="fp8 split")
+
+
+# ------------------------------------------------------------------------------ sparse
+def _sparse(B, H, lens, topk, seed, window=16):
+    c = inputs.make_case(B, H, lens, seed=seed, extra_pages=2)
+    c.indices = inputs.sparse_indices(c.seq_lens, topk, window, seed)
+    return c.to("cuda")
+
+
+def test_sparse_small():
+    check(_sparse(3, 128, [100, 1000, 40], topk=64, seed=1), what="sparse")
+
+
+def test_sparse_padding_duplicates_and_empty():
+    c = _sparse(3, 64, [50, 200, 10], topk=96, seed=2)
+    idx = c.indices.cpu()
+    idx[0, :] = -1                       # all padding
+    idx[1, 5] = idx[1, 6]                # a duplicate
+    idx[1, 10:20] = -1
+    c.indices = idx.cuda()
+    out, lse = check(c, what="sparse pad/dup")
+    assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
+
+
+def test_sparse_all_indices_equals_dense():
+    c = small(2, 128, [333, 64], seed=4)
+    d_out, d_lse, _ = run(c)
+    topk = 333
+    idx = torch.full((2, topk), -1, dtype=torch.int32)
+    idx[0] = torch.randperm(333, generator=torch.Generator().manual_seed(0)).to(torch.int32)
+    idx[1, :64] = torch.arange(64)
+    c.indices = idx.cuda()
+    s_out, s_lse, _ = run(c)
+    torch.testing.assert_close(s_out, d_out, atol=2e-3, rtol=2e-3)
+    torch.testing.assert_close(s_lse, d_lse, atol=1e-4, rtol=0)
+
+
+def test_sparse_split():
+    check(_sparse(2, 128, [9000, 5000], topk=2048, seed=5), num_sms=6, what="sparse split")
+
+
+# ------------------------------------------------------------------------------ errors
+def test_out_of_range_page_is_reported_not_faulted():
+    c = small(2, 16, [100, 100], seed=6)
+    bt = c.block_table.clone()
+    bt[1, 1] = c.num_pages + 5           # caught by the kernel's bounds check
+    c.block_table = bt
+    ws = ops.Workspace(c.B, c.H)
+    ops.plan(ws, c.seq_lens)
+    ops.decode(ws, c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens, c.scale)
+    assert ops.status(ws) == 5
+    assert ops.status(ws) == 0           # cleared after reading
+
+
+def test_out_of_range_sparse_index_is_reported():
+    c = _sparse(1, 16, [100], topk=64, seed=7)
+    idx = c.indices.clone()
+    idx[0, 3] = 100                      # == seq_len: out of range
+    c.indices = idx
+    ws = ops.Workspace(1, 16)
+    ops.plan(ws, None, topk=64)
+    ops.decode_sparse(ws, c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens, c.indices, c.scale)
+    assert ops.status(ws) == 5
+
+
+def test_plan_mismatch_is_reported():
+    c = small(2, 16, [100, 100], seed=8)
+    ws = ops.Workspace(2, 16)
+    ops.plan(ws, None, topk=64)          # a sparse plan used for dense decode
+    ops.decode(ws, c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens, c.scale)
+    assert ops.status(ws) == 3
+
+
+# ------------------------------------------------------------------------------ full size
+def _sampled(name, bs, hs):
+    c = inputs.make_workload(name, device="cuda")
+    out, lse, _ = run(c)
+    ref_out, ref_lse = oracle_for(c, bs, hs)
+    assert_close(out[bs][:, hs], lse[bs][:, hs], ref_out, ref_lse, name)
+    assert torch.isfinite(out).all()
+
+
+def test_full_dsv3_sampled():
+    _sampled("dsv3_dense_b64_h128_l1k_8k", [0, 17, 63], [0, 1, 64, 127])
+
+
+def test_full_long_sampled():
+    _sampled("long_dense_b4_h128_l128k", [0, 3], [0, 77, 127])
+
+
+def test_full_fp8_sampled():
+    _sampled("fp8_ragged_b128_h128_lognormal", [0, 5, 127], [0, 100])
+
+
+def test_full_sparse_sampled():
+    _sampled("dsa_sparse_b64_h128_l64k_top2048", [0, 31, 63], [0, 64, 127])

@@ -1,0 +1,104 @@
+"""Properties of the split-KV planner (host twin of the device planner; CPU only)."""
+import numpy as np
+import pytest
+
+from mla_latent_kv_17_gb300 import build as mbuild
+from mla_latent_kv_17_gb300 import inputs, ops
+from planview import parse
+
+OVH = 3  # per-piece overhead in tiles, as the planner charges it
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    mbuild.build()
+
+
+def check_plan(seq_lens, H=128, topk=0, num_sms=148):
+    B = len(seq_lens)
+    p = parse(ops.plan_host(seq_lens if topk == 0 else None, B, H, topk, num_sms), B, H)
+    lens = [topk if topk else max(0, int(x)) for x in seq_lens]
+    units = p["units"]
+    assert units == max(1, num_sms // 2)
+    ub = p["unit_begin"]
+    assert ub[0] == 0 and ub[-1] == p["n_items"] and np.all(np.diff(ub) >= 0)
+    assert p["n_items"] <= p["max_items"] == B + units
+    items = p["items"]
+    # coverage: each request's pieces tile [0, len) exactly once, in order, on 64-token bounds
+    per_req = {b: [] for b in range(B)}
+    for b, t0, t1, slot in items:
+        per_req[int(b)].append((int(t0), int(t1), int(slot)))
+    slots = []
+    for b in range(B):
+        pcs = per_req[b]
+        assert len(pcs) == p["num_splits"][b] >= 1
+        if lens[b] == 0:
+            assert pcs == [(0, 0, -1)]
+            continue
+        pos = 0
+        for t0, t1, _ in pcs:
+            assert t0 == pos and t1 > t0 and t0 % 64 == 0
+            pos = t1
+        assert pos == lens[b]
+        if len(pcs) == 1:
+            assert pcs[0][2] == -1 and p["split_base"][b] == -1
+        else:
+            s = [x[2] for x in pcs]
+            assert s == list(range(p["split_base"][b], p["split_base"][b] + len(pcs)))
+            slots += s
+    assert sorted(slots) == list(range(len(slots))) and len(slots) == p["n_partials"]
+    assert p["n_partials"] <= p["max_partials"]
+    # balance: no unit exceeds its budget except the last one (which takes any remainder)
+    cost = np.zeros(units, dtype=np.int64)
+    for u in range(units):
+        for i in range(ub[u], ub[u + 1]):
+            b, t0, t1, _ = items[i]
+            if t1 > t0:
+                cost[u] += (t1 - t0 + 63) // 64 + OVH
+    assert np.all(cost[:-1] <= p["per"])
+    return p, cost
+
+
+@pytest.mark.parametrize("name", list(inputs.WORKLOADS))
+def test_workload_plans(name):
+    sl = inputs.workload_seq_lens(name).tolist()
+    topk = 2048 if "sparse" in name else 0
+    p, cost = check_plan(sl, topk=topk)
+    tiles = sum((topk or L) // 64 + ((topk or L) % 64 > 0) for L in sl)
+    # the busiest unit carries at most ~its fair share plus one piece overhead and a tile
+    assert cost.max() <= tiles / p["units"] + 2 * OVH + 4
+
+
+def test_edge_lengths():
+    check_plan([1, 63, 64, 65, 0, 128, 129])
+    check_plan([0])
+    check_plan([0, 0, 0])
+    check_plan([1])
+    check_plan([131072] * 4)
+    check_plan([5] * 300)                   # more requests than units
+    check_plan(list(range(0, 5000, 37)))
+
+
+@pytest.mark.parametrize("num_sms", [2, 3, 8, 148, 152])
+def test_sm_counts(num_sms):
+    rng = np.random.default_rng(num_sms)
+    check_plan(rng.integers(0, 9000, size=37).tolist(), num_sms=num_sms)
+
+
+def test_sparse_plan_uses_topk():
+    p, _ = check_plan([10, 100000, 3], topk=2048)
+    assert p["topk"] == 2048
+
+
+def test_long_requests_are_split_and_short_batches_are_not():
+    p, _ = check_plan([131072] * 4)
+    assert all(n > 1 for n in p["num_splits"])
+    p, _ = check_plan([256])
+    assert p["num_splits"][0] == 1 and p["n_partials"] == 0
+
+
+def test_plan_is_deterministic():
+    sl = inputs.workload_seq_lens("dsv3_dense_b64_h128_l1k_8k").tolist()
+    a = ops.plan_host(sl, 64, 128, 0, 148)
+    b = ops.plan_host(sl, 64, 128, 0, 148)
+    assert np.array_equal(a, b)
