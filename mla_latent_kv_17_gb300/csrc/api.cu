@@ -12,13 +12,75 @@ namespace mla {
 namespace {
 
 // ---------------------------------------------------------------------------------
-// Device planner: one thread runs the same sequential planner as the host twin.
+// Device planner: one CTA.  Each thread owns a contiguous slice of requests; block-wide
+// exclusive scans give every request its budget position, item offset and first partial
+// slot, then each thread writes its requests' pieces.  Same functions as the host twin.
 // ---------------------------------------------------------------------------------
-__global__ void plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int num_units,
-                            unsigned char *ws) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) {
-        build_plan(seq_lens, B, H, topk, num_units, ws);
-        *reinterpret_cast<int *>(ws + ws_layout(B, H, num_units).status) = 0;
+constexpr int kPlanThreads = 1024;
+
+__device__ int64_t block_exclusive_scan(int64_t v, int64_t *total, int64_t *sh) {
+    const int t = threadIdx.x;
+    sh[t] = v;
+    __syncthreads();
+    for (int off = 1; off < kPlanThreads; off <<= 1) {
+        int64_t x = t >= off ? sh[t - off] : 0;
+        __syncthreads();
+        sh[t] += x;
+        __syncthreads();
+    }
+    const int64_t incl = sh[t];
+    *total = sh[kPlanThreads - 1];
+    __syncthreads();
+    return incl - v;
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int units, unsigned char *ws) {
+    __shared__ int64_t sh[kPlanThreads];
+    const WsLayout L = ws_layout(B, H, units);
+    int64_t *req_start = reinterpret_cast<int64_t *>(ws + L.req_start);
+    int32_t *num_splits = reinterpret_cast<int32_t *>(ws + L.num_splits);
+    int32_t *split_base = reinterpret_cast<int32_t *>(ws + L.split_base);
+    int32_t *unit_begin = reinterpret_cast<int32_t *>(ws + L.unit_begin);
+    const int32_t *item_unit = reinterpret_cast<const int32_t *>(ws + L.item_unit);
+    const int chunk = (B + kPlanThreads - 1) / kPlanThreads;
+    const int b0 = min(B, (int)threadIdx.x * chunk), b1 = min(B, b0 + chunk);
+
+    int64_t local = 0;
+    for (int b = b0; b < b1; ++b) local += req_cost(req_tiles(seq_lens, topk, b));
+    int64_t total;
+    int64_t pos = block_exclusive_scan(local, &total, sh);
+    for (int b = b0; b < b1; ++b) {
+        req_start[b] = pos;
+        pos += req_cost(req_tiles(seq_lens, topk, b));
+    }
+    const int64_t per = plan_budget(total, units);
+
+    int64_t n_local = 0, s_local = 0;
+    for (int b = b0; b < b1; ++b) {
+        const ReqSplit r = req_split(req_start[b], req_tiles(seq_lens, topk, b), per, units);
+        n_local += r.n;
+        if (r.n > 1) s_local += r.n;
+    }
+    int64_t n_total, s_total;
+    int64_t off = block_exclusive_scan(n_local, &n_total, sh);
+    int64_t slot = block_exclusive_scan(s_local, &s_total, sh);
+    for (int b = b0; b < b1; ++b) {
+        const ReqSplit r = req_split(req_start[b], req_tiles(seq_lens, topk, b), per, units);
+        num_splits[b] = r.n;
+        split_base[b] = r.n > 1 ? (int32_t)slot : -1;
+        emit_request(ws, L, seq_lens, topk, b, req_start[b], per, units, (int32_t)off,
+                     split_base[b]);
+        off += r.n;
+        if (r.n > 1) slot += r.n;
+    }
+    __syncthreads();
+    for (int u = threadIdx.x; u <= units; u += kPlanThreads)
+        unit_begin[u] = u == units ? (int32_t)n_total
+                                   : lower_bound_unit(item_unit, (int32_t)n_total, u);
+    if (threadIdx.x == 0) {
+        write_header(ws, L, B, H, topk, units, (int32_t)n_total, per, (int32_t)s_total);
+        *reinterpret_cast<int *>(ws + L.status) = 0;
     }
 }
 
@@ -126,8 +188,8 @@ mla_status mla_decode_plan(const int32_t *seq_lens, int B, int H, int topk, int 
     if (num_sms <= 0) return MLA_ERR_CUDA;
     const int units = num_units_for(num_sms);
     if (ws_bytes < ws_layout(B, H, units).total) return MLA_ERR_WORKSPACE;
-    plan_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(seq_lens, B, H, topk, units,
-                                                    (unsigned char *)workspace);
+    plan_kernel<<<1, kPlanThreads, 0, (cudaStream_t)stream>>>(seq_lens, B, H, topk, units,
+                                                              (unsigned char *)workspace);
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -139,7 +201,7 @@ mla_status mla_decode_plan_host(const int32_t *seq_lens, int B, int H, int topk,
     const int units = num_units_for(num_sms);
     const WsLayout L = ws_layout(B, H, units);
     if (ws_bytes < L.plan_end) return MLA_ERR_WORKSPACE;
-    build_plan(seq_lens, B, H, topk, units, (unsigned char *)workspace_host);
+    build_plan_serial(seq_lens, B, H, topk, units, (unsigned char *)workspace_host);
     *reinterpret_cast<int *>((unsigned char *)workspace_host + L.status) = 0;
     return MLA_OK;
 }

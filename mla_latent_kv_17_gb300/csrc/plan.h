@@ -49,10 +49,11 @@ struct WorkItem {
 
 MLA_HD size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Byte offsets inside the workspace.  Everything up to `plan_end` is the plan proper.
+// Byte offsets inside the workspace.  Everything up to `plan_end` is the plan proper;
+// req_start and item_unit are planner scratch that the decode does not read.
 struct WsLayout {
-    size_t header, status, unit_begin, items, num_splits, split_base, plan_end;
-    size_t part_lse, part_o, total;
+    size_t header, status, unit_begin, items, num_splits, split_base, req_start, item_unit;
+    size_t plan_end, part_lse, part_o, total;
     int max_items, max_partials, num_units;
 };
 
@@ -72,6 +73,10 @@ MLA_HD WsLayout ws_layout(int B, int H, int num_units) {
     o = align_up(o + sizeof(int32_t) * (size_t)B, 256);
     L.split_base = o;
     o = align_up(o + sizeof(int32_t) * (size_t)B, 256);
+    L.req_start = o;
+    o = align_up(o + sizeof(int64_t) * (size_t)B, 256);
+    L.item_unit = o;
+    o = align_up(o + sizeof(int32_t) * (size_t)L.max_items, 256);
     L.plan_end = o;
     L.part_lse = o;
     o = align_up(o + sizeof(float) * (size_t)L.max_partials * H, 256);
@@ -86,130 +91,163 @@ MLA_HD int num_units_for(int num_sms) {
     return u < 1 ? 1 : u;
 }
 
-// Length (in tokens or index slots) that request b is planned over.
-MLA_HD int32_t planned_len(const int32_t *seq_lens, int topk, int b) {
+// Tiles request b is planned over (tokens, or index slots for sparse decode).
+MLA_HD int32_t req_len(const int32_t *seq_lens, int topk, int b) {
     if (topk > 0) return topk;
     int32_t L = seq_lens[b];
     return L < 0 ? 0 : L;
 }
+MLA_HD int32_t req_tiles(const int32_t *seq_lens, int topk, int b) {
+    return (req_len(seq_lens, topk, b) + kTileTokens - 1) / kTileTokens;
+}
+MLA_HD int64_t req_cost(int32_t tiles) { return tiles > 0 ? tiles + kPieceOverheadTiles : 0; }
 
-// Walks the requests with a per-unit budget of `per` cost units (tiles + a fixed overhead
-// per piece), filling units in order.  With `emit`, writes the items, unit_begin and
-// num_splits; always returns the cost that lands on the last unit (which takes whatever
-// remains), so the caller can search for the smallest budget that does not overflow it.
-MLA_HD long long walk_plan(const int32_t *seq_lens, int B, int topk, int num_units,
-                           long long per, bool emit, int32_t *unit_begin, WorkItem *items,
-                           int32_t *num_splits, int *n_items) {
-    int n = 0;
-    int u = 0;
-    long long cap = per;
-    if (emit)
-        for (int i = 0; i <= num_units; ++i) unit_begin[i] = 0;
-    for (int b = 0; b < B; ++b) {
-        int32_t len = planned_len(seq_lens, topk, b);
-        int32_t tiles = (len + kTileTokens - 1) / kTileTokens;
-        if (emit) num_splits[b] = 0;
-        if (tiles == 0) {
-            if (emit) {
-                items[n].b = b; items[n].t0 = 0; items[n].t1 = 0; items[n].slot = -1;
-                num_splits[b] = 1;
-            }
-            ++n;
-            continue;
-        }
-        int32_t t = 0;
-        while (t < tiles) {
-            long long avail = cap - kPieceOverheadTiles;
-            int32_t rest = tiles - t;
-            int32_t take;
-            if (avail >= rest || u == num_units - 1) {
-                take = rest;
-            } else {
-                take = avail < 0 ? 0 : (int32_t)avail;
-                if (rest - take < kMinPieceTiles) take = rest - kMinPieceTiles;
-                if (take < kMinPieceTiles) {
-                    // too little room left here: continue in the next unit
-                    if (emit) unit_begin[u + 1] = n;
-                    ++u;
-                    cap = per;
-                    continue;
-                }
-            }
-            if (emit) {
-                items[n].b = b;
-                items[n].t0 = t * kTileTokens;
-                int32_t e = (t + take) * kTileTokens;
-                items[n].t1 = e < len ? e : len;
-                items[n].slot = -1;
-                ++num_splits[b];
-            }
-            ++n;
-            t += take;
-            cap -= take + kPieceOverheadTiles;
-            if (cap <= kPieceOverheadTiles && u < num_units - 1 && t < tiles) {
-                if (emit) unit_begin[u + 1] = n;
-                ++u;
-                cap = per;
-            }
-        }
-    }
-    if (emit)
-        for (int i = u + 1; i <= num_units; ++i) unit_begin[i] = n;
-    *n_items = n;
-    return u == num_units - 1 ? per - cap : 0;
+// The budget axis: request b occupies cost positions [S_b, S_b + cost_b); its overhead
+// comes first, so tile t sits at S_b + overhead + t.  Unit u owns positions
+// [u * per, (u + 1) * per); the last unit also takes anything beyond.
+MLA_HD int32_t unit_of(int64_t pos, int64_t per, int units) {
+    int64_t u = pos / per;
+    return u >= units ? units - 1 : (int32_t)u;
 }
 
-// Builds the plan into `ws` (host or device memory laid out by ws_layout).  Sequential;
-// on the device it runs on one thread.  The budget is the smallest one (binary search)
-// for which the last unit is not overloaded.
-MLA_HD void build_plan(const int32_t *seq_lens, int B, int H, int topk, int num_units,
-                       unsigned char *ws) {
-    WsLayout L = ws_layout(B, H, num_units);
-    PlanHeader *hd = reinterpret_cast<PlanHeader *>(ws + L.header);
-    int32_t *unit_begin = reinterpret_cast<int32_t *>(ws + L.unit_begin);
-    WorkItem *items = reinterpret_cast<WorkItem *>(ws + L.items);
-    int32_t *num_splits = reinterpret_cast<int32_t *>(ws + L.num_splits);
-    int32_t *split_base = reinterpret_cast<int32_t *>(ws + L.split_base);
+// How request b is cut into pieces.  Unit boundaries inside the request give runs of
+// tiles that belong to one unit; a first or last run shorter than kMinPieceTiles is folded
+// into its neighbour.  Cut k (1 <= k <= uf_last - uf) would start unit uf + k at tile
+// (uf + k) * per - p0; cuts kfirst..klast are kept, so the request has
+// klast - kfirst + 2 pieces.
+struct ReqSplit {
+    int64_t p0;
+    int32_t uf, kfirst, klast, tiles, n;
+};
 
-    long long total_cost = 0;
-    for (int b = 0; b < B; ++b) {
-        int32_t tiles = (planned_len(seq_lens, topk, b) + kTileTokens - 1) / kTileTokens;
-        total_cost += tiles + (tiles > 0 ? kPieceOverheadTiles : 0);
+MLA_HD ReqSplit req_split(int64_t S, int32_t tiles, int64_t per, int units) {
+    ReqSplit r;
+    r.p0 = S + kPieceOverheadTiles;
+    r.tiles = tiles;
+    if (tiles <= 0) {
+        r.uf = unit_of(S, per, units);
+        r.kfirst = 1;
+        r.klast = 0;
+        r.n = 1;
+        return r;
     }
-    long long lo = (total_cost + num_units - 1) / num_units;
-    if (lo < kPieceOverheadTiles + kMinPieceTiles) lo = kPieceOverheadTiles + kMinPieceTiles;
-    long long hi = total_cost + kPieceOverheadTiles + kMinPieceTiles;
-    int n = 0;
-    while (lo < hi) {
-        long long mid = lo + (hi - lo) / 2;
-        if (walk_plan(seq_lens, B, topk, num_units, mid, false, nullptr, nullptr, nullptr, &n) <= mid)
-            hi = mid;
-        else
-            lo = mid + 1;
+    r.uf = unit_of(r.p0, per, units);
+    const int32_t ul = unit_of(r.p0 + tiles - 1, per, units);
+    r.kfirst = 1;
+    r.klast = ul - r.uf;
+    if (r.klast >= 1) {
+        const int64_t first_len = (int64_t)(r.uf + 1) * per - r.p0;
+        if (first_len < kMinPieceTiles) r.kfirst = 2;
+        const int64_t last_len = tiles - ((int64_t)ul * per - r.p0);
+        if (last_len < kMinPieceTiles && r.klast >= r.kfirst) r.klast -= 1;
     }
-    const long long per = lo;
-    walk_plan(seq_lens, B, topk, num_units, per, true, unit_begin, items, num_splits, &n);
-    // Partial slots for requests with more than one piece, in item order.
-    for (int b = 0; b < B; ++b) split_base[b] = -1;
-    int slots = 0;
-    for (int i = 0; i < n; ++i) {
-        int b = items[i].b;
-        if (num_splits[b] > 1) {
-            if (split_base[b] < 0) split_base[b] = slots;
-            items[i].slot = slots++;
-        }
+    r.n = r.klast - r.kfirst + 2;
+    return r;
+}
+
+// Tile range [tb, te) and unit of piece i of a request.
+MLA_HD void req_piece(const ReqSplit &r, int i, int64_t per, int units, int32_t *tb, int32_t *te,
+                      int32_t *unit) {
+    if (r.tiles <= 0) {
+        *tb = 0;
+        *te = 0;
+        *unit = r.uf;
+        return;
     }
+    const int32_t k = r.kfirst + i;  // cut that ends piece i (if k <= klast)
+    const int32_t b = i == 0 ? 0 : (int32_t)((int64_t)(r.uf + k - 1) * per - r.p0);
+    const int32_t e = k <= r.klast ? (int32_t)((int64_t)(r.uf + k) * per - r.p0) : r.tiles;
+    *tb = b;
+    *te = e;
+    *unit = unit_of(r.p0 + (b + e - 1) / 2, per, units);
+}
+
+MLA_HD int64_t plan_budget(int64_t total_cost, int units) {
+    int64_t per = (total_cost + units - 1) / units;
+    const int64_t lo = kPieceOverheadTiles + kMinPieceTiles;
+    return per < lo ? lo : per;
+}
+
+// Writes the pieces of request b (its item offset `off`, its first partial slot `slot0`
+// or -1) into the workspace.
+MLA_HD void emit_request(unsigned char *ws, const WsLayout &L, const int32_t *seq_lens, int topk,
+                         int b, int64_t S, int64_t per, int units, int32_t off, int32_t slot0) {
+    WorkItem *items = reinterpret_cast<WorkItem *>(ws + L.items);
+    int32_t *item_unit = reinterpret_cast<int32_t *>(ws + L.item_unit);
+    const int32_t len = req_len(seq_lens, topk, b);
+    const int32_t tiles = (len + kTileTokens - 1) / kTileTokens;
+    const ReqSplit r = req_split(S, tiles, per, units);
+    for (int i = 0; i < r.n; ++i) {
+        int32_t tb, te, u;
+        req_piece(r, i, per, units, &tb, &te, &u);
+        WorkItem w;
+        w.b = b;
+        w.t0 = tb * kTileTokens;
+        const int32_t e = te * kTileTokens;
+        w.t1 = e < len ? e : len;
+        w.slot = r.n > 1 ? slot0 + i : -1;
+        items[off + i] = w;
+        item_unit[off + i] = u;
+    }
+}
+
+MLA_HD void write_header(unsigned char *ws, const WsLayout &L, int B, int H, int topk, int units,
+                         int n_items, int64_t per, int n_partials) {
+    PlanHeader *hd = reinterpret_cast<PlanHeader *>(ws + L.header);
     hd->magic = kPlanMagic;
     hd->B = B;
     hd->H = H;
     hd->topk = topk;
-    hd->num_units = num_units;
-    hd->num_items = n;
+    hd->num_units = units;
+    hd->num_items = n_items;
     hd->max_items = L.max_items;
     hd->max_partials = L.max_partials;
     hd->tiles_per_unit = (int32_t)per;
-    hd->num_partials = slots;
+    hd->num_partials = n_partials;
     for (int i = 0; i < 6; ++i) hd->reserved[i] = 0;
+}
+
+// First item index whose unit is >= u (items are ordered by unit).
+MLA_HD int32_t lower_bound_unit(const int32_t *item_unit, int32_t n, int32_t u) {
+    int32_t lo = 0, hi = n;
+    while (lo < hi) {
+        int32_t mid = (lo + hi) / 2;
+        if (item_unit[mid] < u)
+            lo = mid + 1;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+// Host planner: the same per-request functions in serial loops.  The device planner
+// (plan kernel) computes the same prefix sums in parallel and writes identical bytes.
+inline void build_plan_serial(const int32_t *seq_lens, int B, int H, int topk, int units,
+                              unsigned char *ws) {
+    const WsLayout L = ws_layout(B, H, units);
+    int32_t *num_splits = reinterpret_cast<int32_t *>(ws + L.num_splits);
+    int32_t *split_base = reinterpret_cast<int32_t *>(ws + L.split_base);
+    int64_t *req_start = reinterpret_cast<int64_t *>(ws + L.req_start);
+    int32_t *unit_begin = reinterpret_cast<int32_t *>(ws + L.unit_begin);
+    int32_t *item_unit = reinterpret_cast<int32_t *>(ws + L.item_unit);
+    int64_t S = 0;
+    for (int b = 0; b < B; ++b) {
+        req_start[b] = S;
+        S += req_cost(req_tiles(seq_lens, topk, b));
+    }
+    const int64_t per = plan_budget(S, units);
+    int32_t off = 0, slots = 0;
+    for (int b = 0; b < B; ++b) {
+        const ReqSplit r = req_split(req_start[b], req_tiles(seq_lens, topk, b), per, units);
+        num_splits[b] = r.n;
+        split_base[b] = r.n > 1 ? slots : -1;
+        emit_request(ws, L, seq_lens, topk, b, req_start[b], per, units, off, split_base[b]);
+        off += r.n;
+        if (r.n > 1) slots += r.n;
+    }
+    for (int u = 0; u <= units; ++u)
+        unit_begin[u] = u == units ? off : lower_bound_unit(item_unit, off, u);
+    write_header(ws, L, B, H, topk, units, off, per, slots);
 }
 
 }  // namespace mla

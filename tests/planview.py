@@ -20,6 +20,10 @@ def parse(buf, B, H):
     o = _up(o + 4 * B)
     sb = buf[o:o + 4 * B].view(np.int32).copy()
     o = _up(o + 4 * B)
-    return dict(topk=topk, units=units, n_items=n_items, max_items=max_items,
+    rs = buf[o:o + 8 * B].view(np.int64).copy()
+    o = _up(o + 8 * B)
+    iu = buf[o:o + 4 * max_items].view(np.int32)[:n_items].copy()
+    o = _up(o + 4 * max_items)
+    return dict(req_start=rs, item_unit=iu, topk=topk, units=units, n_items=n_items, max_items=max_items,
                 max_partials=max_partials, per=per, n_partials=n_part, unit_begin=ub,
                 items=items, num_splits=ns, split_base=sb, plan_end=o)

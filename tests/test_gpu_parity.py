@@ -70,7 +70,7 @@ def test_dense_zero_length_request():
     assert_close(out, lse, ref_out, ref_lse, "zero-length")
 
 
-@pytest.mark.parametrize("num_sms", [2, 4, 10])
+@pytest.mark.parametrize("num_sms", [6, 10, 16])
 def test_dense_split_kv_and_combine(num_sms):
     # few SMs force long requests into several pieces merged by the combine step
     c = small(3, 128, [3000, 1000, 4097], seed=num_sms)

@@ -7,6 +7,7 @@ from mla_latent_kv_17_gb300 import inputs, ops
 from planview import parse
 
 OVH = 3  # per-piece overhead in tiles, as the planner charges it
+MIN = 4  # shortest piece the planner makes
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -48,14 +49,23 @@ def check_plan(seq_lens, H=128, topk=0, num_sms=148):
             slots += s
     assert sorted(slots) == list(range(len(slots))) and len(slots) == p["n_partials"]
     assert p["n_partials"] <= p["max_partials"]
-    # balance: no unit exceeds its budget except the last one (which takes any remainder)
+    # items are grouped by unit in order, and each unit's load stays near the budget: at most
+    # one folded short run (< MIN tiles) and one extra piece overhead beyond it
+    assert np.all(np.diff(p["item_unit"]) >= 0)
+    for u in range(units):
+        assert np.all(p["item_unit"][ub[u]:ub[u + 1]] == u)
     cost = np.zeros(units, dtype=np.int64)
     for u in range(units):
         for i in range(ub[u], ub[u + 1]):
             b, t0, t1, _ = items[i]
             if t1 > t0:
                 cost[u] += (t1 - t0 + 63) // 64 + OVH
-    assert np.all(cost[:-1] <= p["per"])
+    assert np.all(cost <= p["per"] + MIN + 2 * OVH), (cost.max(), p["per"])
+    # pieces are never shorter than MIN tiles unless the whole request is
+    for b in range(B):
+        pcs = per_req[b]
+        if len(pcs) > 1:
+            assert all((t1 - t0 + 63) // 64 >= MIN for t0, t1, _ in pcs)
     return p, cost
 
 
@@ -65,8 +75,12 @@ def test_workload_plans(name):
     topk = 2048 if "sparse" in name else 0
     p, cost = check_plan(sl, topk=topk)
     tiles = sum((topk or L) // 64 + ((topk or L) % 64 > 0) for L in sl)
-    # the busiest unit carries at most ~its fair share plus one piece overhead and a tile
-    assert cost.max() <= tiles / p["units"] + 2 * OVH + 4
+    ub, items = p["unit_begin"], p["items"]
+    load = [sum((t1 - t0 + 63) // 64 for _, t0, t1, _ in items[ub[u]:ub[u + 1]])
+            for u in range(p["units"])]
+    # the busiest unit carries at most its share plus two folded short runs
+    assert max(load) <= p["per"] + 2 * (MIN - 1), (max(load), p["per"])
+    assert sum(load) == tiles
 
 
 def test_edge_lengths():
