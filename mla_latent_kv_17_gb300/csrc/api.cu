@@ -147,6 +147,7 @@ mla_status check_common(const void *ws, size_t ws_bytes, const void *q_nope, con
         return MLA_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || max_pages < 1 || num_pages < 1) return MLA_ERR_INVALID_ARG;
     if (H > kMaxHeads) return MLA_ERR_UNSUPPORTED;
+    if (num_pages > (int64_t)(INT32_MAX / kPageRows)) return MLA_ERR_UNSUPPORTED;
     if (!isfinite(scale)) return MLA_ERR_INVALID_ARG;
     if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(cache) || !aligned16(out))
         return MLA_ERR_INVALID_ARG;
@@ -154,11 +155,24 @@ mla_status check_common(const void *ws, size_t ws_bytes, const void *q_nope, con
     return MLA_OK;
 }
 
+// Work units for `num_sms` SMs: one per SM pair, capped by the clusters that fit at once.
+int units_for(int num_sms) {
+    int u = num_units_for(num_sms);
+    const int mc = sm103_max_units();
+    if (mc > 0 && u > mc) u = mc;
+    return u;
+}
+
 mla_status run_decode(const DecodeArgs &a, cudaStream_t stream) {
     int sms = device_sm_count();
     if (sms <= 0) return MLA_ERR_CUDA;
-    int units = num_units_for(sms);
-    if (launch_decode_simt(a, units, stream) != cudaSuccess) return MLA_ERR_CUDA;
+    const int units = units_for(sms);
+    cudaError_t e;
+    if (!a.kv_fp8 && !a.indices)
+        e = launch_decode_sm103(a, units, stream);
+    else
+        e = launch_decode_simt(a, units, stream);
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
     dim3 cgrid(a.B, a.H);
     combine_kernel<<<cgrid, kCombineThreads, 0, stream>>>(a);
     if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
@@ -176,7 +190,7 @@ size_t mla_decode_workspace_size(int B, int H, int num_sms) {
     if (B < 1 || H < 1 || H > kMaxHeads || num_sms < 0) return 0;
     if (num_sms == 0) num_sms = device_sm_count();
     if (num_sms <= 0) return 0;
-    return ws_layout(B, H, num_units_for(num_sms)).total;
+    return ws_layout(B, H, units_for(num_sms)).total;
 }
 
 mla_status mla_decode_plan(const int32_t *seq_lens, int B, int H, int topk, int num_sms,
@@ -186,7 +200,7 @@ mla_status mla_decode_plan(const int32_t *seq_lens, int B, int H, int topk, int 
     if (topk == 0 && !seq_lens) return MLA_ERR_INVALID_ARG;
     if (num_sms == 0) num_sms = device_sm_count();
     if (num_sms <= 0) return MLA_ERR_CUDA;
-    const int units = num_units_for(num_sms);
+    const int units = units_for(num_sms);
     if (ws_bytes < ws_layout(B, H, units).total) return MLA_ERR_WORKSPACE;
     plan_kernel<<<1, kPlanThreads, 0, (cudaStream_t)stream>>>(seq_lens, B, H, topk, units,
                                                               (unsigned char *)workspace);
