@@ -105,6 +105,26 @@ mla_status mla_decode_status(void *workspace, size_t ws_bytes, void *stream);
 /* Static description of a status code. */
 const char *mla_status_string(mla_status status);
 
+/* Dense decode (plan + decode + split merge) that allocates nothing and takes no
+ * workspace.  It is for callers that cannot allocate device memory at decode time: all
+ * memory handed to an arena up front, a real-time loop that must not call cudaMalloc
+ * (it may synchronise the device), or a plugin whose host application owns every
+ * allocation.  The pages have no counterpart; this is a usage variant of mla_decode.
+ * The workspace is a fixed 48 MiB array in the library's device image, held on every
+ * GPU that uses this call until the process exits.  B x H beyond what the array holds
+ * (mla_decode_workspace_size(B, H, 0) > 48 MiB, e.g. more than about 110 requests of 128
+ * heads on a 152-SM GB300) returns MLA_ERR_WORKSPACE and enqueues nothing.
+ * All calls on one device share the array: calls whose work overlaps on the GPU (two
+ * streams) race; calls on one stream are safe.  The first call on a device does a
+ * one-time set-up (it looks up the array's device address); make it before any stream
+ * capture.  Arguments are those of mla_decode; device_status (optional, device int32)
+ * receives this call's status word (MLA_OK or a device-side error code) in stream order. */
+mla_status mla_decode_static(const void *q_nope, const void *q_rope, const void *cache,
+                             mla_kv_dtype kv_dtype, int64_t num_pages,
+                             const int32_t *block_table, int max_pages,
+                             const int32_t *seq_lens, int B, int H, float softmax_scale,
+                             float *out, float *lse, int32_t *device_status, void *stream);
+
 /* Host twin of mla_decode_plan for tests and tooling: plans from a HOST array
  * seq_lens[B] (NULL with topk > 0) into a HOST buffer of mla_decode_workspace_size()
  * bytes, producing exactly the bytes the device planner writes into the plan region.

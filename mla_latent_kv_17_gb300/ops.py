@@ -53,6 +53,8 @@ def lib():
             L.mla_decode.restype = I
             L.mla_decode_sparse.argtypes = [P, SZ, P, P, P, I64, P, I, P, P, I, I, I, F, P, P, P]
             L.mla_decode_sparse.restype = I
+            L.mla_decode_static.argtypes = [P, P, P, I, I64, P, I, P, I, I, F, P, P, P, P]
+            L.mla_decode_static.restype = I
             L.mla_decode_status.argtypes = [P, SZ, P]
             L.mla_decode_status.restype = I
             L.mla_status_string.argtypes = [I]
@@ -172,6 +174,33 @@ def decode_sparse(ws: Workspace, q_nope, q_rope, cache, block_table, seq_lens, i
                                  _ptr(seq_lens), _ptr(indices), indices.shape[1], B, H,
                                  float(softmax_scale), _ptr(out), _ptr(lse), _stream(stream))
     _check("mla_decode_sparse", st)
+    return out, lse
+
+
+def decode_static(q_nope, q_rope, cache, block_table, seq_lens, softmax_scale: float,
+                  out=None, lse=None, device_status=None, stream=None):
+    """Dense plan + decode + merge with the library's fixed device scratch: no workspace
+    argument and no allocation inside the call.  device_status: optional int32 CUDA
+    tensor [1] that receives the call's device-side status word."""
+    B, H = _queries(q_nope, q_rope)
+    _i32(block_table, "block_table")
+    _i32(seq_lens, "seq_lens")
+    if cache.dtype == torch.bfloat16 and cache.shape[1:] == (64, 576):
+        kv = KV_BF16
+    elif cache.dtype == torch.uint8 and cache.shape[1:] == (64, 656):
+        kv = KV_FP8
+    else:
+        raise ValueError("cache must be bf16 [P,64,576] or uint8 [P,64,656]")
+    if not cache.is_contiguous():
+        raise ValueError("cache must be contiguous")
+    out, lse = _outputs(B, H, q_nope.device, out, lse)
+    if device_status is not None:
+        _i32(device_status, "device_status")
+    st = lib().mla_decode_static(_ptr(q_nope), _ptr(q_rope), _ptr(cache), kv, cache.shape[0],
+                                 _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, H,
+                                 float(softmax_scale), _ptr(out), _ptr(lse), _ptr(device_status),
+                                 _stream(stream))
+    _check("mla_decode_static", st)
     return out, lse
 
 
