@@ -52,7 +52,7 @@ extern "C" {
 
 typedef enum {
     MLA_OK = 0,
-    MLA_ERR_INVALID_ARG = 1, /* null pointer, bad size or alignment, non-finite scale   */
+    MLA_ERR_INVALID_ARG = 1, /* null pointer, bad size or alignment, scale not in (0,inf) */
     MLA_ERR_UNSUPPORTED = 2, /* H > 128, no sm_103a device, ...                          */
     MLA_ERR_WORKSPACE = 3,   /* workspace too small, or it does not hold a matching plan */
     MLA_ERR_CUDA = 4,        /* a CUDA runtime call failed                               */
@@ -80,7 +80,7 @@ mla_status mla_decode_plan(const int32_t *seq_lens, int B, int H, int topk, int 
 
 /* Dense decode over the paged cache with the plan in `workspace` (built by
  * mla_decode_plan with topk = 0 for the same B, H and seq_lens).  Writes out and lse.
- * kv_dtype selects the cache layout above.  softmax_scale must be finite. */
+ * kv_dtype selects the cache layout above.  softmax_scale must be finite and > 0. */
 mla_status mla_decode(const void *workspace, size_t ws_bytes, const void *q_nope,
                       const void *q_rope, const void *cache, mla_kv_dtype kv_dtype,
                       int64_t num_pages, const int32_t *block_table, int max_pages,

@@ -148,7 +148,7 @@ mla_status check_common(const void *ws, size_t ws_bytes, const void *q_nope, con
     if (B < 1 || H < 1 || max_pages < 1 || num_pages < 1) return MLA_ERR_INVALID_ARG;
     if (H > kMaxHeads) return MLA_ERR_UNSUPPORTED;
     if (num_pages > (int64_t)(INT32_MAX / kPageRows)) return MLA_ERR_UNSUPPORTED;
-    if (!isfinite(scale)) return MLA_ERR_INVALID_ARG;
+    if (!isfinite(scale) || !(scale > 0.f)) return MLA_ERR_INVALID_ARG;
     if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(cache) || !aligned16(out))
         return MLA_ERR_INVALID_ARG;
     if (ws_bytes < ws_layout(B, H, 1).plan_end) return MLA_ERR_WORKSPACE;

@@ -1,24 +1,30 @@
 // Tensor-core decode kernel for sm_103a (bf16 paged cache).
 //
 // One work unit = a cluster of two CTAs on two SMs.  Both CTAs walk the same work items
-// (request b, token range) tile by tile, one 64-token page per tile; CTA r owns output
-// latent columns [256 r, 256 r + 256).
-//
-//   cache tile (TMA, 128-B swizzle)   CTA 0: latent 0..255          (4 boxes of 64 columns)
-//                                     CTA 1: latent 256..511 + RoPE (5 boxes)
-//   QK^T  S_r[h, t] = Q_r[h, :] . C_r[t, :]   tcgen05.mma M=128 (heads), N=64 (tokens),
-//         A = the CTA's query slice held in TMEM, B = the cache tile (K-major)
-//   S exchange: each CTA sends its fp32 partial scores to the peer through distributed
-//         shared memory; both then hold S = S_0 + S_1 (the full 576-wide score), bitwise
-//         identical, so both take identical softmax decisions.
-//   softmax: one thread per head; online maximum with lazy rescaling (O is rescaled only
-//         when the running maximum grows by more than 2^8), p = 2^(s*scale*log2e - m)
-//         rounded to bf16 into TMEM.
-//   PV    O_r[h, :] += P[h, :] . C_r[:, latent half]   M=128, N=256, K=64 tokens,
-//         A = P in TMEM, B = the same cache tile (MN-major); O_r (128 x 256 fp32) in TMEM.
+// (request b, token range) tile by tile, one 64-token page per tile.  CTA r owns
+//   * the scores of the page's tokens [32 r, 32 r + 32) — full 576-wide dot products, so no
+//     partial score ever crosses between the SMs, and
+//   * the output latent columns [256 r, 256 r + 256) of every head (its O half, 128 x 256
+//     fp32 in TMEM; the full 128 x 512 accumulator does not fit one SM's TMEM).
+// Per tile:
+//   TMA (128-B swizzle)  own-half latent of all 64 tokens (PV operand, kept until PV) and
+//                        the other 320 columns (other latent half + RoPE) of its own 32
+//                        tokens (QK operand only, released after QK).
+//   QK^T  S[h, i] = q[h, :] . entry[own token i, :]   tcgen05.mma M=128 heads, N=32,
+//         K=576: 448 K from the query slice held in TMEM, 128 K from shared memory.
+//   softmax (one thread per head): x = s * scale * log2(e); reference r = the running
+//         maximum m, or the tile's own maximum if that exceeds m by more than 8; own
+//         weights p = 2^(x - r) in bf16 go to a shared-memory tile, followed by r and the
+//         fp32 sum of p.  One bulk copy (9 KB) puts them into the peer's copy of the tile.
+//   merge: with both CTAs' (r, sum) both compute the same new maximum m', rescale a half
+//         whose reference was below m' (2^(r - m')), the sum l and — when m' > m — O, so
+//         both hold bitwise identical weights for all 64 tokens.
+//   PV    O_r[h, :] += P[h, 0:64] . C[0:64, own latent half]   M=128, N=256, K=64,
+//         A = the probability tile (64-B swizzle), B = the own-half cache tile (MN-major).
 //   epilogue: out = O / l, lse = (m + log2 l) ln 2, or a partial result for the merge.
 //
-// TMEM columns: O [0,256)  S [256,320)  P [320,352)  Q [352,512).
+// TMEM columns: O [0,256)  S [256,288)  query [288,512) (own latent half, RoPE, first 128
+// columns of the other half; the last 128 columns of the other half sit in shared memory).
 // Warp roles: warps 0-3 softmax/epilogue (thread = head, warp w reads TMEM lanes
 // 32w..32w+31), warp 4 TMA producer, warp 5 MMA issuer (and TMEM owner).
 // Every wait is bounded: on timeout the kernel records MLA_ERR_TIMEOUT, stops issuing,
@@ -35,35 +41,51 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kStages = 3;
-constexpr uint32_t kBoxBytes = 64 * 128;            // 64 rows x 64 bf16 (128 B), SW128
-constexpr uint32_t kStageBytes = 5 * kBoxBytes;      // 4 latent boxes + the RoPE box
-constexpr uint32_t kXBytes = 128 * 64 * 4;           // one exchange buffer: 128 heads x 64 fp32
+constexpr int kDhStages = 3;   // own-half latent tiles (live until PV)
+constexpr int kOthStages = 2;  // other-columns tiles (live until QK)
+constexpr int kPSlots = 3;     // probability tiles (live until both CTAs' PV)
+constexpr uint32_t kHalfBox = 32 * 128;          // 32 rows x 64 bf16, 128-B swizzle
+constexpr uint32_t kDhBlock = 2 * kHalfBox;      // 64 token rows x 64 columns
+constexpr uint32_t kDhBytes = 4 * kDhBlock;      // 256 columns
+constexpr uint32_t kOthBytes = 5 * kHalfBox;     // 4 x 64 latent columns + RoPE, 32 rows
+constexpr uint32_t kQsBox = 128 * 128;           // 128 heads x 64 bf16
+constexpr uint32_t kQsBytes = 2 * kQsBox;
+constexpr uint32_t kPHalf = 128 * 64;            // 128 heads x 32 tokens bf16, 64-B swizzle
+constexpr uint32_t kRlBytes = 1024;              // r[128] and sum[128], fp32
+constexpr uint32_t kPSlotBytes = 2 * kPHalf + 2 * kRlBytes;
+constexpr uint32_t kMsgBytes = kPHalf + kRlBytes;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 352;
+constexpr uint32_t kColO = 0, kColS = 256, kColQ = 288;
+constexpr uint32_t kColQRope = kColQ + 128, kColQOther = kColQ + 160;
 constexpr float kRescaleLog2 = 8.0f;
-constexpr long long kSpinCycles = 4000000000LL;      // about two seconds
+constexpr long long kSpinCycles = 4000000000LL;  // about two seconds
 
-constexpr uint32_t kOffStages = 0;
-constexpr uint32_t kOffX = kStages * kStageBytes;
-constexpr uint32_t kOffBar = kOffX + 2 * kXBytes;
+constexpr uint32_t kOffDh = 0;
+constexpr uint32_t kOffOth = kOffDh + kDhStages * kDhBytes;
+constexpr uint32_t kOffQs = kOffOth + kOthStages * kOthBytes;
+constexpr uint32_t kOffP = kOffQs + kQsBytes;
+constexpr uint32_t kOffBar = kOffP + kPSlots * kPSlotBytes;
 constexpr uint32_t kOffMisc = kOffBar + 8 * 32;
 constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + slack for 1024-B alignment
+static_assert(kSmemBytes <= 232448, "shared memory");
 
 enum {
-    B_KV_FULL = 0,
-    B_KV_EMPTY = kStages,
-    B_S_FULL = 2 * kStages,
+    B_DH_FULL = 0,
+    B_DH_EMPTY = B_DH_FULL + kDhStages,
+    B_OTH_FULL = B_DH_EMPTY + kDhStages,
+    B_OTH_EMPTY = B_OTH_FULL + kOthStages,
+    B_S_FULL = B_OTH_EMPTY + kOthStages,
     B_S_FREE,
-    B_P_FULL,
-    B_O_DONE,
+    B_O_DONE,                     // every PV (waited only before an O rescale)
+    B_O_FINAL,                    // the last PV of a work item (waited by the epilogue)
     B_Q_READY,
-    B_X_FULL0,
-    B_X_FULL1,
-    B_X_EMPTY0,
-    B_X_EMPTY1,
-    B_COUNT
+    B_XO_READY,                   // all four softmax warps wrote this tile's message
+    B_OWNREAD,                    // this CTA's last message has been read by its bulk copy
+    B_RFULL,                      // peer's message for probability slot s has landed
+    B_PFREE = B_RFULL + kPSlots,  // both CTAs' PV have finished reading slot s
+    B_P_FULL = B_PFREE + kPSlots, // slot s holds the merged weights of its tile
+    B_COUNT = B_P_FULL + kPSlots
 };
 static_assert(B_COUNT <= 32, "barrier area");
 
@@ -100,6 +122,23 @@ __device__ __forceinline__ bool warp_wait(const Ctx &c, uint32_t b, uint32_t par
     return __all_sync(0xffffffffu, ok);
 }
 
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ void scale_row16(uint4 *prow, float f) {
+    for (int q = 0; q < 4; ++q) {
+        uint4 v = prow[q];
+        v.x = pack_bf16(bf16lo(v.x) * f, bf16hi(v.x) * f);
+        v.y = pack_bf16(bf16lo(v.y) * f, bf16hi(v.y) * f);
+        v.z = pack_bf16(bf16lo(v.z) * f, bf16hi(v.z) * f);
+        v.w = pack_bf16(bf16lo(v.w) * f, bf16hi(v.w) * f);
+        prow[q] = v;
+    }
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -113,22 +152,30 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
     volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(gbase + kOffMisc);
-    // misc[0]: TMEM base address, misc[1]: abort flag, misc[2 + s]: stage s holds no data
+    // misc[0]: TMEM base address, misc[1]: abort flag, misc[2 + s]: own-half tile s holds
+    // no data (its page id was out of range)
     Ctx c{base, a.status, misc + 1};
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar(base, B_KV_FULL + s), 1);
-            mbar_init(bar(base, B_KV_EMPTY + s), 1);
+        for (int s = 0; s < kDhStages; ++s) {
+            mbar_init(bar(base, B_DH_FULL + s), 1);
+            mbar_init(bar(base, B_DH_EMPTY + s), 1);
+        }
+        for (int s = 0; s < kOthStages; ++s) {
+            mbar_init(bar(base, B_OTH_FULL + s), 1);
+            mbar_init(bar(base, B_OTH_EMPTY + s), 1);
         }
         mbar_init(bar(base, B_S_FULL), 1);
         mbar_init(bar(base, B_S_FREE), 4);
-        mbar_init(bar(base, B_P_FULL), 4);
         mbar_init(bar(base, B_O_DONE), 1);
+        mbar_init(bar(base, B_O_FINAL), 1);
         mbar_init(bar(base, B_Q_READY), 4);
-        for (int k = 0; k < 2; ++k) {
-            mbar_init(bar(base, B_X_FULL0 + k), 4);
-            mbar_init(bar(base, B_X_EMPTY0 + k), 4);
+        mbar_init(bar(base, B_XO_READY), 4);
+        mbar_init(bar(base, B_OWNREAD), 1);
+        for (int s = 0; s < kPSlots; ++s) {
+            mbar_init(bar(base, B_RFULL + s), 1);  // + the message bytes
+            mbar_init(bar(base, B_PFREE + s), 2);  // one commit from each CTA's PV
+            mbar_init(bar(base, B_P_FULL + s), 4);
         }
         misc[1] = 0u;
         fence_mbar_init();
@@ -155,35 +202,44 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
     if (warp == 4) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            const int nbox = 4 + (int)rank;
-            const int x0 = rank == 0 ? 0 : 256;
-            uint32_t kv_it = 0;
+            const int xown = 256 * (int)rank, xoth = 256 * (int)peer;
+            uint32_t g = 0;
             bool ok = true;
             for (int u = cl; u < units && ok; u += ncl) {
                 for (int it = unit_begin[u]; it < unit_begin[u + 1] && ok; ++it) {
                     const WorkItem w = items[it];
-                    for (int t = w.t0; t < w.t1; t += kTileTokens, ++kv_it) {
-                        const int st = (int)(kv_it % kStages);
-                        const uint32_t ph = (kv_it / kStages) & 1u;
-                        if (!wait_bar(c, bar(base, B_KV_EMPTY + st), ph ^ 1u, false)) {
+                    for (int t = w.t0; t < w.t1; t += kTileTokens, ++g) {
+                        const int ds = (int)(g % kDhStages), os = (int)(g % kOthStages);
+                        const uint32_t dph = (g / kDhStages) & 1u, oph = (g / kOthStages) & 1u;
+                        if (!wait_bar(c, bar(base, B_DH_EMPTY + ds), dph ^ 1u, false) ||
+                            !wait_bar(c, bar(base, B_OTH_EMPTY + os), oph ^ 1u, false)) {
                             ok = false;
                             break;
                         }
                         const int lp = t / kPageRows;
                         const int64_t page =
                             lp < a.max_pages ? (int64_t)a.block_table[(int64_t)w.b * a.max_pages + lp] : -1;
-                        const uint32_t dst = base + kOffStages + st * kStageBytes;
-                        const uint32_t fb = bar(base, B_KV_FULL + st);
+                        const uint32_t dfb = bar(base, B_DH_FULL + ds), ofb = bar(base, B_OTH_FULL + os);
                         if (page >= 0 && page < a.num_pages) {
-                            misc[2 + st] = 0u;
-                            mbar_arrive_expect_tx(fb, nbox * kBoxBytes);
-                            for (int i = 0; i < nbox; ++i)
-                                tma_load_2d(dst + i * kBoxBytes, &tmap, x0 + 64 * i,
-                                            (int32_t)(page * kPageRows), fb);
+                            misc[2 + ds] = 0u;
+                            const int32_t y = (int32_t)(page * kPageRows);
+                            const uint32_t dst_dh = base + kOffDh + ds * kDhBytes;
+                            const uint32_t dst_ot = base + kOffOth + os * kOthBytes;
+                            mbar_arrive_expect_tx(dfb, kDhBytes);
+                            for (int i = 0; i < 4; ++i)
+                                for (int hf = 0; hf < 2; ++hf)
+                                    tma_load_2d(dst_dh + i * kDhBlock + hf * kHalfBox, &tmap, xown + 64 * i,
+                                                y + 32 * hf, dfb);
+                            mbar_arrive_expect_tx(ofb, kOthBytes);
+                            const int yo = y + 32 * (int)rank;
+                            for (int i = 0; i < 4; ++i)
+                                tma_load_2d(dst_ot + i * kHalfBox, &tmap, xoth + 64 * i, yo, ofb);
+                            tma_load_2d(dst_ot + 4 * kHalfBox, &tmap, kDLatent, yo, ofb);
                         } else {
                             record_error(a.status, MLA_ERR_INDEX);
-                            misc[2 + st] = 1u;
-                            mbar_arrive(fb);
+                            misc[2 + ds] = 1u;
+                            mbar_arrive(dfb);
+                            mbar_arrive(ofb);
                         }
                     }
                 }
@@ -198,22 +254,28 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
     } else if (warp == 5) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const int nk = 16 + 4 * (int)rank;  // QK^T K-steps of 16
-            constexpr uint32_t idesc_qk = idesc_bf16(128, 64, false);
+            constexpr uint32_t idesc_qk = idesc_bf16(128, 32, false);
             constexpr uint32_t idesc_pv = idesc_bf16(128, 256, true);
-            uint32_t kv_it = 0, g = 0, nitem = 0;
+            uint32_t g = 0, nitem = 0;
             bool ok = true;
-            auto issue_pv = [&](int stage, uint32_t gp, bool first) -> bool {
-                if (!wait_bar(c, bar(base, B_P_FULL), gp & 1u, false)) return false;
+            // Per-slot barriers: a slot is only reused after both CTAs' PV of its previous
+            // tile, so no barrier here can run two phases ahead of its waiter.
+            auto issue_pv = [&](uint32_t gp, bool first, bool last) -> bool {
+                if (!wait_bar(c, bar(base, B_P_FULL + (int)(gp % kPSlots)), (gp / kPSlots) & 1u, false))
+                    return false;
                 tc_fence_after();
-                const uint32_t sb = base + kOffStages + stage * kStageBytes;
+                const int ds = (int)(gp % kDhStages);
+                const uint32_t dh = base + kOffDh + ds * kDhBytes;
+                const uint32_t ps = base + kOffP + (gp % kPSlots) * kPSlotBytes;
                 for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t bd = smem_desc_sw128(sb + kk * 2048u, kBoxBytes, 1024u);
-                    mma_ts(tmem + kColO, tmem + kColP + 8u * kk, bd, idesc_pv,
-                           (first && kk == 0) ? 0u : 1u);
+                    const uint64_t ad = smem_desc_sw64(ps + (kk >> 1) * kPHalf + (kk & 1) * 32u, 512u);
+                    const uint64_t bd = smem_desc_sw128(dh + kk * 2048u, kDhBlock, 1024u);
+                    mma_ss(tmem + kColO, ad, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
                 }
                 mma_commit(bar(base, B_O_DONE));
-                mma_commit(bar(base, B_KV_EMPTY + stage));
+                mma_commit(bar(base, B_DH_EMPTY + ds));
+                mma_commit_multicast(bar(base, B_PFREE + (int)(gp % kPSlots)), (uint16_t)3);
+                if (last) mma_commit(bar(base, B_O_FINAL));
                 return true;
             };
             for (int u = cl; u < units && ok; u += ncl) {
@@ -227,30 +289,47 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
                     }
                     ++nitem;
                     tc_fence_after();
-                    int prev = 0;
-                    for (int j = 0; j < ntiles; ++j, ++kv_it, ++g) {
-                        const int st = (int)(kv_it % kStages);
-                        const uint32_t ph = (kv_it / kStages) & 1u;
-                        if (!wait_bar(c, bar(base, B_KV_FULL + st), ph, false) ||
+                    for (int j = 0; j < ntiles; ++j, ++g) {
+                        const int ds = (int)(g % kDhStages), os = (int)(g % kOthStages);
+                        const uint32_t dph = (g / kDhStages) & 1u, oph = (g / kOthStages) & 1u;
+                        if (!wait_bar(c, bar(base, B_DH_FULL + ds), dph, false) ||
+                            !wait_bar(c, bar(base, B_OTH_FULL + os), oph, false) ||
                             (g > 0 && !wait_bar(c, bar(base, B_S_FREE), (g - 1) & 1u, false))) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t sb = base + kOffStages + st * kStageBytes;
-                        for (int k = 0; k < nk; ++k) {
-                            const uint64_t bd = smem_desc_sw128(sb + (k >> 2) * kBoxBytes + (k & 3) * 32u,
-                                                                16u, 1024u);
-                            mma_ts(tmem + kColS, tmem + kColQ + 8u * k, bd, idesc_qk, k > 0 ? 1u : 0u);
-                        }
+                        const uint32_t dh = base + kOffDh + ds * kDhBytes + rank * kHalfBox;
+                        const uint32_t ot = base + kOffOth + os * kOthBytes;
+                        const uint32_t qs = base + kOffQs;
+                        // own latent half: query columns from TMEM, own token rows of the PV tile
+                        for (int k = 0; k < 16; ++k)
+                            mma_ts(tmem + kColS, tmem + kColQ + 8u * k,
+                                   smem_desc_sw128(dh + (k >> 2) * kDhBlock + (k & 3) * 32u, 16u, 1024u),
+                                   idesc_qk, k > 0 ? 1u : 0u);
+                        // RoPE
+                        for (int k = 0; k < 4; ++k)
+                            mma_ts(tmem + kColS, tmem + kColQRope + 8u * k,
+                                   smem_desc_sw128(ot + 4 * kHalfBox + k * 32u, 16u, 1024u), idesc_qk, 1u);
+                        // other latent half, first 128 columns: query from TMEM
+                        for (int k = 0; k < 8; ++k)
+                            mma_ts(tmem + kColS, tmem + kColQOther + 8u * k,
+                                   smem_desc_sw128(ot + (k >> 2) * kHalfBox + (k & 3) * 32u, 16u, 1024u),
+                                   idesc_qk, 1u);
+                        // other latent half, last 128 columns: query from shared memory
+                        for (int k = 0; k < 8; ++k)
+                            mma_ss(tmem + kColS,
+                                   smem_desc_sw128(qs + (k >> 2) * kQsBox + (k & 3) * 32u, 16u, 1024u),
+                                   smem_desc_sw128(ot + (2 + (k >> 2)) * kHalfBox + (k & 3) * 32u, 16u, 1024u),
+                                   idesc_qk, 1u);
                         mma_commit(bar(base, B_S_FULL));
-                        if (j > 0 && !issue_pv(prev, g - 1, j == 1)) {
+                        mma_commit(bar(base, B_OTH_EMPTY + os));
+                        if (j > 0 && !issue_pv(g - 1, j == 1, false)) {
                             ok = false;
                             break;
                         }
-                        prev = st;
                     }
-                    if (ok && !issue_pv(prev, g - 1, ntiles == 1)) ok = false;
+                    if (ok && !issue_pv(g - 1, ntiles == 1, true)) ok = false;
                 }
             }
             if (!ok) {
@@ -264,9 +343,9 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
         // ------------------------------------------------------------ softmax + epilogue
         const int h = threadIdx.x;  // head row = TMEM lane
         const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-        const uint32_t xbase = base + kOffX;
-        const uint32_t peer_x = mapa(xbase, peer);
-        uint32_t kv_it = 0, g = 0, nitem = 0;
+        const uint32_t peer_p = mapa(base + kOffP, peer);
+        const float sc = a.scale_log2;  // > 0, checked on the host
+        uint32_t g = 0, nitem = 0;
         bool ok = true;
         for (int u = cl; u < units && ok; u += ncl) {
             for (int it = unit_begin[u]; it < unit_begin[u + 1] && ok; ++it) {
@@ -290,17 +369,18 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
                     }
                     continue;
                 }
-                // query slice -> TMEM (K-major bf16 pairs, one head per lane)
+                // ---- query of this request: 448 columns into TMEM, 128 into shared memory
                 {
-                    const uint16_t *qn = a.q_nope + ((int64_t)b * a.H + h) * kDLatent + rank * 256;
+                    const uint16_t *qn = a.q_nope + ((int64_t)b * a.H + h) * kDLatent;
                     const uint16_t *qr = a.q_rope + ((int64_t)b * a.H + h) * kDRope;
-                    const int nch = 4 + (int)rank;
-                    for (int cb = 0; cb < nch; ++cb) {
+                    for (int cb = 0; cb < 7; ++cb) {
+                        const uint16_t *src = cb < 4   ? qn + 256 * rank + 64 * cb
+                                              : cb == 4 ? qr
+                                                        : qn + 256 * peer + 64 * (cb - 5);
                         uint32_t v[32];
-                        const uint4 *src = reinterpret_cast<const uint4 *>(cb < 4 ? qn + cb * 64 : qr);
                         for (int q = 0; q < 8; ++q) {
                             uint4 x = make_uint4(0u, 0u, 0u, 0u);
-                            if (h < a.H) x = src[q];
+                            if (h < a.H) x = reinterpret_cast<const uint4 *>(src)[q];
                             v[4 * q] = x.x;
                             v[4 * q + 1] = x.y;
                             v[4 * q + 2] = x.z;
@@ -308,139 +388,184 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
                         }
                         tmem_st32(trow + kColQ + 32u * cb, v);
                     }
+                    for (int bx = 0; bx < 2; ++bx) {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(qn + 256 * peer + 128 + 64 * bx);
+                        uint8_t *row = gbase + kOffQs + bx * kQsBox + h * 128;
+                        for (int q = 0; q < 8; ++q) {
+                            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+                            if (h < a.H) x = src[q];
+                            *reinterpret_cast<uint4 *>(row + ((q ^ (h & 7)) * 16)) = x;
+                        }
+                    }
+                    fence_proxy_async_smem();
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(base, B_Q_READY));
-                    ++nitem;
                 }
                 float m = -INFINITY, l = 0.f;
-                for (int j = 0; j < ntiles; ++j, ++kv_it, ++g) {
+                for (int j = 0; j < ntiles; ++j, ++g) {
                     const int t = w.t0 + kTileTokens * j;
-                    const int st = (int)(kv_it % kStages);
-                    const uint32_t ph = (kv_it / kStages) & 1u;
-                    if (!warp_wait(c, bar(base, B_S_FULL), g & 1u, false)) {
+                    const int ds = (int)(g % kDhStages);
+                    const uint32_t dph = (g / kDhStages) & 1u;
+                    const int slot = (int)(g % kPSlots);
+                    const uint32_t su = g / kPSlots;
+                    // ---- scores of the own 32 tokens
+                    if (!warp_wait(c, bar(base, B_S_FULL), g & 1u, false) ||
+                        !warp_wait(c, bar(base, B_DH_FULL + ds), dph, false)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    uint32_t sr[64];
+                    float s[32];
                     {
-                        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[0]);
-                        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[32]);
-                        tmem_ld32(trow + kColS, lo);
-                        tmem_ld32(trow + kColS + 32u, hi);
+                        uint32_t sr[32];
+                        tmem_ld32(trow + kColS, sr);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(sr[i]);
                     }
-                    tmem_wait_ld();
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(base, B_S_FREE));
-
-                    // ---- exchange partial scores with the peer CTA
-                    const uint32_t xb = g & 1u, xu = g >> 1;
-                    if (g >= 2 && !warp_wait(c, bar(base, B_X_EMPTY0 + xb), (xu - 1u) & 1u, true)) {
+                    const bool bad = misc[2 + ds] != 0u;
+                    const int nvalid = bad ? 0 : min(kTileTokens, w.t1 - t);  // page rows attended
+                    const int nown = max(0, min(32, nvalid - 32 * (int)rank));
+                    if (nown < 32) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (i >= nown) s[i] = -INFINITY;
+                    }
+                    float mraw = s[0];
+#pragma unroll
+                    for (int i = 1; i < 32; ++i) mraw = fmaxf(mraw, s[i]);
+                    const float mloc = mraw * sc;
+                    const float rown = mloc > m + kRescaleLog2 ? mloc : m;  // m = -inf: own max
+                    const float nr = rown == -INFINITY ? 0.f : -rown;
+                    uint32_t pk[16];
+                    float lown = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = ex2_approx(fmaf(s[2 * i], sc, nr));
+                        const float p1 = ex2_approx(fmaf(s[2 * i + 1], sc, nr));
+                        lown += p0 + p1;
+                        pk[i] = pack_bf16(p0, p1);
+                    }
+                    // ---- message: own weights into this CTA's copy of the probability tile,
+                    // then (r, sum); one bulk copy sends both to the peer's copy
+                    if (g >= (uint32_t)kPSlots &&
+                        !warp_wait(c, bar(base, B_PFREE + slot), (su - 1u) & 1u, true)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t rdst = peer_x + xb * kXBytes + (uint32_t)h * 256u;
-                    for (int q = 0; q < 16; ++q) {
-                        const uint32_t pos = (uint32_t)(q ^ (h & 7));
-                        st_cluster_v4(rdst + pos * 16u, sr[4 * q], sr[4 * q + 1], sr[4 * q + 2],
-                                      sr[4 * q + 3]);
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(mapa(bar(base, B_X_FULL0 + xb), peer));
-                    if (!warp_wait(c, bar(base, B_X_FULL0 + xb), xu & 1u, true)) {
-                        ok = false;
-                        break;
-                    }
-                    float s[64];
+                    uint8_t *ps = gbase + kOffP + slot * kPSlotBytes;
                     {
-                        const float4 *xs = reinterpret_cast<const float4 *>(gbase + kOffX + xb * kXBytes +
-                                                                            (uint32_t)h * 256u);
-                        for (int q = 0; q < 16; ++q) {
-                            const float4 v = xs[q ^ (h & 7)];
-                            s[4 * q] = __uint_as_float(sr[4 * q]) + v.x;
-                            s[4 * q + 1] = __uint_as_float(sr[4 * q + 1]) + v.y;
-                            s[4 * q + 2] = __uint_as_float(sr[4 * q + 2]) + v.z;
-                            s[4 * q + 3] = __uint_as_float(sr[4 * q + 3]) + v.w;
+                        uint8_t *prow = ps + rank * kPHalf + h * 64;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            *reinterpret_cast<uint4 *>(prow + ((q ^ ((h >> 1) & 3)) * 16)) =
+                                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                        float *rl = reinterpret_cast<float *>(ps + 2 * kPHalf + rank * kRlBytes);
+                        rl[h] = rown;
+                        rl[128 + h] = lown;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(base, B_XO_READY));
+                    const uint32_t rfull = bar(base, B_RFULL + slot);
+                    if (threadIdx.x == 0) {
+                        mbar_arrive_expect_tx(rfull, kMsgBytes);
+                        if (!wait_bar(c, bar(base, B_XO_READY), g & 1u, false)) {
+                            ok = false;
+                        } else {
+                            const uint32_t off = kOffP + slot * kPSlotBytes;
+                            const uint32_t rb = mapa(rfull, peer);
+                            bulk_copy_s2peer(peer_p + slot * kPSlotBytes + rank * kPHalf,
+                                             base + off + rank * kPHalf, kPHalf, rb);
+                            bulk_copy_s2peer(peer_p + slot * kPSlotBytes + 2 * kPHalf + rank * kRlBytes,
+                                             base + off + 2 * kPHalf + rank * kRlBytes, kRlBytes, rb);
+                            bulk_commit();
                         }
                     }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(mapa(bar(base, B_X_EMPTY0 + xb), peer));
-
-                    // ---- online softmax (identical decisions in both CTAs)
-                    if (!warp_wait(c, bar(base, B_KV_FULL + st), ph, false)) {
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    // ---- merge with the peer's half (identical arithmetic in both CTAs)
+                    if (!warp_wait(c, rfull, su & 1u, true)) {
                         ok = false;
                         break;
                     }
-                    const bool bad = misc[2 + st] != 0u;
-                    const int nvalid = bad ? 0 : min(kTileTokens, w.t1 - t);
-                    float mt = -INFINITY;
-#pragma unroll
-                    for (int i = 0; i < 64; ++i) {
-                        s[i] = i < nvalid ? s[i] * a.scale_log2 : -INFINITY;
-                        mt = fmaxf(mt, s[i]);
+                    if (threadIdx.x == 0) {
+                        bulk_wait_read_all();  // own weights may now be rewritten
+                        mbar_arrive(bar(base, B_OWNREAD));
                     }
-                    float alpha = 1.f;
-                    bool resc = false;
-                    if (mt > m + kRescaleLog2) {
-                        alpha = exp2f(m - mt);
-                        l *= alpha;
-                        m = mt;
-                        resc = true;
+                    const float *rlp = reinterpret_cast<const float *>(ps + 2 * kPHalf + peer * kRlBytes);
+                    const float rpeer = rlp[h], lpeer = rlp[128 + h];
+                    const float r0 = rank == 0 ? rown : rpeer, r1 = rank == 0 ? rpeer : rown;
+                    const float l0 = rank == 0 ? lown : lpeer, l1 = rank == 0 ? lpeer : lown;
+                    const float mn = fmaxf(m, fmaxf(r0, r1));
+                    float f0 = 1.f, f1 = 1.f, alpha = 1.f;
+                    if (mn != -INFINITY) {
+                        f0 = ex2_approx(r0 - mn);
+                        f1 = ex2_approx(r1 - mn);
+                        alpha = ex2_approx(m - mn);
+                        l = l * alpha + l0 * f0 + l1 * f1;
                     }
-                    const float mref = m == -INFINITY ? 0.f : m;
-                    uint32_t pk[32];
-                    float psum = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float p0 = exp2f(s[2 * i] - mref), p1 = exp2f(s[2 * i + 1] - mref);
-                        psum += p0 + p1;
-                        __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
-                        pk[i] = *reinterpret_cast<uint32_t *>(&v);
+                    const bool resc_o = j > 0 && mn > m;
+                    m = mn;
+                    // a half whose reference lies below the new maximum is rescaled in place
+                    // (this CTA's own half only after its bulk copy has read it)
+                    const float fown = rank == 0 ? f0 : f1, fpeer = rank == 0 ? f1 : f0;
+                    bool wrote = false;
+                    if (__any_sync(0xffffffffu, fown < 1.f)) {
+                        if (!warp_wait(c, bar(base, B_OWNREAD), g & 1u, false)) {
+                            ok = false;
+                            break;
+                        }
+                        if (fown < 1.f) scale_row16(reinterpret_cast<uint4 *>(ps + rank * kPHalf + h * 64), fown);
+                        wrote = true;
                     }
-                    l += psum;
-
-                    // ---- P buffer and O belong to PV of the previous tile until it completes
-                    if (j > 0) {
+                    if (fpeer < 1.f) {
+                        scale_row16(reinterpret_cast<uint4 *>(ps + peer * kPHalf + h * 64), fpeer);
+                        wrote = true;
+                    }
+                    // cache rows this tile must not contribute (page tail, missing page): the
+                    // PV operand must hold zeros there, not whatever the page holds
+                    if (nvalid < kTileTokens) {
+                        const uint32_t dh = kOffDh + ds * kDhBytes;
+                        const int nz = (kTileTokens - nvalid) * 32;  // 16-B chunks in 4 blocks
+                        for (int i = h; i < nz; i += 128) {
+                            const int row = nvalid + i / 32, ch = i % 32;
+                            *reinterpret_cast<uint4 *>(gbase + dh + (ch / 8) * kDhBlock + row * 128 + (ch % 8) * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        wrote = true;
+                    }
+                    if (__any_sync(0xffffffffu, wrote)) fence_proxy_async_smem();
+                    // ---- O rescale: PV of the previous tile must have finished
+                    if (__any_sync(0xffffffffu, resc_o)) {
                         if (!warp_wait(c, bar(base, B_O_DONE), (g - 1) & 1u, false)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        if (__any_sync(0xffffffffu, resc)) {
-                            const float al = resc ? alpha : 1.f;
-                            for (int cb = 0; cb < 256; cb += 32) {
-                                uint32_t o[32];
-                                tmem_ld32(trow + kColO + cb, o);
-                                tmem_wait_ld();
+                        const float al = resc_o ? alpha : 1.f;
+                        for (int cb = 0; cb < 256; cb += 32) {
+                            uint32_t o[32];
+                            tmem_ld32(trow + kColO + cb, o);
+                            tmem_wait_ld();
 #pragma unroll
-                                for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * al);
-                                tmem_st32(trow + kColO + cb, o);
-                            }
+                            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * al);
+                            tmem_st32(trow + kColO + cb, o);
                         }
+                        tmem_wait_st();
                     }
-                    // ---- cache rows this tile must not contribute (page tail, missing page)
-                    if (nvalid < kTileTokens) {
-                        const uint32_t sb = kOffStages + st * kStageBytes;
-                        const int nz = (kTileTokens - nvalid) * 32;  // 16-B chunks in 4 boxes
-                        for (int i = h; i < nz; i += 128) {
-                            const int row = nvalid + i / 32, ch = i % 32;
-                            *reinterpret_cast<uint4 *>(gbase + sb + (ch / 8) * kBoxBytes + row * 128 + (ch % 8) * 16) =
-                                make_uint4(0u, 0u, 0u, 0u);
-                        }
-                        fence_proxy_async_smem();
-                    }
-                    tmem_st32(trow + kColP, pk);
-                    tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(base, B_P_FULL));
+                    if (lane == 0) mbar_arrive(bar(base, B_P_FULL + slot));
                 }
                 if (!ok) break;
                 // ---- epilogue: wait for the last PV, normalise, store
-                if (!warp_wait(c, bar(base, B_O_DONE), (g - 1) & 1u, false)) {
+                if (!warp_wait(c, bar(base, B_O_FINAL), nitem & 1u, false)) {
                     ok = false;
                     break;
                 }
@@ -460,15 +585,17 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
                     }
                 }
                 if (rank == 0 && h < a.H) *lrow = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+                ++nitem;
                 tc_fence_before();
             }
         }
     }
 
     // ---------------------------------------------------------------- teardown
+    if (threadIdx.x == 0) bulk_wait_read_all();
     tc_fence_before();
     __syncthreads();
-    cluster_sync();  // the peer may still have been writing into this CTA's shared memory
+    cluster_sync();  // the peer may still be copying into this CTA's shared memory
     if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -503,8 +630,10 @@ int sm103_max_units() {
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (cached >= 0 && cached_dev == dev) return cached;
     if (cudaFuncSetAttribute(decode_sm103_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess)
+                             (int)kSmemBytes) != cudaSuccess) {
+        cudaGetLastError();
         return 0;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -532,7 +661,7 @@ cudaError_t launch_decode_sm103(const DecodeArgs &a, int num_clusters, cudaStrea
     CUtensorMap tmap;
     const cuuint64_t dims[2] = {(cuuint64_t)kDEntry, (cuuint64_t)a.num_pages * kPageRows};
     const cuuint64_t strides[1] = {(cuuint64_t)kDEntry * 2};
-    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t box[2] = {64, 32};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<unsigned char *>(a.cache),
                      dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

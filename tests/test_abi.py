@@ -79,6 +79,8 @@ def test_decode_rejects_bad_arguments_on_host(L):
     assert call(num_pages=0) == 1
     assert call(scale=float("nan")) == 1
     assert call(scale=float("inf")) == 1
+    assert call(scale=0.0) == 1
+    assert call(scale=-0.07) == 1
     assert call(kv=7) == 1
     assert call(qn=P(4098)) == 1          # not 16-byte aligned
     assert call(cache=P(4104)) == 1

