@@ -15,7 +15,8 @@
 //   softmax (one thread per head): x = s * scale * log2(e); reference r = the running
 //         maximum m, or the tile's own maximum if that exceeds m by more than 8; own
 //         weights p = 2^(x - r) in bf16 go to a shared-memory tile, followed by r and the
-//         fp32 sum of p.  One bulk copy (9 KB) puts them into the peer's copy of the tile.
+//         fp32 sum of p; each warp bulk-copies its 32 rows of that (2.25 KB) into the peer's
+//         copy of the tile, completing on the peer's mbarrier (9 KB per tile in all).
 //   merge: with both CTAs' (r, sum) both compute the same new maximum m', rescale a half
 //         whose reference was below m' (2^(r - m')), the sum l and — when m' > m — O, so
 //         both hold bitwise identical weights for all 64 tokens.
@@ -26,7 +27,9 @@
 // TMEM columns: O [0,256)  S [256,288)  query [288,512) (own latent half, RoPE, first 128
 // columns of the other half; the last 128 columns of the other half sit in shared memory).
 // Warp roles: warps 0-3 softmax/epilogue (thread = head, warp w reads TMEM lanes
-// 32w..32w+31), warp 4 TMA producer, warp 5 MMA issuer (and TMEM owner).
+// 32w..32w+31), warp 4 TMA producer, warp 5 issues QK^T (and owns TMEM), warp 6 issues
+// PV.  Two issuing threads let the tensor pipe take a tile's PV as soon as its weights
+// are ready instead of after the next tile's QK^T has been queued.
 // Every wait is bounded: on timeout the kernel records MLA_ERR_TIMEOUT, stops issuing,
 // and all roles fall through to a clean exit.
 #include <cuda.h>
@@ -54,7 +57,7 @@ constexpr uint32_t kPHalf = 128 * 64;            // 128 heads x 32 tokens bf16, 
 constexpr uint32_t kRlBytes = 1024;              // r[128] and sum[128], fp32
 constexpr uint32_t kPSlotBytes = 2 * kPHalf + 2 * kRlBytes;
 constexpr uint32_t kMsgBytes = kPHalf + kRlBytes;
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 288;
 constexpr uint32_t kColQRope = kColQ + 128, kColQOther = kColQ + 160;
@@ -77,11 +80,8 @@ enum {
     B_OTH_EMPTY = B_OTH_FULL + kOthStages,
     B_S_FULL = B_OTH_EMPTY + kOthStages,
     B_S_FREE,
-    B_O_DONE,                     // every PV (waited only before an O rescale)
     B_O_FINAL,                    // the last PV of a work item (waited by the epilogue)
     B_Q_READY,
-    B_XO_READY,                   // all four softmax warps wrote this tile's message
-    B_OWNREAD,                    // this CTA's last message has been read by its bulk copy
     B_RFULL,                      // peer's message for probability slot s has landed
     B_PFREE = B_RFULL + kPSlots,  // both CTAs' PV have finished reading slot s
     B_P_FULL = B_PFREE + kPSlots, // slot s holds the merged weights of its tile
@@ -167,11 +167,8 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
         }
         mbar_init(bar(base, B_S_FULL), 1);
         mbar_init(bar(base, B_S_FREE), 4);
-        mbar_init(bar(base, B_O_DONE), 1);
         mbar_init(bar(base, B_O_FINAL), 1);
         mbar_init(bar(base, B_Q_READY), 4);
-        mbar_init(bar(base, B_XO_READY), 4);
-        mbar_init(bar(base, B_OWNREAD), 1);
         for (int s = 0; s < kPSlots; ++s) {
             mbar_init(bar(base, B_RFULL + s), 1);  // + the message bytes
             mbar_init(bar(base, B_PFREE + s), 2);  // one commit from each CTA's PV
@@ -252,32 +249,11 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
             }
         }
     } else if (warp == 5) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ QK^T issuer
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16(128, 32, false);
-            constexpr uint32_t idesc_pv = idesc_bf16(128, 256, true);
             uint32_t g = 0, nitem = 0;
             bool ok = true;
-            // Per-slot barriers: a slot is only reused after both CTAs' PV of its previous
-            // tile, so no barrier here can run two phases ahead of its waiter.
-            auto issue_pv = [&](uint32_t gp, bool first, bool last) -> bool {
-                if (!wait_bar(c, bar(base, B_P_FULL + (int)(gp % kPSlots)), (gp / kPSlots) & 1u, false))
-                    return false;
-                tc_fence_after();
-                const int ds = (int)(gp % kDhStages);
-                const uint32_t dh = base + kOffDh + ds * kDhBytes;
-                const uint32_t ps = base + kOffP + (gp % kPSlots) * kPSlotBytes;
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t ad = smem_desc_sw64(ps + (kk >> 1) * kPHalf + (kk & 1) * 32u, 512u);
-                    const uint64_t bd = smem_desc_sw128(dh + kk * 2048u, kDhBlock, 1024u);
-                    mma_ss(tmem + kColO, ad, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
-                }
-                mma_commit(bar(base, B_O_DONE));
-                mma_commit(bar(base, B_DH_EMPTY + ds));
-                mma_commit_multicast(bar(base, B_PFREE + (int)(gp % kPSlots)), (uint16_t)3);
-                if (last) mma_commit(bar(base, B_O_FINAL));
-                return true;
-            };
             for (int u = cl; u < units && ok; u += ncl) {
                 for (int it = unit_begin[u]; it < unit_begin[u + 1] && ok; ++it) {
                     const WorkItem w = items[it];
@@ -324,12 +300,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
                                    idesc_qk, 1u);
                         mma_commit(bar(base, B_S_FULL));
                         mma_commit(bar(base, B_OTH_EMPTY + os));
-                        if (j > 0 && !issue_pv(g - 1, j == 1, false)) {
-                            ok = false;
-                            break;
-                        }
                     }
-                    if (ok && !issue_pv(g - 1, ntiles == 1, true)) ok = false;
                 }
             }
             if (!ok) {
@@ -339,14 +310,60 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
                 }
             }
         }
+    } else if (warp == 6) {
+        // ------------------------------------------------------------ PV issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_pv = idesc_bf16(128, 256, true);
+            uint32_t g = 0;
+            bool ok = true;
+            for (int u = cl; u < units && ok; u += ncl) {
+                for (int it = unit_begin[u]; it < unit_begin[u + 1] && ok; ++it) {
+                    const WorkItem w = items[it];
+                    const int ntiles = (w.t1 - w.t0 + kTileTokens - 1) / kTileTokens;
+                    for (int j = 0; j < ntiles; ++j, ++g) {
+                        // Per-slot barriers: a slot is only reused after both CTAs' PV of its
+                        // previous tile, so no barrier here can run two phases ahead.
+                        const int slot = (int)(g % kPSlots);
+                        if (!wait_bar(c, bar(base, B_P_FULL + slot), (g / kPSlots) & 1u, false)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const int ds = (int)(g % kDhStages);
+                        const uint32_t dh = base + kOffDh + ds * kDhBytes;
+                        const uint32_t ps = base + kOffP + slot * kPSlotBytes;
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t ad = smem_desc_sw64(ps + (kk >> 1) * kPHalf + (kk & 1) * 32u, 512u);
+                            const uint64_t bd = smem_desc_sw128(dh + kk * 2048u, kDhBlock, 1024u);
+                            mma_ss(tmem + kColO, ad, bd, idesc_pv, (j == 0 && kk == 0) ? 0u : 1u);
+                        }
+                        mma_commit(bar(base, B_DH_EMPTY + ds));
+                        mma_commit_multicast(bar(base, B_PFREE + slot), (uint16_t)3);
+                        if (j == ntiles - 1) mma_commit(bar(base, B_O_FINAL));
+                    }
+                }
+            }
+            if (!ok) {
+                const long long t0 = (long long)clock64_now();
+                while ((long long)clock64_now() - t0 < 20000000LL) {
+                }
+            }
+        }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
+        // Per tile: part A (scores -> own weights -> message to the peer), then part B
+        // (merge with the peer's message -> PV may start).
         const int h = threadIdx.x;  // head row = TMEM lane
         const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
         const uint32_t peer_p = mapa(base + kOffP, peer);
         const float sc = a.scale_log2;  // > 0, checked on the host
         uint32_t g = 0, nitem = 0;
         bool ok = true;
+        struct Pending {
+            uint32_t g;
+            int j, nvalid;
+            float rown, lown;
+        };
         for (int u = cl; u < units && ok; u += ncl) {
             for (int it = unit_begin[u]; it < unit_begin[u + 1] && ok; ++it) {
                 const WorkItem w = items[it];
@@ -404,167 +421,179 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
                     if (lane == 0) mbar_arrive(bar(base, B_Q_READY));
                 }
                 float m = -INFINITY, l = 0.f;
-                for (int j = 0; j < ntiles; ++j, ++g) {
-                    const int t = w.t0 + kTileTokens * j;
-                    const int ds = (int)(g % kDhStages);
-                    const uint32_t dph = (g / kDhStages) & 1u;
-                    const int slot = (int)(g % kPSlots);
-                    const uint32_t su = g / kPSlots;
-                    // ---- scores of the own 32 tokens
-                    if (!warp_wait(c, bar(base, B_S_FULL), g & 1u, false) ||
-                        !warp_wait(c, bar(base, B_DH_FULL + ds), dph, false)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    float s[32];
-                    {
-                        uint32_t sr[32];
-                        tmem_ld32(trow + kColS, sr);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(sr[i]);
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(base, B_S_FREE));
-                    const bool bad = misc[2 + ds] != 0u;
-                    const int nvalid = bad ? 0 : min(kTileTokens, w.t1 - t);  // page rows attended
-                    const int nown = max(0, min(32, nvalid - 32 * (int)rank));
-                    if (nown < 32) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (i >= nown) s[i] = -INFINITY;
-                    }
-                    float mraw = s[0];
-#pragma unroll
-                    for (int i = 1; i < 32; ++i) mraw = fmaxf(mraw, s[i]);
-                    const float mloc = mraw * sc;
-                    const float rown = mloc > m + kRescaleLog2 ? mloc : m;  // m = -inf: own max
-                    const float nr = rown == -INFINITY ? 0.f : -rown;
-                    uint32_t pk[16];
-                    float lown = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float p0 = ex2_approx(fmaf(s[2 * i], sc, nr));
-                        const float p1 = ex2_approx(fmaf(s[2 * i + 1], sc, nr));
-                        lown += p0 + p1;
-                        pk[i] = pack_bf16(p0, p1);
-                    }
-                    // ---- message: own weights into this CTA's copy of the probability tile,
-                    // then (r, sum); one bulk copy sends both to the peer's copy
-                    if (g >= (uint32_t)kPSlots &&
-                        !warp_wait(c, bar(base, B_PFREE + slot), (su - 1u) & 1u, true)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t *ps = gbase + kOffP + slot * kPSlotBytes;
-                    {
-                        uint8_t *prow = ps + rank * kPHalf + h * 64;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            *reinterpret_cast<uint4 *>(prow + ((q ^ ((h >> 1) & 3)) * 16)) =
-                                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                        float *rl = reinterpret_cast<float *>(ps + 2 * kPHalf + rank * kRlBytes);
-                        rl[h] = rown;
-                        rl[128 + h] = lown;
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(base, B_XO_READY));
-                    const uint32_t rfull = bar(base, B_RFULL + slot);
-                    if (threadIdx.x == 0) {
-                        mbar_arrive_expect_tx(rfull, kMsgBytes);
-                        if (!wait_bar(c, bar(base, B_XO_READY), g & 1u, false)) {
-                            ok = false;
-                        } else {
-                            const uint32_t off = kOffP + slot * kPSlotBytes;
-                            const uint32_t rb = mapa(rfull, peer);
-                            bulk_copy_s2peer(peer_p + slot * kPSlotBytes + rank * kPHalf,
-                                             base + off + rank * kPHalf, kPHalf, rb);
-                            bulk_copy_s2peer(peer_p + slot * kPSlotBytes + 2 * kPHalf + rank * kRlBytes,
-                                             base + off + 2 * kPHalf + rank * kRlBytes, kRlBytes, rb);
-                            bulk_commit();
-                        }
-                    }
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    // ---- merge with the peer's half (identical arithmetic in both CTAs)
-                    if (!warp_wait(c, rfull, su & 1u, true)) {
-                        ok = false;
-                        break;
-                    }
-                    if (threadIdx.x == 0) {
-                        bulk_wait_read_all();  // own weights may now be rewritten
-                        mbar_arrive(bar(base, B_OWNREAD));
-                    }
-                    const float *rlp = reinterpret_cast<const float *>(ps + 2 * kPHalf + peer * kRlBytes);
-                    const float rpeer = rlp[h], lpeer = rlp[128 + h];
-                    const float r0 = rank == 0 ? rown : rpeer, r1 = rank == 0 ? rpeer : rown;
-                    const float l0 = rank == 0 ? lown : lpeer, l1 = rank == 0 ? lpeer : lown;
-                    const float mn = fmaxf(m, fmaxf(r0, r1));
-                    float f0 = 1.f, f1 = 1.f, alpha = 1.f;
-                    if (mn != -INFINITY) {
-                        f0 = ex2_approx(r0 - mn);
-                        f1 = ex2_approx(r1 - mn);
-                        alpha = ex2_approx(m - mn);
-                        l = l * alpha + l0 * f0 + l1 * f1;
-                    }
-                    const bool resc_o = j > 0 && mn > m;
-                    m = mn;
-                    // a half whose reference lies below the new maximum is rescaled in place
-                    // (this CTA's own half only after its bulk copy has read it)
-                    const float fown = rank == 0 ? f0 : f1, fpeer = rank == 0 ? f1 : f0;
-                    bool wrote = false;
-                    if (__any_sync(0xffffffffu, fown < 1.f)) {
-                        if (!warp_wait(c, bar(base, B_OWNREAD), g & 1u, false)) {
-                            ok = false;
-                            break;
-                        }
-                        if (fown < 1.f) scale_row16(reinterpret_cast<uint4 *>(ps + rank * kPHalf + h * 64), fown);
-                        wrote = true;
-                    }
-                    if (fpeer < 1.f) {
-                        scale_row16(reinterpret_cast<uint4 *>(ps + peer * kPHalf + h * 64), fpeer);
-                        wrote = true;
-                    }
-                    // cache rows this tile must not contribute (page tail, missing page): the
-                    // PV operand must hold zeros there, not whatever the page holds
-                    if (nvalid < kTileTokens) {
-                        const uint32_t dh = kOffDh + ds * kDhBytes;
-                        const int nz = (kTileTokens - nvalid) * 32;  // 16-B chunks in 4 blocks
-                        for (int i = h; i < nz; i += 128) {
-                            const int row = nvalid + i / 32, ch = i % 32;
-                            *reinterpret_cast<uint4 *>(gbase + dh + (ch / 8) * kDhBlock + row * 128 + (ch % 8) * 16) =
-                                make_uint4(0u, 0u, 0u, 0u);
-                        }
-                        wrote = true;
-                    }
-                    if (__any_sync(0xffffffffu, wrote)) fence_proxy_async_smem();
-                    // ---- O rescale: PV of the previous tile must have finished
-                    if (__any_sync(0xffffffffu, resc_o)) {
-                        if (!warp_wait(c, bar(base, B_O_DONE), (g - 1) & 1u, false)) {
+                Pending pend{0u, -1, 0, 0.f, 0.f};
+                for (int j = 0; j < ntiles && ok; ++j) {
+                    Pending cur{g, j, 0, 0.f, 0.f};
+                    if (j < ntiles) {
+                        // ================= part A of tile j
+                        const int t = w.t0 + kTileTokens * j;
+                        const int ds = (int)(g % kDhStages);
+                        const uint32_t dph = (g / kDhStages) & 1u;
+                        const int slot = (int)(g % kPSlots);
+                        const uint32_t su = g / kPSlots;
+                        if (!warp_wait(c, bar(base, B_S_FULL), g & 1u, false) ||
+                            !warp_wait(c, bar(base, B_DH_FULL + ds), dph, false)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const float al = resc_o ? alpha : 1.f;
-                        for (int cb = 0; cb < 256; cb += 32) {
-                            uint32_t o[32];
-                            tmem_ld32(trow + kColO + cb, o);
+                        float s[32];
+                        {
+                            uint32_t sr[32];
+                            tmem_ld32(trow + kColS, sr);
                             tmem_wait_ld();
 #pragma unroll
-                            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * al);
-                            tmem_st32(trow + kColO + cb, o);
+                            for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(sr[i]);
                         }
-                        tmem_wait_st();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(base, B_S_FREE));
+                        const bool bad = misc[2 + ds] != 0u;
+                        const int nvalid = bad ? 0 : min(kTileTokens, w.t1 - t);  // page rows attended
+                        const int nown = max(0, min(32, nvalid - 32 * (int)rank));
+                        if (nown < 32) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (i >= nown) s[i] = -INFINITY;
+                        }
+                        float mraw = s[0];
+#pragma unroll
+                        for (int i = 1; i < 32; ++i) mraw = fmaxf(mraw, s[i]);
+                        const float mloc = mraw * sc;
+                        // reference: the running maximum (known after part B of tile j-1 only
+                        // for the tiles before it; any value works as long as both CTAs send
+                        // the one they used)
+                        const float mk = m;
+                        const float rown = mloc > mk + kRescaleLog2 ? mloc : mk;
+                        const float nr = rown == -INFINITY ? 0.f : -rown;
+                        uint32_t pk[16];
+                        float lown = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float p0 = ex2_approx(fmaf(s[2 * i], sc, nr));
+                            const float p1 = ex2_approx(fmaf(s[2 * i + 1], sc, nr));
+                            lown += p0 + p1;
+                            pk[i] = pack_bf16(p0, p1);
+                        }
+                        // slot reuse: both CTAs' PV of tile g-3 must be done
+                        if (g >= (uint32_t)kPSlots &&
+                            !warp_wait(c, bar(base, B_PFREE + slot), (su - 1u) & 1u, true)) {
+                            ok = false;
+                            break;
+                        }
+                        uint8_t *ps = gbase + kOffP + slot * kPSlotBytes;
+                        const uint32_t poff = kOffP + slot * kPSlotBytes;
+                        {
+                            uint8_t *prow = ps + rank * kPHalf + h * 64;
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                *reinterpret_cast<uint4 *>(prow + ((q ^ ((h >> 1) & 3)) * 16)) =
+                                    make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                            float *rl = reinterpret_cast<float *>(ps + 2 * kPHalf + rank * kRlBytes);
+                            rl[h] = rown;
+                            rl[128 + h] = lown;
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        const uint32_t rfull = bar(base, B_RFULL + slot);
+                        if (threadIdx.x == 0) mbar_arrive_expect_tx(rfull, kMsgBytes);
+                        if (lane == 0) {
+                            const uint32_t rb = mapa(rfull, peer);
+                            const uint32_t prows = poff + rank * kPHalf + warp * 32 * 64;
+                            const uint32_t rls = poff + 2 * kPHalf + rank * kRlBytes + warp * 32 * 4;
+                            bulk_copy_s2peer(peer_p - kOffP + prows, base + prows, 32 * 64, rb);
+                            bulk_copy_s2peer(peer_p - kOffP + rls, base + rls, 32 * 4, rb);
+                            bulk_copy_s2peer(peer_p - kOffP + rls + 512, base + rls + 512, 32 * 4, rb);
+                            bulk_commit();
+                        }
+                        cur.nvalid = nvalid;
+                        cur.rown = rown;
+                        cur.lown = lown;
+                        ++g;
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(base, B_P_FULL + slot));
+                    pend = cur;
+                    if (pend.j >= 0) {
+                        // ================= part B of tile pend.j (merge, then PV may start)
+                        const uint32_t gp = pend.g;
+                        const int ds = (int)(gp % kDhStages);
+                        const int slot = (int)(gp % kPSlots);
+                        const uint32_t su = gp / kPSlots;
+                        const uint32_t rfull = bar(base, B_RFULL + slot);
+                        if (!warp_wait(c, rfull, su & 1u, true)) {
+                            ok = false;
+                            break;
+                        }
+                        uint8_t *ps = gbase + kOffP + slot * kPSlotBytes;
+                        const float *rlp = reinterpret_cast<const float *>(ps + 2 * kPHalf + peer * kRlBytes);
+                        const float rpeer = rlp[h], lpeer = rlp[128 + h];
+                        const float r0 = rank == 0 ? pend.rown : rpeer, r1 = rank == 0 ? rpeer : pend.rown;
+                        const float l0 = rank == 0 ? pend.lown : lpeer, l1 = rank == 0 ? lpeer : pend.lown;
+                        const float mn = fmaxf(m, fmaxf(r0, r1));
+                        float f0 = 1.f, f1 = 1.f, alpha = 1.f;
+                        if (mn != -INFINITY) {
+                            f0 = ex2_approx(r0 - mn);
+                            f1 = ex2_approx(r1 - mn);
+                            alpha = ex2_approx(m - mn);
+                            l = l * alpha + l0 * f0 + l1 * f1;
+                        }
+                        const bool resc_o = pend.j > 0 && mn > m;
+                        m = mn;
+                        // a half whose reference lies below the new maximum is rescaled in
+                        // place (this CTA's own rows only after the warp's bulk copies have
+                        // read them)
+                        const float fown = rank == 0 ? f0 : f1, fpeer = rank == 0 ? f1 : f0;
+                        bool wrote = false;
+                        if (__any_sync(0xffffffffu, fown < 1.f)) {
+                            if (lane == 0) bulk_wait_read_all();
+                            __syncwarp();
+                            if (fown < 1.f) scale_row16(reinterpret_cast<uint4 *>(ps + rank * kPHalf + h * 64), fown);
+                            wrote = true;
+                        }
+                        if (fpeer < 1.f) {
+                            scale_row16(reinterpret_cast<uint4 *>(ps + peer * kPHalf + h * 64), fpeer);
+                            wrote = true;
+                        }
+                        // cache rows this tile must not contribute (page tail, missing page):
+                        // the PV operand must hold zeros there, not whatever the page holds
+                        if (pend.nvalid < kTileTokens) {
+                            const uint32_t dh = kOffDh + ds * kDhBytes;
+                            const int nz = (kTileTokens - pend.nvalid) * 32;  // 16-B chunks in 4 blocks
+                            for (int i = h; i < nz; i += 128) {
+                                const int row = pend.nvalid + i / 32, ch = i % 32;
+                                *reinterpret_cast<uint4 *>(gbase + dh + (ch / 8) * kDhBlock + row * 128 + (ch % 8) * 16) =
+                                    make_uint4(0u, 0u, 0u, 0u);
+                            }
+                            wrote = true;
+                        }
+                        if (__any_sync(0xffffffffu, wrote)) fence_proxy_async_smem();
+                        // O rescale: PV of the previous tile must have finished.  Its slot's
+                        // barrier completes when both CTAs' PV of that tile are done and cannot
+                        // complete again before this tile's PV, so its parity is unambiguous.
+                        if (__any_sync(0xffffffffu, resc_o)) {
+                            const uint32_t gq = gp - 1u;
+                            if (!warp_wait(c, bar(base, B_PFREE + (int)(gq % kPSlots)), (gq / kPSlots) & 1u, true)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const float al = resc_o ? alpha : 1.f;
+                            for (int cb = 0; cb < 256; cb += 32) {
+                                uint32_t o[32];
+                                tmem_ld32(trow + kColO + cb, o);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * al);
+                                tmem_st32(trow + kColO + cb, o);
+                            }
+                            tmem_wait_st();
+                        }
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(base, B_P_FULL + slot));
+                    }
                 }
                 if (!ok) break;
-                // ---- epilogue: wait for the last PV, normalise, store
+                // ---- epilogue: wait for the last PV of this item, normalise, store
                 if (!warp_wait(c, bar(base, B_O_FINAL), nitem & 1u, false)) {
                     ok = false;
                     break;
@@ -592,7 +621,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
     }
 
     // ---------------------------------------------------------------- teardown
-    if (threadIdx.x == 0) bulk_wait_read_all();
+    if (warp < 4 && lane == 0) bulk_wait_read_all();
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // the peer may still be copying into this CTA's shared memory
