@@ -1,35 +1,38 @@
 // Tensor-core decode kernel for sm_103a (bf16 paged cache).
 //
 // One work unit = a cluster of two CTAs on two SMs.  Both CTAs walk the same work items
-// (request b, token range) tile by tile, one 64-token page per tile.  CTA r owns
-//   * the scores of the page's tokens [32 r, 32 r + 32) — full 576-wide dot products, so no
-//     partial score ever crosses between the SMs, and
+// (request b, token range) tile by tile; a tile is two 64-token pages.  CTA r owns
+//   * the scores of page r of the tile — full 576-wide dot products for its 64 tokens, so
+//     no partial score ever crosses between the SMs, and
 //   * the output latent columns [256 r, 256 r + 256) of every head (its O half, 128 x 256
 //     fp32 in TMEM; the full 128 x 512 accumulator does not fit one SM's TMEM).
 // Per tile:
-//   TMA (128-B swizzle)  own-half latent of all 64 tokens (PV operand, kept until PV) and
-//                        the other 320 columns (other latent half + RoPE) of its own 32
-//                        tokens (QK operand only, released after QK).
-//   QK^T  S[h, i] = q[h, :] . entry[own token i, :]   tcgen05.mma M=128 heads, N=32,
-//         K=576: 448 K from the query slice held in TMEM, 128 K from shared memory.
+//   TMA (128-B swizzle, 64-row boxes)  own-half latent of both pages (PV operand; the own
+//        page's copy is also the QK operand for those columns) and the other 320 columns
+//        (other latent half + RoPE) of the own page (QK operand only, released once QK^T
+//        has read it).  Page ids are read one tile ahead, off the loaders' critical path,
+//        and each stage costs the loader one wait and one expect-tx.
+//   QK^T  S[h, i] = q[h, :] . entry[own page row i, :]   tcgen05.mma M=128 heads, N=64,
+//         K=576: 384 K from the query slice held in TMEM, 192 K from shared memory.
 //   softmax (one thread per head): x = s * scale * log2(e); reference r = the running
-//         maximum m, or the tile's own maximum if that exceeds m by more than 8; own
+//         maximum m, or the page's own maximum if that exceeds m by more than 8; own
 //         weights p = 2^(x - r) in bf16 go to a shared-memory tile, followed by r and the
-//         fp32 sum of p; each warp bulk-copies its 32 rows of that (2.25 KB) into the peer's
-//         copy of the tile, completing on the peer's mbarrier (9 KB per tile in all).
-//   merge: with both CTAs' (r, sum) both compute the same new maximum m', rescale a half
+//         fp32 sum of p; each warp bulk-copies its 32 rows of that (4.25 KB) into the
+//         peer's copy of the tile, completing on the peer's mbarrier (17 KB per tile).
+//   merge: with both CTAs' (r, sum) both compute the same new maximum m', rescale a page
 //         whose reference was below m' (2^(r - m')), the sum l and — when m' > m — O, so
-//         both hold bitwise identical weights for all 64 tokens.
-//   PV    O_r[h, :] += P[h, 0:64] . C[0:64, own latent half]   M=128, N=256, K=64,
-//         A = the probability tile (64-B swizzle), B = the own-half cache tile (MN-major).
+//         both hold bitwise identical weights for all 128 tokens.
+//   PV    O_r[h, :] += P[h, 0:128] . C[0:128, own latent half]   M=128, N=256, K=128,
+//         A = the probability tile, B = the own-half cache tiles (MN-major); the peer's
+//         page first, so that its buffer is handed back to the loader early.
 //   epilogue: out = O / l, lse = (m + log2 l) ln 2, or a partial result for the merge.
 //
-// TMEM columns: O [0,256)  S [256,288)  query [288,512) (own latent half, RoPE, first 128
-// columns of the other half; the last 128 columns of the other half sit in shared memory).
+// TMEM columns: O [0,256)  S [256,320)  query [320,512) (own latent half, RoPE, first 64
+// columns of the other half; the other half's last 192 columns sit in shared memory).
 // Warp roles: warps 0-3 softmax/epilogue (thread = head, warp w reads TMEM lanes
-// 32w..32w+31), warp 4 TMA producer, warp 5 issues QK^T (and owns TMEM), warp 6 issues
-// PV.  Two issuing threads let the tensor pipe take a tile's PV as soon as its weights
-// are ready instead of after the next tile's QK^T has been queued.
+// 32w..32w+31), warp 4 loads the latent-half ring, warp 7 the other-columns ring (two
+// warps, so that neither loader's waits hold up the other), warp 5 issues QK^T (and owns
+// TMEM), warp 6 issues PV.
 // Every wait is bounded: on timeout the kernel records MLA_ERR_TIMEOUT, stops issuing,
 // and all roles fall through to a clean exit.
 #include <cuda.h>
@@ -44,48 +47,46 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kDhStages = 3;   // own-half latent tiles (live until PV)
-constexpr int kOthStages = 2;  // other-columns tiles (live until QK)
-constexpr int kPSlots = 3;     // probability tiles (live until both CTAs' PV)
-constexpr uint32_t kHalfBox = 32 * 128;          // 32 rows x 64 bf16, 128-B swizzle
-constexpr uint32_t kDhBlock = 2 * kHalfBox;      // 64 token rows x 64 columns
-constexpr uint32_t kDhBytes = 4 * kDhBlock;      // 256 columns
-constexpr uint32_t kOthBytes = 5 * kHalfBox;     // 4 x 64 latent columns + RoPE, 32 rows
+constexpr int kTile = 2 * kPageRows;             // tokens per tile
+constexpr int kDhSlots = 3;                      // own-half latent of one page (until PV)
+constexpr int kOthBoxes = 5;                     // other latent half (4 boxes) + RoPE, one stage
+constexpr uint32_t kBox = 64 * 128;              // 64 rows x 64 bf16, 128-B swizzle
+constexpr uint32_t kDhBytes = 4 * kBox;          // one page, 256 latent columns
 constexpr uint32_t kQsBox = 128 * 128;           // 128 heads x 64 bf16
-constexpr uint32_t kQsBytes = 2 * kQsBox;
-constexpr uint32_t kPHalf = 128 * 64;            // 128 heads x 32 tokens bf16, 64-B swizzle
+constexpr uint32_t kQsBytes = 3 * kQsBox;
+constexpr uint32_t kPPage = 128 * 128;           // 128 heads x 64 tokens bf16, 128-B swizzle
 constexpr uint32_t kRlBytes = 1024;              // r[128] and sum[128], fp32
-constexpr uint32_t kPSlotBytes = 2 * kPHalf + 2 * kRlBytes;
-constexpr uint32_t kMsgBytes = kPHalf + kRlBytes;
-constexpr int kThreads = 224;
+constexpr uint32_t kPBytes = 2 * kPPage + 2 * kRlBytes;
+constexpr uint32_t kMsgBytes = kPPage + kRlBytes;
+constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0, kColS = 256, kColQ = 288;
+constexpr uint32_t kColO = 0, kColS = 256, kColQ = 320;
 constexpr uint32_t kColQRope = kColQ + 128, kColQOther = kColQ + 160;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr long long kSpinCycles = 4000000000LL;  // about two seconds
 
 constexpr uint32_t kOffDh = 0;
-constexpr uint32_t kOffOth = kOffDh + kDhStages * kDhBytes;
-constexpr uint32_t kOffQs = kOffOth + kOthStages * kOthBytes;
+constexpr uint32_t kOffOth = kOffDh + kDhSlots * kDhBytes;
+constexpr uint32_t kOffQs = kOffOth + kOthBoxes * kBox;
 constexpr uint32_t kOffP = kOffQs + kQsBytes;
-constexpr uint32_t kOffBar = kOffP + kPSlots * kPSlotBytes;
+constexpr uint32_t kOffBar = kOffP + kPBytes;
 constexpr uint32_t kOffMisc = kOffBar + 8 * 32;
 constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + slack for 1024-B alignment
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 enum {
     B_DH_FULL = 0,
-    B_DH_EMPTY = B_DH_FULL + kDhStages,
-    B_OTH_FULL = B_DH_EMPTY + kDhStages,
-    B_OTH_EMPTY = B_OTH_FULL + kOthStages,
-    B_S_FULL = B_OTH_EMPTY + kOthStages,
+    B_DH_EMPTY = B_DH_FULL + kDhSlots,
+    B_OTH_FULL = B_DH_EMPTY + kDhSlots,
+    B_OTH_EMPTY,
+    B_S_FULL,
     B_S_FREE,
-    B_O_FINAL,                    // the last PV of a work item (waited by the epilogue)
+    B_O_FINAL,  // the last PV of a work item (waited by the epilogue)
     B_Q_READY,
-    B_RFULL,                      // peer's message for probability slot s has landed
-    B_PFREE = B_RFULL + kPSlots,  // both CTAs' PV have finished reading slot s
-    B_P_FULL = B_PFREE + kPSlots, // slot s holds the merged weights of its tile
-    B_COUNT = B_P_FULL + kPSlots
+    B_RFULL,    // the peer's message for the current tile has landed
+    B_PFREE,    // both CTAs' PV have finished reading the probability tile
+    B_P_FULL,   // the probability tile holds the merged weights of its tile
+    B_COUNT
 };
 static_assert(B_COUNT <= 32, "barrier area");
 
@@ -122,14 +123,24 @@ __device__ __forceinline__ bool warp_wait(const Ctx &c, uint32_t b, uint32_t par
     return __all_sync(0xffffffffu, ok);
 }
 
+// Gives TMA loads or MMAs already in flight a bounded time to finish before an aborting
+// role leaves (shared memory and TMEM must outlive them).
+__device__ __forceinline__ void drain_pause() {
+    const long long t0 = (long long)clock64_now();
+    while ((long long)clock64_now() - t0 < 20000000LL) {
+    }
+}
+
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
 }
-__device__ __forceinline__ void scale_row16(uint4 *prow, float f) {
-    for (int q = 0; q < 4; ++q) {
+// Multiplies one 128-B row of bf16 weights by f (the chunk order inside the row does not
+// matter).
+__device__ __forceinline__ void scale_row(uint4 *prow, float f) {
+    for (int q = 0; q < 8; ++q) {
         uint4 v = prow[q];
         v.x = pack_bf16(bf16lo(v.x) * f, bf16hi(v.x) * f);
         v.y = pack_bf16(bf16lo(v.y) * f, bf16hi(v.y) * f);
@@ -137,6 +148,80 @@ __device__ __forceinline__ void scale_row16(uint4 *prow, float f) {
         v.w = pack_bf16(bf16lo(v.w) * f, bf16hi(v.w) * f);
         prow[q] = v;
     }
+}
+
+// Page p (0 or 1) of the tile starting at token t of item w: its valid rows (0 when the page
+// lies past the item's end) and its physical id (-1 when that id is out of range).
+struct PageRef {
+    int rows;
+    int64_t id;
+};
+__device__ __forceinline__ PageRef page_of(const DecodeArgs &a, const WorkItem &w, int t, int p) {
+    const int t_p = t + kPageRows * p;
+    PageRef r{0, -1};
+    if (t_p >= w.t1) return r;
+    r.rows = min(kPageRows, w.t1 - t_p);
+    const int lp = t_p / kPageRows;
+    const int64_t id = lp < a.max_pages ? (int64_t)a.block_table[(int64_t)w.b * a.max_pages + lp] : -1;
+    r.id = (id >= 0 && id < a.num_pages) ? id : -1;
+    return r;
+}
+
+// Walks the tiles of this cluster's work in order: units cl, cl + ncl, ..., their items
+// (those with tokens), and each item's 128-token tiles.
+struct TileCursor {
+    const int32_t *ub;
+    const WorkItem *items;
+    int units, ncl;
+    int u, it;   // current unit and item; u >= units once every tile has been visited
+    WorkItem w;  // items[it]
+    int t;       // first token of the current tile
+    __device__ void find() {
+        while (u < units) {
+            const int end = ub[u + 1];
+            for (; it < end; ++it) {
+                w = items[it];
+                if (w.t1 > w.t0) {
+                    t = w.t0;
+                    return;
+                }
+            }
+            u += ncl;
+            if (u < units) it = ub[u];
+        }
+    }
+    __device__ void begin(const int32_t *unit_begin, const WorkItem *its, int nunits, int cl, int n) {
+        ub = unit_begin;
+        items = its;
+        units = nunits;
+        ncl = n;
+        u = cl;
+        it = u < units ? ub[u] : 0;
+        find();
+    }
+    __device__ bool done() const { return u >= units; }
+    __device__ void next() {
+        if (done()) return;
+        t += kTile;
+        if (t < w.t1) return;
+        ++it;
+        find();
+    }
+};
+
+// Request of the first item with tokens after item `it` of unit `u`, in this cluster's
+// order (units u, u + ncl, ...), or -1.
+__device__ int next_request(const int32_t *ub, const WorkItem *items, int units, int ncl, int u, int it) {
+    int nit = it + 1;
+    while (u < units) {
+        for (; nit < ub[u + 1]; ++nit) {
+            const WorkItem w = items[nit];
+            if (w.t1 > w.t0) return w.b;
+        }
+        u += ncl;
+        if (u < units) nit = ub[u];
+    }
+    return -1;
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -152,28 +237,23 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
     volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(gbase + kOffMisc);
-    // misc[0]: TMEM base address, misc[1]: abort flag, misc[2 + s]: own-half tile s holds
-    // no data (its page id was out of range)
+    // misc[0]: TMEM base address, misc[1]: abort flag
     Ctx c{base, a.status, misc + 1};
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kDhStages; ++s) {
+        for (int s = 0; s < kDhSlots; ++s) {
             mbar_init(bar(base, B_DH_FULL + s), 1);
             mbar_init(bar(base, B_DH_EMPTY + s), 1);
         }
-        for (int s = 0; s < kOthStages; ++s) {
-            mbar_init(bar(base, B_OTH_FULL + s), 1);
-            mbar_init(bar(base, B_OTH_EMPTY + s), 1);
-        }
+        mbar_init(bar(base, B_OTH_FULL), 1);
+        mbar_init(bar(base, B_OTH_EMPTY), 1);
         mbar_init(bar(base, B_S_FULL), 1);
         mbar_init(bar(base, B_S_FREE), 4);
         mbar_init(bar(base, B_O_FINAL), 1);
         mbar_init(bar(base, B_Q_READY), 4);
-        for (int s = 0; s < kPSlots; ++s) {
-            mbar_init(bar(base, B_RFULL + s), 1);  // + the message bytes
-            mbar_init(bar(base, B_PFREE + s), 2);  // one commit from each CTA's PV
-            mbar_init(bar(base, B_P_FULL + s), 4);
-        }
+        mbar_init(bar(base, B_RFULL), 1);  // + the message bytes
+        mbar_init(bar(base, B_PFREE), 2);  // one commit from each CTA's PV
+        mbar_init(bar(base, B_P_FULL), 4);
         misc[1] = 0u;
         fence_mbar_init();
     }
@@ -196,119 +276,146 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
     const int units = hd->num_units;
     const int cl = (int)cluster_id_x(), ncl = (int)nclusters_x();
 
-    if (warp == 4) {
-        // ------------------------------------------------------------ TMA producer
+    // Latent-half slots are taken in the order (own page of tile g, peer page of tile g):
+    // sequence number 2g + 0 / 2g + 1, slot n % kDhSlots.
+    if (warp == 4 || warp == 7) {
+        // ------------------------------------------------------------ TMA producers
         if (lane == 0) {
-            const int xown = 256 * (int)rank, xoth = 256 * (int)peer;
-            uint32_t g = 0;
-            bool ok = true;
-            for (int u = cl; u < units && ok; u += ncl) {
-                for (int it = unit_begin[u]; it < unit_begin[u + 1] && ok; ++it) {
-                    const WorkItem w = items[it];
-                    for (int t = w.t0; t < w.t1; t += kTileTokens, ++g) {
-                        const int ds = (int)(g % kDhStages), os = (int)(g % kOthStages);
-                        const uint32_t dph = (g / kDhStages) & 1u, oph = (g / kOthStages) & 1u;
-                        if (!wait_bar(c, bar(base, B_DH_EMPTY + ds), dph ^ 1u, false) ||
-                            !wait_bar(c, bar(base, B_OTH_EMPTY + os), oph ^ 1u, false)) {
+            TileCursor cur, nx;
+            cur.begin(unit_begin, items, units, cl, ncl);
+            nx = cur;
+            nx.next();
+            if (warp == 4) {
+                // own latent half of both pages
+                const int xown = 256 * (int)rank;
+                PageRef pr0{0, -1}, pr1{0, -1};
+                if (!cur.done()) {
+                    pr0 = page_of(a, cur.w, cur.t, (int)rank);
+                    pr1 = page_of(a, cur.w, cur.t, (int)peer);
+                }
+                bool ok = true;
+                for (uint32_t g = 0; !cur.done() && ok; ++g) {
+                    PageRef np0{0, -1}, np1{0, -1};  // next tile's pages, read ahead of the waits
+                    if (!nx.done()) {
+                        np0 = page_of(a, nx.w, nx.t, (int)rank);
+                        np1 = page_of(a, nx.w, nx.t, (int)peer);
+                    }
+                    for (int e = 0; e < 2; ++e) {
+                        const uint32_t n = 2 * g + e;
+                        const int ds = (int)(n % kDhSlots);
+                        if (!wait_bar(c, bar(base, B_DH_EMPTY + ds), ((n / kDhSlots) & 1u) ^ 1u, false)) {
                             ok = false;
                             break;
                         }
-                        const int lp = t / kPageRows;
-                        const int64_t page =
-                            lp < a.max_pages ? (int64_t)a.block_table[(int64_t)w.b * a.max_pages + lp] : -1;
-                        const uint32_t dfb = bar(base, B_DH_FULL + ds), ofb = bar(base, B_OTH_FULL + os);
-                        if (page >= 0 && page < a.num_pages) {
-                            misc[2 + ds] = 0u;
-                            const int32_t y = (int32_t)(page * kPageRows);
-                            const uint32_t dst_dh = base + kOffDh + ds * kDhBytes;
-                            const uint32_t dst_ot = base + kOffOth + os * kOthBytes;
-                            mbar_arrive_expect_tx(dfb, kDhBytes);
-                            for (int i = 0; i < 4; ++i)
-                                for (int hf = 0; hf < 2; ++hf)
-                                    tma_load_2d(dst_dh + i * kDhBlock + hf * kHalfBox, &tmap, xown + 64 * i,
-                                                y + 32 * hf, dfb);
-                            mbar_arrive_expect_tx(ofb, kOthBytes);
-                            const int yo = y + 32 * (int)rank;
-                            for (int i = 0; i < 4; ++i)
-                                tma_load_2d(dst_ot + i * kHalfBox, &tmap, xoth + 64 * i, yo, ofb);
-                            tma_load_2d(dst_ot + 4 * kHalfBox, &tmap, kDLatent, yo, ofb);
+                        const PageRef pg = e == 0 ? pr0 : pr1;
+                        const uint32_t fb = bar(base, B_DH_FULL + ds);
+                        if (pg.rows > 0 && pg.id >= 0) {
+                            const int32_t y = (int32_t)(pg.id * kPageRows);
+                            const uint32_t dst = base + kOffDh + ds * kDhBytes;
+                            mbar_arrive_expect_tx(fb, kDhBytes);
+                            for (int i = 0; i < 4; ++i) tma_load_2d(dst + i * kBox, &tmap, xown + 64 * i, y, fb);
                         } else {
-                            record_error(a.status, MLA_ERR_INDEX);
-                            misc[2 + ds] = 1u;
-                            mbar_arrive(dfb);
-                            mbar_arrive(ofb);
+                            if (pg.rows > 0) record_error(a.status, MLA_ERR_INDEX);
+                            mbar_arrive(fb);
                         }
                     }
+                    pr0 = np0;
+                    pr1 = np1;
+                    cur = nx;
+                    nx.next();
                 }
-            }
-            if (!ok) {
-                // give loads already in flight a bounded time to land before exit
-                const long long t0 = (long long)clock64_now();
-                while ((long long)clock64_now() - t0 < 20000000LL) {
+                if (!ok) drain_pause();
+            } else {
+                // other latent half + RoPE of the own page, one stage
+                const int xoth = 256 * (int)peer;
+                PageRef pg{0, -1};
+                if (!cur.done()) pg = page_of(a, cur.w, cur.t, (int)rank);
+                bool ok = true;
+                for (uint32_t g = 0; !cur.done() && ok; ++g) {
+                    PageRef np{0, -1};  // next tile's page, read ahead of the wait
+                    if (!nx.done()) np = page_of(a, nx.w, nx.t, (int)rank);
+                    if (!wait_bar(c, bar(base, B_OTH_EMPTY), (g & 1u) ^ 1u, false)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = bar(base, B_OTH_FULL);
+                    if (pg.rows > 0 && pg.id >= 0) {
+                        const int32_t y = (int32_t)(pg.id * kPageRows);
+                        mbar_arrive_expect_tx(fb, kOthBoxes * kBox);
+                        for (int i = 0; i < kOthBoxes; ++i)
+                            tma_load_2d(base + kOffOth + i * kBox, &tmap, i < 4 ? xoth + 64 * i : kDLatent, y, fb);
+                    } else {
+                        mbar_arrive(fb);
+                    }
+                    pg = np;
+                    cur = nx;
+                    nx.next();
                 }
+                if (!ok) drain_pause();
             }
         }
     } else if (warp == 5) {
         // ------------------------------------------------------------ QK^T issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16(128, 32, false);
+            constexpr uint32_t idesc_qk = idesc_bf16(128, 64, false);
             uint32_t g = 0, nitem = 0;
             bool ok = true;
             for (int u = cl; u < units && ok; u += ncl) {
                 for (int it = unit_begin[u]; it < unit_begin[u + 1] && ok; ++it) {
                     const WorkItem w = items[it];
-                    const int ntiles = (w.t1 - w.t0 + kTileTokens - 1) / kTileTokens;
-                    if (ntiles <= 0) continue;
+                    if (w.t1 <= w.t0) continue;
                     if (!wait_bar(c, bar(base, B_Q_READY), nitem & 1u, false)) {
                         ok = false;
                         break;
                     }
                     ++nitem;
                     tc_fence_after();
-                    for (int j = 0; j < ntiles; ++j, ++g) {
-                        const int ds = (int)(g % kDhStages), os = (int)(g % kOthStages);
-                        const uint32_t dph = (g / kDhStages) & 1u, oph = (g / kOthStages) & 1u;
-                        if (!wait_bar(c, bar(base, B_DH_FULL + ds), dph, false) ||
-                            !wait_bar(c, bar(base, B_OTH_FULL + os), oph, false) ||
-                            (g > 0 && !wait_bar(c, bar(base, B_S_FREE), (g - 1) & 1u, false))) {
+                    for (int t = w.t0; t < w.t1 && ok; t += kTile, ++g) {
+                        if (g > 0 && !wait_bar(c, bar(base, B_S_FREE), (g - 1) & 1u, false)) {
+                            ok = false;
+                            break;
+                        }
+                        const bool have = t + kPageRows * (int)rank < w.t1;  // own page exists
+                        // other latent half and RoPE first: their stage goes back to the loader
+                        // while the own-half rows may still wait for the previous tile's PV
+                        if (!wait_bar(c, bar(base, B_OTH_FULL), g & 1u, false)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t dh = base + kOffDh + ds * kDhBytes + rank * kHalfBox;
-                        const uint32_t ot = base + kOffOth + os * kOthBytes;
-                        const uint32_t qs = base + kOffQs;
-                        // own latent half: query columns from TMEM, own token rows of the PV tile
-                        for (int k = 0; k < 16; ++k)
-                            mma_ts(tmem + kColS, tmem + kColQ + 8u * k,
-                                   smem_desc_sw128(dh + (k >> 2) * kDhBlock + (k & 3) * 32u, 16u, 1024u),
-                                   idesc_qk, k > 0 ? 1u : 0u);
-                        // RoPE
-                        for (int k = 0; k < 4; ++k)
-                            mma_ts(tmem + kColS, tmem + kColQRope + 8u * k,
-                                   smem_desc_sw128(ot + 4 * kHalfBox + k * 32u, 16u, 1024u), idesc_qk, 1u);
-                        // other latent half, first 128 columns: query from TMEM
-                        for (int k = 0; k < 8; ++k)
-                            mma_ts(tmem + kColS, tmem + kColQOther + 8u * k,
-                                   smem_desc_sw128(ot + (k >> 2) * kHalfBox + (k & 3) * 32u, 16u, 1024u),
-                                   idesc_qk, 1u);
-                        // other latent half, last 128 columns: query from shared memory
-                        for (int k = 0; k < 8; ++k)
-                            mma_ss(tmem + kColS,
-                                   smem_desc_sw128(qs + (k >> 2) * kQsBox + (k & 3) * 32u, 16u, 1024u),
-                                   smem_desc_sw128(ot + (2 + (k >> 2)) * kHalfBox + (k & 3) * 32u, 16u, 1024u),
-                                   idesc_qk, 1u);
+                        for (int i = 0; i < kOthBoxes && have; ++i) {
+                            const uint32_t ot = base + kOffOth + i * kBox;
+                            for (int k = 0; k < 4; ++k) {
+                                const uint64_t bd = smem_desc_sw128(ot + k * 32u, 16u, 1024u);
+                                if (i == 0)
+                                    mma_ts(tmem + kColS, tmem + kColQOther + 8u * k, bd, idesc_qk, k > 0 ? 1u : 0u);
+                                else if (i == 4)
+                                    mma_ts(tmem + kColS, tmem + kColQRope + 8u * k, bd, idesc_qk, 1u);
+                                else
+                                    mma_ss(tmem + kColS,
+                                           smem_desc_sw128(base + kOffQs + (i - 1) * kQsBox + k * 32u, 16u, 1024u),
+                                           bd, idesc_qk, 1u);
+                            }
+                        }
+                        mma_commit(bar(base, B_OTH_EMPTY));
+                        const uint32_t n = 2 * g;
+                        const int ds = (int)(n % kDhSlots);
+                        if (!wait_bar(c, bar(base, B_DH_FULL + ds), (n / kDhSlots) & 1u, false)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (have) {
+                            const uint32_t dh = base + kOffDh + ds * kDhBytes;
+                            for (int k = 0; k < 16; ++k)
+                                mma_ts(tmem + kColS, tmem + kColQ + 8u * k,
+                                       smem_desc_sw128(dh + (k >> 2) * kBox + (k & 3) * 32u, 16u, 1024u), idesc_qk, 1u);
+                        }
                         mma_commit(bar(base, B_S_FULL));
-                        mma_commit(bar(base, B_OTH_EMPTY + os));
                     }
                 }
             }
-            if (!ok) {
-                // let issued MMAs drain before TMEM is released
-                const long long t0 = (long long)clock64_now();
-                while ((long long)clock64_now() - t0 < 20000000LL) {
-                }
-            }
+            if (!ok) drain_pause();
         }
     } else if (warp == 6) {
         // ------------------------------------------------------------ PV issuer
@@ -319,35 +426,43 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
             for (int u = cl; u < units && ok; u += ncl) {
                 for (int it = unit_begin[u]; it < unit_begin[u + 1] && ok; ++it) {
                     const WorkItem w = items[it];
-                    const int ntiles = (w.t1 - w.t0 + kTileTokens - 1) / kTileTokens;
-                    for (int j = 0; j < ntiles; ++j, ++g) {
-                        // Per-slot barriers: a slot is only reused after both CTAs' PV of its
-                        // previous tile, so no barrier here can run two phases ahead.
-                        const int slot = (int)(g % kPSlots);
-                        if (!wait_bar(c, bar(base, B_P_FULL + slot), (g / kPSlots) & 1u, false)) {
+                    bool first = true;
+                    for (int t = w.t0; t < w.t1; t += kTile, ++g) {
+                        // the probability tile is reused only after both CTAs' PV of the
+                        // previous tile, so P_FULL never runs two phases ahead
+                        if (!wait_bar(c, bar(base, B_P_FULL), g & 1u, false)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const int ds = (int)(g % kDhStages);
-                        const uint32_t dh = base + kOffDh + ds * kDhBytes;
-                        const uint32_t ps = base + kOffP + slot * kPSlotBytes;
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad = smem_desc_sw64(ps + (kk >> 1) * kPHalf + (kk & 1) * 32u, 512u);
-                            const uint64_t bd = smem_desc_sw128(dh + kk * 2048u, kDhBlock, 1024u);
-                            mma_ss(tmem + kColO, ad, bd, idesc_pv, (j == 0 && kk == 0) ? 0u : 1u);
+                        const int nvalid = min(kTile, w.t1 - t);
+                        const uint32_t ps = base + kOffP;
+                        for (int e = 1; e >= 0; --e) {  // peer page, then own page
+                            const int p = e == 0 ? (int)rank : (int)peer;
+                            const uint32_t n = 2 * g + e;
+                            const int ds = (int)(n % kDhSlots);
+                            const int ksteps = min(4, max(0, (nvalid - kPageRows * p + 15) / 16));
+                            if (ksteps > 0 && !wait_bar(c, bar(base, B_DH_FULL + ds), (n / kDhSlots) & 1u, false)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t dh = base + kOffDh + ds * kDhBytes;
+                            for (int kk = 0; kk < ksteps; ++kk) {
+                                const uint64_t ad = smem_desc_sw128(ps + p * kPPage + kk * 32u, 16u, 1024u);
+                                const uint64_t bd = smem_desc_sw128(dh + kk * 2048u, kBox, 1024u);
+                                mma_ss(tmem + kColO, ad, bd, idesc_pv, first ? 0u : 1u);
+                                first = false;
+                            }
+                            mma_commit(bar(base, B_DH_EMPTY + ds));
                         }
-                        mma_commit(bar(base, B_DH_EMPTY + ds));
-                        mma_commit_multicast(bar(base, B_PFREE + slot), (uint16_t)3);
-                        if (j == ntiles - 1) mma_commit(bar(base, B_O_FINAL));
+                        if (!ok) break;
+                        mma_commit_multicast(bar(base, B_PFREE), (uint16_t)3);
+                        if (t + kTile >= w.t1) mma_commit(bar(base, B_O_FINAL));
                     }
                 }
             }
-            if (!ok) {
-                const long long t0 = (long long)clock64_now();
-                while ((long long)clock64_now() - t0 < 20000000LL) {
-                }
-            }
+            if (!ok) drain_pause();
         }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
@@ -357,18 +472,56 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
         const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
         const uint32_t peer_p = mapa(base + kOffP, peer);
         const float sc = a.scale_log2;  // > 0, checked on the host
-        uint32_t g = 0, nitem = 0;
-        bool ok = true;
-        struct Pending {
-            uint32_t g;
-            int j, nvalid;
-            float rown, lown;
+        uint8_t *ps = gbase + kOffP;
+        // Query of request bq: 384 columns into TMEM (own latent half, RoPE, the other
+        // half's first 64), 192 into shared memory (the other half's last 192); three
+        // batches of 24 independent 16-byte loads per thread.
+        auto load_q = [&](int bq) {
+            const uint4 *qn = reinterpret_cast<const uint4 *>(a.q_nope + ((int64_t)bq * a.H + h) * kDLatent);
+            const uint4 *qr = reinterpret_cast<const uint4 *>(a.q_rope + ((int64_t)bq * a.H + h) * kDRope);
+            for (int batch = 0; batch < 3; ++batch) {
+                uint4 x[24];
+#pragma unroll
+                for (int i = 0; i < 24; ++i) {
+                    // block 0-3: own half, 4: RoPE, 5: other half 0-63, 6-8: other half 64-255
+                    const int blk = 3 * batch + i / 8;
+                    const uint4 *src = blk < 4 ? qn + (256 * rank + 64 * blk) / 8
+                                       : blk == 4 ? qr
+                                                  : qn + (256 * peer + 64 * (blk - 5)) / 8;
+                    x[i] = h < a.H ? src[i % 8] : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int j = 0; j < 3; ++j) {
+                    const int blk = 3 * batch + j;
+                    if (blk < 6) {
+                        uint32_t v[32];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            v[4 * q] = x[8 * j + q].x;
+                            v[4 * q + 1] = x[8 * j + q].y;
+                            v[4 * q + 2] = x[8 * j + q].z;
+                            v[4 * q + 3] = x[8 * j + q].w;
+                        }
+                        tmem_st32(trow + kColQ + 32u * blk, v);
+                    } else {
+                        uint8_t *row = gbase + kOffQs + (blk - 6) * kQsBox + h * 128;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4 *>(row + ((q ^ (h & 7)) * 16)) = x[8 * j + q];
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(base, B_Q_READY));
         };
+        uint32_t g = 0, nitem = 0;
+        bool ok = true, q_ready = false;  // q_ready: the current item's query is in place
         for (int u = cl; u < units && ok; u += ncl) {
             for (int it = unit_begin[u]; it < unit_begin[u + 1] && ok; ++it) {
                 const WorkItem w = items[it];
                 const int b = w.b;
-                const int ntiles = (w.t1 - w.t0 + kTileTokens - 1) / kTileTokens;
                 float *orow;
                 float *lrow;
                 if (w.slot < 0) {
@@ -378,7 +531,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
                     orow = part_o + ((int64_t)w.slot * a.H + h) * kDLatent + rank * 256;
                     lrow = part_lse + (int64_t)w.slot * a.H + h;
                 }
-                if (ntiles <= 0) {
+                if (w.t1 <= w.t0) {
                     if (h < a.H) {
                         for (int q = 0; q < 64; ++q)
                             reinterpret_cast<float4 *>(orow)[q] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -386,213 +539,172 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
                     }
                     continue;
                 }
-                // ---- query of this request: 448 columns into TMEM, 128 into shared memory
-                {
-                    const uint16_t *qn = a.q_nope + ((int64_t)b * a.H + h) * kDLatent;
-                    const uint16_t *qr = a.q_rope + ((int64_t)b * a.H + h) * kDRope;
-                    for (int cb = 0; cb < 7; ++cb) {
-                        const uint16_t *src = cb < 4   ? qn + 256 * rank + 64 * cb
-                                              : cb == 4 ? qr
-                                                        : qn + 256 * peer + 64 * (cb - 5);
-                        uint32_t v[32];
-                        for (int q = 0; q < 8; ++q) {
-                            uint4 x = make_uint4(0u, 0u, 0u, 0u);
-                            if (h < a.H) x = reinterpret_cast<const uint4 *>(src)[q];
-                            v[4 * q] = x.x;
-                            v[4 * q + 1] = x.y;
-                            v[4 * q + 2] = x.z;
-                            v[4 * q + 3] = x.w;
-                        }
-                        tmem_st32(trow + kColQ + 32u * cb, v);
-                    }
-                    for (int bx = 0; bx < 2; ++bx) {
-                        const uint4 *src = reinterpret_cast<const uint4 *>(qn + 256 * peer + 128 + 64 * bx);
-                        uint8_t *row = gbase + kOffQs + bx * kQsBox + h * 128;
-                        for (int q = 0; q < 8; ++q) {
-                            uint4 x = make_uint4(0u, 0u, 0u, 0u);
-                            if (h < a.H) x = src[q];
-                            *reinterpret_cast<uint4 *>(row + ((q ^ (h & 7)) * 16)) = x;
-                        }
-                    }
-                    fence_proxy_async_smem();
-                    tmem_wait_st();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(base, B_Q_READY));
+                if (!q_ready) load_q(b);
+                q_ready = false;
+                // the next item's query is loaded at the end of this one: bring it into L2 now
+                const int bnext = next_request(unit_begin, items, units, ncl, u, it);
+                if (bnext >= 0 && threadIdx.x == 0) {
+                    prefetch_l2(a.q_nope + (int64_t)bnext * a.H * kDLatent, (uint32_t)(a.H * kDLatent * 2));
+                    prefetch_l2(a.q_rope + (int64_t)bnext * a.H * kDRope, (uint32_t)(a.H * kDRope * 2));
                 }
                 float m = -INFINITY, l = 0.f;
-                Pending pend{0u, -1, 0, 0.f, 0.f};
-                for (int j = 0; j < ntiles && ok; ++j) {
-                    Pending cur{g, j, 0, 0.f, 0.f};
-                    if (j < ntiles) {
-                        // ================= part A of tile j
-                        const int t = w.t0 + kTileTokens * j;
-                        const int ds = (int)(g % kDhStages);
-                        const uint32_t dph = (g / kDhStages) & 1u;
-                        const int slot = (int)(g % kPSlots);
-                        const uint32_t su = g / kPSlots;
-                        if (!warp_wait(c, bar(base, B_S_FULL), g & 1u, false) ||
-                            !warp_wait(c, bar(base, B_DH_FULL + ds), dph, false)) {
+                for (int t = w.t0, j = 0; t < w.t1; t += kTile, ++j, ++g) {
+                    // ================= part A: own page's scores -> weights -> message
+                    const int nvalid = min(kTile, w.t1 - t);
+                    const PageRef pg0 = page_of(a, w, t, 0), pg1 = page_of(a, w, t, 1);  // read early
+                    const int nown = rank == 0 ? (pg0.id >= 0 ? pg0.rows : 0) : (pg1.id >= 0 ? pg1.rows : 0);
+                    if (!warp_wait(c, bar(base, B_S_FULL), g & 1u, false)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    float s[64];
+                    {
+                        uint32_t sr[64];
+                        tmem_ld32(trow + kColS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+                        tmem_ld32(trow + kColS + 32u, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(sr[i]);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(base, B_S_FREE));
+                    if (nown < 64) {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i)
+                            if (i >= nown) s[i] = -INFINITY;
+                    }
+                    float mraw = s[0];
+#pragma unroll
+                    for (int i = 1; i < 64; ++i) mraw = fmaxf(mraw, s[i]);
+                    const float mloc = mraw * sc;
+                    // reference: the running maximum; any value works as long as both CTAs
+                    // use the one they send
+                    const float rown = mloc > m + kRescaleLog2 ? mloc : m;
+                    const float nr = rown == -INFINITY ? 0.f : -rown;
+                    uint32_t pk[32];
+                    float lown = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float p0 = ex2_approx(fmaf(s[2 * i], sc, nr));
+                        const float p1 = ex2_approx(fmaf(s[2 * i + 1], sc, nr));
+                        lown += p0 + p1;
+                        pk[i] = pack_bf16(p0, p1);
+                    }
+                    // the tile is reused: both CTAs' PV of the previous tile must be done
+                    if (g > 0 && !warp_wait(c, bar(base, B_PFREE), (g - 1) & 1u, true)) {
+                        ok = false;
+                        break;
+                    }
+                    {
+                        uint8_t *prow = ps + rank * kPPage + h * 128;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            *reinterpret_cast<uint4 *>(prow + ((q ^ (h & 7)) * 16)) =
+                                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                        float *rl = reinterpret_cast<float *>(ps + 2 * kPPage + rank * kRlBytes);
+                        rl[h] = rown;
+                        rl[128 + h] = lown;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    const uint32_t rfull = bar(base, B_RFULL);
+                    if (threadIdx.x == 0) mbar_arrive_expect_tx(rfull, kMsgBytes);
+                    if (lane == 0) {
+                        const uint32_t rb = mapa(rfull, peer);
+                        const uint32_t prows = kOffP + rank * kPPage + warp * 32 * 128;
+                        const uint32_t rls = kOffP + 2 * kPPage + rank * kRlBytes + warp * 32 * 4;
+                        bulk_copy_s2peer(peer_p - kOffP + prows, base + prows, 32 * 128, rb);
+                        bulk_copy_s2peer(peer_p - kOffP + rls, base + rls, 32 * 4, rb);
+                        bulk_copy_s2peer(peer_p - kOffP + rls + 512, base + rls + 512, 32 * 4, rb);
+                        bulk_commit();
+                    }
+                    // ================= part B: merge with the peer's message
+                    if (!warp_wait(c, rfull, g & 1u, true)) {
+                        ok = false;
+                        break;
+                    }
+                    const float *rlp = reinterpret_cast<const float *>(ps + 2 * kPPage + peer * kRlBytes);
+                    const float rpeer = rlp[h], lpeer = rlp[128 + h];
+                    const float r0 = rank == 0 ? rown : rpeer, r1 = rank == 0 ? rpeer : rown;
+                    const float l0 = rank == 0 ? lown : lpeer, l1 = rank == 0 ? lpeer : lown;
+                    const float mn = fmaxf(m, fmaxf(r0, r1));
+                    float f0 = 1.f, f1 = 1.f, alpha = 1.f;
+                    if (mn != -INFINITY) {
+                        f0 = ex2_approx(r0 - mn);
+                        f1 = ex2_approx(r1 - mn);
+                        alpha = ex2_approx(m - mn);
+                        l = l * alpha + l0 * f0 + l1 * f1;
+                    }
+                    const bool resc_o = j > 0 && mn > m;
+                    m = mn;
+                    // a page whose reference lies below the new maximum is rescaled in place
+                    // (this CTA's own rows only after the warp's bulk copies have read them)
+                    const float fown = rank == 0 ? f0 : f1, fpeer = rank == 0 ? f1 : f0;
+                    bool wrote = false;
+                    if (__any_sync(0xffffffffu, fown < 1.f)) {
+                        if (lane == 0) bulk_wait_read_all();
+                        __syncwarp();
+                        if (fown < 1.f) scale_row(reinterpret_cast<uint4 *>(ps + rank * kPPage + h * 128), fown);
+                        wrote = true;
+                    }
+                    if (fpeer < 1.f) {
+                        scale_row(reinterpret_cast<uint4 *>(ps + peer * kPPage + h * 128), fpeer);
+                        wrote = true;
+                    }
+                    // cache rows that PV reads but must not contribute (the rows of the last
+                    // 16-row step past the end; a page whose id was out of range) must hold
+                    // zeros there, not whatever the page holds
+                    for (int p = 0; p < 2; ++p) {
+                        const PageRef pr = p == 0 ? pg0 : pg1;
+                        const int z0 = pr.id >= 0 ? pr.rows : 0, z1 = min(kPageRows, (pr.rows + 15) & ~15);
+                        if (z1 <= z0) continue;
+                        const uint32_t n = 2 * g + (p == (int)rank ? 0u : 1u);
+                        const int ds = (int)(n % kDhSlots);
+                        // wait for the slot's load (or its empty arrival) to land first
+                        if (!warp_wait(c, bar(base, B_DH_FULL + ds), (n / kDhSlots) & 1u, false)) {
                             ok = false;
                             break;
                         }
+                        const int nz = (z1 - z0) * 32;  // 16-B chunks over 4 boxes
+                        uint8_t *dh = gbase + kOffDh + ds * kDhBytes;
+                        for (int i = h; i < nz; i += 128) {
+                            const int row = z0 + i / 32, ch = i % 32;
+                            *reinterpret_cast<uint4 *>(dh + (ch / 8) * kBox + row * 128 + (ch % 8) * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        wrote = true;
+                    }
+                    if (!ok) break;
+                    if (__any_sync(0xffffffffu, wrote)) fence_proxy_async_smem();
+                    // O rescale: the previous tile's PV is done (waited above before the
+                    // probability tile was rewritten)
+                    if (__any_sync(0xffffffffu, resc_o)) {
                         tc_fence_after();
-                        float s[32];
-                        {
-                            uint32_t sr[32];
-                            tmem_ld32(trow + kColS, sr);
+                        const float al = resc_o ? alpha : 1.f;
+                        for (int cb = 0; cb < 256; cb += 32) {
+                            uint32_t o[32];
+                            tmem_ld32(trow + kColO + cb, o);
                             tmem_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(sr[i]);
+                            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * al);
+                            tmem_st32(trow + kColO + cb, o);
                         }
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bar(base, B_S_FREE));
-                        const bool bad = misc[2 + ds] != 0u;
-                        const int nvalid = bad ? 0 : min(kTileTokens, w.t1 - t);  // page rows attended
-                        const int nown = max(0, min(32, nvalid - 32 * (int)rank));
-                        if (nown < 32) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                if (i >= nown) s[i] = -INFINITY;
-                        }
-                        float mraw = s[0];
-#pragma unroll
-                        for (int i = 1; i < 32; ++i) mraw = fmaxf(mraw, s[i]);
-                        const float mloc = mraw * sc;
-                        // reference: the running maximum (known after part B of tile j-1 only
-                        // for the tiles before it; any value works as long as both CTAs send
-                        // the one they used)
-                        const float mk = m;
-                        const float rown = mloc > mk + kRescaleLog2 ? mloc : mk;
-                        const float nr = rown == -INFINITY ? 0.f : -rown;
-                        uint32_t pk[16];
-                        float lown = 0.f;
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float p0 = ex2_approx(fmaf(s[2 * i], sc, nr));
-                            const float p1 = ex2_approx(fmaf(s[2 * i + 1], sc, nr));
-                            lown += p0 + p1;
-                            pk[i] = pack_bf16(p0, p1);
-                        }
-                        // slot reuse: both CTAs' PV of tile g-3 must be done
-                        if (g >= (uint32_t)kPSlots &&
-                            !warp_wait(c, bar(base, B_PFREE + slot), (su - 1u) & 1u, true)) {
-                            ok = false;
-                            break;
-                        }
-                        uint8_t *ps = gbase + kOffP + slot * kPSlotBytes;
-                        const uint32_t poff = kOffP + slot * kPSlotBytes;
-                        {
-                            uint8_t *prow = ps + rank * kPHalf + h * 64;
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                *reinterpret_cast<uint4 *>(prow + ((q ^ ((h >> 1) & 3)) * 16)) =
-                                    make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                            float *rl = reinterpret_cast<float *>(ps + 2 * kPHalf + rank * kRlBytes);
-                            rl[h] = rown;
-                            rl[128 + h] = lown;
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        const uint32_t rfull = bar(base, B_RFULL + slot);
-                        if (threadIdx.x == 0) mbar_arrive_expect_tx(rfull, kMsgBytes);
-                        if (lane == 0) {
-                            const uint32_t rb = mapa(rfull, peer);
-                            const uint32_t prows = poff + rank * kPHalf + warp * 32 * 64;
-                            const uint32_t rls = poff + 2 * kPHalf + rank * kRlBytes + warp * 32 * 4;
-                            bulk_copy_s2peer(peer_p - kOffP + prows, base + prows, 32 * 64, rb);
-                            bulk_copy_s2peer(peer_p - kOffP + rls, base + rls, 32 * 4, rb);
-                            bulk_copy_s2peer(peer_p - kOffP + rls + 512, base + rls + 512, 32 * 4, rb);
-                            bulk_commit();
-                        }
-                        cur.nvalid = nvalid;
-                        cur.rown = rown;
-                        cur.lown = lown;
-                        ++g;
+                        tmem_wait_st();
                     }
-                    pend = cur;
-                    if (pend.j >= 0) {
-                        // ================= part B of tile pend.j (merge, then PV may start)
-                        const uint32_t gp = pend.g;
-                        const int ds = (int)(gp % kDhStages);
-                        const int slot = (int)(gp % kPSlots);
-                        const uint32_t su = gp / kPSlots;
-                        const uint32_t rfull = bar(base, B_RFULL + slot);
-                        if (!warp_wait(c, rfull, su & 1u, true)) {
-                            ok = false;
-                            break;
-                        }
-                        uint8_t *ps = gbase + kOffP + slot * kPSlotBytes;
-                        const float *rlp = reinterpret_cast<const float *>(ps + 2 * kPHalf + peer * kRlBytes);
-                        const float rpeer = rlp[h], lpeer = rlp[128 + h];
-                        const float r0 = rank == 0 ? pend.rown : rpeer, r1 = rank == 0 ? rpeer : pend.rown;
-                        const float l0 = rank == 0 ? pend.lown : lpeer, l1 = rank == 0 ? lpeer : pend.lown;
-                        const float mn = fmaxf(m, fmaxf(r0, r1));
-                        float f0 = 1.f, f1 = 1.f, alpha = 1.f;
-                        if (mn != -INFINITY) {
-                            f0 = ex2_approx(r0 - mn);
-                            f1 = ex2_approx(r1 - mn);
-                            alpha = ex2_approx(m - mn);
-                            l = l * alpha + l0 * f0 + l1 * f1;
-                        }
-                        const bool resc_o = pend.j > 0 && mn > m;
-                        m = mn;
-                        // a half whose reference lies below the new maximum is rescaled in
-                        // place (this CTA's own rows only after the warp's bulk copies have
-                        // read them)
-                        const float fown = rank == 0 ? f0 : f1, fpeer = rank == 0 ? f1 : f0;
-                        bool wrote = false;
-                        if (__any_sync(0xffffffffu, fown < 1.f)) {
-                            if (lane == 0) bulk_wait_read_all();
-                            __syncwarp();
-                            if (fown < 1.f) scale_row16(reinterpret_cast<uint4 *>(ps + rank * kPHalf + h * 64), fown);
-                            wrote = true;
-                        }
-                        if (fpeer < 1.f) {
-                            scale_row16(reinterpret_cast<uint4 *>(ps + peer * kPHalf + h * 64), fpeer);
-                            wrote = true;
-                        }
-                        // cache rows this tile must not contribute (page tail, missing page):
-                        // the PV operand must hold zeros there, not whatever the page holds
-                        if (pend.nvalid < kTileTokens) {
-                            const uint32_t dh = kOffDh + ds * kDhBytes;
-                            const int nz = (kTileTokens - pend.nvalid) * 32;  // 16-B chunks in 4 blocks
-                            for (int i = h; i < nz; i += 128) {
-                                const int row = pend.nvalid + i / 32, ch = i % 32;
-                                *reinterpret_cast<uint4 *>(gbase + dh + (ch / 8) * kDhBlock + row * 128 + (ch % 8) * 16) =
-                                    make_uint4(0u, 0u, 0u, 0u);
-                            }
-                            wrote = true;
-                        }
-                        if (__any_sync(0xffffffffu, wrote)) fence_proxy_async_smem();
-                        // O rescale: PV of the previous tile must have finished.  Its slot's
-                        // barrier completes when both CTAs' PV of that tile are done and cannot
-                        // complete again before this tile's PV, so its parity is unambiguous.
-                        if (__any_sync(0xffffffffu, resc_o)) {
-                            const uint32_t gq = gp - 1u;
-                            if (!warp_wait(c, bar(base, B_PFREE + (int)(gq % kPSlots)), (gq / kPSlots) & 1u, true)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            const float al = resc_o ? alpha : 1.f;
-                            for (int cb = 0; cb < 256; cb += 32) {
-                                uint32_t o[32];
-                                tmem_ld32(trow + kColO + cb, o);
-                                tmem_wait_ld();
-#pragma unroll
-                                for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * al);
-                                tmem_st32(trow + kColO + cb, o);
-                            }
-                            tmem_wait_st();
-                        }
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bar(base, B_P_FULL + slot));
-                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(base, B_P_FULL));
                 }
                 if (!ok) break;
+                // ---- the next item's query: this item's QK^T is complete (its last S was
+                // read), so the query columns are free; loading now lets the next item's
+                // QK^T overlap this item's last PV and epilogue
+                if (bnext >= 0) {
+                    load_q(bnext);
+                    q_ready = true;
+                }
                 // ---- epilogue: wait for the last PV of this item, normalise, store
                 if (!warp_wait(c, bar(base, B_O_FINAL), nitem & 1u, false)) {
                     ok = false;
@@ -690,7 +802,7 @@ cudaError_t launch_decode_sm103(const DecodeArgs &a, int num_clusters, cudaStrea
     CUtensorMap tmap;
     const cuuint64_t dims[2] = {(cuuint64_t)kDEntry, (cuuint64_t)a.num_pages * kPageRows};
     const cuuint64_t strides[1] = {(cuuint64_t)kDEntry * 2};
-    const cuuint32_t box[2] = {64, 32};
+    const cuuint32_t box[2] = {64, kPageRows};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<unsigned char *>(a.cache),
                      dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
