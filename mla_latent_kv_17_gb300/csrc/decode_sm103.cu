@@ -48,7 +48,7 @@ namespace {
 using namespace ptx;
 
 constexpr int kTile = 2 * kPageRows;             // tokens per tile
-constexpr int kDhSlots = 3;                      // own-half latent of one page (until PV)
+constexpr int kDhSlots = 3;                      // own-half latent of one page (until PV); see dh_slot
 constexpr int kOthBoxes = 5;                     // other latent half (4 boxes) + RoPE, one stage
 constexpr uint32_t kBox = 64 * 128;              // 64 rows x 64 bf16, 128-B swizzle
 constexpr uint32_t kDhBytes = 4 * kBox;          // one page, 256 latent columns
@@ -167,6 +167,22 @@ __device__ __forceinline__ PageRef page_of(const DecodeArgs &a, const WorkItem &
     return r;
 }
 
+// Latent-half slots.  Tile g's own page (e = 0) sits in slot g % 3 and its peer page (e = 1)
+// in slot (g + 2) % 3; the loader issues own(0), own(1), then peer(g), own(g + 2) for
+// g = 0, 1, ...  PV of tile g hands back the peer page's slot first, and own(g + 2) — the
+// page the scores need soonest — takes exactly that slot, ahead of peer(g + 1), which takes
+// own(g)'s.  Each slot alternates own and peer pages; `fill` counts the slot's loads before
+// this one (its full barrier's phase).
+struct DhSlot {
+    int slot;
+    uint32_t fill;
+};
+__device__ __forceinline__ DhSlot dh_slot(uint32_t g, int e) {
+    const uint32_t q = g / 3u, r = g % 3u;
+    if (e == 0) return DhSlot{(int)r, 2u * q + (r == 2u ? 1u : 0u)};
+    return DhSlot{(int)((r + 2u) % 3u), 2u * q + (r != 0u ? 1u : 0u)};
+}
+
 // Walks the tiles of this cluster's work in order: units cl, cl + ncl, ..., their items
 // (those with tokens), and each item's 128-token tiles.
 struct TileCursor {
@@ -276,8 +292,6 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
     const int units = hd->num_units;
     const int cl = (int)cluster_id_x(), ncl = (int)nclusters_x();
 
-    // Latent-half slots are taken in the order (own page of tile g, peer page of tile g):
-    // sequence number 2g + 0 / 2g + 1, slot n % kDhSlots.
     if (warp == 4 || warp == 7) {
         // ------------------------------------------------------------ TMA producers
         if (lane == 0) {
@@ -286,43 +300,38 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
             nx = cur;
             nx.next();
             if (warp == 4) {
-                // own latent half of both pages
+                // own latent half of both pages, in the order own(0), own(1), peer(0), own(2),
+                // peer(1), own(3), ...
                 const int xown = 256 * (int)rank;
-                PageRef pr0{0, -1}, pr1{0, -1};
-                if (!cur.done()) {
-                    pr0 = page_of(a, cur.w, cur.t, (int)rank);
-                    pr1 = page_of(a, cur.w, cur.t, (int)peer);
-                }
+                // loads page (rank if e == 0, else peer) of tile g at cursor position t
+                auto load = [&](const TileCursor &t, uint32_t g, int e) -> bool {
+                    const PageRef pg = page_of(a, t.w, t.t, e == 0 ? (int)rank : (int)peer);  // read before the wait
+                    const DhSlot d = dh_slot(g, e);
+                    if (d.fill > 0 && !wait_bar(c, bar(base, B_DH_EMPTY + d.slot), (d.fill - 1u) & 1u, false))
+                        return false;
+                    const uint32_t fb = bar(base, B_DH_FULL + d.slot);
+                    if (pg.rows > 0 && pg.id >= 0) {
+                        const int32_t y = (int32_t)(pg.id * kPageRows);
+                        const uint32_t dst = base + kOffDh + d.slot * kDhBytes;
+                        mbar_arrive_expect_tx(fb, kDhBytes);
+                        for (int i = 0; i < 4; ++i) tma_load_2d(dst + i * kBox, &tmap, xown + 64 * i, y, fb);
+                    } else {
+                        if (pg.rows > 0) record_error(a.status, MLA_ERR_INDEX);
+                        mbar_arrive(fb);
+                    }
+                    return true;
+                };
+                TileCursor co = cur;  // next own page: tile go
+                uint32_t go = 0, gp = 0;
                 bool ok = true;
-                for (uint32_t g = 0; !cur.done() && ok; ++g) {
-                    PageRef np0{0, -1}, np1{0, -1};  // next tile's pages, read ahead of the waits
-                    if (!nx.done()) {
-                        np0 = page_of(a, nx.w, nx.t, (int)rank);
-                        np1 = page_of(a, nx.w, nx.t, (int)peer);
+                for (; go < 2 && !co.done() && ok; ++go, co.next()) ok = load(co, go, 0);
+                for (; !cur.done() && ok; ++gp, cur.next()) {  // cur: next peer page, tile gp
+                    ok = load(cur, gp, 1);
+                    if (ok && !co.done()) {
+                        ok = load(co, go, 0);
+                        ++go;
+                        co.next();
                     }
-                    for (int e = 0; e < 2; ++e) {
-                        const uint32_t n = 2 * g + e;
-                        const int ds = (int)(n % kDhSlots);
-                        if (!wait_bar(c, bar(base, B_DH_EMPTY + ds), ((n / kDhSlots) & 1u) ^ 1u, false)) {
-                            ok = false;
-                            break;
-                        }
-                        const PageRef pg = e == 0 ? pr0 : pr1;
-                        const uint32_t fb = bar(base, B_DH_FULL + ds);
-                        if (pg.rows > 0 && pg.id >= 0) {
-                            const int32_t y = (int32_t)(pg.id * kPageRows);
-                            const uint32_t dst = base + kOffDh + ds * kDhBytes;
-                            mbar_arrive_expect_tx(fb, kDhBytes);
-                            for (int i = 0; i < 4; ++i) tma_load_2d(dst + i * kBox, &tmap, xown + 64 * i, y, fb);
-                        } else {
-                            if (pg.rows > 0) record_error(a.status, MLA_ERR_INDEX);
-                            mbar_arrive(fb);
-                        }
-                    }
-                    pr0 = np0;
-                    pr1 = np1;
-                    cur = nx;
-                    nx.next();
                 }
                 if (!ok) drain_pause();
             } else {
@@ -398,9 +407,9 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
                             }
                         }
                         mma_commit(bar(base, B_OTH_EMPTY));
-                        const uint32_t n = 2 * g;
-                        const int ds = (int)(n % kDhSlots);
-                        if (!wait_bar(c, bar(base, B_DH_FULL + ds), (n / kDhSlots) & 1u, false)) {
+                        const DhSlot dso = dh_slot(g, 0);
+                        const int ds = dso.slot;
+                        if (!wait_bar(c, bar(base, B_DH_FULL + ds), dso.fill & 1u, false)) {
                             ok = false;
                             break;
                         }
@@ -439,10 +448,10 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
                         const uint32_t ps = base + kOffP;
                         for (int e = 1; e >= 0; --e) {  // peer page, then own page
                             const int p = e == 0 ? (int)rank : (int)peer;
-                            const uint32_t n = 2 * g + e;
-                            const int ds = (int)(n % kDhSlots);
+                            const DhSlot d = dh_slot(g, e);
+                            const int ds = d.slot;
                             const int ksteps = min(4, max(0, (nvalid - kPageRows * p + 15) / 16));
-                            if (ksteps > 0 && !wait_bar(c, bar(base, B_DH_FULL + ds), (n / kDhSlots) & 1u, false)) {
+                            if (ksteps > 0 && !wait_bar(c, bar(base, B_DH_FULL + ds), d.fill & 1u, false)) {
                                 ok = false;
                                 break;
                             }
@@ -660,10 +669,10 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
                         const PageRef pr = p == 0 ? pg0 : pg1;
                         const int z0 = pr.id >= 0 ? pr.rows : 0, z1 = min(kPageRows, (pr.rows + 15) & ~15);
                         if (z1 <= z0) continue;
-                        const uint32_t n = 2 * g + (p == (int)rank ? 0u : 1u);
-                        const int ds = (int)(n % kDhSlots);
+                        const DhSlot d = dh_slot(g, p == (int)rank ? 0 : 1);
+                        const int ds = d.slot;
                         // wait for the slot's load (or its empty arrival) to land first
-                        if (!warp_wait(c, bar(base, B_DH_FULL + ds), (n / kDhSlots) & 1u, false)) {
+                        if (!warp_wait(c, bar(base, B_DH_FULL + ds), d.fill & 1u, false)) {
                             ok = false;
                             break;
                         }
