@@ -14,29 +14,42 @@ namespace {
 // ---------------------------------------------------------------------------------
 // Device planner: one CTA.  Each thread owns a contiguous slice of requests; block-wide
 // exclusive scans give every request its budget position, item offset and first partial
-// slot, then each thread writes its requests' pieces.  Same functions as the host twin.
+// slot, then each thread writes its requests' pieces, and one pass over the items marks
+// where each unit's items begin.  Same per-request functions as the host twin, so the
+// two produce identical plans.
 // ---------------------------------------------------------------------------------
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 256;
+constexpr int kPlanWarps = kPlanThreads / 32;
 
+// Exclusive prefix sum of v over the block (shuffles within each warp, then one warp over
+// the warp totals); *total receives the sum over the block.  sh holds kPlanWarps values.
 __device__ int64_t block_exclusive_scan(int64_t v, int64_t *total, int64_t *sh) {
-    const int t = threadIdx.x;
-    sh[t] = v;
-    __syncthreads();
-    for (int off = 1; off < kPlanThreads; off <<= 1) {
-        int64_t x = t >= off ? sh[t - off] : 0;
-        __syncthreads();
-        sh[t] += x;
-        __syncthreads();
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int64_t x = v;
+    for (int off = 1; off < 32; off <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
     }
-    const int64_t incl = sh[t];
-    *total = sh[kPlanThreads - 1];
+    if (lane == 31) sh[wid] = x;
     __syncthreads();
-    return incl - v;
+    if (wid == 0) {
+        int64_t t = lane < kPlanWarps ? sh[lane] : 0;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, t, off);
+            if (lane >= off) t += y;
+        }
+        if (lane < kPlanWarps) sh[lane] = t;
+    }
+    __syncthreads();
+    const int64_t r = (wid > 0 ? sh[wid - 1] : 0) + x - v;
+    *total = sh[kPlanWarps - 1];
+    __syncthreads();  // sh is reused by the next scan
+    return r;
 }
 
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int units, unsigned char *ws) {
-    __shared__ int64_t sh[kPlanThreads];
+    __shared__ int64_t sh[kPlanWarps];
     const WsLayout L = ws_layout(B, H, units);
     int64_t *req_start = reinterpret_cast<int64_t *>(ws + L.req_start);
     int32_t *num_splits = reinterpret_cast<int32_t *>(ws + L.num_splits);
@@ -74,12 +87,19 @@ plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int units, unsigned
         off += r.n;
         if (r.n > 1) slot += r.n;
     }
-    __syncthreads();
+    __syncthreads();  // item_unit is complete (global writes of this block are now visible)
+    // unit_begin[u] = first item whose unit is >= u (items are grouped by unit in order):
+    // item i starts the units (unit of item i-1, unit of item i]
+    const int32_t n = (int32_t)n_total;
+    for (int32_t i = threadIdx.x; i < n; i += kPlanThreads) {
+        const int32_t uc = item_unit[i], up = i == 0 ? -1 : item_unit[i - 1];
+        for (int32_t u = up + 1; u <= uc; ++u) unit_begin[u] = i;
+    }
+    const int32_t last = n > 0 ? item_unit[n - 1] : -1;
     for (int u = threadIdx.x; u <= units; u += kPlanThreads)
-        unit_begin[u] = u == units ? (int32_t)n_total
-                                   : lower_bound_unit(item_unit, (int32_t)n_total, u);
+        if (u > last) unit_begin[u] = n;
     if (threadIdx.x == 0) {
-        write_header(ws, L, B, H, topk, units, (int32_t)n_total, per, (int32_t)s_total);
+        write_header(ws, L, B, H, topk, units, n, per, (int32_t)s_total);
         *reinterpret_cast<int *>(ws + L.status) = 0;
     }
 }

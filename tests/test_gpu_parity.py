@@ -81,16 +81,31 @@ def test_dense_split_kv_and_combine(num_sms):
     assert_close(out, lse, ref_out, ref_lse, f"split num_sms={num_sms}")
 
 
-def test_device_plan_equals_host_plan():
-    sl = inputs.workload_seq_lens("dsv3_dense_b64_h128_l1k_8k")
-    ws = ops.Workspace(64, 128)
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    ops.plan(ws, sl.cuda(), num_sms=sms)
+def _plan_cases():
+    rng = np.random.default_rng(5)
+    cases = [(name, inputs.workload_seq_lens(name).numpy(), 2048 if "sparse" in name else 0)
+             for name in inputs.WORKLOADS]
+    cases += [("zeros", np.zeros(3, np.int32), 0), ("edges", np.array([1, 63, 64, 65, 0, 128, 129], np.int32), 0),
+              ("many_short", np.full(300, 5, np.int32), 0),
+              ("b700", rng.integers(0, 9000, size=700).astype(np.int32), 0)]
+    return cases
+
+
+@pytest.mark.parametrize("num_sms", [None, 16])
+@pytest.mark.parametrize("case", _plan_cases(), ids=lambda c: c[0])
+def test_device_plan_equals_host_plan(case, num_sms):
+    _, sl, topk = case
+    B = len(sl)
+    sms = num_sms or torch.cuda.get_device_properties(0).multi_processor_count
+    ws = ops.Workspace(B, 128)
+    ops.plan(ws, None if topk else torch.from_numpy(sl).cuda(), topk=topk, num_sms=sms)
     torch.cuda.synchronize()
     dev = ws.buf.cpu().numpy()
-    host = ops.plan_host(sl.numpy(), 64, 128, 0, sms)
-    end = parse(host, 64, 128)["plan_end"]
-    assert np.array_equal(dev[:128], host[:128]) and np.array_equal(dev[256:end], host[256:end])
+    host = ops.plan_host(None if topk else sl, B, 128, topk, sms)
+    assert np.array_equal(dev[:64], host[:64])  # header
+    d, h = parse(dev, B, 128), parse(host, B, 128)
+    for key in ("unit_begin", "items", "num_splits", "split_base", "req_start", "item_unit"):
+        assert np.array_equal(d[key], h[key]), key
 
 
 def test_large_query_scale_is_stable():
