@@ -721,17 +721,32 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
                 }
                 tc_fence_after();
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-                for (int cb = 0; cb < 256; cb += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(trow + kColO + cb, o);
-                    tmem_wait_ld();
-                    if (h < a.H) {
-                        float4 *dst = reinterpret_cast<float4 *>(orow + cb);
+                // Each 32-column slice goes through this CTA's own probability rows (free
+                // until the next tile's weights; the peer never writes them) so that every
+                // warp store covers whole 128-B lines: thread h holds row h, but rows are
+                // 2 KB apart in the output.  Warp w writes back its own rows 32w..32w+31.
+                {
+                    uint8_t *stg = ps + rank * kPPage;
+                    float *obase = orow - (int64_t)h * kDLatent;  // row 0 of this item's output
+                    if (lane == 0) bulk_wait_read_all();  // this warp's last message has left these rows
+                    __syncwarp();
+                    for (int cb = 0; cb < 256; cb += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(trow + kColO + cb, o);
+                        tmem_wait_ld();
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
-                            dst[q] = make_float4(__uint_as_float(o[4 * q]) * inv, __uint_as_float(o[4 * q + 1]) * inv,
-                                                 __uint_as_float(o[4 * q + 2]) * inv,
-                                                 __uint_as_float(o[4 * q + 3]) * inv);
+                            *reinterpret_cast<float4 *>(stg + h * 128 + ((q ^ (h & 7)) * 16)) =
+                                make_float4(__uint_as_float(o[4 * q]) * inv, __uint_as_float(o[4 * q + 1]) * inv,
+                                            __uint_as_float(o[4 * q + 2]) * inv, __uint_as_float(o[4 * q + 3]) * inv);
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int row = warp * 32 + 4 * i + (lane >> 3), q = lane & 7;
+                            const float4 v = *reinterpret_cast<const float4 *>(stg + row * 128 + ((q ^ (row & 7)) * 16));
+                            if (row < a.H) *reinterpret_cast<float4 *>(obase + (int64_t)row * kDLatent + cb + 4 * q) = v;
+                        }
+                        __syncwarp();
                     }
                 }
                 if (rank == 0 && h < a.H) *lrow = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
