@@ -107,47 +107,58 @@ plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int units, unsigned
 // ---------------------------------------------------------------------------------
 // Merge of split-KV partial results through their log-sum-exp:
 //   lse = ln sum_i exp(lse_i),  out = sum_i exp(lse_i - lse) * out_i.
-// One CTA per (request, head); requests with a single piece were written directly.
+// One warp per (request, head), kCombineHeads heads per CTA; a lane covers 16 of the 512
+// columns, so every load and store of a warp spans 512 contiguous bytes.  Requests with
+// a single piece were written directly by the decode kernel.
 // ---------------------------------------------------------------------------------
-constexpr int kCombineThreads = 128;
+constexpr int kCombineHeads = 8;
+constexpr int kCombineThreads = 32 * kCombineHeads;
 
 __global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(DecodeArgs a) {
     if (!plan_matches(a)) return;
     const unsigned char *ws = a.ws;
     const int H = a.H;
-    float *out = a.out, *lse = a.lse;
     const PlanHeader *hd = reinterpret_cast<const PlanHeader *>(ws);
     const WsLayout L = ws_layout(hd->B, hd->H, hd->num_units);
-    const int b = blockIdx.x, h = blockIdx.y;
+    const int b = blockIdx.x;
     const int32_t n = reinterpret_cast<const int32_t *>(ws + L.num_splits)[b];
     if (n <= 1) return;
+    const int h = blockIdx.y * kCombineHeads + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (h >= H) return;
     const int32_t base = reinterpret_cast<const int32_t *>(ws + L.split_base)[b];
-    const float *plse = reinterpret_cast<const float *>(ws + L.part_lse);
-    const float *po = reinterpret_cast<const float *>(ws + L.part_o);
+    const float *plse = reinterpret_cast<const float *>(ws + L.part_lse) + (int64_t)base * H + h;
+    const float *po = reinterpret_cast<const float *>(ws + L.part_o) + ((int64_t)base * H + h) * kDLatent;
     float m = -INFINITY;
-    for (int i = 0; i < n; ++i) m = fmaxf(m, plse[(int64_t)(base + i) * H + h]);
+    for (int i = lane; i < n; i += 32) m = fmaxf(m, plse[(int64_t)i * H]);
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float z = 0.f;
     if (m != -INFINITY)
-        for (int i = 0; i < n; ++i) z += exp2f((plse[(int64_t)(base + i) * H + h] - m) * kLog2e);
+        for (int i = lane; i < n; i += 32) z += exp2f((plse[(int64_t)i * H] - m) * kLog2e);
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
     const float total = m == -INFINITY ? -INFINITY : m + logf(z);
-    float4 acc[1];
-    for (int d4 = threadIdx.x; d4 < kDLatent / 4; d4 += kCombineThreads) {
-        float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (m != -INFINITY) {
-            for (int i = 0; i < n; ++i) {
-                float w = exp2f((plse[(int64_t)(base + i) * H + h] - total) * kLog2e);
-                float4 v = reinterpret_cast<const float4 *>(po + ((int64_t)(base + i) * H + h) * kDLatent)[d4];
-                r.x = fmaf(w, v.x, r.x);
-                r.y = fmaf(w, v.y, r.y);
-                r.z = fmaf(w, v.z, r.z);
-                r.w = fmaf(w, v.w, r.w);
+    float4 acc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (m != -INFINITY) {
+#pragma unroll 2
+        for (int i = 0; i < n; ++i) {
+            const float w = exp2f((plse[(int64_t)i * H] - total) * kLog2e);
+            const float4 *row = reinterpret_cast<const float4 *>(po + (int64_t)i * H * kDLatent);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float4 v = row[lane + 32 * k];
+                acc[k].x = fmaf(w, v.x, acc[k].x);
+                acc[k].y = fmaf(w, v.y, acc[k].y);
+                acc[k].z = fmaf(w, v.z, acc[k].z);
+                acc[k].w = fmaf(w, v.w, acc[k].w);
             }
         }
-        acc[0] = r;
-        reinterpret_cast<float4 *>(out + ((int64_t)b * H + h) * kDLatent)[d4] = acc[0];
     }
-    if (threadIdx.x == 0) lse[(int64_t)b * H + h] = total;
+    float4 *dst = reinterpret_cast<float4 *>(a.out + ((int64_t)b * H + h) * kDLatent);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) dst[lane + 32 * k] = acc[k];
+    if (lane == 0) a.lse[(int64_t)b * H + h] = total;
 }
 
 int device_sm_count() {
@@ -193,7 +204,7 @@ mla_status run_decode(const DecodeArgs &a, cudaStream_t stream) {
     else
         e = launch_decode_simt(a, units, stream);
     if (e != cudaSuccess) return MLA_ERR_CUDA;
-    dim3 cgrid(a.B, a.H);
+    dim3 cgrid(a.B, (a.H + kCombineHeads - 1) / kCombineHeads);
     combine_kernel<<<cgrid, kCombineThreads, 0, stream>>>(a);
     if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
     return MLA_OK;
