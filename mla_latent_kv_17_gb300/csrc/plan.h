@@ -2,8 +2,9 @@
 // host twin (mla_decode_plan_host).  The same function runs on both sides so the two
 // produce byte-identical plans.
 //
-// A request's tokens are cut into 64-token tiles (one cache page each).  The persistent
-// decode workers ("units", one per pair of SMs) each get an equal budget of tiles; the
+// A request's tokens are cut into 128-token tiles (two cache pages; the tensor-core kernel
+// works on one such tile per step, a page per SM of the pair).  The persistent decode
+// workers ("units", one per pair of SMs) each get an equal budget of tiles; the
 // planner walks the requests in order and fills units one after another, so a request
 // that straddles a unit boundary is cut into pieces (split-KV).  Each piece costs its
 // tiles plus a fixed overhead (query load, epilogue), and no piece is made smaller than
@@ -28,10 +29,10 @@ constexpr int kDEntry = 576;
 constexpr int kPageRows = 64;
 constexpr int kFp8RecordBytes = 656;
 constexpr int kMaxHeads = 128;
-constexpr int kTileTokens = 64;
+constexpr int kTileTokens = 128;
 constexpr int kSmsPerUnit = 2;
-constexpr int kPieceOverheadTiles = 3;
-constexpr int kMinPieceTiles = 4;
+constexpr int kPieceOverheadTiles = 2;
+constexpr int kMinPieceTiles = 2;
 constexpr uint32_t kPlanMagic = 0x4D4C4150u;  // "MLAP"
 
 struct PlanHeader {

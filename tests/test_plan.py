@@ -6,8 +6,9 @@ from mla_latent_kv_17_gb300 import build as mbuild
 from mla_latent_kv_17_gb300 import inputs, ops
 from planview import parse
 
-OVH = 3  # per-piece overhead in tiles, as the planner charges it
-MIN = 4  # shortest piece the planner makes
+OVH = 2  # per-piece overhead in tiles, as the planner charges it
+MIN = 2  # shortest piece the planner makes
+TILE = 128  # tokens per planner tile
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -25,7 +26,7 @@ def check_plan(seq_lens, H=128, topk=0, num_sms=148):
     assert ub[0] == 0 and ub[-1] == p["n_items"] and np.all(np.diff(ub) >= 0)
     assert p["n_items"] <= p["max_items"] == B + units
     items = p["items"]
-    # coverage: each request's pieces tile [0, len) exactly once, in order, on 64-token bounds
+    # coverage: each request's pieces tile [0, len) exactly once, in order, on tile bounds
     per_req = {b: [] for b in range(B)}
     for b, t0, t1, slot in items:
         per_req[int(b)].append((int(t0), int(t1), int(slot)))
@@ -38,7 +39,7 @@ def check_plan(seq_lens, H=128, topk=0, num_sms=148):
             continue
         pos = 0
         for t0, t1, _ in pcs:
-            assert t0 == pos and t1 > t0 and t0 % 64 == 0
+            assert t0 == pos and t1 > t0 and t0 % TILE == 0
             pos = t1
         assert pos == lens[b]
         if len(pcs) == 1:
@@ -59,13 +60,13 @@ def check_plan(seq_lens, H=128, topk=0, num_sms=148):
         for i in range(ub[u], ub[u + 1]):
             b, t0, t1, _ = items[i]
             if t1 > t0:
-                cost[u] += (t1 - t0 + 63) // 64 + OVH
+                cost[u] += (t1 - t0 + TILE - 1) // TILE + OVH
     assert np.all(cost <= p["per"] + MIN + 2 * OVH), (cost.max(), p["per"])
     # pieces are never shorter than MIN tiles unless the whole request is
     for b in range(B):
         pcs = per_req[b]
         if len(pcs) > 1:
-            assert all((t1 - t0 + 63) // 64 >= MIN for t0, t1, _ in pcs)
+            assert all((t1 - t0 + TILE - 1) // TILE >= MIN for t0, t1, _ in pcs)
     return p, cost
 
 
@@ -74,9 +75,9 @@ def test_workload_plans(name):
     sl = inputs.workload_seq_lens(name).tolist()
     topk = 2048 if "sparse" in name else 0
     p, cost = check_plan(sl, topk=topk)
-    tiles = sum((topk or L) // 64 + ((topk or L) % 64 > 0) for L in sl)
+    tiles = sum(((topk or L) + TILE - 1) // TILE for L in sl)
     ub, items = p["unit_begin"], p["items"]
-    load = [sum((t1 - t0 + 63) // 64 for _, t0, t1, _ in items[ub[u]:ub[u + 1]])
+    load = [sum((t1 - t0 + TILE - 1) // TILE for _, t0, t1, _ in items[ub[u]:ub[u + 1]])
             for u in range(p["units"])]
     # the busiest unit carries at most its share plus two folded short runs
     assert max(load) <= p["per"] + 2 * (MIN - 1), (max(load), p["per"])
