@@ -24,6 +24,7 @@ import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -62,63 +63,82 @@ def dram_traffic(workload: str):
 
 
 class Clocks:
-    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+    """Samples the SM clock and the clock-event (throttle) reasons while the timed region runs.
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    Reads NVML directly (libnvidia-ml through ctypes) from a background thread every half
+    millisecond, so that even a timed region of a few milliseconds gets samples; the GPU is
+    matched by UUID (NVML does not see CUDA_VISIBLE_DEVICES).  Only reads settings."""
 
-    def __init__(self, index: int):
-        self.index = index
-        self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv")
+    # clock-event reason bits of the NVML API
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index: int, period_s: float = 0.0005):
+        self.device_index = device_index
+        self.period = period_s
+        self.samples = []
+        self.max_mhz = None
+        self.error = None
+        self.nvml = None
+        self.thread = None
+        self.stop = threading.Event()
+
+    def _open(self):
+        import ctypes
+        import torch
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        handle = ctypes.c_void_p()
+        props = torch.cuda.get_device_properties(self.device_index)
+        uuid = getattr(props, "uuid", None)
+        rc = -1
+        if uuid is not None:
+            rc = nv.nvmlDeviceGetHandleByUUID(("GPU-" + str(uuid)).encode(), ctypes.byref(handle))
+        if rc != 0:
+            bus = "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+            rc = nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(handle))
+        if rc != 0:
+            raise RuntimeError("no NVML handle for this GPU")
+        mx = ctypes.c_uint()
+        if nv.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0:  # 1: SM clock
+            self.max_mhz = float(mx.value)
+        reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.nvml = (nv, handle, reasons_fn)
+
+    def _run(self):
+        import ctypes
+        nv, handle, reasons_fn = self.nvml
+        mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(handle, 1, ctypes.byref(mhz)) == 0 and \
+                    reasons_fn(handle, ctypes.byref(rs)) == 0:
+                self.samples.append((float(mhz.value), int(rs.value)))
+            time.sleep(self.period)
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=self.f, stderr=subprocess.DEVNULL)
-        except Exception:
-            self.proc = None
+            self._open()
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
+        except Exception as e:  # no NVML on this machine
+            self.error = str(e)
         return self
 
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except Exception:
-                self.proc.kill()
-            self.f.close()
+        if self.thread is not None:
+            self.stop.set()
+            self.thread.join(timeout=5)
 
     def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
-        rows = []
-        for line in open(self.path):
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                rows.append(parts)
-            except ValueError:
-                pass
-        try:
-            os.remove(self.path)
-        except OSError:
-            pass
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock samples"]}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(rows)}
+        if self.error is not None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [f"clock sampling unavailable: {self.error}"]}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no clock samples"]}
+        reasons = sorted({name for _, r in self.samples for bit, name in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(m for m, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples)}
 
 
 def dist_env():
