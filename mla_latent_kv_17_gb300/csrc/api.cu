@@ -199,8 +199,8 @@ mla_status run_decode(const DecodeArgs &a, cudaStream_t stream) {
     if (sms <= 0) return MLA_ERR_CUDA;
     const int units = units_for(sms);
     cudaError_t e;
-    if (!a.kv_fp8 && !a.indices)
-        e = launch_decode_sm103(a, units, stream);
+    if (!a.kv_fp8)
+        e = launch_decode_sm103(a, units, stream);  // dense or sparse bf16 cache
     else
         e = launch_decode_simt(a, units, stream);
     if (e != cudaSuccess) return MLA_ERR_CUDA;

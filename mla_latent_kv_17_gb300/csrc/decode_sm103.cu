@@ -75,8 +75,8 @@ constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + slack for 1024-B ali
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 enum {
-    B_DH_FULL = 0,
-    B_DH_EMPTY = B_DH_FULL + kDhSlots,
+    B_DH_FULL = 0,                       // 2 per slot: own-page and peer-page loads
+    B_DH_EMPTY = B_DH_FULL + 2 * kDhSlots,
     B_OTH_FULL = B_DH_EMPTY + kDhSlots,
     B_OTH_EMPTY,
     B_S_FULL,
@@ -167,20 +167,96 @@ __device__ __forceinline__ PageRef page_of(const DecodeArgs &a, const WorkItem &
     return r;
 }
 
+// Sparse tiles: row j of page p holds index slot t + 64 p + j of the item.  Lane l
+// resolves slots l and l + 32: the cache row (page * 64 + row; row 0 for an invalid slot,
+// which is never attended and is zeroed before PV) and whether the slot is attended
+// (inside the item, index in [0, seq_len), page id in range).  Warp-collective.
+struct SparseRows {
+    int32_t row0, row1;
+    uint32_t lo, hi;  // validity of slots 0-31 and 32-63
+};
+__device__ SparseRows sparse_rows(const DecodeArgs &a, const WorkItem &w, int t, int p, int lane, bool report) {
+    const int L = max(0, a.seq_lens[w.b]);
+    int32_t rows[2] = {0, 0};
+    bool ok[2] = {false, false};
+    for (int k = 0; k < 2; ++k) {
+        const int s = t + kPageRows * p + lane + 32 * k;
+        if (s >= w.t1) continue;
+        const int idx = a.indices[(int64_t)w.b * a.topk + s];
+        if (idx < 0) {
+            if (idx < -1 && report) record_error(a.status, MLA_ERR_INDEX);
+            continue;
+        }
+        const int lp = idx / kPageRows;
+        const int64_t id = idx < L && lp < a.max_pages ? (int64_t)a.block_table[(int64_t)w.b * a.max_pages + lp] : -1;
+        if (id < 0 || id >= a.num_pages) {
+            if (report) record_error(a.status, MLA_ERR_INDEX);
+            continue;
+        }
+        rows[k] = (int32_t)(id * kPageRows + idx % kPageRows);
+        ok[k] = true;
+    }
+    return SparseRows{rows[0], rows[1], __ballot_sync(0xffffffffu, ok[0]), __ballot_sync(0xffffffffu, ok[1])};
+}
+
+// Gathers the 64 rows of `r` (columns x_of(i) .. + 63 for box i < nbox) into consecutive
+// 8-KB boxes at dst, four rows per tile::gather4; lanes 0-15 take row groups, the two
+// half-warps alternate boxes.
+template <typename XOf>
+__device__ __forceinline__ void gather_rows(const SparseRows &r, int lane, uint32_t dst, const void *tmap, int nbox,
+                                            XOf x_of, uint32_t bar) {
+    const int l = lane & 15;
+    int32_t r4[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int j = 4 * l + k;
+        const int32_t a0 = __shfl_sync(0xffffffffu, r.row0, j & 31), a1 = __shfl_sync(0xffffffffu, r.row1, j & 31);
+        r4[k] = j < 32 ? a0 : a1;
+    }
+    for (int i = lane >> 4; i < nbox; i += 2)
+        tma_gather4(dst + i * kBox + 512u * l, tmap, x_of(i), r4[0], r4[1], r4[2], r4[3], bar);
+}
+
+// Which of page p's 64 rows attend (`valid`) and how many rows of the page lie inside the
+// item (`cnt`; PV reads them in whole 16-row steps).  Warp-collective for sparse tiles.
+struct PageMask {
+    uint64_t valid;
+    int cnt;
+};
+template <bool kSparse>
+__device__ __forceinline__ PageMask page_mask(const DecodeArgs &a, const WorkItem &w, int t, int p, int lane) {
+    PageMask m;
+    m.cnt = max(0, min(kPageRows, w.t1 - (t + kPageRows * p)));
+    if constexpr (kSparse) {
+        const SparseRows r = sparse_rows(a, w, t, p, lane, false);
+        m.valid = (uint64_t)r.lo | ((uint64_t)r.hi << 32);
+    } else {
+        const PageRef pg = page_of(a, w, t, p);
+        m.valid = pg.id >= 0 && pg.rows > 0 ? (pg.rows >= 64 ? ~0ull : ((1ull << pg.rows) - 1ull)) : 0ull;
+    }
+    return m;
+}
+
 // Latent-half slots.  Tile g's own page (e = 0) sits in slot g % 3 and its peer page (e = 1)
 // in slot (g + 2) % 3; the loader issues own(0), own(1), then peer(g), own(g + 2) for
 // g = 0, 1, ...  PV of tile g hands back the peer page's slot first, and own(g + 2) — the
 // page the scores need soonest — takes exactly that slot, ahead of peer(g + 1), which takes
-// own(g)'s.  Each slot alternates own and peer pages; `fill` counts the slot's loads before
-// this one (its full barrier's phase).
+// own(g)'s.  Each slot alternates own and peer pages.  `fill` counts the slot's loads before
+// this one (the phase of its empty barrier).  Own-page and peer-page loads complete on
+// separate full barriers (`full`, phase `phase` = g / 3): the score issuer waits for own
+// pages only, and with one barrier per slot a parity wait for the next own page could be
+// satisfied by an older phase while the peer page between them is still loading.
 struct DhSlot {
     int slot;
     uint32_t fill;
+    int full;        // barrier index
+    uint32_t phase;
 };
 __device__ __forceinline__ DhSlot dh_slot(uint32_t g, int e) {
     const uint32_t q = g / 3u, r = g % 3u;
-    if (e == 0) return DhSlot{(int)r, 2u * q + (r == 2u ? 1u : 0u)};
-    return DhSlot{(int)((r + 2u) % 3u), 2u * q + (r != 0u ? 1u : 0u)};
+    const int slot = e == 0 ? (int)r : (int)((r + 2u) % 3u);
+    const uint32_t fill = e == 0 ? 2u * q + (r == 2u ? 1u : 0u) : 2u * q + (r != 0u ? 1u : 0u);
+    return DhSlot{slot, fill, B_DH_FULL + 2 * slot + e, q};
 }
 
 // Walks the tiles of this cluster's work in order: units cl, cl + ncl, ..., their items
@@ -240,6 +316,9 @@ __device__ int next_request(const int32_t *ub, const WorkItem *items, int units,
     return -1;
 }
 
+// kSparse: tiles are 128 index slots (DSA top-k lists) gathered row by row; otherwise 128
+// consecutive tokens (two pages) loaded as 64-row boxes.
+template <bool kSparse>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -258,7 +337,8 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kDhSlots; ++s) {
-            mbar_init(bar(base, B_DH_FULL + s), 1);
+            mbar_init(bar(base, B_DH_FULL + 2 * s), 1);
+            mbar_init(bar(base, B_DH_FULL + 2 * s + 1), 1);
             mbar_init(bar(base, B_DH_EMPTY + s), 1);
         }
         mbar_init(bar(base, B_OTH_FULL), 1);
@@ -293,75 +373,101 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
     const int cl = (int)cluster_id_x(), ncl = (int)nclusters_x();
 
     if (warp == 4 || warp == 7) {
-        // ------------------------------------------------------------ TMA producers
-        if (lane == 0) {
-            TileCursor cur, nx;
-            cur.begin(unit_begin, items, units, cl, ncl);
-            nx = cur;
-            nx.next();
-            if (warp == 4) {
-                // own latent half of both pages, in the order own(0), own(1), peer(0), own(2),
-                // peer(1), own(3), ...
-                const int xown = 256 * (int)rank;
-                // loads page (rank if e == 0, else peer) of tile g at cursor position t
-                auto load = [&](const TileCursor &t, uint32_t g, int e) -> bool {
-                    const PageRef pg = page_of(a, t.w, t.t, e == 0 ? (int)rank : (int)peer);  // read before the wait
-                    const DhSlot d = dh_slot(g, e);
-                    if (d.fill > 0 && !wait_bar(c, bar(base, B_DH_EMPTY + d.slot), (d.fill - 1u) & 1u, false))
+        // ------------------------------------------------------------ TMA loaders (whole warps)
+        TileCursor cur, nx;
+        cur.begin(unit_begin, items, units, cl, ncl);
+        nx = cur;
+        nx.next();
+        if (warp == 4) {
+            // own latent half of both pages, in the order own(0), own(1), peer(0), own(2),
+            // peer(1), own(3), ...
+            const int xown = 256 * (int)rank;
+            // loads page (rank if e == 0, else peer) of tile g at cursor position t
+            auto load = [&](const TileCursor &t, uint32_t g, int e) -> bool {
+                const int p = e == 0 ? (int)rank : (int)peer;
+                const DhSlot d = dh_slot(g, e);
+                const uint32_t fb = bar(base, d.full), dst = base + kOffDh + d.slot * kDhBytes;
+                if constexpr (kSparse) {
+                    const SparseRows r = sparse_rows(a, t.w, t.t, p, lane, true);  // read before the wait
+                    if (d.fill > 0 && !warp_wait(c, bar(base, B_DH_EMPTY + d.slot), (d.fill - 1u) & 1u, false))
                         return false;
-                    const uint32_t fb = bar(base, B_DH_FULL + d.slot);
-                    if (pg.rows > 0 && pg.id >= 0) {
-                        const int32_t y = (int32_t)(pg.id * kPageRows);
-                        const uint32_t dst = base + kOffDh + d.slot * kDhBytes;
-                        mbar_arrive_expect_tx(fb, kDhBytes);
-                        for (int i = 0; i < 4; ++i) tma_load_2d(dst + i * kBox, &tmap, xown + 64 * i, y, fb);
-                    } else {
-                        if (pg.rows > 0) record_error(a.status, MLA_ERR_INDEX);
+                    if (t.t + kPageRows * p < t.w.t1) {
+                        if (lane == 0) mbar_arrive_expect_tx(fb, kDhBytes);
+                        __syncwarp();
+                        gather_rows(r, lane, dst, &tmap, 4, [&](int i) { return xown + 64 * i; }, fb);
+                    } else if (lane == 0) {
                         mbar_arrive(fb);
                     }
-                    return true;
-                };
-                TileCursor co = cur;  // next own page: tile go
-                uint32_t go = 0, gp = 0;
-                bool ok = true;
-                for (; go < 2 && !co.done() && ok; ++go, co.next()) ok = load(co, go, 0);
-                for (; !cur.done() && ok; ++gp, cur.next()) {  // cur: next peer page, tile gp
-                    ok = load(cur, gp, 1);
-                    if (ok && !co.done()) {
-                        ok = load(co, go, 0);
-                        ++go;
-                        co.next();
+                } else {
+                    const PageRef pg = page_of(a, t.w, t.t, p);  // read before the wait
+                    if (d.fill > 0 && !warp_wait(c, bar(base, B_DH_EMPTY + d.slot), (d.fill - 1u) & 1u, false))
+                        return false;
+                    if (lane == 0) {
+                        if (pg.rows > 0 && pg.id >= 0) {
+                            const int32_t y = (int32_t)(pg.id * kPageRows);
+                            mbar_arrive_expect_tx(fb, kDhBytes);
+                            for (int i = 0; i < 4; ++i) tma_load_2d(dst + i * kBox, &tmap, xown + 64 * i, y, fb);
+                        } else {
+                            if (pg.rows > 0) record_error(a.status, MLA_ERR_INDEX);
+                            mbar_arrive(fb);
+                        }
                     }
                 }
-                if (!ok) drain_pause();
-            } else {
-                // other latent half + RoPE of the own page, one stage
-                const int xoth = 256 * (int)peer;
-                PageRef pg{0, -1};
-                if (!cur.done()) pg = page_of(a, cur.w, cur.t, (int)rank);
-                bool ok = true;
-                for (uint32_t g = 0; !cur.done() && ok; ++g) {
-                    PageRef np{0, -1};  // next tile's page, read ahead of the wait
-                    if (!nx.done()) np = page_of(a, nx.w, nx.t, (int)rank);
-                    if (!wait_bar(c, bar(base, B_OTH_EMPTY), (g & 1u) ^ 1u, false)) {
+                return true;
+            };
+            TileCursor co = cur;  // next own page: tile go
+            uint32_t go = 0, gp = 0;
+            bool ok = true;
+            for (; go < 2 && !co.done() && ok; ++go, co.next()) ok = load(co, go, 0);
+            for (; !cur.done() && ok; ++gp, cur.next()) {  // cur: next peer page, tile gp
+                ok = load(cur, gp, 1);
+                if (ok && !co.done()) {
+                    ok = load(co, go, 0);
+                    ++go;
+                    co.next();
+                }
+            }
+            if (!ok && lane == 0) drain_pause();
+        } else {
+            // other latent half + RoPE of the own page, one stage
+            const int xoth = 256 * (int)peer;
+            auto x_of = [&](int i) { return i < 4 ? xoth + 64 * i : kDLatent; };
+            bool ok = true;
+            for (uint32_t g = 0; !cur.done() && ok; ++g) {
+                const uint32_t fb = bar(base, B_OTH_FULL), dst = base + kOffOth;
+                if constexpr (kSparse) {
+                    const SparseRows r = sparse_rows(a, cur.w, cur.t, (int)rank, lane, false);  // before the wait
+                    if (!warp_wait(c, bar(base, B_OTH_EMPTY), (g & 1u) ^ 1u, false)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = bar(base, B_OTH_FULL);
-                    if (pg.rows > 0 && pg.id >= 0) {
-                        const int32_t y = (int32_t)(pg.id * kPageRows);
-                        mbar_arrive_expect_tx(fb, kOthBoxes * kBox);
-                        for (int i = 0; i < kOthBoxes; ++i)
-                            tma_load_2d(base + kOffOth + i * kBox, &tmap, i < 4 ? xoth + 64 * i : kDLatent, y, fb);
-                    } else {
+                    if (cur.t + kPageRows * (int)rank < cur.w.t1) {
+                        if (lane == 0) mbar_arrive_expect_tx(fb, kOthBoxes * kBox);
+                        __syncwarp();
+                        gather_rows(r, lane, dst, &tmap, kOthBoxes, x_of, fb);
+                    } else if (lane == 0) {
                         mbar_arrive(fb);
                     }
-                    pg = np;
-                    cur = nx;
-                    nx.next();
+                } else {
+                    const PageRef pg = page_of(a, cur.w, cur.t, (int)rank);  // before the wait
+                    if (!warp_wait(c, bar(base, B_OTH_EMPTY), (g & 1u) ^ 1u, false)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        if (pg.rows > 0 && pg.id >= 0) {
+                            const int32_t y = (int32_t)(pg.id * kPageRows);
+                            mbar_arrive_expect_tx(fb, kOthBoxes * kBox);
+                            for (int i = 0; i < kOthBoxes; ++i) tma_load_2d(dst + i * kBox, &tmap, x_of(i), y, fb);
+                        } else {
+                            mbar_arrive(fb);
+                        }
+                    }
                 }
-                if (!ok) drain_pause();
+                cur = nx;
+                nx.next();
             }
+            if (!ok && lane == 0) drain_pause();
         }
     } else if (warp == 5) {
         // ------------------------------------------------------------ QK^T issuer
@@ -409,7 +515,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
                         mma_commit(bar(base, B_OTH_EMPTY));
                         const DhSlot dso = dh_slot(g, 0);
                         const int ds = dso.slot;
-                        if (!wait_bar(c, bar(base, B_DH_FULL + ds), dso.fill & 1u, false)) {
+                        if (!wait_bar(c, bar(base, dso.full), dso.phase & 1u, false)) {
                             ok = false;
                             break;
                         }
@@ -451,7 +557,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
                             const DhSlot d = dh_slot(g, e);
                             const int ds = d.slot;
                             const int ksteps = min(4, max(0, (nvalid - kPageRows * p + 15) / 16));
-                            if (ksteps > 0 && !wait_bar(c, bar(base, B_DH_FULL + ds), d.fill & 1u, false)) {
+                            if (ksteps > 0 && !wait_bar(c, bar(base, d.full), d.phase & 1u, false)) {
                                 ok = false;
                                 break;
                             }
@@ -560,8 +666,9 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
                 for (int t = w.t0, j = 0; t < w.t1; t += kTile, ++j, ++g) {
                     // ================= part A: own page's scores -> weights -> message
                     const int nvalid = min(kTile, w.t1 - t);
-                    const PageRef pg0 = page_of(a, w, t, 0), pg1 = page_of(a, w, t, 1);  // read early
-                    const int nown = rank == 0 ? (pg0.id >= 0 ? pg0.rows : 0) : (pg1.id >= 0 ? pg1.rows : 0);
+                    // which rows of each page attend (read early; warp-collective)
+                    const PageMask pm0 = page_mask<kSparse>(a, w, t, 0, lane), pm1 = page_mask<kSparse>(a, w, t, 1, lane);
+                    const uint64_t vown = rank == 0 ? pm0.valid : pm1.valid;
                     if (!warp_wait(c, bar(base, B_S_FULL), g & 1u, false)) {
                         ok = false;
                         break;
@@ -579,10 +686,10 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(base, B_S_FREE));
-                    if (nown < 64) {
+                    if (vown != ~0ull) {
 #pragma unroll
                         for (int i = 0; i < 64; ++i)
-                            if (i >= nown) s[i] = -INFINITY;
+                            if (!((vown >> i) & 1ull)) s[i] = -INFINITY;
                     }
                     float mraw = s[0];
 #pragma unroll
@@ -662,26 +769,28 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
                         scale_row(reinterpret_cast<uint4 *>(ps + peer * kPPage + h * 128), fpeer);
                         wrote = true;
                     }
-                    // cache rows that PV reads but must not contribute (the rows of the last
-                    // 16-row step past the end; a page whose id was out of range) must hold
-                    // zeros there, not whatever the page holds
+                    // cache rows that PV reads but must not contribute (rows of the last
+                    // 16-row step past the end, a page whose id was out of range, sparse slots
+                    // that are padding or out of range) must hold zeros there, not whatever
+                    // the loaded row holds
                     for (int p = 0; p < 2; ++p) {
-                        const PageRef pr = p == 0 ? pg0 : pg1;
-                        const int z0 = pr.id >= 0 ? pr.rows : 0, z1 = min(kPageRows, (pr.rows + 15) & ~15);
-                        if (z1 <= z0) continue;
+                        const PageMask pm = p == 0 ? pm0 : pm1;
+                        const int z1 = min(kPageRows, (pm.cnt + 15) & ~15);
+                        const uint64_t zero = ~pm.valid & (z1 >= 64 ? ~0ull : ((1ull << z1) - 1ull));
+                        if (zero == 0ull) continue;
                         const DhSlot d = dh_slot(g, p == (int)rank ? 0 : 1);
                         const int ds = d.slot;
                         // wait for the slot's load (or its empty arrival) to land first
-                        if (!warp_wait(c, bar(base, B_DH_FULL + ds), d.fill & 1u, false)) {
+                        if (!warp_wait(c, bar(base, d.full), d.phase & 1u, false)) {
                             ok = false;
                             break;
                         }
-                        const int nz = (z1 - z0) * 32;  // 16-B chunks over 4 boxes
                         uint8_t *dh = gbase + kOffDh + ds * kDhBytes;
-                        for (int i = h; i < nz; i += 128) {
-                            const int row = z0 + i / 32, ch = i % 32;
-                            *reinterpret_cast<uint4 *>(dh + (ch / 8) * kBox + row * 128 + (ch % 8) * 16) =
-                                make_uint4(0u, 0u, 0u, 0u);
+                        for (int i = h; i < z1 * 32; i += 128) {  // 16-B chunks over 4 boxes
+                            const int row = i / 32, ch = i % 32;
+                            if ((zero >> row) & 1ull)
+                                *reinterpret_cast<uint4 *>(dh + (ch / 8) * kBox + row * 128 + (ch % 8) * 16) =
+                                    make_uint4(0u, 0u, 0u, 0u);
                         }
                         wrote = true;
                     }
@@ -786,6 +895,23 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// Sets the shared-memory limit of both kernel variants once per device.
+bool set_smem_attr() {
+    static bool done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (done[dev]) return true;
+    if (cudaFuncSetAttribute(decode_sm103_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(decode_sm103_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    done[dev] = true;
+    return true;
+}
+
 }  // namespace
 
 int sm103_max_units() {
@@ -794,11 +920,7 @@ int sm103_max_units() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (cached >= 0 && cached_dev == dev) return cached;
-    if (cudaFuncSetAttribute(decode_sm103_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
+    if (!set_smem_attr()) return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -811,7 +933,7 @@ int sm103_max_units() {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, decode_sm103_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, decode_sm103_kernel<false>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -823,24 +945,23 @@ int sm103_max_units() {
 cudaError_t launch_decode_sm103(const DecodeArgs &a, int num_clusters, cudaStream_t stream) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
+    const bool sparse = a.indices != nullptr;
     CUtensorMap tmap;
     const cuuint64_t dims[2] = {(cuuint64_t)kDEntry, (cuuint64_t)a.num_pages * kPageRows};
     const cuuint64_t strides[1] = {(cuuint64_t)kDEntry * 2};
-    const cuuint32_t box[2] = {64, kPageRows};
+    // dense: 64-row boxes (one page); sparse: one-row boxes for tile::gather4
+    const cuuint32_t box[2] = {64, sparse ? 1u : (cuuint32_t)kPageRows};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<unsigned char *>(a.cache),
                      dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_sm103_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    decode_sm103_kernel<<<dim3(2 * num_clusters), dim3(kThreads), kSmemBytes, stream>>>(tmap, a);
+    if (!set_smem_attr()) return cudaErrorInvalidValue;
+    if (sparse)
+        decode_sm103_kernel<true><<<dim3(2 * num_clusters), dim3(kThreads), kSmemBytes, stream>>>(tmap, a);
+    else
+        decode_sm103_kernel<false><<<dim3(2 * num_clusters), dim3(kThreads), kSmemBytes, stream>>>(tmap, a);
     return cudaGetLastError();
 }
 

@@ -202,6 +202,18 @@ def test_sparse_split():
     check(_sparse(2, 128, [9000, 5000], topk=2048, seed=5), num_sms=6, what="sparse split")
 
 
+@pytest.mark.parametrize("L,num_sms", [(896, 2), (1024, 0), (2000, 6)])
+def test_sparse_contiguous_equals_dense_bitwise(L, num_sms):
+    # indices 0..L-1 make the sparse path gather exactly the rows the dense path loads as
+    # page boxes, into the same layout, so the two results are bitwise equal; long items
+    # also exercise every latent-buffer phase while the gathered loads run slowly
+    c = small(1, 128, [L], seed=7)
+    d_out, d_lse, _ = run(c, num_sms=num_sms)
+    c.indices = torch.arange(L, dtype=torch.int32)[None].cuda()
+    s_out, s_lse, _ = run(c, num_sms=num_sms)
+    assert torch.equal(d_out, s_out) and torch.equal(d_lse, s_lse)
+
+
 # ------------------------------------------------------------------------------ errors
 def test_out_of_range_page_is_reported_not_faulted():
     c = small(2, 16, [100, 100], seed=6)
