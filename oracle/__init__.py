@@ -70,6 +70,8 @@ def _load():
             lib.mla_oracle_combine_f64.restype = None
             lib.mla_oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
             lib.mla_oracle_e4m3_to_double.restype = D
+            lib.mla_oracle_fp8_latent.argtypes = [ctypes.c_uint8, ctypes.c_float]
+            lib.mla_oracle_fp8_latent.restype = D
             lib.mla_oracle_default_threads.argtypes = []
             lib.mla_oracle_default_threads.restype = I
             common = [I, I, P, P, P, I64, P, I, P]
@@ -95,6 +97,11 @@ def default_threads() -> int:
 def e4m3_to_float(code: int) -> float:
     """Value of one e4m3 "fn" code (bias 7, no infinities, 0x7F/0xFF NaN)."""
     return float(_load().mla_oracle_e4m3_to_double(int(code) & 0xFF))
+
+
+def fp8_latent(code: int, scale: float) -> float:
+    """One dequantized FP8 latent value: bf16_rne(fp32(e4m3(code)) * fp32(scale))."""
+    return float(_load().mla_oracle_fp8_latent(int(code) & 0xFF, float(scale)))
 
 
 def attend_f64(q_nope, q_rope, C, Kr, scale):

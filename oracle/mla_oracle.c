@@ -29,7 +29,10 @@
  *    tokens only.
  *  - Same guide, §5.3: the FP8 latent cache.  The pages do not fix the FP8 format; this
  *    oracle reads e4m3 "fn" (bias 7, no infinities, S.1111.111 is NaN) with one fp32
- *    scale per 128 latent channels, x = e4m3(code) * scale.
+ *    scale per 128 latent channels.  The dequantized latent is the bf16 operand of the
+ *    bf16 contraction that follows (the guide's FP8 cache feeds bf16/FP8 compute; the
+ *    pages fix no intermediate precision): x = bf16_rne(fp32(e4m3(code)) * scale), the
+ *    product formed in fp32 (exact for the code; one rounding) and rounded once to bf16.
  *
  * Readings where the pages are silent: the scale multiplies the raw score before the
  * exponential; lse is the natural log of the normaliser of the scaled scores; an empty
@@ -60,6 +63,16 @@ static double bf16_bits_to_double(uint16_t bits) {
     return (double)f;
 }
 
+/* binary32 -> nearest bfloat16 (ties to even), returned as a double; NaN stays NaN. */
+static double f32_to_bf16_double(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0) return NAN;
+    u = (u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
 /* e4m3 "fn": 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; no infinities;
  * exponent 1111 with mantissa 111 is NaN; exponent 0000 is subnormal. */
 double mla_oracle_e4m3_to_double(uint8_t code) {
@@ -73,6 +86,12 @@ double mla_oracle_e4m3_to_double(uint8_t code) {
     else
         v = ldexp(1.0 + (double)m / 8.0, e - 7);
     return sign ? -v : v;
+}
+
+/* One dequantized latent value of an FP8 record: code times its block scale, formed in
+ * binary32 and rounded once to bfloat16 (see the header). */
+double mla_oracle_fp8_latent(uint8_t code, float scale) {
+    return f32_to_bf16_double((float)mla_oracle_e4m3_to_double(code) * scale);
 }
 
 static double f32_bits_to_double(const uint8_t *p) {
@@ -179,10 +198,9 @@ static int load_token(const job_t *J, int b, int64_t t, double *c, double *kr) {
         for (int i = 0; i < D_ROPE; ++i) kr[i] = bf16_bits_to_double(e[D_LATENT + i]);
     } else {
         const uint8_t *e = (const uint8_t *)J->cache + (size_t)row * FP8_RECORD_BYTES;
-        double sc[4];
-        for (int g = 0; g < 4; ++g) sc[g] = f32_bits_to_double(e + 512 + 4 * g);
-        for (int i = 0; i < D_LATENT; ++i)
-            c[i] = mla_oracle_e4m3_to_double(e[i]) * sc[i / 128];
+        float sc[4];
+        for (int g = 0; g < 4; ++g) sc[g] = (float)f32_bits_to_double(e + 512 + 4 * g);
+        for (int i = 0; i < D_LATENT; ++i) c[i] = mla_oracle_fp8_latent(e[i], sc[i / 128]);
         const uint8_t *rp = e + 528;
         for (int i = 0; i < D_ROPE; ++i) {
             uint16_t bits = (uint16_t)(rp[2 * i] | (rp[2 * i + 1] << 8));
