@@ -199,10 +199,7 @@ mla_status run_decode(const DecodeArgs &a, cudaStream_t stream) {
     if (sms <= 0) return MLA_ERR_CUDA;
     const int units = units_for(sms);
     cudaError_t e;
-    if (!a.kv_fp8)
-        e = launch_decode_sm103(a, units, stream);  // dense or sparse bf16 cache
-    else
-        e = launch_decode_simt(a, units, stream);
+    e = launch_decode_sm103(a, units, stream);  // dense bf16, DSA sparse, or FP8 records
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     dim3 cgrid(a.B, (a.H + kCombineHeads - 1) / kCombineHeads);
     combine_kernel<<<cgrid, kCombineThreads, 0, stream>>>(a);

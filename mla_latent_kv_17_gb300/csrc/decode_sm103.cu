@@ -37,6 +37,8 @@
 // and all roles fall through to a clean exit.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "launch.h"
@@ -58,7 +60,8 @@ constexpr uint32_t kPPage = 128 * 128;           // 128 heads x 64 tokens bf16, 
 constexpr uint32_t kRlBytes = 1024;              // r[128] and sum[128], fp32
 constexpr uint32_t kPBytes = 2 * kPPage + 2 * kRlBytes;
 constexpr uint32_t kMsgBytes = kPPage + kRlBytes;
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;         // dense and sparse tiles
+constexpr int kThreadsFp8 = 288;      // + a raw-load warp for FP8 records
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 320;
 constexpr uint32_t kColQRope = kColQ + 128, kColQOther = kColQ + 160;
@@ -71,7 +74,11 @@ constexpr uint32_t kOffQs = kOffOth + kOthBoxes * kBox;
 constexpr uint32_t kOffP = kOffQs + kQsBytes;
 constexpr uint32_t kOffBar = kOffP + kPBytes;
 constexpr uint32_t kOffMisc = kOffBar + 8 * 32;
-constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + slack for 1024-B alignment
+// FP8 records: per-row scales of the three latent-half slots and the other-columns stage
+constexpr uint32_t kOffScale = (kOffMisc + 64 + 1023) / 1024 * 1024;
+constexpr uint32_t kScaleBytes = 64 * 16;  // 64 rows x 4 fp32
+constexpr uint32_t kRawOff = 16384;         // FP8 codes land in the upper half of their bf16 destination
+constexpr uint32_t kSmemBytes = kOffScale + 4 * kScaleBytes + 1024;  // + slack for 1024-B alignment
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 enum {
@@ -86,6 +93,8 @@ enum {
     B_RFULL,    // the peer's message for the current tile has landed
     B_PFREE,    // both CTAs' PV have finished reading the probability tile
     B_P_FULL,   // the probability tile holds the merged weights of its tile
+    B_RAW,      // FP8: raw codes + scales of latent slot s (s < 3) or of the other-columns stage (3)
+    B_DQ_SYNC = B_RAW + 4,  // FP8: both dequant warps have read the current job's raw codes
     B_COUNT
 };
 static_assert(B_COUNT <= 32, "barrier area");
@@ -318,9 +327,56 @@ __device__ int next_request(const int32_t *ub, const WorkItem *items, int units,
 
 // kSparse: tiles are 128 index slots (DSA top-k lists) gathered row by row; otherwise 128
 // consecutive tokens (two pages) loaded as 64-row boxes.
-template <bool kSparse>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
+// Two e4m3 codes (low byte first) times their block scale, as a packed bf16 pair.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two, float s) {
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+    return pack_bf16(f.x * s, f.y * s);
+}
+
+// FP8 records: the raw loads and their expansion run as one sequence of jobs, in the order
+// other-columns(0), own(0), own(1), then for g = 0, 1, ...: peer(g), other-columns(g + 1),
+// own(g + 2) — the latent-half order of the bf16 loaders with each tile's other columns
+// slotted in.  f(kind, g, cursor): kind 0 own page, 1 peer page, 2 other columns.
+template <typename F>
+__device__ bool fp8_jobs(const TileCursor &start, F &&f) {
+    TileCursor co = start, cp = start, ch = start;
+    uint32_t go = 0, gp = 0, gh = 0;
+    if (!ch.done()) {
+        if (!f(2, gh, ch)) return false;
+        ++gh;
+        ch.next();
+    }
+    for (int i = 0; i < 2 && !co.done(); ++i, ++go, co.next())
+        if (!f(0, go, co)) return false;
+    for (; !cp.done(); ++gp, cp.next()) {
+        if (!f(1, gp, cp)) return false;
+        if (!ch.done()) {
+            if (!f(2, gh, ch)) return false;
+            ++gh;
+            ch.next();
+        }
+        if (!co.done()) {
+            if (!f(0, go, co)) return false;
+            ++go;
+            co.next();
+        }
+    }
+    return true;
+}
+
+// kMode 0: dense bf16 tiles (128 consecutive tokens, two pages, 64-row boxes).
+// kMode 1: DSA sparse tiles (128 index slots gathered row by row, tile::gather4).
+// kMode 2: dense FP8 records: raw e4m3 codes and scales are loaded by an extra warp and
+//          expanded to bf16 operand tiles by the two loader warps; RoPE goes in directly.
+// tmap: the cache (kMode 2: its bytes, 256-B boxes of codes); tmap_sc / tmap_rope: FP8
+// scales (16-B boxes) and RoPE (bf16, 128-B swizzle), unused otherwise.
+template <int kMode>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMode == 2 ? kThreadsFp8 : kThreads, 1)
+decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_sc,
+                    const __grid_constant__ CUtensorMap tmap_rope, DecodeArgs a) {
+    constexpr bool kSparse = kMode == 1, kFp8 = kMode == 2;
+    constexpr uint32_t kFullCount = kFp8 ? 2u : 1u;  // arrivals that complete a latent / other-columns stage
     extern __shared__ uint8_t smem_raw[];
     if (!plan_matches(a)) {
         if (threadIdx.x == 0 && blockIdx.x == 0) record_error(a.status, MLA_ERR_WORKSPACE);
@@ -337,11 +393,13 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kDhSlots; ++s) {
-            mbar_init(bar(base, B_DH_FULL + 2 * s), 1);
-            mbar_init(bar(base, B_DH_FULL + 2 * s + 1), 1);
+            mbar_init(bar(base, B_DH_FULL + 2 * s), kFullCount);
+            mbar_init(bar(base, B_DH_FULL + 2 * s + 1), kFullCount);
             mbar_init(bar(base, B_DH_EMPTY + s), 1);
         }
-        mbar_init(bar(base, B_OTH_FULL), 1);
+        for (int s = 0; s < 4; ++s) mbar_init(bar(base, B_RAW + s), 1);
+        mbar_init(bar(base, B_DQ_SYNC), 2);
+        mbar_init(bar(base, B_OTH_FULL), kFullCount);
         mbar_init(bar(base, B_OTH_EMPTY), 1);
         mbar_init(bar(base, B_S_FULL), 1);
         mbar_init(bar(base, B_S_FREE), 4);
@@ -357,7 +415,13 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
         tmem_alloc(smem_u32(const_cast<uint32_t *>(misc)), kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) prefetch_tmap(&tmap);
+    if (warp == 4 && lane == 0) {
+        prefetch_tmap(&tmap);
+        if (kFp8) {
+            prefetch_tmap(&tmap_sc);
+            prefetch_tmap(&tmap_rope);
+        }
+    }
     tc_fence_before();
     cluster_sync();
     tc_fence_after();
@@ -372,7 +436,121 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
     const int units = hd->num_units;
     const int cl = (int)cluster_id_x(), ncl = (int)nclusters_x();
 
-    if (warp == 4 || warp == 7) {
+    if (kFp8 && (warp == 4 || warp == 7)) {
+        // ------------------------------------------------------------ FP8 expansion (two warps)
+        // Thread dt expands row dt of each job: reads its 256 codes and two block scales,
+        // waits until the other warp has read its rows too (the bf16 output overwrites the
+        // raw codes in the upper half of the same buffer), then writes 256 scaled bf16 values
+        // into the 128-B-swizzled boxes.
+        const int dt = (warp == 4 ? 0 : 32) + lane;
+        TileCursor start;
+        start.begin(unit_begin, items, units, cl, ncl);
+        uint32_t job = 0;
+        const bool ok = fp8_jobs(start, [&](int kind, uint32_t g, const TileCursor &t) -> bool {
+            // a page that was not loaded (past the item's end, or an id out of range) is not
+            // expanded; its stage only completes
+            const PageRef pg = page_of(a, t.w, t.t, kind == 1 ? (int)peer : (int)rank);
+            const bool present = pg.rows > 0 && pg.id >= 0;
+            int raw_bar, half;
+            uint32_t raw_phase, region, scale_off, full_bar;
+            if (kind == 2) {
+                raw_bar = B_RAW + 3;
+                raw_phase = g;
+                region = kOffOth;
+                scale_off = kOffScale + 3 * kScaleBytes;
+                half = (int)peer;
+                full_bar = bar(base, B_OTH_FULL);
+            } else {
+                const DhSlot d = dh_slot(g, kind);
+                raw_bar = B_RAW + d.slot;
+                raw_phase = d.fill;
+                region = kOffDh + d.slot * kDhBytes;
+                scale_off = kOffScale + d.slot * kScaleBytes;
+                half = (int)rank;
+                full_bar = bar(base, d.full);
+            }
+            if (!warp_wait(c, bar(base, raw_bar), raw_phase & 1u, false)) return false;
+            if (!present) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(base, B_DQ_SYNC));
+                if (!warp_wait(c, bar(base, B_DQ_SYNC), job & 1u, false)) return false;
+                ++job;
+                if (lane == 0) mbar_arrive(full_bar);
+                return true;
+            }
+            uint4 raw[16];  // raw[i]: codes of channels 16 ((i + dt) % 16) .. + 15 (rotated: no bank conflicts)
+            const uint8_t *rrow = gbase + region + kRawOff + dt * 256;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) raw[i] = *reinterpret_cast<const uint4 *>(rrow + ((i + dt) & 15) * 16);
+            const float *srow = reinterpret_cast<const float *>(gbase + scale_off + dt * 16);
+            const float s0 = srow[2 * half], s1 = srow[2 * half + 1];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(base, B_DQ_SYNC));
+            if (!warp_wait(c, bar(base, B_DQ_SYNC), job & 1u, false)) return false;
+            ++job;
+            uint8_t *out = gbase + region + dt * 128;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int cidx = (i + dt) & 15;
+                const float sc_ = cidx < 8 ? s0 : s1;
+                const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+                uint32_t o[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    o[2 * k] = e4m3x2_to_bf16x2(w[k], sc_);
+                    o[2 * k + 1] = e4m3x2_to_bf16x2(w[k] >> 16, sc_);
+                }
+                const int bx = cidx >> 2, q0 = (cidx & 3) * 2;
+                *reinterpret_cast<uint4 *>(out + bx * kBox + ((q0 ^ (dt & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
+                *reinterpret_cast<uint4 *>(out + bx * kBox + (((q0 + 1) ^ (dt & 7)) * 16)) =
+                    make_uint4(o[4], o[5], o[6], o[7]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full_bar);
+            return true;
+        });
+        if (!ok && lane == 0) drain_pause();
+    } else if (kFp8 && warp == 8) {
+        // ------------------------------------------------------------ FP8 raw loads (one thread)
+        if (lane == 0) {
+            TileCursor start;
+            start.begin(unit_begin, items, units, cl, ncl);
+            const bool ok = fp8_jobs(start, [&](int kind, uint32_t g, const TileCursor &t) -> bool {
+                if (kind == 2) {
+                    const PageRef pg = page_of(a, t.w, t.t, (int)rank);  // read before the wait
+                    if (!wait_bar(c, bar(base, B_OTH_EMPTY), (g & 1u) ^ 1u, false)) return false;
+                    const uint32_t rb = bar(base, B_RAW + 3), dst = base + kOffOth;
+                    if (pg.rows > 0 && pg.id >= 0) {
+                        const int32_t y = (int32_t)(pg.id * kPageRows);
+                        mbar_arrive_expect_tx(rb, 16384 + kScaleBytes + kBox);
+                        tma_load_2d(dst + kRawOff, &tmap, 256 * (int)peer, y, rb);  // other latent half, codes
+                        tma_load_2d(base + kOffScale + 3 * kScaleBytes, &tmap_sc, kDLatent, y, rb);
+                        tma_load_2d(dst + 4 * kBox, &tmap_rope, (kDLatent + 16) / 2, y, rb);  // RoPE, bf16
+                    } else {
+                        mbar_arrive(rb);
+                    }
+                    return true;
+                }
+                const PageRef pg = page_of(a, t.w, t.t, kind == 0 ? (int)rank : (int)peer);
+                const DhSlot d = dh_slot(g, kind);
+                if (d.fill > 0 && !wait_bar(c, bar(base, B_DH_EMPTY + d.slot), (d.fill - 1u) & 1u, false))
+                    return false;
+                const uint32_t rb = bar(base, B_RAW + d.slot), dst = base + kOffDh + d.slot * kDhBytes;
+                if (pg.rows > 0 && pg.id >= 0) {
+                    const int32_t y = (int32_t)(pg.id * kPageRows);
+                    mbar_arrive_expect_tx(rb, 16384 + kScaleBytes);
+                    tma_load_2d(dst + kRawOff, &tmap, 256 * (int)rank, y, rb);  // own latent half, codes
+                    tma_load_2d(base + kOffScale + d.slot * kScaleBytes, &tmap_sc, kDLatent, y, rb);
+                } else {
+                    if (pg.rows > 0) record_error(a.status, MLA_ERR_INDEX);
+                    mbar_arrive(rb);
+                }
+                return true;
+            });
+            if (!ok) drain_pause();
+        }
+    } else if (warp == 4 || warp == 7) {
         // ------------------------------------------------------------ TMA loaders (whole warps)
         TileCursor cur, nx;
         cur.begin(unit_begin, items, units, cl, ncl);
@@ -557,7 +735,11 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, DecodeArgs a) {
                             const DhSlot d = dh_slot(g, e);
                             const int ds = d.slot;
                             const int ksteps = min(4, max(0, (nvalid - kPageRows * p + 15) / 16));
-                            if (ksteps > 0 && !wait_bar(c, bar(base, d.full), d.phase & 1u, false)) {
+                            // wait even for a page that is absent (ksteps 0): the buffer is handed
+                            // back below, and for FP8 records its expansion (a stage between the raw
+                            // load and this barrier) must have passed first, or the raw loader could
+                            // run two phases ahead of it
+                            if (!wait_bar(c, bar(base, d.full), d.phase & 1u, false)) {
                                 ok = false;
                                 break;
                             }
@@ -895,21 +1077,36 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Sets the shared-memory limit of both kernel variants once per device.
+// Sets the shared-memory limit of the kernel variants once per device.
 bool set_smem_attr() {
     static bool done[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
     if (done[dev]) return true;
-    if (cudaFuncSetAttribute(decode_sm103_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(decode_sm103_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess) {
+    if (cudaFuncSetAttribute(decode_sm103_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(decode_sm103_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(decode_sm103_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+            cudaSuccess) {
         cudaGetLastError();
         return false;
     }
     done[dev] = true;
     return true;
+}
+
+// 2-D tensor map over the cache's rows (num_pages * 64 of `row_bytes` each).
+bool make_tmap(CUtensorMap *m, const void *cache, int64_t num_pages, CUtensorMapDataType dtype, int elem_bytes,
+               uint64_t row_bytes, uint32_t box_x, uint32_t box_y, CUtensorMapSwizzle swz) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / elem_bytes), (cuuint64_t)num_pages * kPageRows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {box_x, box_y};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, dtype, 2, const_cast<void *>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -923,7 +1120,7 @@ int sm103_max_units() {
     if (!set_smem_attr()) return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(kThreadsFp8, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -933,7 +1130,7 @@ int sm103_max_units() {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, decode_sm103_kernel<false>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, decode_sm103_kernel<2>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -943,25 +1140,33 @@ int sm103_max_units() {
 }
 
 cudaError_t launch_decode_sm103(const DecodeArgs &a, int num_clusters, cudaStream_t stream) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return cudaErrorNotSupported;
-    const bool sparse = a.indices != nullptr;
-    CUtensorMap tmap;
-    const cuuint64_t dims[2] = {(cuuint64_t)kDEntry, (cuuint64_t)a.num_pages * kPageRows};
-    const cuuint64_t strides[1] = {(cuuint64_t)kDEntry * 2};
-    // dense: 64-row boxes (one page); sparse: one-row boxes for tile::gather4
-    const cuuint32_t box[2] = {64, sparse ? 1u : (cuuint32_t)kPageRows};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<unsigned char *>(a.cache),
-                     dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (!set_smem_attr()) return cudaErrorInvalidValue;
-    if (sparse)
-        decode_sm103_kernel<true><<<dim3(2 * num_clusters), dim3(kThreads), kSmemBytes, stream>>>(tmap, a);
-    else
-        decode_sm103_kernel<false><<<dim3(2 * num_clusters), dim3(kThreads), kSmemBytes, stream>>>(tmap, a);
+    const dim3 grid(2 * num_clusters);
+    CUtensorMap tm, tm_sc, tm_rope;
+    if (a.kv_fp8) {
+        // records of 656 B: codes as bytes (256-B boxes, one latent half of 64 rows), the 16-B
+        // scale block, and the RoPE part as bf16 (element 264 = byte 528, 128-B swizzle)
+        if (!make_tmap(&tm, a.cache, a.num_pages, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kFp8RecordBytes, 256, kPageRows,
+                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !make_tmap(&tm_sc, a.cache, a.num_pages, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kFp8RecordBytes, 16, kPageRows,
+                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !make_tmap(&tm_rope, a.cache, a.num_pages, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kFp8RecordBytes, 64,
+                       kPageRows, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+        decode_sm103_kernel<2><<<grid, dim3(kThreadsFp8), kSmemBytes, stream>>>(tm, tm_sc, tm_rope, a);
+    } else if (a.indices) {
+        // one-row boxes for tile::gather4
+        if (!make_tmap(&tm, a.cache, a.num_pages, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)kDEntry * 2, 64, 1,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+        decode_sm103_kernel<1><<<grid, dim3(kThreads), kSmemBytes, stream>>>(tm, tm, tm, a);
+    } else {
+        // 64-row boxes: one page
+        if (!make_tmap(&tm, a.cache, a.num_pages, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)kDEntry * 2, 64,
+                       kPageRows, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+        decode_sm103_kernel<0><<<grid, dim3(kThreads), kSmemBytes, stream>>>(tm, tm, tm, a);
+    }
     return cudaGetLastError();
 }
 

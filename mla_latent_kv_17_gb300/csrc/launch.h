@@ -6,10 +6,8 @@
 
 namespace mla {
 
-cudaError_t launch_decode_simt(const DecodeArgs &a, int num_units, cudaStream_t stream);
-
-// Tensor-core kernel (bf16 cache, dense or DSA-sparse when a.indices is set): one cluster of
-// two CTAs per work unit.
+// Tensor-core kernel (bf16 cache dense or DSA-sparse when a.indices is set, or FP8 records
+// when a.kv_fp8 is set): one cluster of two CTAs per work unit.
 cudaError_t launch_decode_sm103(const DecodeArgs &a, int num_clusters, cudaStream_t stream);
 // Clusters of that kernel that fit on the current device at once (0 if unknown).
 int sm103_max_units();

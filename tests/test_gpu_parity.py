@@ -214,6 +214,15 @@ def test_sparse_contiguous_equals_dense_bitwise(L, num_sms):
     assert torch.equal(d_out, s_out) and torch.equal(d_lse, s_lse)
 
 
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("lens", [[130, 130, 130], [64, 64, 64, 64], [4262, 623, 662, 2157]])
+def test_odd_page_items_back_to_back_on_one_unit(kv, lens):
+    # one work unit takes every item in turn; odd page counts leave the second page of each
+    # item's last tile absent, so every buffer stage sees loads that carry no data
+    c = inputs.make_case(len(lens), 128, lens, seed=11, kv_dtype=kv).to("cuda")
+    check(c, num_sms=2, what=f"{kv} {lens}")
+
+
 # ------------------------------------------------------------------------------ errors
 def test_out_of_range_page_is_reported_not_faulted():
     c = small(2, 16, [100, 100], seed=6)
