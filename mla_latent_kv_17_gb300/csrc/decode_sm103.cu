@@ -61,7 +61,7 @@ constexpr uint32_t kRlBytes = 1024;              // r[128] and sum[128], fp32
 constexpr uint32_t kPBytes = 2 * kPPage + 2 * kRlBytes;
 constexpr uint32_t kMsgBytes = kPPage + kRlBytes;
 constexpr int kThreads = 256;         // dense and sparse tiles
-constexpr int kThreadsFp8 = 288;      // + a raw-load warp for FP8 records
+constexpr int kThreadsFp8 = 384;      // FP8 records: + raw-load and expansion warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 320;
 constexpr uint32_t kColQRope = kColQ + 128, kColQOther = kColQ + 160;
@@ -94,8 +94,8 @@ enum {
     B_PFREE,    // both CTAs' PV have finished reading the probability tile
     B_P_FULL,   // the probability tile holds the merged weights of its tile
     B_RAW,      // FP8: raw codes + scales of latent slot s (s < 3) or of the other-columns stage (3)
-    B_DQ_SYNC = B_RAW + 4,  // FP8: both dequant warps have read the current job's raw codes
-    B_COUNT
+    B_DQ_SYNC = B_RAW + 4,  // FP8, 2: both expansion warps of a group have read the job's raw codes
+    B_COUNT = B_DQ_SYNC + 2
 };
 static_assert(B_COUNT <= 32, "barrier area");
 
@@ -334,28 +334,23 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two, float s) {
     return pack_bf16(f.x * s, f.y * s);
 }
 
-// FP8 records: the raw loads and their expansion run as one sequence of jobs, in the order
-// other-columns(0), own(0), own(1), then for g = 0, 1, ...: peer(g), other-columns(g + 1),
-// own(g + 2) — the latent-half order of the bf16 loaders with each tile's other columns
-// slotted in.  f(kind, g, cursor): kind 0 own page, 1 peer page, 2 other columns.
+// FP8 records: the jobs of the latent-half ring (which 0: own(0), own(1), then peer(g),
+// own(g + 2) for g = 0, 1, ..., the order of the bf16 loader) or of the other-columns stage
+// (which 1: one per tile).  f(kind, g, cursor): kind 0 own page, 1 peer page, 2 other columns.
 template <typename F>
-__device__ bool fp8_jobs(const TileCursor &start, F &&f) {
-    TileCursor co = start, cp = start, ch = start;
-    uint32_t go = 0, gp = 0, gh = 0;
-    if (!ch.done()) {
-        if (!f(2, gh, ch)) return false;
-        ++gh;
-        ch.next();
+__device__ bool fp8_jobs(const TileCursor &start, int which, F &&f) {
+    if (which == 1) {
+        TileCursor ch = start;
+        for (uint32_t g = 0; !ch.done(); ++g, ch.next())
+            if (!f(2, g, ch)) return false;
+        return true;
     }
+    TileCursor co = start, cp = start;
+    uint32_t go = 0, gp = 0;
     for (int i = 0; i < 2 && !co.done(); ++i, ++go, co.next())
         if (!f(0, go, co)) return false;
     for (; !cp.done(); ++gp, cp.next()) {
         if (!f(1, gp, cp)) return false;
-        if (!ch.done()) {
-            if (!f(2, gh, ch)) return false;
-            ++gh;
-            ch.next();
-        }
         if (!co.done()) {
             if (!f(0, go, co)) return false;
             ++go;
@@ -367,8 +362,9 @@ __device__ bool fp8_jobs(const TileCursor &start, F &&f) {
 
 // kMode 0: dense bf16 tiles (128 consecutive tokens, two pages, 64-row boxes).
 // kMode 1: DSA sparse tiles (128 index slots gathered row by row, tile::gather4).
-// kMode 2: dense FP8 records: raw e4m3 codes and scales are loaded by an extra warp and
-//          expanded to bf16 operand tiles by the two loader warps; RoPE goes in directly.
+// kMode 2: dense FP8 records: raw e4m3 codes and scales are loaded by two extra warps (one
+//          for the latent-half ring, one for the other-columns stage) and expanded to bf16
+//          operand tiles by two pairs of warps; RoPE goes in directly.
 // tmap: the cache (kMode 2: its bytes, 256-B boxes of codes); tmap_sc / tmap_rope: FP8
 // scales (16-B boxes) and RoPE (bf16, 128-B swizzle), unused otherwise.
 template <int kMode>
@@ -399,6 +395,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
         }
         for (int s = 0; s < 4; ++s) mbar_init(bar(base, B_RAW + s), 1);
         mbar_init(bar(base, B_DQ_SYNC), 2);
+        mbar_init(bar(base, B_DQ_SYNC + 1), 2);
         mbar_init(bar(base, B_OTH_FULL), kFullCount);
         mbar_init(bar(base, B_OTH_EMPTY), 1);
         mbar_init(bar(base, B_S_FULL), 1);
@@ -436,17 +433,20 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
     const int units = hd->num_units;
     const int cl = (int)cluster_id_x(), ncl = (int)nclusters_x();
 
-    if (kFp8 && (warp == 4 || warp == 7)) {
-        // ------------------------------------------------------------ FP8 expansion (two warps)
-        // Thread dt expands row dt of each job: reads its 256 codes and two block scales,
-        // waits until the other warp has read its rows too (the bf16 output overwrites the
-        // raw codes in the upper half of the same buffer), then writes 256 scaled bf16 values
-        // into the 128-B-swizzled boxes.
-        const int dt = (warp == 4 ? 0 : 32) + lane;
+    if (kFp8 && (warp == 4 || warp == 10 || warp == 7 || warp == 9)) {
+        // ------------------------------------------------------------ FP8 expansion (two pairs)
+        // Warps 4 and 10 expand the latent-half ring, warps 7 and 9 the other-columns stage
+        // (one of each pair per SM sub-partition).  Thread dt expands row dt of each job:
+        // reads its 256 codes and two block scales, waits until the other warp of its pair
+        // has read its rows too (the bf16 output overwrites the raw codes in the upper half
+        // of the same buffer), then writes 256 scaled bf16 values into the swizzled boxes.
+        const int which = (warp == 4 || warp == 10) ? 0 : 1;
+        const int dt = ((warp == 4 || warp == 7) ? 0 : 32) + lane;
+        const uint32_t sync_bar = bar(base, B_DQ_SYNC + which);
         TileCursor start;
         start.begin(unit_begin, items, units, cl, ncl);
         uint32_t job = 0;
-        const bool ok = fp8_jobs(start, [&](int kind, uint32_t g, const TileCursor &t) -> bool {
+        const bool ok = fp8_jobs(start, which, [&](int kind, uint32_t g, const TileCursor &t) -> bool {
             // a page that was not loaded (past the item's end, or an id out of range) is not
             // expanded; its stage only completes
             const PageRef pg = page_of(a, t.w, t.t, kind == 1 ? (int)peer : (int)rank);
@@ -472,8 +472,8 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
             if (!warp_wait(c, bar(base, raw_bar), raw_phase & 1u, false)) return false;
             if (!present) {
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(base, B_DQ_SYNC));
-                if (!warp_wait(c, bar(base, B_DQ_SYNC), job & 1u, false)) return false;
+                if (lane == 0) mbar_arrive(sync_bar);
+                if (!warp_wait(c, sync_bar, job & 1u, false)) return false;
                 ++job;
                 if (lane == 0) mbar_arrive(full_bar);
                 return true;
@@ -485,8 +485,8 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
             const float *srow = reinterpret_cast<const float *>(gbase + scale_off + dt * 16);
             const float s0 = srow[2 * half], s1 = srow[2 * half + 1];
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(base, B_DQ_SYNC));
-            if (!warp_wait(c, bar(base, B_DQ_SYNC), job & 1u, false)) return false;
+            if (lane == 0) mbar_arrive(sync_bar);
+            if (!warp_wait(c, sync_bar, job & 1u, false)) return false;
             ++job;
             uint8_t *out = gbase + region + dt * 128;
 #pragma unroll
@@ -511,12 +511,13 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
             return true;
         });
         if (!ok && lane == 0) drain_pause();
-    } else if (kFp8 && warp == 8) {
-        // ------------------------------------------------------------ FP8 raw loads (one thread)
+    } else if (kFp8 && (warp == 8 || warp == 11)) {
+        // ------------------------------------------------------------ FP8 raw loads (one thread each:
+        // warp 8 the latent-half ring, warp 11 the other-columns stage)
         if (lane == 0) {
             TileCursor start;
             start.begin(unit_begin, items, units, cl, ncl);
-            const bool ok = fp8_jobs(start, [&](int kind, uint32_t g, const TileCursor &t) -> bool {
+            const bool ok = fp8_jobs(start, warp == 8 ? 0 : 1, [&](int kind, uint32_t g, const TileCursor &t) -> bool {
                 if (kind == 2) {
                     const PageRef pg = page_of(a, t.w, t.t, (int)rank);  // read before the wait
                     if (!wait_bar(c, bar(base, B_OTH_EMPTY), (g & 1u) ^ 1u, false)) return false;
