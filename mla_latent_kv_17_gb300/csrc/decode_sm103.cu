@@ -77,7 +77,6 @@ constexpr uint32_t kOffMisc = kOffBar + 8 * 32;
 // FP8 records: per-row scales of the three latent-half slots and the other-columns stage
 constexpr uint32_t kOffScale = (kOffMisc + 64 + 1023) / 1024 * 1024;
 constexpr uint32_t kScaleBytes = 64 * 16;  // 64 rows x 4 fp32
-constexpr uint32_t kRawOff = 16384;         // FP8 codes land in the upper half of their bf16 destination
 constexpr uint32_t kSmemBytes = kOffScale + 4 * kScaleBytes + 1024;  // + slack for 1024-B alignment
 static_assert(kSmemBytes <= 232448, "shared memory");
 
@@ -94,8 +93,7 @@ enum {
     B_PFREE,    // both CTAs' PV have finished reading the probability tile
     B_P_FULL,   // the probability tile holds the merged weights of its tile
     B_RAW,      // FP8: raw codes + scales of latent slot s (s < 3) or of the other-columns stage (3)
-    B_DQ_SYNC = B_RAW + 4,  // FP8, 2: both expansion warps of a group have read the job's raw codes
-    B_COUNT = B_DQ_SYNC + 2
+    B_COUNT = B_RAW + 4
 };
 static_assert(B_COUNT <= 32, "barrier area");
 
@@ -334,45 +332,67 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two, float s) {
     return pack_bf16(f.x * s, f.y * s);
 }
 
-// FP8 records: the jobs of the latent-half ring (which 0: own(0), own(1), then peer(g),
-// own(g + 2) for g = 0, 1, ..., the order of the bf16 loader) or of the other-columns stage
-// (which 1: one per tile).  f(kind, g, cursor): kind 0 own page, 1 peer page, 2 other columns.
+// Expands 16 e4m3 codes (v) with block scale s into the 16-code chunk q (0..3) of row r of a
+// bf16 box: box points at row r of a box of 64 columns stored as 128-B rows in the 128-B
+// swizzle (16-B unit u of row r at u ^ (r % 8)); chunk q covers units 2q and 2q + 1.
+__device__ __forceinline__ void expand_chunk(uint4 v, float s, uint8_t *box, int q, int r) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        o[2 * k] = e4m3x2_to_bf16x2(w[k], s);
+        o[2 * k + 1] = e4m3x2_to_bf16x2(w[k] >> 16, s);
+    }
+    *reinterpret_cast<uint4 *>(box + (((2 * q) ^ (r & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4 *>(box + (((2 * q + 1) ^ (r & 7)) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// FP8 records: the jobs of the latent-half ring (which 0: own(0), own(1), peer(0), then
+// peer(g + 1), own(g + 2) for g = 0, 1, ...), of the other-columns stage (which 1: oth(g),
+// one per tile), or all of them in the order they are consumed (which 2: oth(0), own(0),
+// own(1), peer(0), then oth(g + 1), peer(g + 1), own(g + 2)).  f(kind, g, cursor): kind 0 own
+// page, 1 peer page, 2 other columns.  Every job comes after the jobs whose consumers free its
+// buffer: peer(g + 1) and own(g + 2) take the slots PV(g) frees, oth(g + 1) the stage QK(g)
+// frees; and peer(g + 1), which PV(g + 1) waits for, goes before own(g + 2), which only
+// QK(g + 2) needs.  One call site of f: the job bodies are large.
 template <typename F>
 __device__ bool fp8_jobs(const TileCursor &start, int which, F &&f) {
-    if (which == 1) {
-        TileCursor ch = start;
-        for (uint32_t g = 0; !ch.done(); ++g, ch.next())
-            if (!f(2, g, ch)) return false;
-        return true;
-    }
-    TileCursor co = start, cp = start;
-    uint32_t go = 0, gp = 0;
-    for (int i = 0; i < 2 && !co.done(); ++i, ++go, co.next())
-        if (!f(0, go, co)) return false;
-    for (; !cp.done(); ++gp, cp.next()) {
-        if (!f(1, gp, cp)) return false;
-        if (!co.done()) {
-            if (!f(0, go, co)) return false;
-            ++go;
-            co.next();
+    TileCursor cur[3] = {start, start, start};  // next own, peer, other-columns job
+    uint32_t gk[3] = {0u, 0u, 0u};
+    for (int step = 0;; ++step) {
+        int kind;
+        if (which == 1) {
+            kind = 2;
+        } else if (which == 0) {
+            kind = step < 3 ? (step < 2 ? 0 : 1) : ((step - 3) & 1) ? 0 : 1;
+        } else {
+            const int k = (step - 4) % 3;
+            kind = step < 4 ? (step == 0 ? 2 : step < 3 ? 0 : 1) : k == 0 ? 2 : k == 1 ? 1 : 0;
         }
+        if (cur[kind].done()) {
+            const bool dh_done = cur[0].done() && cur[1].done();
+            if (which == 0 ? dh_done : which == 1 ? true : dh_done && cur[2].done()) return true;
+            continue;
+        }
+        if (!f(kind, gk[kind], cur[kind])) return false;
+        ++gk[kind];
+        cur[kind].next();
     }
-    return true;
 }
 
 // kMode 0: dense bf16 tiles (128 consecutive tokens, two pages, 64-row boxes).
 // kMode 1: DSA sparse tiles (128 index slots gathered row by row, tile::gather4).
 // kMode 2: dense FP8 records: raw e4m3 codes and scales are loaded by two extra warps (one
 //          for the latent-half ring, one for the other-columns stage) and expanded to bf16
-//          operand tiles by two pairs of warps; RoPE goes in directly.
-// tmap: the cache (kMode 2: its bytes, 256-B boxes of codes); tmap_sc / tmap_rope: FP8
+//          operand tiles by four warps; RoPE goes in directly.
+// tmap: the cache (kMode 2: its bytes, 128-B boxes of codes); tmap_sc / tmap_rope: FP8
 // scales (16-B boxes) and RoPE (bf16, 128-B swizzle), unused otherwise.
 template <int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMode == 2 ? kThreadsFp8 : kThreads, 1)
 decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_sc,
                     const __grid_constant__ CUtensorMap tmap_rope, DecodeArgs a) {
     constexpr bool kSparse = kMode == 1, kFp8 = kMode == 2;
-    constexpr uint32_t kFullCount = kFp8 ? 2u : 1u;  // arrivals that complete a latent / other-columns stage
+    constexpr uint32_t kFullCount = kFp8 ? 4u : 1u;  // arrivals that complete a latent / other-columns stage
     extern __shared__ uint8_t smem_raw[];
     if (!plan_matches(a)) {
         if (threadIdx.x == 0 && blockIdx.x == 0) record_error(a.status, MLA_ERR_WORKSPACE);
@@ -394,8 +414,6 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
             mbar_init(bar(base, B_DH_EMPTY + s), 1);
         }
         for (int s = 0; s < 4; ++s) mbar_init(bar(base, B_RAW + s), 1);
-        mbar_init(bar(base, B_DQ_SYNC), 2);
-        mbar_init(bar(base, B_DQ_SYNC + 1), 2);
         mbar_init(bar(base, B_OTH_FULL), kFullCount);
         mbar_init(bar(base, B_OTH_EMPTY), 1);
         mbar_init(bar(base, B_S_FULL), 1);
@@ -434,23 +452,21 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
     const int cl = (int)cluster_id_x(), ncl = (int)nclusters_x();
 
     if (kFp8 && (warp == 4 || warp == 10 || warp == 7 || warp == 9)) {
-        // ------------------------------------------------------------ FP8 expansion (two pairs)
-        // Warps 4 and 10 expand the latent-half ring, warps 7 and 9 the other-columns stage
-        // (one of each pair per SM sub-partition).  Thread dt expands row dt of each job:
-        // reads its 256 codes and two block scales, waits until the other warp of its pair
-        // has read its rows too (the bf16 output overwrites the raw codes in the upper half
-        // of the same buffer), then writes 256 scaled bf16 values into the swizzled boxes.
-        const int which = (warp == 4 || warp == 10) ? 0 : 1;
-        const int dt = ((warp == 4 || warp == 7) ? 0 : 32) + lane;
-        const uint32_t sync_bar = bar(base, B_DQ_SYNC + which);
+        // ------------------------------------------------------------ FP8 expansion (4 warps)
+        // Warps 4, 10, 7 and 9 (one per SM sub-partition) expand every job, in the order the
+        // jobs are consumed.  Thread (r, p) expands part p (codes 128 p .. 128 p + 127) of row
+        // r.  The codes of part p of row r arrive as one 128-B row of box 2p of the bf16
+        // destination, the box that receives the first half of that part's output; the second
+        // half goes to box 2p + 1 first, then the first half lands on the codes it came from,
+        // read into registers beforehand.  No thread writes another thread's codes.
+        const int eidx = warp == 4 ? 0 : warp == 10 ? 1 : warp == 7 ? 2 : 3;
+        const int r = 32 * (eidx & 1) + lane, p = eidx >> 1;
         TileCursor start;
         start.begin(unit_begin, items, units, cl, ncl);
-        uint32_t job = 0;
-        const bool ok = fp8_jobs(start, which, [&](int kind, uint32_t g, const TileCursor &t) -> bool {
+        const bool ok = fp8_jobs(start, 2, [&](int kind, uint32_t g, const TileCursor &t) -> bool {
             // a page that was not loaded (past the item's end, or an id out of range) is not
             // expanded; its stage only completes
             const PageRef pg = page_of(a, t.w, t.t, kind == 1 ? (int)peer : (int)rank);
-            const bool present = pg.rows > 0 && pg.id >= 0;
             int raw_bar, half;
             uint32_t raw_phase, region, scale_off, full_bar;
             if (kind == 2) {
@@ -470,42 +486,26 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                 full_bar = bar(base, d.full);
             }
             if (!warp_wait(c, bar(base, raw_bar), raw_phase & 1u, false)) return false;
-            if (!present) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(sync_bar);
-                if (!warp_wait(c, sync_bar, job & 1u, false)) return false;
-                ++job;
-                if (lane == 0) mbar_arrive(full_bar);
-                return true;
-            }
-            uint4 raw[16];  // raw[i]: codes of channels 16 ((i + dt) % 16) .. + 15 (rotated: no bank conflicts)
-            const uint8_t *rrow = gbase + region + kRawOff + dt * 256;
+            if (pg.rows > 0 && pg.id >= 0) {
+                const float sc = reinterpret_cast<const float *>(gbase + scale_off + r * 16)[2 * half + p];
+                uint8_t *row = gbase + region + r * 128;                 // row r of box 0
+                const uint8_t *codes = row + 2 * p * kBox;               // its 8 chunks of 16 codes
+                uint8_t *first = row + 2 * p * kBox, *second = first + kBox;
+                uint4 v[4];  // chunks (i + r) % 4, read before their box is overwritten
 #pragma unroll
-            for (int i = 0; i < 16; ++i) raw[i] = *reinterpret_cast<const uint4 *>(rrow + ((i + dt) & 15) * 16);
-            const float *srow = reinterpret_cast<const float *>(gbase + scale_off + dt * 16);
-            const float s0 = srow[2 * half], s1 = srow[2 * half + 1];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sync_bar);
-            if (!warp_wait(c, sync_bar, job & 1u, false)) return false;
-            ++job;
-            uint8_t *out = gbase + region + dt * 128;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int cidx = (i + dt) & 15;
-                const float sc_ = cidx < 8 ? s0 : s1;
-                const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-                uint32_t o[8];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    o[2 * k] = e4m3x2_to_bf16x2(w[k], sc_);
-                    o[2 * k + 1] = e4m3x2_to_bf16x2(w[k] >> 16, sc_);
+                for (int i = 0; i < 4; ++i) v[i] = *reinterpret_cast<const uint4 *>(codes + ((i + r) & 3) * 16);
+                // chunks 4 + (i + r) % 4 -> second box (rotated: no bank conflicts on the stores)
+                uint4 nxt = *reinterpret_cast<const uint4 *>(codes + (4 + (r & 3)) * 16);
+#pragma unroll 1
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 cur = nxt;
+                    if (i < 3) nxt = *reinterpret_cast<const uint4 *>(codes + (4 + ((i + 1 + r) & 3)) * 16);
+                    expand_chunk(cur, sc, second, (i + r) & 3, r);
                 }
-                const int bx = cidx >> 2, q0 = (cidx & 3) * 2;
-                *reinterpret_cast<uint4 *>(out + bx * kBox + ((q0 ^ (dt & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
-                *reinterpret_cast<uint4 *>(out + bx * kBox + (((q0 + 1) ^ (dt & 7)) * 16)) =
-                    make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) expand_chunk(v[i], sc, first, (i + r) & 3, r);
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(full_bar);
             return true;
@@ -525,7 +525,8 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                     if (pg.rows > 0 && pg.id >= 0) {
                         const int32_t y = (int32_t)(pg.id * kPageRows);
                         mbar_arrive_expect_tx(rb, 16384 + kScaleBytes + kBox);
-                        tma_load_2d(dst + kRawOff, &tmap, 256 * (int)peer, y, rb);  // other latent half, codes
+                        tma_load_2d(dst, &tmap, 256 * (int)peer, y, rb);  // other latent half, codes
+                        tma_load_2d(dst + 2 * kBox, &tmap, 256 * (int)peer + 128, y, rb);
                         tma_load_2d(base + kOffScale + 3 * kScaleBytes, &tmap_sc, kDLatent, y, rb);
                         tma_load_2d(dst + 4 * kBox, &tmap_rope, (kDLatent + 16) / 2, y, rb);  // RoPE, bf16
                     } else {
@@ -541,7 +542,8 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                 if (pg.rows > 0 && pg.id >= 0) {
                     const int32_t y = (int32_t)(pg.id * kPageRows);
                     mbar_arrive_expect_tx(rb, 16384 + kScaleBytes);
-                    tma_load_2d(dst + kRawOff, &tmap, 256 * (int)rank, y, rb);  // own latent half, codes
+                    tma_load_2d(dst, &tmap, 256 * (int)rank, y, rb);  // own latent half, codes
+                    tma_load_2d(dst + 2 * kBox, &tmap, 256 * (int)rank + 128, y, rb);
                     tma_load_2d(base + kOffScale + d.slot * kScaleBytes, &tmap_sc, kDLatent, y, rb);
                 } else {
                     if (pg.rows > 0) record_error(a.status, MLA_ERR_INDEX);
@@ -762,7 +764,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
             }
             if (!ok) drain_pause();
         }
-    } else {
+    } else if (warp < 4) {
         // ------------------------------------------------------------ softmax + epilogue
         // Per tile: part A (scores -> own weights -> message to the peer), then part B
         // (merge with the peer's message -> PV may start).
@@ -1145,9 +1147,9 @@ cudaError_t launch_decode_sm103(const DecodeArgs &a, int num_clusters, cudaStrea
     const dim3 grid(2 * num_clusters);
     CUtensorMap tm, tm_sc, tm_rope;
     if (a.kv_fp8) {
-        // records of 656 B: codes as bytes (256-B boxes, one latent half of 64 rows), the 16-B
+        // records of 656 B: codes as bytes (128-B boxes, a quarter of the latent of 64 rows), the 16-B
         // scale block, and the RoPE part as bf16 (element 264 = byte 528, 128-B swizzle)
-        if (!make_tmap(&tm, a.cache, a.num_pages, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kFp8RecordBytes, 256, kPageRows,
+        if (!make_tmap(&tm, a.cache, a.num_pages, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kFp8RecordBytes, 128, kPageRows,
                        CU_TENSOR_MAP_SWIZZLE_NONE) ||
             !make_tmap(&tm_sc, a.cache, a.num_pages, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kFp8RecordBytes, 16, kPageRows,
                        CU_TENSOR_MAP_SWIZZLE_NONE) ||
