@@ -92,6 +92,7 @@ enum {
     B_RFULL,    // the peer's message for the current tile has landed
     B_PFREE,    // both CTAs' PV have finished reading the probability tile
     B_P_FULL,   // the probability tile holds the merged weights of its tile
+    B_QLD,      // a round of query boxes has landed in the query area
     B_RAW,      // FP8: raw codes + scales of latent slot s (s < 3) or of the other-columns stage (3)
     B_COUNT = B_RAW + 4
 };
@@ -163,13 +164,20 @@ struct PageRef {
     int rows;
     int64_t id;
 };
+// The block-table entry is read with a volatile load: it is issued where page_of is called
+// (callers call it ahead of a barrier wait) and not sunk to the first use of the id.
+__device__ __forceinline__ int32_t ld_early(const int32_t *p) {
+    int32_t v;
+    asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
 __device__ __forceinline__ PageRef page_of(const DecodeArgs &a, const WorkItem &w, int t, int p) {
     const int t_p = t + kPageRows * p;
     PageRef r{0, -1};
     if (t_p >= w.t1) return r;
     r.rows = min(kPageRows, w.t1 - t_p);
     const int lp = t_p / kPageRows;
-    const int64_t id = lp < a.max_pages ? (int64_t)a.block_table[(int64_t)w.b * a.max_pages + lp] : -1;
+    const int64_t id = lp < a.max_pages ? (int64_t)ld_early(a.block_table + (int64_t)w.b * a.max_pages + lp) : -1;
     r.id = (id >= 0 && id < a.num_pages) ? id : -1;
     return r;
 }
@@ -386,11 +394,13 @@ __device__ bool fp8_jobs(const TileCursor &start, int which, F &&f) {
 //          for the latent-half ring, one for the other-columns stage) and expanded to bf16
 //          operand tiles by four warps; RoPE goes in directly.
 // tmap: the cache (kMode 2: its bytes, 128-B boxes of codes); tmap_sc / tmap_rope: FP8
-// scales (16-B boxes) and RoPE (bf16, 128-B swizzle), unused otherwise.
+// scales (16-B boxes) and RoPE (bf16, 128-B swizzle), unused otherwise; tmap_qn / tmap_qr:
+// the queries (64 columns x 128 heads of one request, 128-B swizzle).
 template <int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMode == 2 ? kThreadsFp8 : kThreads, 1)
 decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_sc,
-                    const __grid_constant__ CUtensorMap tmap_rope, DecodeArgs a) {
+                    const __grid_constant__ CUtensorMap tmap_rope, const __grid_constant__ CUtensorMap tmap_qn,
+                    const __grid_constant__ CUtensorMap tmap_qr, DecodeArgs a) {
     constexpr bool kSparse = kMode == 1, kFp8 = kMode == 2;
     constexpr uint32_t kFullCount = kFp8 ? 4u : 1u;  // arrivals that complete a latent / other-columns stage
     extern __shared__ uint8_t smem_raw[];
@@ -423,6 +433,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
         mbar_init(bar(base, B_RFULL), 1);  // + the message bytes
         mbar_init(bar(base, B_PFREE), 2);  // one commit from each CTA's PV
         mbar_init(bar(base, B_P_FULL), 4);
+        mbar_init(bar(base, B_QLD), 1);  // + the boxes' bytes
         misc[1] = 0u;
         fence_mbar_init();
     }
@@ -432,6 +443,8 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
     }
     if (warp == 4 && lane == 0) {
         prefetch_tmap(&tmap);
+        prefetch_tmap(&tmap_qn);
+        prefetch_tmap(&tmap_qr);
         if (kFp8) {
             prefetch_tmap(&tmap_sc);
             prefetch_tmap(&tmap_rope);
@@ -774,47 +787,51 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
         const float sc = a.scale_log2;  // > 0, checked on the host
         uint8_t *ps = gbase + kOffP;
         // Query of request bq: 384 columns into TMEM (own latent half, RoPE, the other
-        // half's first 64), 192 into shared memory (the other half's last 192); three
-        // batches of 24 independent 16-byte loads per thread.
-        auto load_q = [&](int bq) {
-            const uint4 *qn = reinterpret_cast<const uint4 *>(a.q_nope + ((int64_t)bq * a.H + h) * kDLatent);
-            const uint4 *qr = reinterpret_cast<const uint4 *>(a.q_rope + ((int64_t)bq * a.H + h) * kDRope);
-            for (int batch = 0; batch < 3; ++batch) {
-                uint4 x[24];
-#pragma unroll
-                for (int i = 0; i < 24; ++i) {
-                    // block 0-3: own half, 4: RoPE, 5: other half 0-63, 6-8: other half 64-255
-                    const int blk = 3 * batch + i / 8;
-                    const uint4 *src = blk < 4 ? qn + (256 * rank + 64 * blk) / 8
-                                       : blk == 4 ? qr
-                                                  : qn + (256 * peer + 64 * (blk - 5)) / 8;
-                    x[i] = h < a.H ? src[i % 8] : make_uint4(0u, 0u, 0u, 0u);
-                }
-#pragma unroll
-                for (int j = 0; j < 3; ++j) {
-                    const int blk = 3 * batch + j;
-                    if (blk < 6) {
-                        uint32_t v[32];
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            v[4 * q] = x[8 * j + q].x;
-                            v[4 * q + 1] = x[8 * j + q].y;
-                            v[4 * q + 2] = x[8 * j + q].z;
-                            v[4 * q + 3] = x[8 * j + q].w;
-                        }
-                        tmem_st32(trow + kColQ + 32u * blk, v);
-                    } else {
-                        uint8_t *row = gbase + kOffQs + (blk - 6) * kQsBox + h * 128;
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4 *>(row + ((q ^ (h & 7)) * 16)) = x[8 * j + q];
+        // half's first 64), 192 into shared memory (the other half's last 192).  The TMA brings
+        // them in three rounds of three 64-column boxes (128 heads, 128-B swizzle) through the
+        // shared-memory query area: rounds 0 and 1 go on to TMEM, each thread moving its own
+        // head's row; round 2 stays.  Heads at or beyond H lie outside the tensor: zeros.
+        uint32_t qphase = 0;
+        auto load_q = [&](int bq) -> bool {
+            const uint32_t qb = bar(base, B_QLD);
+            for (int round = 0; round < 3; ++round) {
+                if (threadIdx.x == 0) {
+                    mbar_arrive_expect_tx(qb, 3 * kQsBox);
+                    for (int i = 0; i < 3; ++i) {
+                        // block 0-3: own half, 4: RoPE, 5: other half 0-63, 6-8: other half 64-255
+                        const int blk = 3 * round + i;
+                        const uint32_t dst = base + kOffQs + i * kQsBox;
+                        if (blk == 4)
+                            tma_load_3d(dst, &tmap_qr, 0, 0, bq, qb);
+                        else
+                            tma_load_3d(dst, &tmap_qn, blk < 4 ? 256 * (int)rank + 64 * blk : 256 * (int)peer + 64 * (blk - 5),
+                                        0, bq, qb);
                     }
                 }
+                if (!warp_wait(c, qb, qphase & 1u, false)) return false;
+                ++qphase;
+                if (round == 2) break;
+#pragma unroll 1
+                for (int i = 0; i < 3; ++i) {
+                    const uint8_t *row = gbase + kOffQs + i * kQsBox + h * 128;
+                    uint32_t v[32];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const uint4 x = *reinterpret_cast<const uint4 *>(row + ((q ^ (h & 7)) * 16));
+                        v[4 * q] = x.x;
+                        v[4 * q + 1] = x.y;
+                        v[4 * q + 2] = x.z;
+                        v[4 * q + 3] = x.w;
+                    }
+                    tmem_st32(trow + kColQ + 32u * (3 * round + i), v);
+                }
+                named_bar_sync(1, 128);  // every head's rows are read before the next round lands
             }
-            fence_proxy_async_smem();
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(base, B_Q_READY));
+            return true;
         };
         uint32_t g = 0, nitem = 0;
         bool ok = true, q_ready = false;  // q_ready: the current item's query is in place
@@ -839,7 +856,10 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                     }
                     continue;
                 }
-                if (!q_ready) load_q(b);
+                if (!q_ready && !load_q(b)) {
+                    ok = false;
+                    break;
+                }
                 q_ready = false;
                 // the next item's query is loaded at the end of this one: bring it into L2 now
                 const int bnext = next_request(unit_begin, items, units, ncl, u, it);
@@ -893,6 +913,18 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                         lown += p0 + p1;
                         pk[i] = pack_bf16(p0, p1);
                     }
+                    // cache rows that PV reads but must not contribute (rows of the last
+                    // 16-row step past the end, a page whose id was out of range, sparse slots
+                    // that are padding or out of range) must hold zeros there, not whatever
+                    // the loaded row holds; decided here, off the merge's path
+                    uint64_t zmask[2];
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+                        const PageMask pm = p == 0 ? pm0 : pm1;
+                        const int z1 = min(kPageRows, (pm.cnt + 15) & ~15);
+                        zmask[p] = ~pm.valid & (z1 >= 64 ? ~0ull : ((1ull << z1) - 1ull));
+                    }
+                    const bool need_zero = (zmask[0] | zmask[1]) != 0ull;  // the same in every lane
                     // the tile is reused: both CTAs' PV of the previous tile must be done
                     if (g > 0 && !warp_wait(c, bar(base, B_PFREE), (g - 1) & 1u, true)) {
                         ok = false;
@@ -954,15 +986,11 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                         scale_row(reinterpret_cast<uint4 *>(ps + peer * kPPage + h * 128), fpeer);
                         wrote = true;
                     }
-                    // cache rows that PV reads but must not contribute (rows of the last
-                    // 16-row step past the end, a page whose id was out of range, sparse slots
-                    // that are padding or out of range) must hold zeros there, not whatever
-                    // the loaded row holds
-                    for (int p = 0; p < 2; ++p) {
-                        const PageMask pm = p == 0 ? pm0 : pm1;
-                        const int z1 = min(kPageRows, (pm.cnt + 15) & ~15);
-                        const uint64_t zero = ~pm.valid & (z1 >= 64 ? ~0ull : ((1ull << z1) - 1ull));
+                    // zero the rows decided in part A
+                    for (int p = 0; p < 2 && need_zero; ++p) {
+                        const uint64_t zero = zmask[p];
                         if (zero == 0ull) continue;
+                        const int z1 = 64 - __clzll((long long)zero);  // rows below the last one to zero
                         const DhSlot d = dh_slot(g, p == (int)rank ? 0 : 1);
                         const int ds = d.slot;
                         // wait for the slot's load (or its empty arrival) to land first
@@ -1005,7 +1033,10 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                 // read), so the query columns are free; loading now lets the next item's
                 // QK^T overlap this item's last PV and epilogue
                 if (bnext >= 0) {
-                    load_q(bnext);
+                    if (!load_q(bnext)) {
+                        ok = false;
+                        break;
+                    }
                     q_ready = true;
                 }
                 // ---- epilogue: wait for the last PV of this item, normalise, store
@@ -1112,6 +1143,20 @@ bool make_tmap(CUtensorMap *m, const void *cache, int64_t num_pages, CUtensorMap
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Queries [B][H][cols] bf16 as a 3-D tensor (cols, H, B); boxes of 64 columns x 128 heads of
+// one request, 128-B swizzle.  Heads at or beyond H fall outside the tensor and read zeros.
+bool make_tmap_q(CUtensorMap *m, const void *q, int cols, int H, int B) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)H, (cuuint64_t)B};
+    const cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)cols * 2 * H};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 int sm103_max_units() {
@@ -1145,7 +1190,9 @@ int sm103_max_units() {
 cudaError_t launch_decode_sm103(const DecodeArgs &a, int num_clusters, cudaStream_t stream) {
     if (!set_smem_attr()) return cudaErrorInvalidValue;
     const dim3 grid(2 * num_clusters);
-    CUtensorMap tm, tm_sc, tm_rope;
+    CUtensorMap tm, tm_sc, tm_rope, tm_qn, tm_qr;
+    if (!make_tmap_q(&tm_qn, a.q_nope, kDLatent, a.H, a.B) || !make_tmap_q(&tm_qr, a.q_rope, kDRope, a.H, a.B))
+        return cudaErrorInvalidValue;
     if (a.kv_fp8) {
         // records of 656 B: codes as bytes (128-B boxes, a quarter of the latent of 64 rows), the 16-B
         // scale block, and the RoPE part as bf16 (element 264 = byte 528, 128-B swizzle)
@@ -1156,19 +1203,19 @@ cudaError_t launch_decode_sm103(const DecodeArgs &a, int num_clusters, cudaStrea
             !make_tmap(&tm_rope, a.cache, a.num_pages, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kFp8RecordBytes, 64,
                        kPageRows, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
-        decode_sm103_kernel<2><<<grid, dim3(kThreadsFp8), kSmemBytes, stream>>>(tm, tm_sc, tm_rope, a);
+        decode_sm103_kernel<2><<<grid, dim3(kThreadsFp8), kSmemBytes, stream>>>(tm, tm_sc, tm_rope, tm_qn, tm_qr, a);
     } else if (a.indices) {
         // one-row boxes for tile::gather4
         if (!make_tmap(&tm, a.cache, a.num_pages, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)kDEntry * 2, 64, 1,
                        CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
-        decode_sm103_kernel<1><<<grid, dim3(kThreads), kSmemBytes, stream>>>(tm, tm, tm, a);
+        decode_sm103_kernel<1><<<grid, dim3(kThreads), kSmemBytes, stream>>>(tm, tm, tm, tm_qn, tm_qr, a);
     } else {
         // 64-row boxes: one page
         if (!make_tmap(&tm, a.cache, a.num_pages, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)kDEntry * 2, 64,
                        kPageRows, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
-        decode_sm103_kernel<0><<<grid, dim3(kThreads), kSmemBytes, stream>>>(tm, tm, tm, a);
+        decode_sm103_kernel<0><<<grid, dim3(kThreads), kSmemBytes, stream>>>(tm, tm, tm, tm_qn, tm_qr, a);
     }
     return cudaGetLastError();
 }

@@ -131,6 +131,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int3
         :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int32_t x, int32_t y, int32_t z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
 // Four rows (tensor rows r0..r3, columns x .. x + box width) of a 2-D tensor whose box is
 // one row high, written to consecutive rows at dst with the tensor map's swizzle.
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int32_t x, int32_t r0, int32_t r1,
