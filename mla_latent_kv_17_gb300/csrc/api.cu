@@ -48,46 +48,65 @@ __device__ int64_t block_exclusive_scan(int64_t v, int64_t *total, int64_t *sh) 
 }
 
 __global__ void __launch_bounds__(kPlanThreads)
-plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int units, unsigned char *ws) {
+plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int units, unsigned char *ws, int iu_in_smem) {
     __shared__ int64_t sh[kPlanWarps];
+    extern __shared__ int32_t s_iu[];  // items' units (when max_items of them fit)
+    grid_dep_wait();    // seq_lens may come from the kernel before this one on the stream
+    grid_dep_launch();  // the decode kernel may launch now; it waits for this plan to complete
     const WsLayout L = ws_layout(B, H, units);
     int64_t *req_start = reinterpret_cast<int64_t *>(ws + L.req_start);
     int32_t *num_splits = reinterpret_cast<int32_t *>(ws + L.num_splits);
     int32_t *split_base = reinterpret_cast<int32_t *>(ws + L.split_base);
     int32_t *unit_begin = reinterpret_cast<int32_t *>(ws + L.unit_begin);
-    const int32_t *item_unit = reinterpret_cast<const int32_t *>(ws + L.item_unit);
+    const int32_t *item_unit = iu_in_smem ? s_iu : reinterpret_cast<const int32_t *>(ws + L.item_unit);
     const int chunk = (B + kPlanThreads - 1) / kPlanThreads;
     const int b0 = min(B, (int)threadIdx.x * chunk), b1 = min(B, b0 + chunk);
 
+    // budget positions: the running position stays in a register (req_start is only written)
     int64_t local = 0;
     for (int b = b0; b < b1; ++b) local += req_cost(req_tiles(seq_lens, topk, b));
     int64_t total;
-    int64_t pos = block_exclusive_scan(local, &total, sh);
-    for (int b = b0; b < b1; ++b) {
-        req_start[b] = pos;
-        pos += req_cost(req_tiles(seq_lens, topk, b));
-    }
+    const int64_t pos0 = block_exclusive_scan(local, &total, sh);
     const int64_t per = plan_budget(total, units);
 
-    int64_t n_local = 0, s_local = 0;
-    for (int b = b0; b < b1; ++b) {
-        const ReqSplit r = req_split(req_start[b], req_tiles(seq_lens, topk, b), per, units);
-        n_local += r.n;
-        if (r.n > 1) s_local += r.n;
+    int64_t n_local = 0, s_local = 0, r_local = 0;
+    {
+        int64_t pos = pos0;
+        for (int b = b0; b < b1; ++b) {
+            const int32_t tiles = req_tiles(seq_lens, topk, b);
+            const ReqSplit r = req_split(pos, tiles, per, units);
+            req_start[b] = pos;
+            n_local += r.n;
+            if (r.n > 1) {
+                s_local += r.n;
+                ++r_local;
+            }
+            pos += req_cost(tiles);
+        }
     }
-    int64_t n_total, s_total;
+    int64_t n_total, s_total, r_total;
     int64_t off = block_exclusive_scan(n_local, &n_total, sh);
     int64_t slot = block_exclusive_scan(s_local, &s_total, sh);
-    for (int b = b0; b < b1; ++b) {
-        const ReqSplit r = req_split(req_start[b], req_tiles(seq_lens, topk, b), per, units);
-        num_splits[b] = r.n;
-        split_base[b] = r.n > 1 ? (int32_t)slot : -1;
-        emit_request(ws, L, seq_lens, topk, b, req_start[b], per, units, (int32_t)off,
-                     split_base[b]);
-        off += r.n;
-        if (r.n > 1) slot += r.n;
+    int64_t rpos = block_exclusive_scan(r_local, &r_total, sh);
+    int32_t *split_list = reinterpret_cast<int32_t *>(ws + L.split_list);
+    {
+        int64_t pos = pos0;
+        for (int b = b0; b < b1; ++b) {
+            const int32_t tiles = req_tiles(seq_lens, topk, b);
+            const ReqSplit r = req_split(pos, tiles, per, units);
+            num_splits[b] = r.n;
+            split_base[b] = r.n > 1 ? (int32_t)slot : -1;
+            emit_request(ws, L, seq_lens, topk, b, pos, per, units, (int32_t)off, split_base[b],
+                         iu_in_smem ? s_iu : nullptr);
+            off += r.n;
+            if (r.n > 1) {
+                slot += r.n;
+                split_list[rpos++] = b;
+            }
+            pos += req_cost(tiles);
+        }
     }
-    __syncthreads();  // item_unit is complete (global writes of this block are now visible)
+    __syncthreads();  // item_unit is complete (shared, or global writes of this block)
     // unit_begin[u] = first item whose unit is >= u (items are grouped by unit in order):
     // item i starts the units (unit of item i-1, unit of item i]
     const int32_t n = (int32_t)n_total;
@@ -99,66 +118,117 @@ plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int units, unsigned
     for (int u = threadIdx.x; u <= units; u += kPlanThreads)
         if (u > last) unit_begin[u] = n;
     if (threadIdx.x == 0) {
-        write_header(ws, L, B, H, topk, units, n, per, (int32_t)s_total);
+        write_header(ws, L, B, H, topk, units, n, per, (int32_t)s_total, (int32_t)r_total);
         *reinterpret_cast<int *>(ws + L.status) = 0;
     }
 }
 
 // ---------------------------------------------------------------------------------
 // Merge of split-KV partial results through their log-sum-exp:
-//   lse = ln sum_i exp(lse_i),  out = sum_i exp(lse_i - lse) * out_i.
-// One warp per (request, head), kCombineHeads heads per CTA; a lane covers 16 of the 512
-// columns, so every load and store of a warp spans 512 contiguous bytes.  Requests with
-// a single piece were written directly by the decode kernel.
+//   lse = ln sum_i exp(lse_i),  out = sum_i exp(lse_i - lse) * out_i,
+// taken online over groups of four pieces (running maximum M and sum Z of exp(lse_i - M)),
+// so that a group's loads (its lse_i and rows) are in flight together.  A persistent grid
+// (kCombineCtasPerSm CTAs per SM): warp w of the grid merges the (request, head) tasks
+// w, w + warps, ... over the split requests the plan lists; a lane covers 16 of the 512
+// columns, so every load and store of a warp spans 512 contiguous bytes.  Requests with a
+// single piece were written directly by the decode kernel.  Launched as a programmatic
+// dependent of the decode kernel: it waits for it before reading anything.
 // ---------------------------------------------------------------------------------
-constexpr int kCombineHeads = 8;
-constexpr int kCombineThreads = 32 * kCombineHeads;
+constexpr int kCombineThreads = 256;
+constexpr int kCombineCtasPerSm = 2;
+constexpr int kCombineSmemReqs = 1024;  // split requests whose (b, n, s0) are staged in shared memory
 
-__global__ void __launch_bounds__(kCombineThreads)
+__global__ void __launch_bounds__(kCombineThreads, kCombineCtasPerSm)
 combine_kernel(DecodeArgs a) {
+    __shared__ int32_t s_b[kCombineSmemReqs], s_n[kCombineSmemReqs], s_s0[kCombineSmemReqs];
+    grid_dep_wait();
+    grid_dep_launch();  // the next kernel on the stream may launch (it waits for this one)
     if (!plan_matches(a)) return;
     const unsigned char *ws = a.ws;
     const int H = a.H;
     const PlanHeader *hd = reinterpret_cast<const PlanHeader *>(ws);
     const WsLayout L = ws_layout(hd->B, hd->H, hd->num_units);
-    const int b = blockIdx.x;
-    const int32_t n = reinterpret_cast<const int32_t *>(ws + L.num_splits)[b];
-    if (n <= 1) return;
-    const int h = blockIdx.y * kCombineHeads + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (h >= H) return;
-    const int32_t base = reinterpret_cast<const int32_t *>(ws + L.split_base)[b];
-    const float *plse = reinterpret_cast<const float *>(ws + L.part_lse) + (int64_t)base * H + h;
-    const float *po = reinterpret_cast<const float *>(ws + L.part_o) + ((int64_t)base * H + h) * kDLatent;
-    float m = -INFINITY;
-    for (int i = lane; i < n; i += 32) m = fmaxf(m, plse[(int64_t)i * H]);
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float z = 0.f;
-    if (m != -INFINITY)
-        for (int i = lane; i < n; i += 32) z += exp2f((plse[(int64_t)i * H] - m) * kLog2e);
-    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-    const float total = m == -INFINITY ? -INFINITY : m + logf(z);
-    float4 acc[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (m != -INFINITY) {
-#pragma unroll 2
-        for (int i = 0; i < n; ++i) {
-            const float w = exp2f((plse[(int64_t)i * H] - total) * kLog2e);
-            const float4 *row = reinterpret_cast<const float4 *>(po + (int64_t)i * H * kDLatent);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float4 v = row[lane + 32 * k];
-                acc[k].x = fmaf(w, v.x, acc[k].x);
-                acc[k].y = fmaf(w, v.y, acc[k].y);
-                acc[k].z = fmaf(w, v.z, acc[k].z);
-                acc[k].w = fmaf(w, v.w, acc[k].w);
-            }
-        }
+    const int nsr = hd->num_split_reqs;
+    if (nsr <= 0) return;
+    const int32_t *split_list = reinterpret_cast<const int32_t *>(ws + L.split_list);
+    const int32_t *num_splits = reinterpret_cast<const int32_t *>(ws + L.num_splits);
+    const int32_t *split_base = reinterpret_cast<const int32_t *>(ws + L.split_base);
+    for (int k = threadIdx.x; k < nsr && k < kCombineSmemReqs; k += kCombineThreads) {
+        const int b = split_list[k];
+        s_b[k] = b;
+        s_n[k] = num_splits[b];
+        s_s0[k] = split_base[b];
     }
-    float4 *dst = reinterpret_cast<float4 *>(a.out + ((int64_t)b * H + h) * kDLatent);
+    __syncthreads();
+    const float *part_lse = reinterpret_cast<const float *>(ws + L.part_lse);
+    const float4 *part_o = reinterpret_cast<const float4 *>(ws + L.part_o);
+    const int64_t ostep = (int64_t)H * (kDLatent / 4);  // one piece to the next, in float4
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = (int64_t)gridDim.x * (kCombineThreads / 32);
+    const int64_t ntasks = (int64_t)nsr * H;
+    for (int64_t t = (int64_t)blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5); t < ntasks; t += nw) {
+        const int k = (int)(t / H), h = (int)(t % H);
+        int b, n, s0;
+        if (k < kCombineSmemReqs) {
+            b = s_b[k];
+            n = s_n[k];
+            s0 = s_s0[k];
+        } else {
+            b = split_list[k];
+            n = num_splits[b];
+            s0 = split_base[b];
+        }
+        const float *plse = part_lse + (int64_t)s0 * H + h;
+        const float4 *po = part_o + ((int64_t)s0 * H + h) * (kDLatent / 4);
+        float M = -INFINITY, Z = 0.f;
+        float4 acc[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) dst[lane + 32 * k] = acc[k];
-    if (lane == 0) a.lse[(int64_t)b * H + h] = total;
+        for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i0 = 0; i0 < n; i0 += 4) {
+            float li[4];
+            float4 v[4][4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = i0 + j;
+                li[j] = i < n ? plse[(int64_t)i * H] : -INFINITY;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    v[j][q] = i < n ? po[i * ostep + lane + 32 * q] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            float mn = M;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) mn = fmaxf(mn, li[j]);
+            if (mn == -INFINITY) continue;  // every piece so far is empty
+            const float r = exp2f((M - mn) * kLog2e);  // 0 while M is -inf
+            Z *= r;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                acc[q].x *= r;
+                acc[q].y *= r;
+                acc[q].z *= r;
+                acc[q].w *= r;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float wt = exp2f((li[j] - mn) * kLog2e);  // 0 for an empty or absent piece
+                Z += wt;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[q].x = fmaf(wt, v[j][q].x, acc[q].x);
+                    acc[q].y = fmaf(wt, v[j][q].y, acc[q].y);
+                    acc[q].z = fmaf(wt, v[j][q].z, acc[q].z);
+                    acc[q].w = fmaf(wt, v[j][q].w, acc[q].w);
+                }
+            }
+            M = mn;
+        }
+        const float inv = Z > 0.f ? 1.f / Z : 0.f;
+        float4 *dst = reinterpret_cast<float4 *>(a.out + ((int64_t)b * H + h) * kDLatent);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            dst[lane + 32 * q] = make_float4(acc[q].x * inv, acc[q].y * inv, acc[q].z * inv, acc[q].w * inv);
+        if (lane == 0) a.lse[(int64_t)b * H + h] = M == -INFINITY ? -INFINITY : M + logf(Z);
+    }
 }
 
 int device_sm_count() {
@@ -201,9 +271,18 @@ mla_status run_decode(const DecodeArgs &a, cudaStream_t stream) {
     cudaError_t e;
     e = launch_decode_sm103(a, units, stream);  // dense bf16, DSA sparse, or FP8 records
     if (e != cudaSuccess) return MLA_ERR_CUDA;
-    dim3 cgrid(a.B, (a.H + kCombineHeads - 1) / kCombineHeads);
-    combine_kernel<<<cgrid, kCombineThreads, 0, stream>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+    // the merge: a programmatic dependent of the decode kernel (it may launch while the
+    // decode's last CTAs finish, and waits for them before it reads anything)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kCombineCtasPerSm * sms, 1, 1);
+    cfg.blockDim = dim3(kCombineThreads, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, combine_kernel, a) != cudaSuccess) return MLA_ERR_CUDA;
     return MLA_OK;
 }
 
@@ -230,9 +309,24 @@ mla_status mla_decode_plan(const int32_t *seq_lens, int B, int H, int topk, int 
     if (num_sms <= 0) return MLA_ERR_CUDA;
     const int units = units_for(num_sms);
     if (ws_bytes < ws_layout(B, H, units).total) return MLA_ERR_WORKSPACE;
-    plan_kernel<<<1, kPlanThreads, 0, (cudaStream_t)stream>>>(seq_lens, B, H, topk, units,
-                                                              (unsigned char *)workspace);
-    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+    // a programmatic dependent of whatever ran before on the stream (it waits for it before
+    // reading seq_lens); the items' units stay in shared memory when they fit
+    const size_t iu_bytes = sizeof(int32_t) * (size_t)ws_layout(B, H, units).max_items;
+    const int iu_in_smem = iu_bytes <= 48 * 1024 ? 1 : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(kPlanThreads, 1, 1);
+    cfg.dynamicSmemBytes = iu_in_smem ? iu_bytes : 0;
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, plan_kernel, seq_lens, B, H, topk, units, (unsigned char *)workspace,
+                              iu_in_smem) == cudaSuccess
+               ? MLA_OK
+               : MLA_ERR_CUDA;
 }
 
 mla_status mla_decode_plan_host(const int32_t *seq_lens, int B, int H, int topk, int num_sms,

@@ -42,6 +42,13 @@ __device__ __forceinline__ bool plan_matches(const DecodeArgs &a) {
     return true;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization
+// may start while the previous kernel of the stream still runs; grid_dep_wait() returns once
+// that kernel has completed and its memory is visible.  grid_dep_launch() lets the next
+// kernel of the stream start launching (its blocks still wait in their grid_dep_wait()).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // Records the first device-side error; later ones are dropped.
 __device__ __forceinline__ void record_error(int *status, int code) {
     atomicCAS(status, 0, code);

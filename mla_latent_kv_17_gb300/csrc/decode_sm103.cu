@@ -404,6 +404,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
     constexpr bool kSparse = kMode == 1, kFp8 = kMode == 2;
     constexpr uint32_t kFullCount = kFp8 ? 4u : 1u;  // arrivals that complete a latent / other-columns stage
     extern __shared__ uint8_t smem_raw[];
+    grid_dep_wait();  // the plan (or whatever ran before on the stream) is complete
     if (!plan_matches(a)) {
         if (threadIdx.x == 0 && blockIdx.x == 0) record_error(a.status, MLA_ERR_WORKSPACE);
         return;
@@ -1082,6 +1083,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
     }
 
     // ---------------------------------------------------------------- teardown
+    grid_dep_launch();  // the merge kernel may start launching
     if (warp < 4 && lane == 0) bulk_wait_read_all();
     tc_fence_before();
     __syncthreads();
@@ -1187,6 +1189,25 @@ int sm103_max_units() {
     return n;
 }
 
+// Launch with programmatic stream serialization: the grid may start while the plan kernel
+// finishes (every CTA first waits for it in grid_dep_wait()).
+template <typename K>
+cudaError_t launch_pdl(K kernel, dim3 grid, int threads, cudaStream_t stream, const CUtensorMap &t0,
+                       const CUtensorMap &t1, const CUtensorMap &t2, const CUtensorMap &t3, const CUtensorMap &t4,
+                       const DecodeArgs &a) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, t0, t1, t2, t3, t4, a);
+}
+
 cudaError_t launch_decode_sm103(const DecodeArgs &a, int num_clusters, cudaStream_t stream) {
     if (!set_smem_attr()) return cudaErrorInvalidValue;
     const dim3 grid(2 * num_clusters);
@@ -1203,19 +1224,19 @@ cudaError_t launch_decode_sm103(const DecodeArgs &a, int num_clusters, cudaStrea
             !make_tmap(&tm_rope, a.cache, a.num_pages, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kFp8RecordBytes, 64,
                        kPageRows, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
-        decode_sm103_kernel<2><<<grid, dim3(kThreadsFp8), kSmemBytes, stream>>>(tm, tm_sc, tm_rope, tm_qn, tm_qr, a);
+        return launch_pdl(decode_sm103_kernel<2>, grid, kThreadsFp8, stream, tm, tm_sc, tm_rope, tm_qn, tm_qr, a);
     } else if (a.indices) {
         // one-row boxes for tile::gather4
         if (!make_tmap(&tm, a.cache, a.num_pages, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)kDEntry * 2, 64, 1,
                        CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
-        decode_sm103_kernel<1><<<grid, dim3(kThreads), kSmemBytes, stream>>>(tm, tm, tm, tm_qn, tm_qr, a);
+        return launch_pdl(decode_sm103_kernel<1>, grid, kThreads, stream, tm, tm, tm, tm_qn, tm_qr, a);
     } else {
         // 64-row boxes: one page
         if (!make_tmap(&tm, a.cache, a.num_pages, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)kDEntry * 2, 64,
                        kPageRows, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
-        decode_sm103_kernel<0><<<grid, dim3(kThreads), kSmemBytes, stream>>>(tm, tm, tm, tm_qn, tm_qr, a);
+        return launch_pdl(decode_sm103_kernel<0>, grid, kThreads, stream, tm, tm, tm, tm_qn, tm_qr, a);
     }
     return cudaGetLastError();
 }

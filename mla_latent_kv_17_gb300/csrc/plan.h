@@ -38,7 +38,7 @@ constexpr uint32_t kPlanMagic = 0x4D4C4150u;  // "MLAP"
 struct PlanHeader {
     uint32_t magic;
     int32_t B, H, topk, num_units, num_items, max_items, max_partials;
-    int32_t tiles_per_unit, num_partials, reserved[6];
+    int32_t tiles_per_unit, num_partials, num_split_reqs, reserved[5];
 };
 static_assert(sizeof(PlanHeader) == 64, "plan header is 64 bytes");
 
@@ -51,9 +51,10 @@ struct WorkItem {
 MLA_HD size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Byte offsets inside the workspace.  Everything up to `plan_end` is the plan proper;
-// req_start and item_unit are planner scratch that the decode does not read.
+// req_start and item_unit are planner scratch that the decode does not read; split_list
+// holds the requests cut into several pieces, in order (num_split_reqs of them).
 struct WsLayout {
-    size_t header, status, unit_begin, items, num_splits, split_base, req_start, item_unit;
+    size_t header, status, unit_begin, items, num_splits, split_base, req_start, item_unit, split_list;
     size_t plan_end, part_lse, part_o, total;
     int max_items, max_partials, num_units;
 };
@@ -78,6 +79,8 @@ MLA_HD WsLayout ws_layout(int B, int H, int num_units) {
     o = align_up(o + sizeof(int64_t) * (size_t)B, 256);
     L.item_unit = o;
     o = align_up(o + sizeof(int32_t) * (size_t)L.max_items, 256);
+    L.split_list = o;
+    o = align_up(o + sizeof(int32_t) * (size_t)B, 256);
     L.plan_end = o;
     L.part_lse = o;
     o = align_up(o + sizeof(float) * (size_t)L.max_partials * H, 256);
@@ -170,9 +173,10 @@ MLA_HD int64_t plan_budget(int64_t total_cost, int units) {
 }
 
 // Writes the pieces of request b (its item offset `off`, its first partial slot `slot0`
-// or -1) into the workspace.
+// or -1) into the workspace; unit_copy, when given, receives the items' units as well.
 MLA_HD void emit_request(unsigned char *ws, const WsLayout &L, const int32_t *seq_lens, int topk,
-                         int b, int64_t S, int64_t per, int units, int32_t off, int32_t slot0) {
+                         int b, int64_t S, int64_t per, int units, int32_t off, int32_t slot0,
+                         int32_t *unit_copy = nullptr) {
     WorkItem *items = reinterpret_cast<WorkItem *>(ws + L.items);
     int32_t *item_unit = reinterpret_cast<int32_t *>(ws + L.item_unit);
     const int32_t len = req_len(seq_lens, topk, b);
@@ -189,11 +193,12 @@ MLA_HD void emit_request(unsigned char *ws, const WsLayout &L, const int32_t *se
         w.slot = r.n > 1 ? slot0 + i : -1;
         items[off + i] = w;
         item_unit[off + i] = u;
+        if (unit_copy) unit_copy[off + i] = u;
     }
 }
 
 MLA_HD void write_header(unsigned char *ws, const WsLayout &L, int B, int H, int topk, int units,
-                         int n_items, int64_t per, int n_partials) {
+                         int n_items, int64_t per, int n_partials, int n_split_reqs) {
     PlanHeader *hd = reinterpret_cast<PlanHeader *>(ws + L.header);
     hd->magic = kPlanMagic;
     hd->B = B;
@@ -205,7 +210,8 @@ MLA_HD void write_header(unsigned char *ws, const WsLayout &L, int B, int H, int
     hd->max_partials = L.max_partials;
     hd->tiles_per_unit = (int32_t)per;
     hd->num_partials = n_partials;
-    for (int i = 0; i < 6; ++i) hd->reserved[i] = 0;
+    hd->num_split_reqs = n_split_reqs;
+    for (int i = 0; i < 5; ++i) hd->reserved[i] = 0;
 }
 
 // First item index whose unit is >= u (items are ordered by unit).
@@ -231,24 +237,28 @@ inline void build_plan_serial(const int32_t *seq_lens, int B, int H, int topk, i
     int64_t *req_start = reinterpret_cast<int64_t *>(ws + L.req_start);
     int32_t *unit_begin = reinterpret_cast<int32_t *>(ws + L.unit_begin);
     int32_t *item_unit = reinterpret_cast<int32_t *>(ws + L.item_unit);
+    int32_t *split_list = reinterpret_cast<int32_t *>(ws + L.split_list);
     int64_t S = 0;
     for (int b = 0; b < B; ++b) {
         req_start[b] = S;
         S += req_cost(req_tiles(seq_lens, topk, b));
     }
     const int64_t per = plan_budget(S, units);
-    int32_t off = 0, slots = 0;
+    int32_t off = 0, slots = 0, nsr = 0;
     for (int b = 0; b < B; ++b) {
         const ReqSplit r = req_split(req_start[b], req_tiles(seq_lens, topk, b), per, units);
         num_splits[b] = r.n;
         split_base[b] = r.n > 1 ? slots : -1;
         emit_request(ws, L, seq_lens, topk, b, req_start[b], per, units, off, split_base[b]);
         off += r.n;
-        if (r.n > 1) slots += r.n;
+        if (r.n > 1) {
+            slots += r.n;
+            split_list[nsr++] = b;
+        }
     }
     for (int u = 0; u <= units; ++u)
         unit_begin[u] = u == units ? off : lower_bound_unit(item_unit, off, u);
-    write_header(ws, L, B, H, topk, units, off, per, slots);
+    write_header(ws, L, B, H, topk, units, off, per, slots, nsr);
 }
 
 }  // namespace mla
