@@ -191,19 +191,27 @@ struct SparseRows {
     uint32_t lo, hi;  // validity of slots 0-31 and 32-63
 };
 __device__ SparseRows sparse_rows(const DecodeArgs &a, const WorkItem &w, int t, int p, int lane, bool report) {
-    const int L = max(0, a.seq_lens[w.b]);
+    // volatile loads: issued here (ahead of the caller's barrier wait), both slots' indices
+    // and the length together, then the block-table entries
+    int idxs[2] = {-1, -1};
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int s = t + kPageRows * p + lane + 32 * k;
+        if (s < w.t1) idxs[k] = ld_early(a.indices + (int64_t)w.b * a.topk + s);
+    }
+    const int L = max(0, ld_early(a.seq_lens + w.b));
     int32_t rows[2] = {0, 0};
     bool ok[2] = {false, false};
     for (int k = 0; k < 2; ++k) {
         const int s = t + kPageRows * p + lane + 32 * k;
         if (s >= w.t1) continue;
-        const int idx = a.indices[(int64_t)w.b * a.topk + s];
+        const int idx = idxs[k];
         if (idx < 0) {
             if (idx < -1 && report) record_error(a.status, MLA_ERR_INDEX);
             continue;
         }
         const int lp = idx / kPageRows;
-        const int64_t id = idx < L && lp < a.max_pages ? (int64_t)a.block_table[(int64_t)w.b * a.max_pages + lp] : -1;
+        const int64_t id = idx < L && lp < a.max_pages ? (int64_t)ld_early(a.block_table + (int64_t)w.b * a.max_pages + lp) : -1;
         if (id < 0 || id >= a.num_pages) {
             if (report) record_error(a.status, MLA_ERR_INDEX);
             continue;
@@ -869,11 +877,16 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                     prefetch_l2(a.q_rope + (int64_t)bnext * a.H * kDRope, (uint32_t)(a.H * kDRope * 2));
                 }
                 float m = -INFINITY, l = 0.f;
+                // which rows of each page attend (warp-collective), read one tile ahead
+                PageMask nm0 = page_mask<kSparse>(a, w, w.t0, 0, lane), nm1 = page_mask<kSparse>(a, w, w.t0, 1, lane);
                 for (int t = w.t0, j = 0; t < w.t1; t += kTile, ++j, ++g) {
                     // ================= part A: own page's scores -> weights -> message
                     const int nvalid = min(kTile, w.t1 - t);
-                    // which rows of each page attend (read early; warp-collective)
-                    const PageMask pm0 = page_mask<kSparse>(a, w, t, 0, lane), pm1 = page_mask<kSparse>(a, w, t, 1, lane);
+                    const PageMask pm0 = nm0, pm1 = nm1;
+                    if (t + kTile < w.t1) {
+                        nm0 = page_mask<kSparse>(a, w, t + kTile, 0, lane);
+                        nm1 = page_mask<kSparse>(a, w, t + kTile, 1, lane);
+                    }
                     const uint64_t vown = rank == 0 ? pm0.valid : pm1.valid;
                     if (!warp_wait(c, bar(base, B_S_FULL), g & 1u, false)) {
                         ok = false;
