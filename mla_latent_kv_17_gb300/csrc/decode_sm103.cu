@@ -586,12 +586,12 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
             // peer(1), own(3), ...
             const int xown = 256 * (int)rank;
             // loads page (rank if e == 0, else peer) of tile g at cursor position t
-            auto load = [&](const TileCursor &t, uint32_t g, int e) -> bool {
+            // (sparse: the rows r were resolved one load ahead)
+            auto load = [&](const TileCursor &t, uint32_t g, int e, const SparseRows &r) -> bool {
                 const int p = e == 0 ? (int)rank : (int)peer;
                 const DhSlot d = dh_slot(g, e);
                 const uint32_t fb = bar(base, d.full), dst = base + kOffDh + d.slot * kDhBytes;
                 if constexpr (kSparse) {
-                    const SparseRows r = sparse_rows(a, t.w, t.t, p, lane, true);  // read before the wait
                     if (d.fill > 0 && !warp_wait(c, bar(base, B_DH_EMPTY + d.slot), (d.fill - 1u) & 1u, false))
                         return false;
                     if (t.t + kPageRows * p < t.w.t1) {
@@ -618,17 +618,50 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                 }
                 return true;
             };
-            TileCursor co = cur;  // next own page: tile go
+            // the sequence of loads: own(0), own(1), then peer(g), own(g + 2) for g = 0, 1, ...
+            TileCursor co = cur;  // next own page: tile go; cur: next peer page, tile gp
             uint32_t go = 0, gp = 0;
-            bool ok = true;
-            for (; go < 2 && !co.done() && ok; ++go, co.next()) ok = load(co, go, 0);
-            for (; !cur.done() && ok; ++gp, cur.next()) {  // cur: next peer page, tile gp
-                ok = load(cur, gp, 1);
-                if (ok && !co.done()) {
-                    ok = load(co, go, 0);
-                    ++go;
-                    co.next();
+            int step = 0;
+            struct Ld {
+                int e;  // -1: none left
+                uint32_t g;
+                TileCursor t;
+            };
+            auto next_ld = [&]() {
+                Ld x{-1, 0u, co};
+                for (;; ++step) {
+                    const int e = step < 2 ? 0 : ((step - 2) & 1) ? 0 : 1;
+                    if (e == 0 && !co.done()) {
+                        x = Ld{0, go++, co};
+                        co.next();
+                        ++step;
+                        return x;
+                    }
+                    if (e == 1 && !cur.done()) {
+                        x = Ld{1, gp++, cur};
+                        cur.next();
+                        ++step;
+                        return x;
+                    }
+                    if (co.done() && cur.done()) return x;
                 }
+            };
+            auto rows_of = [&](const Ld &x) {
+                SparseRows r{0, 0, 0u, 0u};
+                if constexpr (kSparse) {
+                    if (x.e >= 0) r = sparse_rows(a, x.t.w, x.t.t, x.e == 0 ? (int)rank : (int)peer, lane, true);
+                }
+                return r;
+            };
+            bool ok = true;
+            Ld x = next_ld();
+            SparseRows rx = rows_of(x);
+            while (ok && x.e >= 0) {
+                const Ld xn = next_ld();
+                const SparseRows rn = rows_of(xn);  // issued before this load's wait
+                ok = load(x.t, x.g, x.e, rx);
+                x = xn;
+                rx = rn;
             }
             if (!ok && lane == 0) drain_pause();
         } else {
@@ -636,10 +669,16 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
             const int xoth = 256 * (int)peer;
             auto x_of = [&](int i) { return i < 4 ? xoth + 64 * i : kDLatent; };
             bool ok = true;
+            // sparse: the rows of the next tile are resolved before this tile's wait
+            SparseRows rnext{0, 0, 0u, 0u};
+            if constexpr (kSparse) {
+                if (!cur.done()) rnext = sparse_rows(a, cur.w, cur.t, (int)rank, lane, false);
+            }
             for (uint32_t g = 0; !cur.done() && ok; ++g) {
                 const uint32_t fb = bar(base, B_OTH_FULL), dst = base + kOffOth;
                 if constexpr (kSparse) {
-                    const SparseRows r = sparse_rows(a, cur.w, cur.t, (int)rank, lane, false);  // before the wait
+                    const SparseRows r = rnext;
+                    if (!nx.done()) rnext = sparse_rows(a, nx.w, nx.t, (int)rank, lane, false);
                     if (!warp_wait(c, bar(base, B_OTH_EMPTY), (g & 1u) ^ 1u, false)) {
                         ok = false;
                         break;
