@@ -202,6 +202,18 @@ def test_sparse_split():
     check(_sparse(2, 128, [9000, 5000], topk=2048, seed=5), num_sms=6, what="sparse split")
 
 
+def test_sparse_page_runs_and_near_runs():
+    # 64-slot groups that are a whole cache page in order load as page boxes; groups that
+    # are not (shifted by one position, one padding slot, reversed) load row by row; both
+    # kinds in one request, against the oracle
+    c = small(1, 128, [512], seed=12)
+    parts = [torch.arange(0, 64), torch.arange(65, 129), torch.arange(128, 192).clone(),
+             torch.arange(319, 255, -1), torch.arange(320, 384)]
+    parts[2][17] = -1
+    c.indices = torch.cat(parts).to(torch.int32)[None].cuda()
+    check(c, what="sparse page runs")
+
+
 @pytest.mark.parametrize("L,num_sms", [(896, 2), (1024, 0), (2000, 6)])
 def test_sparse_contiguous_equals_dense_bitwise(L, num_sms):
     # indices 0..L-1 make the sparse path gather exactly the rows the dense path loads as
