@@ -849,22 +849,27 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
         // shared-memory query area: rounds 0 and 1 go on to TMEM, each thread moving its own
         // head's row; round 2 stays.  Heads at or beyond H lie outside the tensor: zeros.
         uint32_t qphase = 0;
-        auto load_q = [&](int bq) -> bool {
+        // issues round `round` of request bq's query boxes (thread 0)
+        auto q_round = [&](int bq, int round) {
+            const uint32_t qb = bar(base, B_QLD);
+            mbar_arrive_expect_tx(qb, 3 * kQsBox);
+            for (int i = 0; i < 3; ++i) {
+                // block 0-3: own half, 4: RoPE, 5: other half 0-63, 6-8: other half 64-255
+                const int blk = 3 * round + i;
+                const uint32_t dst = base + kOffQs + i * kQsBox;
+                if (blk == 4)
+                    tma_load_3d(dst, &tmap_qr, 0, 0, bq, qb);
+                else
+                    tma_load_3d(dst, &tmap_qn, blk < 4 ? 256 * (int)rank + 64 * blk : 256 * (int)peer + 64 * (blk - 5), 0,
+                                bq, qb);
+            }
+        };
+        // round0_issued: round 0 was issued already (as soon as the previous item's last
+        // scores were read, so that its latency hides behind that tile's merge)
+        auto load_q = [&](int bq, bool round0_issued) -> bool {
             const uint32_t qb = bar(base, B_QLD);
             for (int round = 0; round < 3; ++round) {
-                if (threadIdx.x == 0) {
-                    mbar_arrive_expect_tx(qb, 3 * kQsBox);
-                    for (int i = 0; i < 3; ++i) {
-                        // block 0-3: own half, 4: RoPE, 5: other half 0-63, 6-8: other half 64-255
-                        const int blk = 3 * round + i;
-                        const uint32_t dst = base + kOffQs + i * kQsBox;
-                        if (blk == 4)
-                            tma_load_3d(dst, &tmap_qr, 0, 0, bq, qb);
-                        else
-                            tma_load_3d(dst, &tmap_qn, blk < 4 ? 256 * (int)rank + 64 * blk : 256 * (int)peer + 64 * (blk - 5),
-                                        0, bq, qb);
-                    }
-                }
+                if (threadIdx.x == 0 && !(round == 0 && round0_issued)) q_round(bq, round);
                 if (!warp_wait(c, qb, qphase & 1u, false)) return false;
                 ++qphase;
                 if (round == 2) break;
@@ -913,7 +918,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                     }
                     continue;
                 }
-                if (!q_ready && !load_q(b)) {
+                if (!q_ready && !load_q(b, false)) {
                     ok = false;
                     break;
                 }
@@ -953,6 +958,8 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(base, B_S_FREE));
+                    // the item's last scores are read: its query area is free for the next query
+                    if (t + kTile >= w.t1 && bnext >= 0 && threadIdx.x == 0) q_round(bnext, 0);
                     if (vown != ~0ull) {
 #pragma unroll
                         for (int i = 0; i < 64; ++i)
@@ -1095,7 +1102,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                 // read), so the query columns are free; loading now lets the next item's
                 // QK^T overlap this item's last PV and epilogue
                 if (bnext >= 0) {
-                    if (!load_q(bnext)) {
+                    if (!load_q(bnext, true)) {
                         ok = false;
                         break;
                     }
