@@ -17,6 +17,9 @@ Functions follow these passages (page title, section):
 * ``decode_fp8`` / ``e4m3_to_float``: same guide §5.3 (FP8 latent cache).  The format
   (e4m3 "fn", one fp32 scale per 128 channels) is this library's reading; the pages
   name only "FP8".
+* ``append`` / ``e4m3_encode``: the cache append after a decode step (same guide §4,
+  the decode figure: the output token is appended to the cache) and the FP8 record it
+  writes (§5.3; per-128-channel scale max|x|/448, nearest e4m3 code, ties to even).
 * ``combine``: merge of split-KV partial results through their log-sum-exp, the
   "Fused Reduction" the operator survey ("MLA 最佳算子全景调研" §3) pairs with
   weight-absorbed decode.
@@ -72,6 +75,10 @@ def _load():
             lib.mla_oracle_e4m3_to_double.restype = D
             lib.mla_oracle_fp8_latent.argtypes = [ctypes.c_uint8, ctypes.c_float]
             lib.mla_oracle_fp8_latent.restype = D
+            lib.mla_oracle_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.mla_oracle_e4m3_encode.restype = ctypes.c_uint8
+            lib.mla_oracle_append.argtypes = [P, I, I64, P, I, P, P, P, I]
+            lib.mla_oracle_append.restype = I
             lib.mla_oracle_default_threads.argtypes = []
             lib.mla_oracle_default_threads.restype = I
             common = [I, I, P, P, P, I64, P, I, P]
@@ -102,6 +109,32 @@ def e4m3_to_float(code: int) -> float:
 def fp8_latent(code: int, scale: float) -> float:
     """One dequantized FP8 latent value: bf16_rne(fp32(e4m3(code)) * fp32(scale))."""
     return float(_load().mla_oracle_fp8_latent(int(code) & 0xFF, float(scale)))
+
+
+def e4m3_encode(v: float) -> int:
+    """Nearest e4m3 "fn" code to the binary32 value v (|v| <= 448), ties to the even code."""
+    return int(_load().mla_oracle_e4m3_encode(float(v)))
+
+
+def append(cache, fp8: bool, block_table, positions, c_kv, k_rope):
+    """Cache append: returns (a new cache array with each request's token written, error count).
+
+    cache: uint8 bytes of [num_pages][64][576] bf16 or [num_pages][64][656] FP8 records;
+    block_table int32 [B][max_pages]; positions int32 [B] (< 0: skip); c_kv, k_rope: bf16 bits
+    (uint16) [B][512], [B][64]."""
+    lib = _load()
+    cache = np.ascontiguousarray(np.asarray(cache, dtype=np.uint8)).copy()
+    row_bytes = FP8_RECORD_BYTES if fp8 else 2 * D_ENTRY
+    num_pages = cache.size // (row_bytes * PAGE_ROWS)
+    bt = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int32))
+    ck = np.ascontiguousarray(np.asarray(c_kv, dtype=np.uint16))
+    kr = np.ascontiguousarray(np.asarray(k_rope, dtype=np.uint16))
+    B = pos.shape[0]
+    assert bt.shape[0] == B and ck.shape == (B, D_LATENT) and kr.shape == (B, D_ROPE)
+    vp = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    err = lib.mla_oracle_append(vp(cache), 1 if fp8 else 0, num_pages, vp(bt), bt.shape[1], vp(pos), vp(ck), vp(kr), B)
+    return cache, int(err)
 
 
 def attend_f64(q_nope, q_rope, C, Kr, scale):

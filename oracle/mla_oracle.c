@@ -328,3 +328,81 @@ int mla_oracle_decode_sparse(int B, int H, const uint16_t *q_nope, const uint16_
     J.scale = scale; J.out = out; J.lse = lse;
     return run_jobs(&J, nthreads);
 }
+
+/* ------------------------------------------------------------------------------------
+ * Cache append: the step after a decode step ("MLA & DSA 推理性能优化指南", §4, the decode
+ * figure: each step's output token is appended to the cache).  Request b's new token
+ * (latent c[512] and RoPE key k_R[64], bf16 bits) goes to logical position positions[b]:
+ * page block_table[b][positions[b] / 64], row positions[b] % 64.  A bf16 cache stores the
+ * 576 values.  An FP8 record (same guide, §5.3; the format is this library's reading) is
+ * written per block of 128 latent channels: scale = max|x| / 448 in binary32 (1 for an
+ * all-zero block), each code the e4m3 "fn" value nearest to x / scale (binary32 division,
+ * clamped to [-448, 448] first), ties to the even code; then the four scales and the 64
+ * RoPE values as they are.
+ * ------------------------------------------------------------------------------------ */
+
+/* The e4m3 "fn" code nearest to v (|v| <= 448), by exhaustive search over the 127 finite
+ * non-negative codes; of two equally near codes the one with the even mantissa wins; the
+ * sign bit follows v (so -0 gives 0x80). */
+uint8_t mla_oracle_e4m3_encode(float v) {
+    const double a = fabs((double)v);
+    int best = 0;
+    double bestd = a;
+    for (int c = 1; c <= 0x7E; ++c) {
+        const double d = fabs(mla_oracle_e4m3_to_double((uint8_t)c) - a);
+        if (d < bestd || (d == bestd && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            bestd = d;
+        }
+    }
+    return (uint8_t)(best | (signbit(v) ? 0x80 : 0));
+}
+
+/* Appends one token per request.  Returns the number of requests whose position or page
+ * id is out of range (nothing is written for them); positions[b] < 0 skips request b. */
+int mla_oracle_append(uint8_t *cache, int fp8, int64_t num_pages, const int32_t *block_table,
+                      int max_pages, const int32_t *positions, const uint16_t *c_kv,
+                      const uint16_t *k_rope, int B) {
+    int errors = 0;
+    for (int b = 0; b < B; ++b) {
+        const int32_t pos = positions[b];
+        if (pos < 0) continue;
+        const int32_t lp = pos / PAGE_ROWS;
+        if (lp >= max_pages) {
+            ++errors;
+            continue;
+        }
+        const int32_t page = block_table[(int64_t)b * max_pages + lp];
+        if (page < 0 || page >= num_pages) {
+            ++errors;
+            continue;
+        }
+        const int64_t row = (int64_t)page * PAGE_ROWS + pos % PAGE_ROWS;
+        const uint16_t *c = c_kv + (int64_t)b * D_LATENT;
+        const uint16_t *kr = k_rope + (int64_t)b * D_ROPE;
+        if (!fp8) {
+            uint8_t *dst = cache + row * D_ENTRY * 2;
+            memcpy(dst, c, D_LATENT * 2);
+            memcpy(dst + D_LATENT * 2, kr, D_ROPE * 2);
+            continue;
+        }
+        uint8_t *dst = cache + row * FP8_RECORD_BYTES;
+        for (int blk = 0; blk < 4; ++blk) {
+            float amax = 0.0f;
+            for (int i = 0; i < 128; ++i) {
+                const float x = (float)bf16_bits_to_double(c[blk * 128 + i]);
+                if (fabsf(x) > amax) amax = fabsf(x);
+            }
+            const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+            for (int i = 0; i < 128; ++i) {
+                float q = (float)bf16_bits_to_double(c[blk * 128 + i]) / s;
+                if (q > 448.0f) q = 448.0f;
+                if (q < -448.0f) q = -448.0f;
+                dst[blk * 128 + i] = mla_oracle_e4m3_encode(q);
+            }
+            memcpy(dst + D_LATENT + 4 * blk, &s, 4);
+        }
+        memcpy(dst + D_LATENT + 16, kr, D_ROPE * 2);
+    }
+    return errors;
+}

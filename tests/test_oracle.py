@@ -340,3 +340,113 @@ def test_fp8_quantisation_error_within_format_bound():
     assert torch.all(err <= 2.0 ** -4 * r.abs() + sub)
     amax = r.reshape(8, 64, 4, 128).abs().amax(-1)
     torch.testing.assert_close(s * 448.0, amax, rtol=1e-6, atol=0)
+
+
+# ------------------------------------------------------------------------------ cache append
+def _e4m3_values():
+    return np.array([oracle.e4m3_to_float(c) for c in range(0x7F)])
+
+
+def test_e4m3_encode_round_trips_every_finite_code():
+    for c in list(range(0x7F)) + list(range(0x80, 0xFF)):
+        v = oracle.e4m3_to_float(c)
+        assert oracle.e4m3_encode(v) == c, hex(c)
+
+
+def test_e4m3_encode_matches_torch_float8_including_ties():
+    # torch's float8_e4m3fn conversion (round to nearest, ties to even) is an independent
+    # implementation; the values cover every binade, random points and the exact midpoints
+    # between neighbouring codes (where only ties-to-even decides)
+    vals = _e4m3_values()
+    mids = (vals[:-1] + vals[1:]) / 2
+    rng = np.random.default_rng(3)
+    rnd = np.exp(rng.uniform(np.log(1e-4), np.log(448.0), 4000)) * rng.choice([-1.0, 1.0], 4000)
+    xs = np.concatenate([mids, -mids, rnd, [0.0, 1e-12, 448.0, -448.0]]).astype(np.float32)
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(float(x)) for x in xs], dtype=np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def _append_case(fp8, B=5, seed=4):
+    rng = np.random.default_rng(seed)
+    max_pages, num_pages = 3, 16
+    row_bytes = 656 if fp8 else 1152
+    cache = rng.integers(0, 256, size=num_pages * 64 * row_bytes, dtype=np.uint8)
+    bt = rng.permutation(num_pages)[:B * max_pages].reshape(B, max_pages).astype(np.int32)
+    positions = np.array([0, 63, 64, 191, -1][:B], dtype=np.int32)
+    lat = torch.randn(B, 512) * torch.tensor([1.0, 1e-3, 30.0, 0.0]).repeat_interleave(128)
+    c_kv = lat.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    k_rope = torch.randn(B, 64).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    return cache, bt, positions, c_kv, k_rope
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_append_writes_the_mapped_row_and_nothing_else(fp8):
+    cache, bt, positions, c_kv, k_rope = _append_case(fp8)
+    new, err = oracle.append(cache, fp8, bt, positions, c_kv, k_rope)
+    assert err == 0
+    row_bytes = 656 if fp8 else 1152
+    rows = new.reshape(-1, row_bytes)
+    old = cache.reshape(-1, row_bytes)
+    written = set()
+    for b, p in enumerate(positions):
+        if p < 0:
+            continue
+        r = int(bt[b, p // 64]) * 64 + p % 64
+        written.add(r)
+        if not fp8:
+            assert np.array_equal(rows[r, :1024].view(np.uint16), c_kv[b])
+        assert np.array_equal(rows[r, row_bytes - 128:].view(np.uint16), k_rope[b])
+    untouched = [r for r in range(rows.shape[0]) if r not in written]
+    assert np.array_equal(rows[untouched], old[untouched])
+
+
+def test_append_fp8_record_equals_the_generator_quantiser():
+    # the workload generator quantises with torch (amax / 448 scale, float8_e4m3fn cast):
+    # a second implementation of the same record
+    cache, bt, positions, c_kv, k_rope = _append_case(True)
+    new, _ = oracle.append(cache, True, bt, positions, c_kv, k_rope)
+    rows = new.reshape(-1, 656)
+    lat = torch.from_numpy(c_kv.view(np.int16)).view(torch.bfloat16)
+    rope = torch.from_numpy(k_rope.view(np.int16)).view(torch.bfloat16)
+    ref = inputs.quantize_fp8_records(lat.float(), rope).numpy()
+    for b, p in enumerate(positions):
+        if p >= 0:
+            r = int(bt[b, p // 64]) * 64 + p % 64
+            assert np.array_equal(rows[r], ref[b]), b
+    # the all-zero block (channels 384..511) has scale 1 and zero codes (signed zeros keep
+    # their sign bit)
+    r0 = int(bt[0, 0]) * 64
+    assert np.frombuffer(rows[r0, 512 + 12:512 + 16].tobytes(), dtype=np.float32)[0] == 1.0
+    assert not (rows[r0, 384:512] & 0x7F).any()
+
+
+def test_append_dequantises_within_the_format_bound():
+    cache, bt, positions, c_kv, k_rope = _append_case(True)
+    new, _ = oracle.append(cache, True, bt, positions, c_kv, k_rope)
+    rows = new.reshape(-1, 656)
+    x = torch.from_numpy(c_kv.view(np.int16)).view(torch.bfloat16).double().numpy()
+    for b, p in enumerate(positions):
+        if p < 0:
+            continue
+        r = int(bt[b, p // 64]) * 64 + p % 64
+        scales = np.frombuffer(rows[r, 512:528].tobytes(), dtype=np.float32)
+        back = np.array([oracle.e4m3_to_float(c) for c in rows[r, :512]]) * np.repeat(scales, 128)
+        # e4m3 keeps 3 mantissa bits: relative error <= 2^-4 for normals, and an absolute
+        # error <= half the subnormal step (2^-10) times the scale below them
+        bound = np.maximum(np.abs(x[b]) * 2.0 ** -4, np.repeat(scales, 128) * 2.0 ** -10) * 1.0001
+        assert np.all(np.abs(back - x[b]) <= bound)
+
+
+def test_append_reports_out_of_range_and_writes_nothing_for_them():
+    cache, bt, positions, c_kv, k_rope = _append_case(False)
+    bt = bt.copy()
+    bt[1, 0] = 10_000                    # page id out of range (position 63 -> page 0)
+    positions = positions.copy()
+    positions[2] = 3 * 64                # beyond the block table (3 pages)
+    new, err = oracle.append(cache, False, bt, positions, c_kv, k_rope)
+    assert err == 2
+    rows, old = new.reshape(-1, 1152), cache.reshape(-1, 1152)
+    changed = np.nonzero((rows != old).any(axis=1))[0]
+    expect = sorted(int(bt[b, p // 64]) * 64 + p % 64 for b, p in [(0, 0), (3, 191)])
+    assert changed.tolist() == expect
