@@ -125,6 +125,25 @@ mla_status mla_decode_static(const void *q_nope, const void *q_rope, const void 
                              const int32_t *seq_lens, int B, int H, float softmax_scale,
                              float *out, float *lse, int32_t *device_status, void *stream);
 
+/* Cache append, the step after each decode step ("MLA & DSA 推理性能优化指南", §4: the
+ * decode figure appends each step's output token to the cache): request b's new token —
+ * c_kv[b][0..512) (its latent) and k_rope[b][0..64) (its RoPE key), bf16 — goes to logical
+ * position positions[b]: page block_table[b][positions[b] / 64], row positions[b] % 64.
+ * A bf16 cache receives the 576 values.  An FP8 cache (§5.3; the record layout above)
+ * receives, per block of 128 latent channels, scale = max|x| / 448 computed in binary32
+ * (1 for an all-zero block) and each code the e4m3 "fn" value nearest to x / scale (binary32
+ * division; clamped to +-448; ties to the even code), then the four scales and the 64 RoPE
+ * values as given.  positions[b] < 0 skips request b.  A position beyond the block table
+ * or a page id outside [0, num_pages) skips the request and records MLA_ERR_INDEX in
+ * *device_status (optional, device int32; the first error wins, nothing is cleared).
+ * cache, c_kv and k_rope must be 16-byte aligned device pointers; block_table, positions
+ * device int32; c_kv finite.  Rows of different requests must differ (each request
+ * writes one row). */
+mla_status mla_cache_append(void *cache, mla_kv_dtype kv_dtype, int64_t num_pages,
+                            const int32_t *block_table, int max_pages, const int32_t *positions,
+                            const void *c_kv, const void *k_rope, int B, int32_t *device_status,
+                            void *stream);
+
 /* Host twin of mla_decode_plan for tests and tooling: plans from a HOST array
  * seq_lens[B] (NULL with topk > 0) into a HOST buffer of mla_decode_workspace_size()
  * bytes, producing exactly the bytes the device planner writes into the plan region.

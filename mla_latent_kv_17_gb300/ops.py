@@ -55,6 +55,8 @@ def lib():
             L.mla_decode_sparse.restype = I
             L.mla_decode_static.argtypes = [P, P, P, I, I64, P, I, P, I, I, F, P, P, P, P]
             L.mla_decode_static.restype = I
+            L.mla_cache_append.argtypes = [P, I, I64, P, I, P, P, P, I, P, P]
+            L.mla_cache_append.restype = I
             L.mla_decode_status.argtypes = [P, SZ, P]
             L.mla_decode_status.restype = I
             L.mla_status_string.argtypes = [I]
@@ -157,6 +159,33 @@ def decode(ws: Workspace, q_nope, q_rope, cache, block_table, seq_lens, softmax_
                           B, H, float(softmax_scale), _ptr(out), _ptr(lse), _stream(stream))
     _check("mla_decode", st)
     return out, lse
+
+
+def cache_append(cache, block_table, positions, c_kv, k_rope, device_status=None, stream=None):
+    """Writes request b's new token (c_kv [B,512], k_rope [B,64], bf16) at position positions[b]
+    (int32 [B], < 0 skips) of the paged cache: bf16 [P,64,576] or uint8 FP8 records [P,64,656]
+    (quantised on the way in).  device_status: optional int32 [1] tensor for MLA_ERR_INDEX."""
+    _i32(block_table, "block_table")
+    _i32(positions, "positions")
+    if cache.dtype == torch.bfloat16 and cache.shape[1:] == (64, 576):
+        kv = KV_BF16
+    elif cache.dtype == torch.uint8 and cache.shape[1:] == (64, 656):
+        kv = KV_FP8
+    else:
+        raise ValueError("cache must be bf16 [P,64,576] or uint8 [P,64,656]")
+    B = positions.shape[0]
+    for t, n, d in ((c_kv, "c_kv", 512), (k_rope, "k_rope", 64)):
+        if t.dtype != torch.bfloat16 or t.shape != (B, d) or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{n} must be contiguous CUDA bf16 [{B},{d}]")
+    if not cache.is_contiguous():
+        raise ValueError("cache must be contiguous")
+    if device_status is not None:
+        _i32(device_status, "device_status")
+    st = lib().mla_cache_append(_ptr(cache), kv, cache.shape[0], _ptr(block_table), block_table.shape[1],
+                                _ptr(positions), _ptr(c_kv), _ptr(k_rope), B, _ptr(device_status),
+                                _stream(stream))
+    _check("mla_cache_append", st)
+    return cache
 
 
 def decode_sparse(ws: Workspace, q_nope, q_rope, cache, block_table, seq_lens, indices,
