@@ -365,6 +365,30 @@ def main():
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         e2e_ms = float(t.item())
 
+    # ---- cache append (the step after decode): one token per request, timed alone -------
+    # (written at each request's last position, inside its block table; after every decode
+    # measurement, since it changes the cache)
+    g_app = torch.Generator().manual_seed(7)
+    a_lat = torch.randn(case.B, 512, generator=g_app).to(torch.bfloat16).to(dev)
+    a_rope = torch.randn(case.B, 64, generator=g_app).to(torch.bfloat16).to(dev)
+    a_pos = (case.seq_lens - 1).clamp(min=-1).to(torch.int32).contiguous()
+    for _ in range(3):
+        ops.cache_append(case.cache, case.block_table, a_pos, a_lat, a_rope, stream=stream)
+    torch.cuda.synchronize()
+    a_ms = []
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        ops.cache_append(case.cache, case.block_table, a_pos, a_lat, a_rope, stream=stream)
+        eb.record(stream)
+        eb.synchronize()
+        a_ms.append(ea.elapsed_time(eb))
+    app_ms = sum(a_ms) / len(a_ms)
+    rec_bytes = 656 if case.kv_dtype == "fp8" else 1152
+    n_app = int((a_pos >= 0).sum().item())
+    app_bytes = n_app * (rec_bytes + 1024 + 128 + 4 + 4)  # record out; latent, rope, position, page id in
+
     pk, pk_kind = peaks()
     tf = alg["flops"] / (ms_per_step * 1e-3) / 1e12 * ws_n
     gbs = alg["bytes"] / (ms_per_step * 1e-3) / 1e9
@@ -395,6 +419,9 @@ def main():
         "e2e": {"value": alg["flops"] / (e2e_ms * 1e-3) / 1e12 * ws_n, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": 3 * args.steps,
+        "append": {"kernel": "cache append (mla_cache_append), one token per request", "requests": n_app,
+                   "kv": case.kv_dtype, "us": app_ms * 1e3, "bytes": app_bytes,
+                   "gbs": app_bytes / (app_ms * 1e-3) / 1e9},
         "clocks": clk.summary(),
         "wall_s_timed_region": t_wall,
     }

@@ -27,6 +27,11 @@ append_kernel(unsigned char *cache, int fp8, int64_t num_pages, const int32_t *b
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
     if (b >= B) return;
+    // the token's values and its position are read together, then the page id
+    const uint4 *src = reinterpret_cast<const uint4 *>(c_kv + (int64_t)b * kDLatent + 16 * lane);
+    const uint4 v0 = src[0], v1 = src[1];
+    const uint4 rp = lane < 8 ? reinterpret_cast<const uint4 *>(k_rope + (int64_t)b * kDRope)[lane]
+                              : make_uint4(0u, 0u, 0u, 0u);
     const int32_t pos = positions[b];
     if (pos < 0) return;
     const int32_t lp = pos / kPageRows;
@@ -36,10 +41,6 @@ append_kernel(unsigned char *cache, int fp8, int64_t num_pages, const int32_t *b
         return;
     }
     const int64_t row = page * kPageRows + pos % kPageRows;
-    const uint4 *src = reinterpret_cast<const uint4 *>(c_kv + (int64_t)b * kDLatent + 16 * lane);
-    const uint4 v0 = src[0], v1 = src[1];
-    const uint4 rp = lane < 8 ? reinterpret_cast<const uint4 *>(k_rope + (int64_t)b * kDRope)[lane]
-                              : make_uint4(0u, 0u, 0u, 0u);
     if (!fp8) {
         uint4 *dst = reinterpret_cast<uint4 *>(cache + row * (kDEntry * 2));
         dst[2 * lane] = v0;
