@@ -20,6 +20,9 @@ Functions follow these passages (page title, section):
 * ``append`` / ``e4m3_encode``: the cache append after a decode step (same guide §4,
   the decode figure: the output token is appended to the cache) and the FP8 record it
   writes (§5.3; per-128-channel scale max|x|/448, nearest e4m3 code, ties to even).
+* ``absorb`` / ``project``: the query absorption q~ = q^C W^UK ("MLA 在极长上下文下的显存
+  带宽突围", run-time matrix absorption) and the value up-projection W^UV applied to the
+  latent output afterwards ("MLA & DSA 推理性能优化指南" §1.1), one matrix per head.
 * ``combine``: merge of split-KV partial results through their log-sum-exp, the
   "Fused Reduction" the operator survey ("MLA 最佳算子全景调研" §3) pairs with
   weight-absorbed decode.
@@ -79,6 +82,10 @@ def _load():
             lib.mla_oracle_e4m3_encode.restype = ctypes.c_uint8
             lib.mla_oracle_append.argtypes = [P, I, I64, P, I, P, P, P, I]
             lib.mla_oracle_append.restype = I
+            lib.mla_oracle_absorb.argtypes = [I, I, I, P, P, P]
+            lib.mla_oracle_absorb.restype = None
+            lib.mla_oracle_project.argtypes = [I, I, I, P, P, P]
+            lib.mla_oracle_project.restype = None
             lib.mla_oracle_default_threads.argtypes = []
             lib.mla_oracle_default_threads.restype = I
             common = [I, I, P, P, P, I64, P, I, P]
@@ -135,6 +142,29 @@ def append(cache, fp8: bool, block_table, positions, c_kv, k_rope):
     vp = lambda a: a.ctypes.data_as(ctypes.c_void_p)
     err = lib.mla_oracle_append(vp(cache), 1 if fp8 else 0, num_pages, vp(bt), bt.shape[1], vp(pos), vp(ck), vp(kr), B)
     return cache, int(err)
+
+
+def absorb(q_c, w_uk):
+    """Absorbed queries: q_c [B][H][dh], w_uk [H][dh][512] (float64) -> [B][H][512]."""
+    qc, pq = _c(q_c, np.float64)
+    w, pw = _c(w_uk, np.float64)
+    B, H, dh = qc.shape
+    assert w.shape == (H, dh, D_LATENT)
+    out = np.zeros((B, H, D_LATENT), np.float64)
+    _load().mla_oracle_absorb(B, H, dh, pq, pw, out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def project(out_latent, w_uv):
+    """Per-head value projection: out [B][H][512], w_uv [H][dh][512] (float64) -> [B][H][dh]."""
+    o, po = _c(out_latent, np.float64)
+    w, pw = _c(w_uv, np.float64)
+    B, H, D = o.shape
+    dh = w.shape[1]
+    assert D == D_LATENT and w.shape == (H, dh, D_LATENT)
+    y = np.zeros((B, H, dh), np.float64)
+    _load().mla_oracle_project(B, H, dh, po, pw, y.ctypes.data_as(ctypes.c_void_p))
+    return y
 
 
 def attend_f64(q_nope, q_rope, C, Kr, scale):

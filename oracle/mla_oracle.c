@@ -24,7 +24,8 @@
  *  - "MLA & DSA 推理性能优化指南", §1.1 (absorbed path: W_UK folded into the query,
  *    attention computed in latent space, only c_t^KV and the 64-d RoPE key cached) and
  *    §4.1 (decode reads (d_c + d_rope) values per token).  The output stays in the
- *    512-d latent space; W^UV is applied afterwards, outside this operation.
+ *    512-d latent space; W^UV is applied afterwards (mla_oracle_project, at the end of
+ *    this file, next to the query absorption mla_oracle_absorb).
  *  - Same guide, §4.2: the token-sparse (DSA) decode attends over the selected top-k
  *    tokens only.
  *  - Same guide, §5.3: the FP8 latent cache.  The pages do not fix the FP8 format; this
@@ -405,4 +406,47 @@ int mla_oracle_append(uint8_t *cache, int fp8, int64_t num_pages, const int32_t 
         memcpy(dst + D_LATENT + 16, kr, D_ROPE * 2);
     }
     return errors;
+}
+
+/* ------------------------------------------------------------------------------------
+ * Absorption and output projection around the decode.
+ *
+ * "MLA 在极长上下文下的显存带宽突围", section "运行期矩阵吸收": the decode query of head h
+ * is q~ = q^C W^UK, the per-head nope query (d_h wide) times that head's up-projection
+ * (d_h x 512), so that the score is taken against the 512-d latent directly.  "MLA & DSA
+ * 推理性能优化指南" §1.1: the absorbed path keeps the output in latent space; the value
+ * up-projection W^UV (latent -> d_h per head) is applied to that output afterwards, which
+ * equals attending over the decompressed values v_t = W^UV c_t (linearity).
+ *
+ * Layouts (row-major): q^C [B][H][dh], W^UK and W^UV [H][dh][512] (row j of head h is the
+ * 512-d latent direction of output channel j), latent output [B][H][512], y [B][H][dh].
+ * Plain double sums in index order.
+ * ------------------------------------------------------------------------------------ */
+
+/* q_abs[b][h][c] = sum_k qc[b][h][k] * w_uk[h][k][c] */
+void mla_oracle_absorb(int B, int H, int dh, const double *qc, const double *w_uk, double *q_abs) {
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h) {
+            const double *q = qc + ((int64_t)b * H + h) * dh;
+            double *o = q_abs + ((int64_t)b * H + h) * D_LATENT;
+            for (int c = 0; c < D_LATENT; ++c) {
+                double s = 0.0;
+                for (int k = 0; k < dh; ++k) s += q[k] * w_uk[((int64_t)h * dh + k) * D_LATENT + c];
+                o[c] = s;
+            }
+        }
+}
+
+/* y[b][h][j] = sum_c w_uv[h][j][c] * out[b][h][c] */
+void mla_oracle_project(int B, int H, int dh, const double *out, const double *w_uv, double *y) {
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h) {
+            const double *o = out + ((int64_t)b * H + h) * D_LATENT;
+            for (int j = 0; j < dh; ++j) {
+                const double *w = w_uv + ((int64_t)h * dh + j) * D_LATENT;
+                double s = 0.0;
+                for (int c = 0; c < D_LATENT; ++c) s += w[c] * o[c];
+                y[((int64_t)b * H + h) * dh + j] = s;
+            }
+        }
 }

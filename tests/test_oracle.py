@@ -59,6 +59,72 @@ def test_absorbed_equals_nonabsorbed(H, N):
     np.testing.assert_allclose(lse, ref_lse, rtol=1e-12, atol=1e-12)
 
 
+def _absorb_project_pins(absorb, project):
+    """Pins of the absorption and output projection, as a list of (name, ok) over the pair.
+
+    1. absorbed decode through absorb/project == non-absorbed attention over decompressed
+       per-head keys and values (the two never share a product);
+    2. W^UK = identity on a head-dependent block of 128 latent columns gives q~ = q^C there
+       and zeros elsewhere; W^UV selecting a head-dependent permutation of latent columns
+       gives y = those entries of out;
+    3. adjoint: <absorb(q, W), X> == <q, project(X, W)> for any X (absorb and project use
+       the same matrix, once as q W and once as W x)."""
+    r = _rng(71)
+    res = []
+    B, H, N, d_h = 2, 3, 13, 128
+    qC = r.standard_normal((B, H, d_h))
+    qR = r.standard_normal((B, H, 64))
+    W_UK = r.standard_normal((H, d_h, 512)) / math.sqrt(512)
+    W_UV = r.standard_normal((H, d_h, 512)) / math.sqrt(512)
+    C = r.standard_normal((N, 512))
+    KR = r.standard_normal((N, 64))
+    q_abs = absorb(qC, W_UK)
+    lat = np.zeros((B, H, 512))
+    ok = True
+    for b in range(B):
+        o, _ = oracle.attend_f64(q_abs[b], qR[b], C, KR, SCALE)
+        lat[b] = o
+    y = project(lat, W_UV)
+    for b in range(B):
+        for h in range(H):
+            K, V = C @ W_UK[h].T, C @ W_UV[h].T
+            sc = (K @ qC[b, h] + KR @ qR[b, h]) * SCALE
+            pr = np.exp(sc - sc.max())
+            ok &= np.allclose(y[b, h], (pr / pr.sum()) @ V, rtol=1e-9, atol=1e-12)
+    res.append(("absorbed == non-absorbed", bool(ok)))
+
+    E = np.zeros((H, d_h, 512))
+    for h in range(H):
+        c0 = 128 * ((h + 1) % 4)
+        E[h, np.arange(d_h), c0 + np.arange(d_h)] = 1.0
+    qa = absorb(qC, E)
+    ok = True
+    for h in range(H):
+        c0 = 128 * ((h + 1) % 4)
+        ok &= np.array_equal(qa[:, h, c0:c0 + d_h], qC[:, h])
+        ok &= not np.any(np.delete(qa[:, h], np.s_[c0:c0 + d_h], axis=1))
+    res.append(("identity block", bool(ok)))
+
+    Pm = np.zeros((H, d_h, 512))
+    perms = [r.permutation(512)[:d_h] for _ in range(H)]
+    for h in range(H):
+        Pm[h, np.arange(d_h), perms[h]] = 1.0
+    X = r.standard_normal((B, H, 512))
+    yp = project(X, Pm)
+    ok = all(np.array_equal(yp[:, h], X[:, h][:, perms[h]]) for h in range(H))
+    res.append(("column selection", bool(ok)))
+
+    lhs = float(np.sum(absorb(qC, W_UK) * X))
+    rhs = float(np.sum(qC * project(X, W_UK)))
+    res.append(("adjoint", abs(lhs - rhs) <= 1e-10 * max(1.0, abs(lhs))))
+    return res
+
+
+def test_absorb_and_project_pins():
+    bad = [n for n, ok in _absorb_project_pins(oracle.absorb, oracle.project) if not ok]
+    assert not bad, bad
+
+
 def test_rope_term_and_scale_matter():
     """Changing only k_R or only the scale must change the result (guards dropped terms)."""
     r = _rng(5)

@@ -30,6 +30,19 @@ MUTANTS = {
 }
 
 
+# slips in the absorption / projection (checked with test_oracle's absorb/project pins)
+PROJ_MUTANTS = {
+    "absorb_head0_weights": ("s += q[k] * w_uk[((int64_t)h * dh + k) * D_LATENT + c];",
+                             "s += q[k] * w_uk[((int64_t)0 * dh + k) * D_LATENT + c];"),
+    "absorb_transposed_w": ("s += q[k] * w_uk[((int64_t)h * dh + k) * D_LATENT + c];",
+                            "s += q[k] * w_uk[(int64_t)h * dh * D_LATENT + ((int64_t)c * dh + k) % (dh * D_LATENT)];"),
+    "project_drops_last": ("for (int c = 0; c < D_LATENT; ++c) s += w[c] * o[c];",
+                           "for (int c = 0; c < D_LATENT - 1; ++c) s += w[c] * o[c];"),
+    "project_wrong_head": ("const double *o = out + ((int64_t)b * H + h) * D_LATENT;\n            for (int j",
+                           "const double *o = out + ((int64_t)b * H + (h + 1) % H) * D_LATENT;\n            for (int j"),
+}
+
+
 def _build(tmp_path, name, old, new):
     src = open(SRC).read()
     assert old in src, name
@@ -86,3 +99,35 @@ def test_mutant_is_caught(tmp_path, name):
     old, new = MUTANTS[name]
     lib = _build(tmp_path, name, old, new)
     assert not _pins_hold(lambda *a: _attend(lib, *a)), f"pins missed mutant {name}"
+
+
+def _proj_fns(lib):
+    P, I = ctypes.c_void_p, ctypes.c_int
+    lib.mla_oracle_absorb.argtypes = [I, I, I, P, P, P]
+    lib.mla_oracle_project.argtypes = [I, I, I, P, P, P]
+    ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+
+    def absorb(q, w):
+        q = np.ascontiguousarray(q, dtype=np.float64)
+        w = np.ascontiguousarray(w, dtype=np.float64)
+        out = np.zeros(q.shape[:2] + (512,))
+        lib.mla_oracle_absorb(q.shape[0], q.shape[1], q.shape[2], ptr(q), ptr(w), ptr(out))
+        return out
+
+    def project(o, w):
+        o = np.ascontiguousarray(o, dtype=np.float64)
+        w = np.ascontiguousarray(w, dtype=np.float64)
+        y = np.zeros(o.shape[:2] + (w.shape[1],))
+        lib.mla_oracle_project(o.shape[0], o.shape[1], w.shape[1], ptr(o), ptr(w), ptr(y))
+        return y
+
+    return absorb, project
+
+
+@pytest.mark.parametrize("name", sorted(PROJ_MUTANTS))
+def test_projection_mutant_is_caught(tmp_path, name):
+    from test_oracle import _absorb_project_pins
+    old, new = PROJ_MUTANTS[name]
+    lib = _build(tmp_path, name, old, new)
+    res = _absorb_project_pins(*_proj_fns(lib))
+    assert not all(ok for _, ok in res), f"pins missed mutant {name}"
