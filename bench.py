@@ -43,11 +43,35 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+# the sources of the decode call (plan, decode kernel, split merge) whose DRAM traffic
+# profiles/traffic.json records
+DECODE_SOURCES = ("api.cu", "common.cuh", "decode_sm103.cu", "launch.h", "plan.h", "sm103_ptx.cuh")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "mla_latent_kv_17_gb300", "csrc", "*"))):
-        h.update(open(f, "rb").read())
+    for f in DECODE_SOURCES:
+        h.update(open(os.path.join(ROOT, "mla_latent_kv_17_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
+
+
+def time_alone(fn, steps, flush, stream):
+    """Mean CUDA-event time (ms) of fn() on `stream`, after 3 warm-up calls, with L2 flushed
+    before every timed call."""
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    ms = []
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        fn()
+        eb.record(stream)
+        eb.synchronize()
+        ms.append(ea.elapsed_time(eb))
+    return sum(ms) / len(ms)
 
 
 def dram_traffic(workload: str):
@@ -389,6 +413,17 @@ def main():
     n_app = int((a_pos >= 0).sum().item())
     app_bytes = n_app * (rec_bytes + 1024 + 128 + 4 + 4)  # record out; latent, rope, position, page id in
 
+    # ---- query absorption before and value projection after the decode (random weights of
+    # the workload's head count; q^C and the latent output of its batch), each timed alone
+    q_c, w_uk, w_uv, lat_out = inputs.projection_inputs(case.B, case.H, seed=8, device=dev)
+    q_abs = torch.empty(case.B, case.H, 512, dtype=torch.bfloat16, device=dev)
+    y_prj = torch.empty(case.B, case.H, 128, dtype=torch.float32, device=dev)
+    ab_ms = time_alone(lambda: ops.absorb_query(q_c, w_uk, q_nope=q_abs, stream=stream), args.steps, flush, stream)
+    pj_ms = time_alone(lambda: ops.project_output(lat_out, w_uv, y=y_prj, stream=stream), args.steps, flush, stream)
+    BH = case.B * case.H
+    ab_bytes = case.H * 128 * 512 * 2 + BH * 128 * 2 + BH * 512 * 2  # W^UK, q^C in; q~ out
+    pj_bytes = case.H * 128 * 512 * 2 + BH * 512 * 4 + BH * 128 * 4  # W^UV, latent out in; y out
+
     pk, pk_kind = peaks()
     tf = alg["flops"] / (ms_per_step * 1e-3) / 1e12 * ws_n
     gbs = alg["bytes"] / (ms_per_step * 1e-3) / 1e9
@@ -422,6 +457,12 @@ def main():
         "append": {"kernel": "cache append (mla_cache_append), one token per request", "requests": n_app,
                    "kv": case.kv_dtype, "us": app_ms * 1e3, "bytes": app_bytes,
                    "gbs": app_bytes / (app_ms * 1e-3) / 1e9},
+        "absorb": {"kernel": "query absorption q~ = q^C W^UK (mla_absorb_query)", "us": ab_ms * 1e3,
+                   "bytes": ab_bytes, "gbs": ab_bytes / (ab_ms * 1e-3) / 1e9,
+                   "frac_hbm": ab_bytes / (ab_ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
+        "project": {"kernel": "value projection y = W^UV out (mla_project_output)", "us": pj_ms * 1e3,
+                    "bytes": pj_bytes, "gbs": pj_bytes / (pj_ms * 1e-3) / 1e9,
+                    "frac_hbm": pj_bytes / (pj_ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
         "clocks": clk.summary(),
         "wall_s_timed_region": t_wall,
     }

@@ -144,6 +144,30 @@ mla_status mla_cache_append(void *cache, mla_kv_dtype kv_dtype, int64_t num_page
                             const void *c_kv, const void *k_rope, int B, int32_t *device_status,
                             void *stream);
 
+/* Query absorption before the decode ("MLA 在极长上下文下的显存带宽突围", run-time matrix
+ * absorption: q~ = q^C W^UK, the up-projection folded into the query so that the score is
+ * taken against the 512-d latent): for every request b and head h,
+ *   q_nope[b][h][c] = bf16_rne( sum_k q_c[b][h][k] * w_uk[h][k][c] ),  c < 512, k < 128,
+ * with bf16 inputs, fp32 accumulation (tensor cores) and one rounding to bf16, ready for
+ * mla_decode.  q_c bf16 [B][H][128] (the per-head nope query, d_h = 128 of the guide's
+ * §5.1), w_uk bf16 [H][128][512], q_nope bf16 [B][H][512]; all device pointers, 16-byte
+ * aligned, caller-owned.  Launched as a programmatic dependent of the previous kernel on
+ * `stream` (it waits for that kernel before reading q_c).  *device_status (optional,
+ * device int32) receives MLA_ERR_TIMEOUT if an internal wait gives up. */
+mla_status mla_absorb_query(const void *q_c, const void *w_uk, int B, int H, void *q_nope,
+                            int32_t *device_status, void *stream);
+
+/* Value up-projection after the decode ("MLA & DSA 推理性能优化指南", §1.1: the absorbed
+ * path attends in latent space and W^UV maps the result back to each head's value space):
+ *   y[b][h][j] = sum_c bf16_rne(out[b][h][c]) * w_uv[h][j][c],  j < 128, c < 512,
+ * fp32 accumulation (tensor cores; the latent output is rounded to bf16, the operand type of
+ * the bf16 MMA), y fp32.  out fp32 [B][H][512] (mla_decode's output), w_uv bf16
+ * [H][128][512], y fp32 [B][H][128]; device pointers, 16-byte aligned, caller-owned.
+ * Launched as a programmatic dependent of the previous kernel on `stream` (it waits for
+ * that kernel before reading out).  device_status as for mla_absorb_query. */
+mla_status mla_project_output(const float *out, const void *w_uv, int B, int H, float *y,
+                              int32_t *device_status, void *stream);
+
 /* Host twin of mla_decode_plan for tests and tooling: plans from a HOST array
  * seq_lens[B] (NULL with topk > 0) into a HOST buffer of mla_decode_workspace_size()
  * bytes, producing exactly the bytes the device planner writes into the plan region.

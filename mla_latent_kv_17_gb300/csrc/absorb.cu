@@ -1,0 +1,369 @@
+// Query absorption before the absorbed decode and the value up-projection after it, one bf16
+// matrix per head ("MLA 在极长上下文下的显存带宽突围", run-time matrix absorption: q~ = q^C W^UK;
+// "MLA & DSA 推理性能优化指南" §1.1: W^UV is applied to the latent output afterwards).  The
+// definitions are in include/mla_decode.h (mla_absorb_query, mla_project_output).
+//
+// Both are batched over the requests of one head, so the request index is the MMA's N side
+// (up to 64 requests per tile) and the weight matrix its M side:
+//   absorb : D[c][b] = sum_k W^UK[h][k][c] q^C[b][h][k]    M = 128 latent columns, K = d_h
+//   project: D[j][b] = sum_c W^UV[h][j][c] out[b][h][c]    M = d_h = 128, K = 512
+// so that one TMEM lane holds one output channel of every request in the tile, and a warp's
+// stores for one request cover 32 consecutive channels.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "mla_decode.h"
+#include "sm103_ptx.cuh"
+
+namespace mla {
+namespace {
+
+using namespace ptx;
+
+constexpr int kDh = 128;     // per-head nope / value width d_h
+constexpr int kNb = 64;      // requests per tile (MMA N, TMEM columns)
+constexpr uint32_t kWBox = 128 * 128;       // 128 rows x 64 bf16 of a weight matrix, 128-B swizzle
+constexpr uint32_t kRBox = kNb * 128;       // 64 requests x 64 bf16, 128-B swizzle
+constexpr long long kSpinCycles = 4000000000LL;  // about two seconds
+
+// absorb: A = W^UK[h][0:128][c0 : c0 + 128] as two MN-major boxes, B = q^C of the tile as two
+// K-major boxes; then three mbarriers and the TMEM address
+constexpr uint32_t kAbsBar = 2 * kWBox + 2 * kRBox;
+constexpr uint32_t kAbsSmem = kAbsBar + 32 + 1024;
+// project: A = W^UV[h] as eight K-major boxes (512 latent columns), B = out of the tile
+// converted to bf16, eight K-major boxes
+constexpr uint32_t kPrjBar = 8 * kWBox + 8 * kRBox;
+constexpr uint32_t kPrjSmem = kPrjBar + 32 + 1024;
+constexpr int kPrjThreads = 256;
+
+__device__ bool wait_bounded(uint32_t bar, uint32_t parity) {
+    const long long t0 = (long long)clock64_now();
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 63u && (long long)clock64_now() - t0 > kSpinCycles) return false;
+    }
+}
+
+// Gives copies or MMAs still in flight a bounded time to land before the CTA leaves.
+__device__ __forceinline__ void drain_pause() {
+    const long long t0 = (long long)clock64_now();
+    while ((long long)clock64_now() - t0 < 20000000LL) {
+    }
+}
+
+// 16-B global load (read-only path) and 8-B shared store as volatile asm, so that all of a
+// thread's loads are issued before its first store.
+__device__ __forceinline__ float4 ld_nc_v4(const float *p) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t a, uint32_t b) {
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float f) {
+    __nv_bfloat16 v = __float2bfloat16_rn(f);
+    return *reinterpret_cast<uint16_t *>(&v);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// One CTA per (latent tile ct of 128 columns, head h, request tile bt): four warps.
+__global__ void __launch_bounds__(128) absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
+                                                     const __grid_constant__ CUtensorMap tm_q, uint16_t *q_abs,
+                                                     int B, int H, int *status) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char *gbase = smem_raw + (base - raw);
+    const uint32_t sA = base, sB = base + 2 * kWBox;
+    const uint32_t bar_full = base + kAbsBar, bar_done = bar_full + 8;
+    volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(gbase + kAbsBar + 16);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ct = blockIdx.x & 3;
+    const int h = (blockIdx.x >> 2) % H;
+    const int bt = (blockIdx.x >> 2) / H;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_init(bar_full, 1);
+            mbar_init(bar_done, 1);
+            fence_mbar_init();
+        }
+        __syncwarp();
+        tmem_alloc(smem_u32(const_cast<uint32_t *>(tslot)), kNb);
+        tmem_relinquish();
+    }
+    grid_dep_wait();  // q^C may come from the previous kernel of the stream
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    bool ok = true;
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(bar_full, 2 * kWBox + 2 * kRBox);
+        for (int i = 0; i < 2; ++i) tma_load_3d(sA + i * kWBox, &tm_w, 128 * ct + 64 * i, 0, h, bar_full);
+        for (int i = 0; i < 2; ++i) tma_load_3d(sB + i * kRBox, &tm_q, 64 * i, h, kNb * bt, bar_full);
+        ok = wait_bounded(bar_full, 0);
+        if (ok) {
+            tc_fence_after();
+            constexpr uint32_t idesc = idesc_bf16_major(128, kNb, true, false);
+            for (int k = 0; k < kDh / 16; ++k) {
+                // A: 16 k-rows of both 64-column boxes; B: 16 k of the request rows
+                const uint64_t ad = smem_desc_sw128(sA + k * 2048u, kWBox, 1024u);
+                const uint64_t bd = smem_desc_sw128(sB + (k >> 2) * kRBox + (k & 3) * 32u, 16u, 1024u);
+                mma_ss(tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
+            }
+            mma_commit(bar_done);
+        }
+    }
+    grid_dep_launch();
+    if (__syncthreads_and(ok ? 1 : 0)) {
+        ok = wait_bounded(bar_done, 0);
+        tc_fence_after();
+        if (ok) {
+            const int c = 128 * ct + 32 * warp + lane;
+            const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
+#pragma unroll 1
+            for (int ch = 0; ch < kNb / 32; ++ch) {
+                uint32_t r[32];
+                tmem_ld32(taddr + 32u * ch, r);
+                tmem_wait_ld();
+                const int b0 = kNb * bt + 32 * ch;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (b0 + i < B) q_abs[((int64_t)(b0 + i) * H + h) * kDLatent + c] = bf16_bits(__uint_as_float(r[i]));
+            }
+        }
+    }
+    if (!ok) {
+        if (status) record_error(status, MLA_ERR_TIMEOUT);
+        drain_pause();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kNb);
+    }
+}
+
+// One CTA per (head h, request tile bt): eight warps convert the tile's fp32 latent output to
+// bf16 while the weights arrive; one thread issues the MMAs; all eight store.
+__global__ void __launch_bounds__(kPrjThreads) project_kernel(const __grid_constant__ CUtensorMap tm_v,
+                                                              const float *__restrict__ out, float *y, int B,
+                                                              int H, int *status) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char *gbase = smem_raw + (base - raw);
+    const uint32_t sA = base, sB = base + 8 * kWBox;
+    const uint32_t bar_a = base + kPrjBar, bar_b = bar_a + 8, bar_done = bar_a + 16;
+    volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(gbase + kPrjBar + 24);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.x % H;
+    const int bt = blockIdx.x / H;
+    const int b0 = kNb * bt;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_init(bar_a, 1);
+            mbar_init(bar_b, kPrjThreads / 32);
+            mbar_init(bar_done, 1);
+            fence_mbar_init();
+        }
+        __syncwarp();
+        tmem_alloc(smem_u32(const_cast<uint32_t *>(tslot)), kNb);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    if (threadIdx.x == 0) {  // the weights do not depend on the previous kernel
+        mbar_arrive_expect_tx(bar_a, 8 * kWBox);
+        for (int i = 0; i < 8; ++i) tma_load_3d(sA + i * kWBox, &tm_v, 64 * i, 0, h, bar_a);
+    }
+    grid_dep_wait();  // the latent output comes from the previous kernel of the stream
+
+    // 64 requests x 128 chunks of four fp32: chunk id = thread + 256 i, request row id / 128,
+    // chunk c4 = id % 128 (columns 4 c4 .. 4 c4 + 3), so a warp reads 512 contiguous bytes.
+    constexpr int kIter = kNb * (kDLatent / 4) / kPrjThreads;
+    float4 v[kIter];
+#pragma unroll
+    for (int i = 0; i < kIter; ++i) {
+        const int id = threadIdx.x + kPrjThreads * i;
+        const int b = b0 + (id >> 7);
+        v[i] = b < B ? ld_nc_v4(out + ((int64_t)b * H + h) * kDLatent + 4 * (id & 127))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncwarp();  // keeps every load ahead of the first store
+#pragma unroll
+    for (int i = 0; i < kIter; ++i) {
+        const int id = threadIdx.x + kPrjThreads * i;
+        const int row = id >> 7, c4 = id & 127;
+        // box c4 / 16 (64 columns); 16-B unit (c4 % 16) / 2 of the row, swizzled by row % 8
+        const uint32_t dst = sB + (c4 >> 4) * kRBox + row * 128 + ((((c4 & 15) >> 1) ^ (row & 7)) << 4) + (c4 & 1) * 8;
+        st_shared_v2(dst, bf16x2_bits(v[i].x, v[i].y), bf16x2_bits(v[i].z, v[i].w));
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_b);
+
+    bool ok = true;
+    if (threadIdx.x == 0) {
+        ok = wait_bounded(bar_a, 0) && wait_bounded(bar_b, 0);
+        if (ok) {
+            tc_fence_after();
+            constexpr uint32_t idesc = idesc_bf16_major(128, kNb, false, false);
+            for (int k = 0; k < kDLatent / 16; ++k) {
+                const uint64_t ad = smem_desc_sw128(sA + (k >> 2) * kWBox + (k & 3) * 32u, 16u, 1024u);
+                const uint64_t bd = smem_desc_sw128(sB + (k >> 2) * kRBox + (k & 3) * 32u, 16u, 1024u);
+                mma_ss(tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
+            }
+            mma_commit(bar_done);
+        }
+    }
+    grid_dep_launch();
+    if (__syncthreads_and(ok ? 1 : 0)) {
+        ok = wait_bounded(bar_done, 0);
+        tc_fence_after();
+        if (ok) {
+            // warp w: TMEM lanes 32 (w % 4) .. (output channels j), requests 32 (w / 4) ..
+            const int j = 32 * (warp & 3) + lane;
+            const int half = warp >> 2;
+            uint32_t r[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32u * half, r);
+            tmem_wait_ld();
+            const int bb = b0 + 32 * half;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (bb + i < B) y[((int64_t)(bb + i) * H + h) * kDh + j] = __uint_as_float(r[i]);
+        }
+    }
+    if (!ok) {
+        if (status) record_error(status, MLA_ERR_TIMEOUT);
+        drain_pause();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kNb);
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 3-D bf16 tensor (d0 innermost, d1, d2) with byte strides s1, s2; boxes b0 x b1 x b2, 128-B
+// swizzle; elements outside the tensor read as zero.
+bool tmap_3d(CUtensorMap *m, const void *p, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
+             uint32_t b0, uint32_t b1, uint32_t b2) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {s1, s2};
+    const cuuint32_t box[3] = {b0, b1, b2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool set_attrs() {
+    static bool done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (done[dev]) return true;
+    if (cudaFuncSetAttribute(absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAbsSmem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrjSmem) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    done[dev] = true;
+    return true;
+}
+
+template <typename K, typename... Args>
+cudaError_t launch_pdl(K kernel, int grid, int threads, uint32_t smem, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" mla_status mla_absorb_query(const void *q_c, const void *w_uk, int B, int H, void *q_nope,
+                                       int32_t *device_status, void *stream) {
+    if (!q_c || !w_uk || !q_nope || B < 1 || H < 1) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q_c) || !aligned16(w_uk) || !aligned16(q_nope)) return MLA_ERR_INVALID_ARG;
+    const int64_t tiles = (int64_t)4 * H * ((B + kNb - 1) / kNb);
+    if (tiles > 0x7FFFFFFF) return MLA_ERR_UNSUPPORTED;
+    if (!set_attrs()) return MLA_ERR_CUDA;
+    CUtensorMap tw, tq;
+    // W^UK [H][128][512]: (c, k, h); q^C [B][H][128]: (k, h, b)
+    if (!tmap_3d(&tw, w_uk, kDLatent, kDh, H, kDLatent * 2, (uint64_t)kDh * kDLatent * 2, 64, 128, 1) ||
+        !tmap_3d(&tq, q_c, kDh, H, B, kDh * 2, (uint64_t)kDh * 2 * H, 64, 1, kNb))
+        return MLA_ERR_CUDA;
+    return launch_pdl(absorb_kernel, (int)tiles, 128, kAbsSmem, (cudaStream_t)stream, tw, tq, (uint16_t *)q_nope,
+                      B, H, (int *)device_status) == cudaSuccess
+               ? MLA_OK
+               : MLA_ERR_CUDA;
+}
+
+extern "C" mla_status mla_project_output(const float *out, const void *w_uv, int B, int H, float *y,
+                                         int32_t *device_status, void *stream) {
+    if (!out || !w_uv || !y || B < 1 || H < 1) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(w_uv) || !aligned16(y)) return MLA_ERR_INVALID_ARG;
+    const int64_t tiles = (int64_t)H * ((B + kNb - 1) / kNb);
+    if (tiles > 0x7FFFFFFF) return MLA_ERR_UNSUPPORTED;
+    if (!set_attrs()) return MLA_ERR_CUDA;
+    CUtensorMap tv;
+    // W^UV [H][128][512]: (c, j, h)
+    if (!tmap_3d(&tv, w_uv, kDLatent, kDh, H, kDLatent * 2, (uint64_t)kDh * kDLatent * 2, 64, 128, 1))
+        return MLA_ERR_CUDA;
+    return launch_pdl(project_kernel, (int)tiles, kPrjThreads, kPrjSmem, (cudaStream_t)stream, tv, out, y, B, H,
+                      (int *)device_status) == cudaSuccess
+               ? MLA_OK
+               : MLA_ERR_CUDA;
+}

@@ -284,6 +284,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Same, with the major order of each operand chosen (MN-major A: bit 15, MN-major B: bit 16).
+__host__ __device__ constexpr uint32_t idesc_bf16_major(int M, int N, bool a_mn_major, bool b_mn_major) {
+    return idesc_bf16(M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
+}
+
 __device__ __forceinline__ uint64_t clock64_now() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%clock64;" : "=l"(t));

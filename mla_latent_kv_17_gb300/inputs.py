@@ -212,3 +212,18 @@ def make_workload(name: str, device="cpu") -> Case:
         c.indices = sparse_indices(sl, 2048, 512, seed + 1000).to(device)
     c.meta["workload"] = name
     return c
+
+
+D_HEAD = 128  # per-head nope query / value width d_h ("MLA & DSA 推理性能优化指南" §5.1)
+
+
+def projection_inputs(B: int, H: int, seed: int, device="cpu"):
+    """Per-head nope queries q^C [B,H,128] ~ N(0,1) and the two up-projections W^UK, W^UV
+    [H,128,512] with N(0, 1/fan_in) entries (fan_in 128 for W^UK, 512 for W^UV), all rounded
+    to bf16, plus a latent output [B,H,512] fp32 ~ N(0,1) for the value projection."""
+    g = _gen(seed, "cpu")
+    q_c = torch.randn(B, H, D_HEAD, generator=g).to(torch.bfloat16)
+    w_uk = (torch.randn(H, D_HEAD, D_LATENT, generator=g) / math.sqrt(D_HEAD)).to(torch.bfloat16)
+    w_uv = (torch.randn(H, D_HEAD, D_LATENT, generator=g) / math.sqrt(D_LATENT)).to(torch.bfloat16)
+    out = torch.randn(B, H, D_LATENT, generator=g)
+    return q_c.to(device), w_uk.to(device), w_uv.to(device), out.to(device)

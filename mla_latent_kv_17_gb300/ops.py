@@ -57,6 +57,10 @@ def lib():
             L.mla_decode_static.restype = I
             L.mla_cache_append.argtypes = [P, I, I64, P, I, P, P, P, I, P, P]
             L.mla_cache_append.restype = I
+            L.mla_absorb_query.argtypes = [P, P, I, I, P, P, P]
+            L.mla_absorb_query.restype = I
+            L.mla_project_output.argtypes = [P, P, I, I, P, P, P]
+            L.mla_project_output.restype = I
             L.mla_decode_status.argtypes = [P, SZ, P]
             L.mla_decode_status.restype = I
             L.mla_status_string.argtypes = [I]
@@ -186,6 +190,49 @@ def cache_append(cache, block_table, positions, c_kv, k_rope, device_status=None
                                 _stream(stream))
     _check("mla_cache_append", st)
     return cache
+
+
+def _weights(w, H, name):
+    if w.dtype != torch.bfloat16 or w.shape != (H, 128, 512) or not w.is_contiguous() or not w.is_cuda:
+        raise ValueError(f"{name} must be contiguous CUDA bf16 [{H},128,512]")
+
+
+def absorb_query(q_c, w_uk, q_nope=None, device_status=None, stream=None):
+    """Absorbed decode query q_nope[b,h] = q_c[b,h] @ w_uk[h] (bf16 [B,H,128] x bf16 [H,128,512]
+    -> bf16 [B,H,512], fp32 accumulation)."""
+    if q_c.dtype != torch.bfloat16 or q_c.dim() != 3 or q_c.shape[2] != 128 or not q_c.is_contiguous() \
+            or not q_c.is_cuda:
+        raise ValueError("q_c must be contiguous CUDA bf16 [B,H,128]")
+    B, H = q_c.shape[0], q_c.shape[1]
+    _weights(w_uk, H, "w_uk")
+    if q_nope is None:
+        q_nope = torch.empty((B, H, 512), dtype=torch.bfloat16, device=q_c.device)
+    elif q_nope.dtype != torch.bfloat16 or q_nope.shape != (B, H, 512) or not q_nope.is_contiguous():
+        raise ValueError(f"q_nope must be contiguous bf16 [{B},{H},512]")
+    if device_status is not None:
+        _i32(device_status, "device_status")
+    st = lib().mla_absorb_query(_ptr(q_c), _ptr(w_uk), B, H, _ptr(q_nope), _ptr(device_status), _stream(stream))
+    _check("mla_absorb_query", st)
+    return q_nope
+
+
+def project_output(out, w_uv, y=None, device_status=None, stream=None):
+    """Per-head value projection y[b,h] = w_uv[h] @ out[b,h] (fp32 [B,H,512], bf16 [H,128,512]
+    -> fp32 [B,H,128]; the latent output enters the bf16 MMA rounded to bf16)."""
+    if out.dtype != torch.float32 or out.dim() != 3 or out.shape[2] != 512 or not out.is_contiguous() \
+            or not out.is_cuda:
+        raise ValueError("out must be contiguous CUDA fp32 [B,H,512]")
+    B, H = out.shape[0], out.shape[1]
+    _weights(w_uv, H, "w_uv")
+    if y is None:
+        y = torch.empty((B, H, 128), dtype=torch.float32, device=out.device)
+    elif y.dtype != torch.float32 or y.shape != (B, H, 128) or not y.is_contiguous():
+        raise ValueError(f"y must be contiguous fp32 [{B},{H},128]")
+    if device_status is not None:
+        _i32(device_status, "device_status")
+    st = lib().mla_project_output(_ptr(out), _ptr(w_uv), B, H, _ptr(y), _ptr(device_status), _stream(stream))
+    _check("mla_project_output", st)
+    return y
 
 
 def decode_sparse(ws: Workspace, q_nope, q_rope, cache, block_table, seq_lens, indices,

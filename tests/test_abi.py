@@ -31,7 +31,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for must in ("mla_decode_workspace_size", "mla_decode_plan", "mla_decode", "mla_decode_sparse",
-                 "mla_decode_status", "mla_status_string", "mla_decode_plan_host"):
+                 "mla_decode_status", "mla_status_string", "mla_decode_plan_host",
+                 "mla_cache_append", "mla_absorb_query", "mla_project_output"):
         assert must in names
 
 
@@ -105,6 +106,22 @@ def test_plan_rejects_bad_arguments_on_host(L):
     assert L.mla_decode_plan(P(4096), 2, 200, 0, 148, P(4096), 1 << 20, None) == 2
     assert L.mla_decode_plan(P(4096), 2, 16, 0, 148, P(4096), 64, None) == 3
     assert L.mla_decode_plan_host(None, 2, 16, 0, 0, P(4096), 1 << 20) == 1
+
+
+def test_absorb_project_append_reject_bad_arguments_on_host(L):
+    P = ctypes.c_void_p
+    f = P(4096)
+    odd = P(4096 + 8)  # not 16-byte aligned
+    assert L.mla_absorb_query(None, f, 4, 16, f, None, None) == 1
+    assert L.mla_absorb_query(f, f, 0, 16, f, None, None) == 1
+    assert L.mla_absorb_query(f, f, 4, 0, f, None, None) == 1
+    assert L.mla_absorb_query(f, odd, 4, 16, f, None, None) == 1
+    assert L.mla_project_output(f, None, 4, 16, f, None, None) == 1
+    assert L.mla_project_output(f, f, -1, 16, f, None, None) == 1
+    assert L.mla_project_output(odd, f, 4, 16, f, None, None) == 1
+    assert L.mla_cache_append(f, 0, 10, f, 4, f, f, f, 0, None, None) == 1
+    assert L.mla_cache_append(f, 7, 10, f, 4, f, f, f, 2, None, None) == 1
+    assert L.mla_cache_append(odd, 0, 10, f, 4, f, f, f, 2, None, None) == 1
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
