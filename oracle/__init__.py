@@ -23,6 +23,10 @@ Functions follow these passages (page title, section):
 * ``absorb`` / ``project``: the query absorption q~ = q^C W^UK ("MLA 在极长上下文下的显存
   带宽突围", run-time matrix absorption) and the value up-projection W^UV applied to the
   latent output afterwards ("MLA & DSA 推理性能优化指南" §1.1), one matrix per head.
+* ``topk_select``: the DSA token selection ("MLA & DSA 推理性能优化指南" §1.2: an indexer scores
+  every earlier token and only the top-k take part in the attention; "GPU partial sort").
+  This library's reading: the k highest scores of positions [0, seq_len), equal scores in
+  ascending position order (-0.0 equals +0.0), returned as ascending positions padded with -1.
 * ``combine``: merge of split-KV partial results through their log-sum-exp, the
   "Fused Reduction" the operator survey ("MLA 最佳算子全景调研" §3) pairs with
   weight-absorbed decode.
@@ -165,6 +169,23 @@ def project(out_latent, w_uv):
     y = np.zeros((B, H, dh), np.float64)
     _load().mla_oracle_project(B, H, dh, po, pw, y.ctypes.data_as(ctypes.c_void_p))
     return y
+
+
+def topk_select(scores, seq_lens, k):
+    """DSA indices: scores float32 [B][Lmax], seq_lens int [B], k -> int32 [B][k].
+
+    Row b keeps the min(k, seq_lens[b]) positions of [0, seq_lens[b]) with the largest scores
+    (a stable sort on the negated scores puts equal scores in ascending position order),
+    listed in ascending position order and padded with -1."""
+    s = np.asarray(scores, dtype=np.float32)
+    B = s.shape[0]
+    out = np.full((B, k), -1, dtype=np.int32)
+    for b in range(B):
+        L = int(seq_lens[b])
+        order = np.argsort(-s[b, :L], kind="stable")
+        sel = np.sort(order[:min(k, L)])
+        out[b, :sel.size] = sel
+    return out
 
 
 def attend_f64(q_nope, q_rope, C, Kr, scale):

@@ -125,6 +125,65 @@ def test_absorb_and_project_pins():
     assert not bad, bad
 
 
+# --------------------------------------------------------------------------------------
+# DSA top-k selection (guide §1.2: the k best-scored earlier tokens, "GPU partial sort")
+# --------------------------------------------------------------------------------------
+def _topk_brute(scores, L, k):
+    """Position t is kept iff fewer than min(k, L) positions beat it: a higher score, or an
+    equal score at a lower position (pure Python, O(L^2))."""
+    K = min(k, L)
+    keep = []
+    for t in range(L):
+        beat = sum(1 for u in range(L) if scores[u] > scores[t] or (scores[u] == scores[t] and u < t))
+        if beat < K:
+            keep.append(t)
+    return keep + [-1] * (k - len(keep))
+
+
+def test_topk_matches_brute_force_on_tiny_inputs():
+    r = _rng(90)
+    for trial in range(40):
+        Lmax = int(r.integers(1, 40))
+        k = int(r.integers(1, 45))
+        B = 3
+        # few distinct values, so ties are common; signed zeros included
+        s = r.choice(np.array([-1.5, -0.0, 0.0, 0.25, 2.0, 7.0], dtype=np.float32), size=(B, Lmax))
+        lens = r.integers(0, Lmax + 1, size=B)
+        got = oracle.topk_select(s, lens, k)
+        for b in range(B):
+            assert got[b].tolist() == _topk_brute(s[b].tolist(), int(lens[b]), k)
+
+
+def test_topk_special_cases():
+    L, k = 100, 16
+    eq = np.ones((1, L), np.float32)
+    assert oracle.topk_select(eq, [L], k)[0].tolist() == list(range(k))          # all tied
+    dec = -np.arange(L, dtype=np.float32)[None]
+    assert oracle.topk_select(dec, [L], k)[0].tolist() == list(range(k))         # decreasing
+    inc = np.arange(L, dtype=np.float32)[None]
+    assert oracle.topk_select(inc, [L], k)[0].tolist() == list(range(L - k, L))  # increasing
+    short = oracle.topk_select(inc, [5], k)[0].tolist()
+    assert short == list(range(5)) + [-1] * (k - 5)                              # L < k
+    assert oracle.topk_select(inc, [0], k)[0].tolist() == [-1] * k               # empty
+    z = np.array([[0.0, -0.0, 0.0, -0.0]], np.float32)                           # -0 == +0
+    assert oracle.topk_select(z, [4], 2)[0].tolist() == [0, 1]
+
+
+def test_topk_invariants_on_random_scores():
+    r = _rng(91)
+    B, Lmax, k = 4, 5000, 700
+    s = r.standard_normal((B, Lmax)).astype(np.float32)
+    lens = np.array([5000, 701, 700, 3])
+    got = oracle.topk_select(s, lens, k)
+    for b in range(B):
+        L = int(lens[b])
+        sel = got[b][got[b] >= 0]
+        assert sel.size == min(k, L) and np.all(np.diff(sel) > 0) and np.all(sel < L)
+        rest = np.setdiff1d(np.arange(L), sel)
+        if rest.size:
+            assert s[b, sel].min() >= s[b, rest].max()
+
+
 def test_rope_term_and_scale_matter():
     """Changing only k_R or only the scale must change the result (guards dropped terms)."""
     r = _rng(5)

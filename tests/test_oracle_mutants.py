@@ -131,3 +131,43 @@ def test_projection_mutant_is_caught(tmp_path, name):
     lib = _build(tmp_path, name, old, new)
     res = _absorb_project_pins(*_proj_fns(lib))
     assert not all(ok for _, ok in res), f"pins missed mutant {name}"
+
+
+# slips in the top-k selection, planted in a copy of oracle.topk_select's source
+TOPK_MUTANTS = {
+    "unsorted_output": ("sel = np.sort(order[:min(k, L)])", "sel = order[:min(k, L)]"),
+    "keeps_lowest": ("np.argsort(-s[b, :L]", "np.argsort(s[b, :L]"),
+    "reads_past_length": ("s[b, :L]", "s[b, :L + 1]"),
+    "ties_to_high_position": ("order = np.argsort(-s[b, :L], kind=\"stable\")",
+                              "order = (L - 1 - np.argsort(-s[b, :L][::-1], kind=\"stable\"))"),
+}
+
+
+def _topk_pins_hold(fn):
+    from test_oracle import _topk_brute
+    r = np.random.default_rng(92)
+    for _ in range(30):
+        Lmax, k = int(r.integers(2, 30)), int(r.integers(1, 30))
+        s = r.choice(np.array([-1.0, 0.0, 0.5, 3.0], dtype=np.float32), size=(2, Lmax))
+        lens = r.integers(0, Lmax, size=2)
+        got = fn(s, lens, k)
+        for b in range(2):
+            if got[b].tolist() != _topk_brute(s[b].tolist(), int(lens[b]), k):
+                return False
+    return True
+
+
+def test_real_topk_passes_pins():
+    assert _topk_pins_hold(oracle.topk_select)
+
+
+@pytest.mark.parametrize("name", sorted(TOPK_MUTANTS))
+def test_topk_mutant_is_caught(name):
+    import inspect
+    import textwrap
+    old, new = TOPK_MUTANTS[name]
+    src = textwrap.dedent(inspect.getsource(oracle.topk_select))
+    assert old in src, name
+    ns = {"np": np}
+    exec(src.replace(old, new), ns)
+    assert not _topk_pins_hold(ns["topk_select"]), f"pins missed mutant {name}"
