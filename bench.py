@@ -420,6 +420,14 @@ def main():
     y_prj = torch.empty(case.B, case.H, 128, dtype=torch.float32, device=dev)
     ab_ms = time_alone(lambda: ops.absorb_query(q_c, w_uk, q_nope=q_abs, stream=stream), args.steps, flush, stream)
     pj_ms = time_alone(lambda: ops.project_output(lat_out, w_uv, y=y_prj, stream=stream), args.steps, flush, stream)
+    # DSA top-k selection over synthetic indexer scores of the workload's lengths (k = 2048)
+    tk_k = 2048
+    tk_lmax = (int(case.seq_lens.max().item()) + 3) // 4 * 4
+    tk_scores = torch.randn(case.B, tk_lmax, generator=torch.Generator(device=dev).manual_seed(9), device=dev)
+    tk_idx = torch.empty(case.B, tk_k, dtype=torch.int32, device=dev)
+    tk_ms = time_alone(lambda: ops.topk_select(tk_scores, case.seq_lens, tk_k, indices=tk_idx, stream=stream),
+                       args.steps, flush, stream)
+    tk_bytes = int(case.seq_lens.sum().item()) * 4 + case.B * (tk_k + 1) * 4  # scores, lengths in; indices out
     BH = case.B * case.H
     ab_bytes = case.H * 128 * 512 * 2 + BH * 128 * 2 + BH * 512 * 2  # W^UK, q^C in; q~ out
     pj_bytes = case.H * 128 * 512 * 2 + BH * 512 * 4 + BH * 128 * 4  # W^UV, latent out in; y out
@@ -463,6 +471,9 @@ def main():
         "project": {"kernel": "value projection y = W^UV out (mla_project_output)", "us": pj_ms * 1e3,
                     "bytes": pj_bytes, "gbs": pj_bytes / (pj_ms * 1e-3) / 1e9,
                     "frac_hbm": pj_bytes / (pj_ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
+        "topk": {"kernel": "DSA top-k selection (mla_topk_select), k = 2048 per request", "us": tk_ms * 1e3,
+                 "bytes": tk_bytes, "gbs": tk_bytes / (tk_ms * 1e-3) / 1e9,
+                 "frac_hbm": tk_bytes / (tk_ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
         "clocks": clk.summary(),
         "wall_s_timed_region": t_wall,
     }

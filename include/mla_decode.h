@@ -168,6 +168,19 @@ mla_status mla_absorb_query(const void *q_c, const void *w_uk, int B, int H, voi
 mla_status mla_project_output(const float *out, const void *w_uv, int B, int H, float *y,
                               int32_t *device_status, void *stream);
 
+/* DSA token selection ("MLA & DSA 推理性能优化指南" §1.2: a lightweight indexer scores every
+ * earlier token and only the top-k join the sparse attention; "GPU partial sort").  For each
+ * request b with L = seq_lens[b] (0 <= L <= Lmax), keeps the min(k, L) positions of [0, L)
+ * with the highest scores[b * row_stride + t] (fp32; equal scores go to the lower position;
+ * -0.0 equals +0.0) and writes them to indices[b][0..k) in ascending position order, padded
+ * with -1 — the index list mla_decode_sparse takes.  Scores must not be NaN.  A length
+ * outside [0, Lmax] writes k times -1 for that request and records MLA_ERR_INDEX in
+ * *device_status (optional, device int32).  scores: device fp32, 16-byte aligned, row_stride
+ * a multiple of 4 and >= Lmax; seq_lens, indices: device int32 ([B], [B][k]).  k >= 1. */
+mla_status mla_topk_select(const float *scores, int64_t row_stride, int Lmax,
+                           const int32_t *seq_lens, int B, int k, int32_t *indices,
+                           int32_t *device_status, void *stream);
+
 /* Host twin of mla_decode_plan for tests and tooling: plans from a HOST array
  * seq_lens[B] (NULL with topk > 0) into a HOST buffer of mla_decode_workspace_size()
  * bytes, producing exactly the bytes the device planner writes into the plan region.

@@ -1,0 +1,197 @@
+// DSA token selection ("MLA & DSA 推理性能优化指南" §1.2: an indexer scores every earlier token
+// and only the top-k take part in the sparse attention; "GPU partial sort"): per request, the
+// k positions of [0, seq_len) with the highest scores, equal scores to the lower position,
+// written as ascending positions padded with -1.  The definition is in include/mla_decode.h
+// (mla_topk_select).
+//
+// One CTA of 1024 threads per request.  Scores map to order-preserving 32-bit keys; three
+// histogram passes (11, 11 and 10 key bits) narrow down the key of the k-th best position
+// (radix select), then one ordered pass writes every position above that key and the
+// first `need` positions equal to it, in position order, through block-wide prefix sums.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "mla_decode.h"
+
+namespace mla {
+namespace {
+
+constexpr int kTkThreads = 1024;
+constexpr int kTkWarps = kTkThreads / 32;
+constexpr int kBins = 2048;
+constexpr int kHistCopies = 8;  // warp w adds into copy w % 8 (fewer collisions on hot bins)
+constexpr uint32_t kTkSmem = kHistCopies * kBins * 4;
+
+// Larger key <=> larger score; -0.0 and +0.0 share a key.
+__device__ __forceinline__ uint32_t order_key(float f) {
+    uint32_t u = __float_as_uint(f);
+    if (u == 0x80000000u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float4 ld4(const float *p) { return __ldg(reinterpret_cast<const float4 *>(p)); }
+
+// Inclusive prefix sum of v over the block in thread order; `total` gets the block's sum.
+__device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t *warp_sums, uint32_t &total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t w = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const uint32_t before = warp ? warp_sums[warp - 1] : 0u;
+    total = warp_sums[kTkWarps - 1];
+    __syncthreads();  // warp_sums is reused by the next scan
+    return x + before;
+}
+
+__global__ void __launch_bounds__(kTkThreads) topk_kernel(const float *__restrict__ scores, int64_t stride, int Lmax,
+                                                          const int32_t *__restrict__ seq_lens, int k,
+                                                          int32_t *indices, int *status) {
+    extern __shared__ uint32_t hist[];  // [kHistCopies][kBins]
+    __shared__ uint32_t warp_sums[kTkWarps];
+    __shared__ uint32_t sel_bin, sel_above;
+    const int b = blockIdx.x;
+    const int L = seq_lens[b];
+    int32_t *out = indices + (int64_t)b * k;
+    if (L < 0 || L > Lmax) {
+        if (threadIdx.x == 0 && status) record_error(status, MLA_ERR_INDEX);
+        for (int i = threadIdx.x; i < k; i += kTkThreads) out[i] = -1;
+        return;
+    }
+    const int K = min(k, L);
+    if (K == L) {  // every position is kept
+        for (int i = threadIdx.x; i < k; i += kTkThreads) out[i] = i < L ? i : -1;
+        return;
+    }
+    const float *s = scores + (int64_t)b * stride;
+    const int n4 = (L + 3) >> 2;
+
+    // ---- radix select: key of the K-th best position, and how many of its ties to keep
+    uint32_t prefix = 0u, pmask = 0u, need = (uint32_t)K;
+    uint32_t *hmine = hist + ((threadIdx.x >> 5) & (kHistCopies - 1)) * kBins;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 21 : pass == 1 ? 10 : 0;
+        const uint32_t bmask = pass == 2 ? 1023u : 2047u;
+        for (int i = threadIdx.x; i < kHistCopies * kBins; i += kTkThreads) hist[i] = 0u;
+        __syncthreads();
+        for (int i = threadIdx.x; i < n4; i += kTkThreads) {
+            const float4 v = ld4(s + 4 * i);
+            const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t key = order_key(f[j]);
+                if (4 * i + j < L && (key & pmask) == prefix) atomicAdd(&hmine[(key >> shift) & bmask], 1u);
+            }
+        }
+        __syncthreads();
+        // thread t holds bins hi = 2047 - 2t and lo = hi - 1, so thread order is descending key
+        const int hi = kBins - 1 - 2 * (int)threadIdx.x, lo = hi - 1;
+        uint32_t ch = 0u, cl = 0u;
+#pragma unroll
+        for (int c = 0; c < kHistCopies; ++c) {
+            ch += hist[c * kBins + hi];
+            cl += hist[c * kBins + lo];
+        }
+        uint32_t total;
+        const uint32_t incl = block_scan(ch + cl, warp_sums, total);
+        const uint32_t above = incl - ch - cl;  // keys (with this prefix) in bins above hi
+        if (above < need && need <= above + ch) {
+            sel_bin = (uint32_t)hi;
+            sel_above = above;
+        } else if (above + ch < need && need <= incl) {
+            sel_bin = (uint32_t)lo;
+            sel_above = above + ch;
+        }
+        __syncthreads();
+        prefix |= sel_bin << shift;
+        pmask |= bmask << shift;
+        need -= sel_above;
+        __syncthreads();  // sel_bin / sel_above and hist are rewritten by the next pass
+    }
+    const uint32_t kstar = prefix;
+
+    // ---- ordered write: positions above kstar, and the first `need` positions equal to it
+    uint32_t base_gt = 0u, base_eq = 0u;
+#pragma unroll 1
+    for (int r0 = 0; r0 < L; r0 += 4 * kTkThreads) {
+        const int p0 = r0 + 4 * (int)threadIdx.x;
+        uint32_t gt = 0u, eq = 0u, ngt = 0u, neq = 0u;
+        if (p0 < L) {
+            const float4 v = ld4(s + p0);
+            const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t key = order_key(f[j]);
+                const bool ok = p0 + j < L;
+                if (ok && key > kstar) gt |= 1u << j;
+                if (ok && key == kstar) eq |= 1u << j;
+            }
+            ngt = __popc(gt);
+            neq = __popc(eq);
+        }
+        uint32_t total;
+        const uint32_t mine = (ngt << 16) | neq;  // at most 4096 of each per round
+        const uint32_t excl = block_scan(mine, warp_sums, total) - mine;
+        const uint32_t gt_before = base_gt + (excl >> 16);
+        uint32_t eq_seen = base_eq + (excl & 0xFFFFu);
+        uint32_t slot = gt_before + min(need, eq_seen);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (gt & (1u << j)) {
+                out[slot++] = p0 + j;
+            } else if (eq & (1u << j)) {
+                if (eq_seen < need) out[slot++] = p0 + j;
+                ++eq_seen;
+            }
+        }
+        base_gt += total >> 16;
+        base_eq += total & 0xFFFFu;
+    }
+    for (int i = K + (int)threadIdx.x; i < k; i += kTkThreads) out[i] = -1;
+}
+
+bool set_topk_attr() {
+    static bool done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (done[dev]) return true;
+    if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTkSmem) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    done[dev] = true;
+    return true;
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" mla_status mla_topk_select(const float *scores, int64_t row_stride, int Lmax, const int32_t *seq_lens,
+                                      int B, int k, int32_t *indices, int32_t *device_status, void *stream) {
+    if (!scores || !seq_lens || !indices || B < 1 || k < 1 || Lmax < 0 || row_stride < Lmax ||
+        (row_stride & 3) != 0 || (reinterpret_cast<uintptr_t>(scores) & 15u) != 0)
+        return MLA_ERR_INVALID_ARG;
+    if (!set_topk_attr()) return MLA_ERR_CUDA;
+    topk_kernel<<<B, kTkThreads, kTkSmem, (cudaStream_t)stream>>>(scores, row_stride, Lmax, seq_lens, k, indices,
+                                                                 (int *)device_status);
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}

@@ -57,6 +57,8 @@ def lib():
             L.mla_decode_static.restype = I
             L.mla_cache_append.argtypes = [P, I, I64, P, I, P, P, P, I, P, P]
             L.mla_cache_append.restype = I
+            L.mla_topk_select.argtypes = [P, I64, I, P, I, I, P, P, P]
+            L.mla_topk_select.restype = I
             L.mla_absorb_query.argtypes = [P, P, I, I, P, P, P]
             L.mla_absorb_query.restype = I
             L.mla_project_output.argtypes = [P, P, I, I, P, P, P]
@@ -190,6 +192,25 @@ def cache_append(cache, block_table, positions, c_kv, k_rope, device_status=None
                                 _stream(stream))
     _check("mla_cache_append", st)
     return cache
+
+
+def topk_select(scores, seq_lens, k: int, indices=None, device_status=None, stream=None):
+    """DSA indices int32 [B,k]: per request the k best-scored positions of [0, seq_len)
+    (scores fp32 [B,Lmax], ties to the lower position), ascending, padded with -1."""
+    if scores.dtype != torch.float32 or scores.dim() != 2 or not scores.is_cuda or scores.stride(1) != 1:
+        raise ValueError("scores must be a CUDA fp32 [B,Lmax] tensor with unit column stride")
+    _i32(seq_lens, "seq_lens")
+    B, Lmax = scores.shape
+    if indices is None:
+        indices = torch.empty((B, k), dtype=torch.int32, device=scores.device)
+    elif indices.dtype != torch.int32 or indices.shape != (B, k) or not indices.is_contiguous():
+        raise ValueError(f"indices must be contiguous int32 [{B},{k}]")
+    if device_status is not None:
+        _i32(device_status, "device_status")
+    st = lib().mla_topk_select(_ptr(scores), scores.stride(0), Lmax, _ptr(seq_lens), B, int(k), _ptr(indices),
+                               _ptr(device_status), _stream(stream))
+    _check("mla_topk_select", st)
+    return indices
 
 
 def _weights(w, H, name):

@@ -32,7 +32,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for must in ("mla_decode_workspace_size", "mla_decode_plan", "mla_decode", "mla_decode_sparse",
                  "mla_decode_status", "mla_status_string", "mla_decode_plan_host",
-                 "mla_cache_append", "mla_absorb_query", "mla_project_output"):
+                 "mla_cache_append", "mla_absorb_query", "mla_project_output", "mla_topk_select"):
         assert must in names
 
 
@@ -119,6 +119,11 @@ def test_absorb_project_append_reject_bad_arguments_on_host(L):
     assert L.mla_project_output(f, None, 4, 16, f, None, None) == 1
     assert L.mla_project_output(f, f, -1, 16, f, None, None) == 1
     assert L.mla_project_output(odd, f, 4, 16, f, None, None) == 1
+    assert L.mla_topk_select(None, 64, 64, f, 2, 8, f, None, None) == 1
+    assert L.mla_topk_select(f, 62, 62, f, 2, 8, f, None, None) == 1     # stride not a multiple of 4
+    assert L.mla_topk_select(f, 64, 65, f, 2, 8, f, None, None) == 1     # stride < Lmax
+    assert L.mla_topk_select(f, 64, 64, f, 2, 0, f, None, None) == 1     # k < 1
+    assert L.mla_topk_select(odd, 64, 64, f, 2, 8, f, None, None) == 1
     assert L.mla_cache_append(f, 0, 10, f, 4, f, f, f, 0, None, None) == 1
     assert L.mla_cache_append(f, 7, 10, f, 4, f, f, f, 2, None, None) == 1
     assert L.mla_cache_append(odd, 0, 10, f, 4, f, f, f, 2, None, None) == 1
