@@ -7,8 +7,9 @@
 // (up to 64 requests per tile) and the weight matrix its M side:
 //   absorb : D[c][b] = sum_k W^UK[h][k][c] q^C[b][h][k]    M = 128 latent columns, K = d_h
 //   project: D[j][b] = sum_c W^UV[h][j][c] out[b][h][c]    M = d_h = 128, K = 512
-// so that one TMEM lane holds one output channel of every request in the tile, and a warp's
-// stores for one request cover 32 consecutive channels.
+// so that one TMEM lane holds one output channel of every request in the tile.  The
+// projection's warps store y straight from TMEM (32 consecutive channels of one request per
+// store); the absorption transposes q~ through shared memory and stores it by the TMA.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -37,7 +38,7 @@ constexpr uint32_t kAbsSmem = kAbsBar + 32 + 1024;
 // converted to bf16, eight K-major boxes
 constexpr uint32_t kPrjBar = 8 * kWBox + 8 * kRBox;
 constexpr uint32_t kPrjSmem = kPrjBar + 32 + 1024;
-constexpr int kPrjThreads = 256;
+constexpr int kPrjThreads = 512;  // sixteen warps: more of the latent output's loads in flight
 
 __device__ bool wait_bounded(uint32_t bar, uint32_t parity) {
     const long long t0 = (long long)clock64_now();
@@ -67,6 +68,19 @@ __device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
 }
 
+// Tile store shared -> global through a 3-D tensor map (bulk group), and the waits for it.
+__device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int32_t x, int32_t y, int32_t z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(src), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until the committed bulk stores have completed (written to global memory).
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
 __device__ __forceinline__ uint16_t bf16_bits(float f) {
     __nv_bfloat16 v = __float2bfloat16_rn(f);
     return *reinterpret_cast<uint16_t *>(&v);
@@ -79,8 +93,9 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
 
 // One CTA per (latent tile ct of 128 columns, head h, request tile bt): four warps.
 __global__ void __launch_bounds__(128) absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
-                                                     const __grid_constant__ CUtensorMap tm_q, uint16_t *q_abs,
-                                                     int B, int H, int *status) {
+                                                     const __grid_constant__ CUtensorMap tm_q,
+                                                     const __grid_constant__ CUtensorMap tm_o, int H,
+                                                     int *status) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -132,19 +147,31 @@ __global__ void __launch_bounds__(128) absorb_kernel(const __grid_constant__ CUt
         ok = wait_bounded(bar_done, 0);
         tc_fence_after();
         if (ok) {
-            const int c = 128 * ct + 32 * warp + lane;
+            // q~ of the tile, transposed into two 64-column boxes [64 requests][64 bf16] (128-B
+            // swizzle) over the weight boxes (the MMAs have read them), then stored by the TMA;
+            // rows past B fall outside the tensor and are not written
+            const int cc = 32 * (warp & 1) + lane;  // column within box warp / 2
+            const uint32_t box = sA + (warp >> 1) * kRBox;
             const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
 #pragma unroll 1
             for (int ch = 0; ch < kNb / 32; ++ch) {
                 uint32_t r[32];
                 tmem_ld32(taddr + 32u * ch, r);
                 tmem_wait_ld();
-                const int b0 = kNb * bt + 32 * ch;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (b0 + i < B) q_abs[((int64_t)(b0 + i) * H + h) * kDLatent + c] = bf16_bits(__uint_as_float(r[i]));
+                for (int i = 0; i < 32; ++i) {
+                    const int b = 32 * ch + i;
+                    st_shared_u16(box + b * 128 + ((((cc >> 3) ^ (b & 7))) << 4) + (cc & 7) * 2,
+                                  bf16_bits(__uint_as_float(r[i])));
+                }
             }
+            fence_proxy_async_smem();
         }
+    }
+    if (__syncthreads_and(ok ? 1 : 0) && threadIdx.x == 0) {
+        for (int q = 0; q < 2; ++q) tma_store_3d(&tm_o, sA + q * kRBox, 128 * ct + 64 * q, h, kNb * bt);
+        bulk_commit_group();
+        bulk_wait_group0();
     }
     if (!ok) {
         if (status) record_error(status, MLA_ERR_TIMEOUT);
@@ -158,8 +185,8 @@ __global__ void __launch_bounds__(128) absorb_kernel(const __grid_constant__ CUt
     }
 }
 
-// One CTA per (head h, request tile bt): eight warps convert the tile's fp32 latent output to
-// bf16 while the weights arrive; one thread issues the MMAs; all eight store.
+// One CTA per (head h, request tile bt): sixteen warps convert the tile's fp32 latent output
+// to bf16 while the weights arrive; one thread issues the MMAs; eight warps store.
 __global__ void __launch_bounds__(kPrjThreads) project_kernel(const __grid_constant__ CUtensorMap tm_v,
                                                               const float *__restrict__ out, float *y, int B,
                                                               int H, int *status) {
@@ -200,14 +227,17 @@ __global__ void __launch_bounds__(kPrjThreads) project_kernel(const __grid_const
     // chunk c4 = id % 128 (columns 4 c4 .. 4 c4 + 3), so a warp reads 512 contiguous bytes.
     constexpr int kIter = kNb * (kDLatent / 4) / kPrjThreads;
     float4 v[kIter];
+    // every load is issued unconditionally (rows past B read row B - 1 and are zeroed after),
+    // so that none waits behind a branch
 #pragma unroll
     for (int i = 0; i < kIter; ++i) {
         const int id = threadIdx.x + kPrjThreads * i;
-        const int b = b0 + (id >> 7);
-        v[i] = b < B ? ld_nc_v4(out + ((int64_t)b * H + h) * kDLatent + 4 * (id & 127))
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        const int b = min(b0 + (id >> 7), B - 1);
+        v[i] = ld_nc_v4(out + ((int64_t)b * H + h) * kDLatent + 4 * (id & 127));
     }
-    __syncwarp();  // keeps every load ahead of the first store
+#pragma unroll
+    for (int i = 0; i < kIter; ++i)
+        if (b0 + ((threadIdx.x + kPrjThreads * i) >> 7) >= B) v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < kIter; ++i) {
         const int id = threadIdx.x + kPrjThreads * i;
@@ -238,8 +268,8 @@ __global__ void __launch_bounds__(kPrjThreads) project_kernel(const __grid_const
     if (__syncthreads_and(ok ? 1 : 0)) {
         ok = wait_bounded(bar_done, 0);
         tc_fence_after();
-        if (ok) {
-            // warp w: TMEM lanes 32 (w % 4) .. (output channels j), requests 32 (w / 4) ..
+        if (ok && warp < 8) {
+            // warp w < 8: TMEM lanes 32 (w % 4) .. (output channels j), requests 32 (w / 4) ..
             const int j = 32 * (warp & 3) + lane;
             const int half = warp >> 2;
             uint32_t r[32];
@@ -340,13 +370,14 @@ extern "C" mla_status mla_absorb_query(const void *q_c, const void *w_uk, int B,
     const int64_t tiles = (int64_t)4 * H * ((B + kNb - 1) / kNb);
     if (tiles > 0x7FFFFFFF) return MLA_ERR_UNSUPPORTED;
     if (!set_attrs()) return MLA_ERR_CUDA;
-    CUtensorMap tw, tq;
-    // W^UK [H][128][512]: (c, k, h); q^C [B][H][128]: (k, h, b)
+    CUtensorMap tw, tq, to;
+    // W^UK [H][128][512]: (c, k, h); q^C [B][H][128]: (k, h, b); q~ [B][H][512]: (c, h, b)
     if (!tmap_3d(&tw, w_uk, kDLatent, kDh, H, kDLatent * 2, (uint64_t)kDh * kDLatent * 2, 64, 128, 1) ||
-        !tmap_3d(&tq, q_c, kDh, H, B, kDh * 2, (uint64_t)kDh * 2 * H, 64, 1, kNb))
+        !tmap_3d(&tq, q_c, kDh, H, B, kDh * 2, (uint64_t)kDh * 2 * H, 64, 1, kNb) ||
+        !tmap_3d(&to, q_nope, kDLatent, H, B, kDLatent * 2, (uint64_t)kDLatent * 2 * H, 64, 1, kNb))
         return MLA_ERR_CUDA;
-    return launch_pdl(absorb_kernel, (int)tiles, 128, kAbsSmem, (cudaStream_t)stream, tw, tq, (uint16_t *)q_nope,
-                      B, H, (int *)device_status) == cudaSuccess
+    return launch_pdl(absorb_kernel, (int)tiles, 128, kAbsSmem, (cudaStream_t)stream, tw, tq, to, H,
+                      (int *)device_status) == cudaSuccess
                ? MLA_OK
                : MLA_ERR_CUDA;
 }

@@ -8,6 +8,8 @@
 // histogram passes (11, 11 and 10 key bits) narrow down the key of the k-th best position
 // (radix select), then one ordered pass writes every position above that key and the
 // first `need` positions equal to it, in position order, through block-wide prefix sums.
+// Loads are batched (several 16-B loads per thread in flight) so that one CTA streams its
+// request's scores at more than one load per thread per memory latency.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -22,6 +24,8 @@ constexpr int kTkWarps = kTkThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kHistCopies = 8;  // warp w adds into copy w % 8 (fewer collisions on hot bins)
 constexpr uint32_t kTkSmem = kHistCopies * kBins * 4;
+constexpr int kLoadsInFlight = 8;  // float4 loads per thread per histogram iteration
+constexpr int kPerThread = 16;     // consecutive positions per thread per ordered-write round
 
 // Larger key <=> larger score; -0.0 and +0.0 share a key.
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -90,13 +94,21 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const float *__restric
         const uint32_t bmask = pass == 2 ? 1023u : 2047u;
         for (int i = threadIdx.x; i < kHistCopies * kBins; i += kTkThreads) hist[i] = 0u;
         __syncthreads();
-        for (int i = threadIdx.x; i < n4; i += kTkThreads) {
-            const float4 v = ld4(s + 4 * i);
-            const float f[4] = {v.x, v.y, v.z, v.w};
+        // kLoadsInFlight float4 loads per thread are issued before any of them is used
+        for (int i0 = threadIdx.x; i0 < n4; i0 += kLoadsInFlight * kTkThreads) {
+            float4 v[kLoadsInFlight];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t key = order_key(f[j]);
-                if (4 * i + j < L && (key & pmask) == prefix) atomicAdd(&hmine[(key >> shift) & bmask], 1u);
+            for (int u = 0; u < kLoadsInFlight; ++u) v[u] = ld4(s + 4 * min(i0 + u * kTkThreads, n4 - 1));
+#pragma unroll
+            for (int u = 0; u < kLoadsInFlight; ++u) {
+                const int i = i0 + u * kTkThreads;
+                const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t key = order_key(f[j]);
+                    if (i < n4 && 4 * i + j < L && (key & pmask) == prefix)
+                        atomicAdd(&hmine[(key >> shift) & bmask], 1u);
+                }
             }
         }
         __syncthreads();
@@ -126,33 +138,35 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const float *__restric
     }
     const uint32_t kstar = prefix;
 
-    // ---- ordered write: positions above kstar, and the first `need` positions equal to it
+    // ---- ordered write: positions above kstar, and the first `need` positions equal to it.
+    // A round covers kPerThread consecutive positions per thread, 16,384 per round.
     uint32_t base_gt = 0u, base_eq = 0u;
 #pragma unroll 1
-    for (int r0 = 0; r0 < L; r0 += 4 * kTkThreads) {
-        const int p0 = r0 + 4 * (int)threadIdx.x;
-        uint32_t gt = 0u, eq = 0u, ngt = 0u, neq = 0u;
-        if (p0 < L) {
-            const float4 v = ld4(s + p0);
-            const float f[4] = {v.x, v.y, v.z, v.w};
+    for (int r0 = 0; r0 < L; r0 += kPerThread * kTkThreads) {
+        const int p0 = r0 + kPerThread * (int)threadIdx.x;
+        float4 v[kPerThread / 4];
+#pragma unroll
+        for (int u = 0; u < kPerThread / 4; ++u) v[u] = ld4(s + min(p0 + 4 * u, 4 * (n4 - 1)));
+        uint32_t gt = 0u, eq = 0u;  // bit j: position p0 + j
+#pragma unroll
+        for (int u = 0; u < kPerThread / 4; ++u) {
+            const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint32_t key = order_key(f[j]);
-                const bool ok = p0 + j < L;
-                if (ok && key > kstar) gt |= 1u << j;
-                if (ok && key == kstar) eq |= 1u << j;
+                const bool ok = p0 + 4 * u + j < L;
+                if (ok && key > kstar) gt |= 1u << (4 * u + j);
+                if (ok && key == kstar) eq |= 1u << (4 * u + j);
             }
-            ngt = __popc(gt);
-            neq = __popc(eq);
         }
         uint32_t total;
-        const uint32_t mine = (ngt << 16) | neq;  // at most 4096 of each per round
+        const uint32_t mine = ((uint32_t)__popc(gt) << 16) | (uint32_t)__popc(eq);  // < 2^16 of each per round
         const uint32_t excl = block_scan(mine, warp_sums, total) - mine;
         const uint32_t gt_before = base_gt + (excl >> 16);
         uint32_t eq_seen = base_eq + (excl & 0xFFFFu);
         uint32_t slot = gt_before + min(need, eq_seen);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < kPerThread; ++j) {
             if (gt & (1u << j)) {
                 out[slot++] = p0 + j;
             } else if (eq & (1u << j)) {
