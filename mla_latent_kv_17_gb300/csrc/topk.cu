@@ -166,11 +166,15 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const float *__restric
         uint32_t eq_seen = base_eq + (excl & 0xFFFFu);
         uint32_t slot = gt_before + min(need, eq_seen);
 #pragma unroll
-        for (int j = 0; j < kPerThread; ++j) {
+        for (int j = 0; j < kPerThread; ++j) {  // slot < K always holds; the check keeps writes in the row
             if (gt & (1u << j)) {
-                out[slot++] = p0 + j;
+                if (slot < (uint32_t)K) out[slot] = p0 + j;
+                ++slot;
             } else if (eq & (1u << j)) {
-                if (eq_seen < need) out[slot++] = p0 + j;
+                if (eq_seen < need) {
+                    if (slot < (uint32_t)K) out[slot] = p0 + j;
+                    ++slot;
+                }
                 ++eq_seen;
             }
         }

@@ -71,6 +71,17 @@ def test_topk_dsa_size_equals_oracle():
     assert np.array_equal(got, oracle.topk_select(s.numpy(), lens, 2048))
 
 
+def test_topk_long_requests_reread_scores():
+    # quarters longer than the shared-memory key cache (36,864 keys per CTA) re-read scores
+    g = torch.Generator().manual_seed(76)
+    s = torch.randn(2, 150000, generator=g)
+    s[1, 1000:3000] = 5.0  # a block of ties above everything else
+    lens = [150000, 149999]
+    got, st = _run(s, lens, 2048)
+    assert st == 0
+    assert np.array_equal(got, oracle.topk_select(s.numpy(), lens, 2048))
+
+
 def test_topk_bad_length_is_reported():
     s = torch.randn(3, 64)
     got, st = _run(s, [10, 65, -1], 8)
