@@ -331,11 +331,7 @@ def main():
     st = ops.status(wsp, stream)
     if st != 0:
         raise RuntimeError(f"device status {ops.STATUS_NAMES.get(st, st)} in the call timing")
-    tot_ms = sum(step_ms)
-    if pg:
-        t = torch.tensor([tot_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        tot_ms = float(t.item())
+    tot_ms = metrics.max_over_ranks(sum(step_ms), pg, dev)
     ms_per_step = tot_ms / args.steps
     dec_avg_ms = sum(dec_ms) / len(dec_ms)
 
@@ -383,11 +379,7 @@ def main():
         b.record(stream)
         b.synchronize()
         e_ms.append(a.elapsed_time(b))
-    e2e_ms = sum(e_ms) / len(e_ms)
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = metrics.max_over_ranks(sum(e_ms) / len(e_ms), pg, dev)
 
     # ---- cache append (the step after decode): one token per request, timed alone -------
     # (written at each request's last position, inside its block table; after every decode
@@ -433,7 +425,7 @@ def main():
     pj_bytes = case.H * 128 * 512 * 2 + BH * 512 * 4 + BH * 128 * 4  # W^UV, latent out in; y out
 
     pk, pk_kind = peaks()
-    tf = alg["flops"] / (ms_per_step * 1e-3) / 1e12 * ws_n
+    tf = metrics.whole_job_rate(alg["flops"], ws_n, ms_per_step * 1e-3) / 1e12
     gbs = alg["bytes"] / (ms_per_step * 1e-3) / 1e9
     ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
     bound = "hbm" if alg["ai"] < ridge else "tensor"
@@ -459,7 +451,7 @@ def main():
                      "peak_source": pk_kind, "ai_flop_per_byte": alg["ai"],
                      "alg_bytes_per_call": alg["bytes"], "alg_flops_per_call": alg["flops"],
                      "call_ms": dec_avg_ms},
-        "e2e": {"value": alg["flops"] / (e2e_ms * 1e-3) / 1e12 * ws_n, "unit": "TFLOP/s",
+        "e2e": {"value": metrics.whole_job_rate(alg["flops"], ws_n, e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": 3 * args.steps,
         "append": {"kernel": "cache append (mla_cache_append), one token per request", "requests": n_app,

@@ -66,3 +66,21 @@ def algorithmic(case) -> dict:
 
 def roofline_seconds(flops: float, nbytes: float, peak_tflops: float, peak_gbs: float) -> float:
     return max(flops / (peak_tflops * 1e12), nbytes / (peak_gbs * 1e9))
+
+
+def max_over_ranks(value: float, dist=None, device="cpu") -> float:
+    """The largest `value` over all ranks of the initialised process group `dist` (the
+    torch.distributed module), or `value` itself when there is none: a multi-rank run is
+    timed by its slowest rank."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world_size: int, seconds: float) -> float:
+    """Units all ranks processed per second when every rank processes `units_per_rank`
+    (weak scaling) and the slowest rank took `seconds`."""
+    return units_per_rank * world_size / seconds
