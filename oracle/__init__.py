@@ -27,6 +27,9 @@ Functions follow these passages (page title, section):
   every earlier token and only the top-k take part in the attention; "GPU partial sort").
   This library's reading: the k highest scores of positions [0, seq_len), equal scores in
   ascending position order (-0.0 equals +0.0), returned as ascending positions padded with -1.
+* ``prefill``: the non-absorbed (MHA-mode) path of the same guide (§3.1, §1.1): latents
+  decompressed into per-head keys and values with W^UK and W^UV, then causal attention with
+  192-wide keys ([K_h | k_R]) and 128-wide values ("MLA 最佳算子全景调研" §4).
 * ``combine``: merge of split-KV partial results through their log-sum-exp, the
   "Fused Reduction" the operator survey ("MLA 最佳算子全景调研" §3) pairs with
   weight-absorbed decode.
@@ -90,6 +93,8 @@ def _load():
             lib.mla_oracle_absorb.restype = None
             lib.mla_oracle_project.argtypes = [I, I, I, P, P, P]
             lib.mla_oracle_project.restype = None
+            lib.mla_oracle_prefill.argtypes = [I, I, I, P, P, P, P, P, D, P, P]
+            lib.mla_oracle_prefill.restype = None
             lib.mla_oracle_default_threads.argtypes = []
             lib.mla_oracle_default_threads.restype = I
             common = [I, I, P, P, P, I64, P, I, P]
@@ -186,6 +191,24 @@ def topk_select(scores, seq_lens, k):
         sel = np.sort(order[:min(k, L)])
         out[b, :sel.size] = sel
     return out
+
+
+def prefill(entries, q_nope, q_rope, w_uk, w_uv, scale):
+    """Non-absorbed causal prefill of one sequence (float64 arrays): entries [L][576],
+    q_nope [L][H][dh], q_rope [L][H][64], w_uk / w_uv [H][dh][512] -> out [L][H][dh], lse [L][H]."""
+    e, pe = _c(entries, np.float64)
+    qn, pqn = _c(q_nope, np.float64)
+    qr, pqr = _c(q_rope, np.float64)
+    wk, pwk = _c(w_uk, np.float64)
+    wv, pwv = _c(w_uv, np.float64)
+    L, H, dh = qn.shape
+    assert e.shape == (L, D_ENTRY) and qr.shape == (L, H, D_ROPE)
+    assert wk.shape == (H, dh, D_LATENT) and wv.shape == (H, dh, D_LATENT)
+    out = np.zeros((L, H, dh), np.float64)
+    lse = np.zeros((L, H), np.float64)
+    _load().mla_oracle_prefill(L, H, dh, pe, pqn, pqr, pwk, pwv, float(scale),
+                               out.ctypes.data_as(ctypes.c_void_p), lse.ctypes.data_as(ctypes.c_void_p))
+    return out, lse
 
 
 def attend_f64(q_nope, q_rope, C, Kr, scale):

@@ -450,3 +450,63 @@ void mla_oracle_project(int B, int H, int dh, const double *out, const double *w
             }
         }
 }
+
+/* ------------------------------------------------------------------------------------
+ * Non-absorbed (MHA-mode) prefill of one sequence.
+ *
+ * "MLA & DSA 推理性能优化指南" §3.1 and §1.1 (non-absorbed path): the cached latents are
+ * first decompressed into per-head keys and values, K_h[t] = W^UK_h c_t and V_h[t] = W^UV_h
+ * c_t (d_h = 128 each), then standard multi-head attention runs with the 192-wide key
+ * [K_h[t] | k_R[t]] and query [q^C_h | q^R_h] ("MLA 最佳算子全景调研" §4: prefill is a
+ * FlashAttention variant with these head widths).  Causal: query i sees keys t <= i.
+ *
+ * entries [L][576] (latent | RoPE key, the cache entry layout), q_nope [L][H][dh], q_rope
+ * [L][H][64], w_uk and w_uv [H][dh][512]; out [L][H][dh], lse [L][H].  Plain double sums,
+ * two-pass softmax per query row.
+ * ------------------------------------------------------------------------------------ */
+void mla_oracle_prefill(int L, int H, int dh, const double *entries, const double *q_nope,
+                        const double *q_rope, const double *w_uk, const double *w_uv,
+                        double scale, double *out, double *lse) {
+    double *K = (double *)malloc(sizeof(double) * (size_t)L * dh);
+    double *V = (double *)malloc(sizeof(double) * (size_t)L * dh);
+    double *s = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+    for (int h = 0; h < H; ++h) {
+        for (int t = 0; t < L; ++t)
+            for (int j = 0; j < dh; ++j) {
+                const double *wk = w_uk + ((int64_t)h * dh + j) * D_LATENT;
+                const double *wv = w_uv + ((int64_t)h * dh + j) * D_LATENT;
+                const double *c = entries + (int64_t)t * D_ENTRY;
+                double sk = 0.0, sv = 0.0;
+                for (int x = 0; x < D_LATENT; ++x) {
+                    sk += wk[x] * c[x];
+                    sv += wv[x] * c[x];
+                }
+                K[(int64_t)t * dh + j] = sk;
+                V[(int64_t)t * dh + j] = sv;
+            }
+        for (int i = 0; i < L; ++i) {
+            const double *qn = q_nope + ((int64_t)i * H + h) * dh;
+            const double *qr = q_rope + ((int64_t)i * H + h) * D_ROPE;
+            double m = -INFINITY;
+            for (int t = 0; t <= i; ++t) {
+                double dot = 0.0;
+                for (int j = 0; j < dh; ++j) dot += qn[j] * K[(int64_t)t * dh + j];
+                for (int r = 0; r < D_ROPE; ++r) dot += qr[r] * entries[(int64_t)t * D_ENTRY + D_LATENT + r];
+                s[t] = scale * dot;
+                if (s[t] > m) m = s[t];
+            }
+            double l = 0.0;
+            for (int t = 0; t <= i; ++t) l += exp(s[t] - m);
+            double *o = out + ((int64_t)i * H + h) * dh;
+            for (int j = 0; j < dh; ++j) o[j] = 0.0;
+            for (int t = 0; t <= i; ++t) {
+                const double w = exp(s[t] - m) / l;
+                for (int j = 0; j < dh; ++j) o[j] += w * V[(int64_t)t * dh + j];
+            }
+            lse[(int64_t)i * H + h] = m + log(l);
+        }
+    }
+    free(K);
+    free(V);
+    free(s);
+}

@@ -184,6 +184,56 @@ def test_topk_invariants_on_random_scores():
             assert s[b, sel].min() >= s[b, rest].max()
 
 
+# --------------------------------------------------------------------------------------
+# Non-absorbed causal prefill (guide §3.1; operator survey §4)
+# --------------------------------------------------------------------------------------
+def _prefill_inputs(L, H, seed):
+    r = _rng(seed)
+    E = r.standard_normal((L, 576))
+    qn = r.standard_normal((L, H, 128))
+    qr = r.standard_normal((L, H, 64))
+    wk = r.standard_normal((H, 128, 512)) / math.sqrt(512)
+    wv = r.standard_normal((H, 128, 512)) / math.sqrt(512)
+    return E, qn, qr, wk, wv
+
+
+def _prefill_pins(prefill):
+    """(name, ok) pairs over a prefill function: rows equal the absorbed decode of the same
+    query over tokens 0..i projected with W^UV (the identity that lets decode skip the
+    decompression); row 0 sees one key (out = W^UV c_0, lse = its scaled score); zero
+    queries give uniform weights over t <= i (mean of the values, lse = ln(i + 1))."""
+    res = []
+    L, H = 9, 3
+    E, qn, qr, wk, wv = _prefill_inputs(L, H, 80)
+    out, lse = prefill(E, qn, qr, wk, wv, SCALE)
+    q_abs = oracle.absorb(qn, wk)
+    ok = True
+    for i in range(L):
+        lat, l2 = oracle.attend_f64(q_abs[i], qr[i], E[:i + 1, :512], E[:i + 1, 512:], SCALE)
+        y = oracle.project(lat[None], wv)[0]
+        ok &= np.allclose(out[i], y, rtol=1e-9, atol=1e-12) and np.allclose(lse[i], l2, rtol=1e-12, atol=1e-12)
+    res.append(("rows == absorbed decode", bool(ok)))
+    ok = True
+    for h in range(H):
+        ok &= np.allclose(out[0, h], wv[h] @ E[0, :512], rtol=1e-12, atol=1e-12)
+        s0 = SCALE * (qn[0, h] @ (wk[h] @ E[0, :512]) + qr[0, h] @ E[0, 512:])
+        ok &= abs(lse[0, h] - s0) < 1e-12
+    res.append(("row 0", bool(ok)))
+    out0, lse0 = prefill(E, np.zeros_like(qn), np.zeros_like(qr), wk, wv, SCALE)
+    ok = True
+    for i in range(L):
+        for h in range(H):
+            ok &= np.allclose(out0[i, h], (wv[h] @ E[:i + 1, :512].T).mean(axis=1), rtol=1e-12, atol=1e-12)
+            ok &= abs(lse0[i, h] - math.log(i + 1)) < 1e-12
+    res.append(("uniform weights", bool(ok)))
+    return res
+
+
+def test_prefill_pins():
+    bad = [n for n, ok in _prefill_pins(oracle.prefill) if not ok]
+    assert not bad, bad
+
+
 def test_rope_term_and_scale_matter():
     """Changing only k_R or only the scale must change the result (guards dropped terms)."""
     r = _rng(5)

@@ -171,3 +171,36 @@ def test_topk_mutant_is_caught(name):
     ns = {"np": np}
     exec(src.replace(old, new), ns)
     assert not _topk_pins_hold(ns["topk_select"]), f"pins missed mutant {name}"
+
+
+# slips in the non-absorbed prefill, planted in copies of the C oracle
+PREFILL_MUTANTS = {
+    "causal_excludes_diagonal": ("for (int t = 0; t <= i; ++t) {\n                double dot",
+                                 "for (int t = 0; t < (i > 0 ? i : 1); ++t) {\n                double dot"),
+    "values_from_w_uk": ("const double *wv = w_uv + ((int64_t)h * dh + j) * D_LATENT;",
+                         "const double *wv = w_uk + ((int64_t)h * dh + j) * D_LATENT;"),
+    "drops_rope_key": ("for (int r = 0; r < D_ROPE; ++r) dot += qr[r] * entries[(int64_t)t * D_ENTRY + D_LATENT + r];",
+                       "(void)qr;"),
+    "rope_key_from_latent": ("dot += qr[r] * entries[(int64_t)t * D_ENTRY + D_LATENT + r];",
+                             "dot += qr[r] * entries[(int64_t)t * D_ENTRY + r];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PREFILL_MUTANTS))
+def test_prefill_mutant_is_caught(tmp_path, name):
+    from test_oracle import _prefill_pins
+    old, new = PREFILL_MUTANTS[name]
+    lib = _build(tmp_path, name, old, new)
+    P, I, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+    lib.mla_oracle_prefill.argtypes = [I, I, I, P, P, P, P, P, D, P, P]
+    ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+
+    def prefill(E, qn, qr, wk, wv, scale):
+        arrs = [np.ascontiguousarray(a, dtype=np.float64) for a in (E, qn, qr, wk, wv)]
+        L, H, dh = arrs[1].shape
+        out = np.zeros((L, H, dh))
+        lse = np.zeros((L, H))
+        lib.mla_oracle_prefill(L, H, dh, *[ptr(a) for a in arrs], scale, ptr(out), ptr(lse))
+        return out, lse
+
+    assert not all(ok for _, ok in _prefill_pins(prefill)), f"pins missed mutant {name}"
