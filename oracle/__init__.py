@@ -93,7 +93,7 @@ def _load():
             lib.mla_oracle_absorb.restype = None
             lib.mla_oracle_project.argtypes = [I, I, I, P, P, P]
             lib.mla_oracle_project.restype = None
-            lib.mla_oracle_prefill.argtypes = [I, I, I, P, P, P, P, P, D, P, P]
+            lib.mla_oracle_prefill.argtypes = [I, I, I, P, P, P, P, P, D, I, P, P]
             lib.mla_oracle_prefill.restype = None
             lib.mla_oracle_default_threads.argtypes = []
             lib.mla_oracle_default_threads.restype = I
@@ -193,9 +193,10 @@ def topk_select(scores, seq_lens, k):
     return out
 
 
-def prefill(entries, q_nope, q_rope, w_uk, w_uv, scale):
+def prefill(entries, q_nope, q_rope, w_uk, w_uv, scale, kv_bf16=False):
     """Non-absorbed causal prefill of one sequence (float64 arrays): entries [L][576],
-    q_nope [L][H][dh], q_rope [L][H][64], w_uk / w_uv [H][dh][512] -> out [L][H][dh], lse [L][H]."""
+    q_nope [L][H][dh], q_rope [L][H][64], w_uk / w_uv [H][dh][512] -> out [L][H][dh], lse [L][H].
+    kv_bf16: the decompressed keys and values are rounded to bf16 (the attention's operands)."""
     e, pe = _c(entries, np.float64)
     qn, pqn = _c(q_nope, np.float64)
     qr, pqr = _c(q_rope, np.float64)
@@ -206,7 +207,7 @@ def prefill(entries, q_nope, q_rope, w_uk, w_uv, scale):
     assert wk.shape == (H, dh, D_LATENT) and wv.shape == (H, dh, D_LATENT)
     out = np.zeros((L, H, dh), np.float64)
     lse = np.zeros((L, H), np.float64)
-    _load().mla_oracle_prefill(L, H, dh, pe, pqn, pqr, pwk, pwv, float(scale),
+    _load().mla_oracle_prefill(L, H, dh, pe, pqn, pqr, pwk, pwv, float(scale), 1 if kv_bf16 else 0,
                                out.ctypes.data_as(ctypes.c_void_p), lse.ctypes.data_as(ctypes.c_void_p))
     return out, lse
 

@@ -462,11 +462,12 @@ void mla_oracle_project(int B, int H, int dh, const double *out, const double *w
  *
  * entries [L][576] (latent | RoPE key, the cache entry layout), q_nope [L][H][dh], q_rope
  * [L][H][64], w_uk and w_uv [H][dh][512]; out [L][H][dh], lse [L][H].  Plain double sums,
- * two-pass softmax per query row.
+ * two-pass softmax per query row.  kv_bf16 != 0 rounds the decompressed keys and values to
+ * bf16 (the tensors the attention reads); 0 keeps them exact.
  * ------------------------------------------------------------------------------------ */
 void mla_oracle_prefill(int L, int H, int dh, const double *entries, const double *q_nope,
                         const double *q_rope, const double *w_uk, const double *w_uv,
-                        double scale, double *out, double *lse) {
+                        double scale, int kv_bf16, double *out, double *lse) {
     double *K = (double *)malloc(sizeof(double) * (size_t)L * dh);
     double *V = (double *)malloc(sizeof(double) * (size_t)L * dh);
     double *s = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
@@ -481,8 +482,11 @@ void mla_oracle_prefill(int L, int H, int dh, const double *entries, const doubl
                     sk += wk[x] * c[x];
                     sv += wv[x] * c[x];
                 }
-                K[(int64_t)t * dh + j] = sk;
-                V[(int64_t)t * dh + j] = sv;
+                /* kv_bf16: keys and values are materialised as bf16 tensors, as the
+                 * attention that consumes them takes bf16 operands (sum rounded to binary32,
+                 * then to bf16, nearest even) */
+                K[(int64_t)t * dh + j] = kv_bf16 ? f32_to_bf16_double((float)sk) : sk;
+                V[(int64_t)t * dh + j] = kv_bf16 ? f32_to_bf16_double((float)sv) : sv;
             }
         for (int i = 0; i < L; ++i) {
             const double *qn = q_nope + ((int64_t)i * H + h) * dh;

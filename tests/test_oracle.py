@@ -234,6 +234,26 @@ def test_prefill_pins():
     assert not bad, bad
 
 
+def test_prefill_bf16_keys_values():
+    """kv_bf16 equals the exact prefill run on keys and values rounded to bf16 beforehand:
+    with W^UK, W^UV the identity on the first 128 latent columns the decompressed K, V are
+    those columns, so rounding the entries themselves to bf16 must give the same result."""
+    L, H = 7, 2
+    E, qn, qr, _, _ = _prefill_inputs(L, H, 82)
+    I = np.zeros((H, 128, 512))
+    I[:, np.arange(128), np.arange(128)] = 1.0
+    got, gl = oracle.prefill(E, qn, qr, I, I, SCALE, kv_bf16=True)
+    Eb = E.copy()
+    f = E[:, :128].astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    u = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16                        # binary32 -> bf16, nearest even
+    Eb[:, :128] = u.astype(np.uint32).view(np.float32).astype(np.float64)
+    ref, rl = oracle.prefill(Eb, qn, qr, I, I, SCALE)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(gl, rl, rtol=1e-12, atol=1e-12)
+    assert np.abs(got - oracle.prefill(E, qn, qr, I, I, SCALE)[0]).max() > 1e-6  # the rounding shows
+
+
 def test_rope_term_and_scale_matter():
     """Changing only k_R or only the scale must change the result (guards dropped terms)."""
     r = _rng(5)

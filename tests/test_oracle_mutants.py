@@ -192,7 +192,7 @@ def test_prefill_mutant_is_caught(tmp_path, name):
     old, new = PREFILL_MUTANTS[name]
     lib = _build(tmp_path, name, old, new)
     P, I, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
-    lib.mla_oracle_prefill.argtypes = [I, I, I, P, P, P, P, P, D, P, P]
+    lib.mla_oracle_prefill.argtypes = [I, I, I, P, P, P, P, P, D, I, P, P]
     ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)
 
     def prefill(E, qn, qr, wk, wv, scale):
@@ -200,7 +200,7 @@ def test_prefill_mutant_is_caught(tmp_path, name):
         L, H, dh = arrs[1].shape
         out = np.zeros((L, H, dh))
         lse = np.zeros((L, H))
-        lib.mla_oracle_prefill(L, H, dh, *[ptr(a) for a in arrs], scale, ptr(out), ptr(lse))
+        lib.mla_oracle_prefill(L, H, dh, *[ptr(a) for a in arrs], scale, 0, ptr(out), ptr(lse))
         return out, lse
 
     assert not all(ok for _, ok in _prefill_pins(prefill)), f"pins missed mutant {name}"
