@@ -420,6 +420,25 @@ def main():
     tk_ms = time_alone(lambda: ops.topk_select(tk_scores, case.seq_lens, tk_k, indices=tk_idx, stream=stream),
                        args.steps, flush, stream)
     tk_bytes = int(case.seq_lens.sum().item()) * 4 + case.B * (tk_k + 1) * 4  # scores, lengths in; indices out
+    # non-absorbed prefill of one 4096-token sequence with the workload's head count:
+    # decompression (K, V with W^UK, W^UV) + causal attention, timed together
+    pf_L = 4096
+    gpf = torch.Generator(device=dev).manual_seed(10)
+    pf_e = torch.randn(pf_L, 576, generator=gpf, device=dev).to(torch.bfloat16)
+    pf_qn = torch.randn(pf_L, case.H, 128, generator=gpf, device=dev).to(torch.bfloat16)
+    pf_qr = torch.randn(pf_L, case.H, 64, generator=gpf, device=dev).to(torch.bfloat16)
+    pf_k = torch.empty(case.H, pf_L, 128, dtype=torch.bfloat16, device=dev)
+    pf_v = torch.empty_like(pf_k)
+    pf_o = torch.empty(pf_L, case.H, 128, dtype=torch.float32, device=dev)
+    pf_l = torch.empty(pf_L, case.H, dtype=torch.float32, device=dev)
+
+    def prefill_call():
+        ops.prefill_decompress(pf_e, w_uk, w_uv, k_nope=pf_k, v=pf_v, stream=stream)
+        ops.prefill_attention(pf_qn, pf_qr, pf_e, pf_k, pf_v, case.scale, out=pf_o, lse=pf_l, stream=stream)
+
+    pf_ms = time_alone(prefill_call, args.steps, flush, stream)
+    pf_dc_flops = 2 * 2 * pf_L * 512 * 128 * case.H
+    pf_at_flops = 2 * case.H * (pf_L * (pf_L + 1) // 2) * (192 + 128)
     BH = case.B * case.H
     ab_bytes = case.H * 128 * 512 * 2 + BH * 128 * 2 + BH * 512 * 2  # W^UK, q^C in; q~ out
     pj_bytes = case.H * 128 * 512 * 2 + BH * 512 * 4 + BH * 128 * 4  # W^UV, latent out in; y out
@@ -466,6 +485,11 @@ def main():
         "topk": {"kernel": "DSA top-k selection (mla_topk_select), k = 2048 per request", "us": tk_ms * 1e3,
                  "bytes": tk_bytes, "gbs": tk_bytes / (tk_ms * 1e-3) / 1e9,
                  "frac_hbm": tk_bytes / (tk_ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
+        "prefill": {"kernel": "non-absorbed prefill (mla_prefill_decompress + mla_prefill_attention), causal",
+                    "tokens": pf_L, "heads": case.H, "us": pf_ms * 1e3,
+                    "flops": pf_dc_flops + pf_at_flops,
+                    "tflops": (pf_dc_flops + pf_at_flops) / (pf_ms * 1e-3) / 1e12,
+                    "frac_bf16": (pf_dc_flops + pf_at_flops) / (pf_ms * 1e-3) / 1e12 / pk["bf16_tflops"]},
         "clocks": clk.summary(),
         "wall_s_timed_region": t_wall,
     }

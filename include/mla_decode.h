@@ -181,6 +181,34 @@ mla_status mla_topk_select(const float *scores, int64_t row_stride, int Lmax,
                            const int32_t *seq_lens, int B, int k, int32_t *indices,
                            int32_t *device_status, void *stream);
 
+/* Non-absorbed prefill, step 1 ("MLA & DSA 推理性能优化指南" §3.1 and §1.1: the latents are
+ * decompressed before standard attention): for a sequence of L tokens whose entries
+ * [L][576] (latent c_t | RoPE key, bf16, the cache entry layout, contiguous) are given,
+ *   k_nope[h][t][j] = bf16_rne( sum_c w_uk[h][j][c] c_t[c] ),
+ *   v[h][t][j]      = bf16_rne( sum_c w_uv[h][j][c] c_t[c] ),   j < 128, c < 512,
+ * fp32 accumulation on the tensor cores.  w_uk, w_uv bf16 [H][128][512]; k_nope, v bf16
+ * [H][L][128].  Device pointers, 16-byte aligned, caller-owned; a programmatic dependent of
+ * the previous kernel on `stream`.  *device_status (optional) gets MLA_ERR_TIMEOUT if an
+ * internal wait gives up. */
+mla_status mla_prefill_decompress(const void *entries, int L, const void *w_uk, const void *w_uv,
+                                  int H, void *k_nope, void *v, int32_t *device_status,
+                                  void *stream);
+
+/* Non-absorbed prefill, step 2 ("MLA 最佳算子全景调研" §4: a FlashAttention variant with
+ * 192-wide keys and 128-wide values): causal multi-head attention of query i over keys
+ * t <= i of the same sequence,
+ *   s_t = softmax_scale * (q_nope[i][h] . k_nope[h][t] + q_rope[i][h] . k_R[t]),
+ *   out[i][h] = sum_t softmax(s)_t v[h][t]  (fp32),  lse[i][h] = ln sum_t e^{s_t},
+ * with k_R[t] = entries[t][512..576).  q_nope bf16 [L][H][128], q_rope bf16 [L][H][64],
+ * k_nope and v as mla_prefill_decompress writes them, out fp32 [L][H][128], lse fp32
+ * [L][H].  Scores and the softmax in fp32, probabilities rounded to bf16 for the
+ * probability x value product, fp32 accumulation.  softmax_scale finite and > 0.  Pointers
+ * as above; a programmatic dependent of the previous kernel on `stream`. */
+mla_status mla_prefill_attention(const void *q_nope, const void *q_rope, const void *entries,
+                                 const void *k_nope, const void *v, int L, int H,
+                                 float softmax_scale, float *out, float *lse,
+                                 int32_t *device_status, void *stream);
+
 /* Host twin of mla_decode_plan for tests and tooling: plans from a HOST array
  * seq_lens[B] (NULL with topk > 0) into a HOST buffer of mla_decode_workspace_size()
  * bytes, producing exactly the bytes the device planner writes into the plan region.

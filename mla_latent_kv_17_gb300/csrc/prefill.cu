@@ -1,0 +1,548 @@
+// Non-absorbed (MHA-mode) prefill of one sequence ("MLA & DSA 推理性能优化指南" §3.1 and §1.1:
+// the latents are decompressed into per-head keys and values, then standard causal
+// attention runs; "MLA 最佳算子全景调研" §4: a FlashAttention variant with 192-wide keys and
+// 128-wide values).  The definitions are in include/mla_decode.h (mla_prefill_decompress,
+// mla_prefill_attention).
+//
+// decompress_kernel: per (head, tile of 256 tokens) D[j][t] = sum_c W[h][j][c] c_t[c] for
+// W = W^UK and W^UV at once (two TMEM accumulators of 256 columns), K = 512 streamed in
+// 64-column chunks through a three-stage TMA ring; the results are transposed through
+// shared memory and written by TMA tile stores as K_h, V_h [H][L][128] bf16.
+//
+// attention_kernel: per (head, tile of 128 queries) a loop over the causal key tiles of 128:
+// S = Q K^T on tcgen05 (K = 128 nope + 64 RoPE) into TMEM, online softmax by four warps
+// (one query row per thread), P as bf16 in shared memory, O += P V on tcgen05 into TMEM
+// (rescaled in place when a row maximum grows).  The next key tile loads while the current
+// one is in softmax and PV; values load while the scores are computed.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "mla_decode.h"
+#include "sm103_ptx.cuh"
+
+namespace mla {
+namespace {
+
+using namespace ptx;
+
+constexpr int kDh = 128;
+constexpr long long kSpinCycles = 4000000000LL;  // about two seconds
+
+__device__ bool wait_bar_bounded(uint32_t bar, uint32_t parity, int *abort_flag) {
+    const long long t0 = (long long)clock64_now();
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 63u) {
+            if (*reinterpret_cast<volatile int *>(abort_flag)) return false;
+            if ((long long)clock64_now() - t0 > kSpinCycles) {
+                *reinterpret_cast<volatile int *>(abort_flag) = 1;
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void drain_pause() {
+    const long long t0 = (long long)clock64_now();
+    while ((long long)clock64_now() - t0 < 20000000LL) {
+    }
+}
+
+__device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int32_t x, int32_t y, int32_t z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(src), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ uint16_t bf16_bits(float f) {
+    __nv_bfloat16 v = __float2bfloat16_rn(f);
+    return *reinterpret_cast<uint16_t *>(&v);
+}
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// ------------------------------------------------------------------ decompression
+constexpr int kDcTok = 256;                       // tokens per CTA (MMA N)
+constexpr uint32_t kDcW = 128 * 128;              // 128 rows x 64 bf16 of W^UK or W^UV
+constexpr uint32_t kDcC = kDcTok * 128;           // 256 tokens x 64 bf16 of the latent
+constexpr uint32_t kDcStage = 2 * kDcW + kDcC;    // 64 KB
+constexpr int kDcStages = 3;
+constexpr uint32_t kDcBar = kDcStages * kDcStage;
+constexpr uint32_t kDcSmem = kDcBar + 128 + 1024;
+constexpr int kDcThreads = 192;                   // warps 0-3 epilogue, 4 loads, 5 MMAs
+
+__global__ void __launch_bounds__(kDcThreads, 1) decompress_kernel(const __grid_constant__ CUtensorMap tm_uk,
+                                                                   const __grid_constant__ CUtensorMap tm_uv,
+                                                                   const __grid_constant__ CUtensorMap tm_c,
+                                                                   const __grid_constant__ CUtensorMap tm_k,
+                                                                   const __grid_constant__ CUtensorMap tm_v,
+                                                                   int H, int *status) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char *gbase = smem_raw + (base - raw);
+    const uint32_t bars = base + kDcBar;  // full[3], empty[3], done
+    int *abort_flag = reinterpret_cast<int *>(gbase + kDcBar + 64);
+    volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(gbase + kDcBar + 72);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.x % H;
+    const int t0 = (blockIdx.x / H) * kDcTok;
+    auto full = [&](int s) { return bars + 8u * s; };
+    auto empty = [&](int s) { return bars + 24u + 8u * s; };
+    const uint32_t done = bars + 48u;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int s = 0; s < kDcStages; ++s) {
+                mbar_init(full(s), 1);
+                mbar_init(empty(s), 1);
+            }
+            mbar_init(done, 1);
+            *abort_flag = 0;
+            fence_mbar_init();
+        }
+        __syncwarp();
+        tmem_alloc(smem_u32(const_cast<uint32_t *>(tslot)), 512);
+        tmem_relinquish();
+    }
+    grid_dep_wait();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;  // K accumulator at column 0, V at 256
+    bool ok = true;
+    constexpr int kChunks = kDLatent / 64;
+    if (warp == 4 && lane == 0) {
+        for (int c = 0; c < kChunks && ok; ++c) {
+            const int s = c % kDcStages;
+            if (c >= kDcStages) ok = wait_bar_bounded(empty(s), ((c / kDcStages) - 1) & 1, abort_flag);
+            if (!ok) break;
+            const uint32_t st = base + s * kDcStage;
+            mbar_arrive_expect_tx(full(s), kDcStage);
+            tma_load_3d(st, &tm_uk, 64 * c, 0, h, full(s));
+            tma_load_3d(st + kDcW, &tm_uv, 64 * c, 0, h, full(s));
+            tma_load_2d(st + 2 * kDcW, &tm_c, 64 * c, t0, full(s));
+        }
+    } else if (warp == 5 && lane == 0) {
+        constexpr uint32_t idesc = idesc_bf16_major(128, kDcTok, false, false);
+        for (int c = 0; c < kChunks && ok; ++c) {
+            const int s = c % kDcStages;
+            ok = wait_bar_bounded(full(s), (c / kDcStages) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t st = base + s * kDcStage;
+            for (int k = 0; k < 4; ++k) {
+                const uint64_t bd = smem_desc_sw128(st + 2 * kDcW + k * 32u, 16u, 1024u);
+                mma_ss(tmem, smem_desc_sw128(st + k * 32u, 16u, 1024u), bd, idesc, (c | k) ? 1u : 0u);
+                mma_ss(tmem + 256u, smem_desc_sw128(st + kDcW + k * 32u, 16u, 1024u), bd, idesc, (c | k) ? 1u : 0u);
+            }
+            mma_commit(empty(s));
+        }
+        if (ok) mma_commit(done);
+    }
+    grid_dep_launch();
+    if (warp < 4) {
+        ok = wait_bar_bounded(done, 0, abort_flag);
+        tc_fence_after();
+        if (ok) {
+            // both results transposed into [256 tokens][64 bf16] boxes over the (finished)
+            // ring: K in boxes 0-1, V in boxes 2-3 (32 KB each)
+            const int j = 32 * warp + lane;
+            const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
+            for (int m = 0; m < 2; ++m) {
+                const uint32_t box = base + (2 * m + (j >> 6)) * (kDcTok * 128);
+                const int jj = j & 63;
+#pragma unroll 1
+                for (int ch = 0; ch < kDcTok / 32; ++ch) {
+                    uint32_t r[32];
+                    tmem_ld32(taddr + 256u * m + 32u * ch, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int t = 32 * ch + i;
+                        st_shared_u16(box + t * 128 + (((jj >> 3) ^ (t & 7)) << 4) + (jj & 7) * 2,
+                                      bf16_bits(__uint_as_float(r[i])));
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+        }
+    }
+    if (__syncthreads_and(ok ? 1 : 0) && threadIdx.x == 0) {
+        for (int q = 0; q < 2; ++q) {
+            tma_store_3d(&tm_k, base + q * (kDcTok * 128), 64 * q, t0, h);
+            tma_store_3d(&tm_v, base + (2 + q) * (kDcTok * 128), 64 * q, t0, h);
+        }
+        bulk_commit_group();
+        bulk_wait_group0();
+    }
+    if (!ok) {
+        if (threadIdx.x == 0 && status) record_error(status, MLA_ERR_TIMEOUT);
+        drain_pause();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------ attention
+constexpr int kAtQ = 128;                  // queries per CTA (MMA M)
+constexpr int kAtK = 128;                  // keys per tile (MMA N of the scores, K of PV)
+constexpr uint32_t kAtBox = 128 * 128;     // 128 rows x 64 bf16
+constexpr uint32_t kOffQ = 0;              // q nope (2 boxes) + q rope (1 box)
+constexpr uint32_t kOffK = 3 * kAtBox;     // k nope (2 boxes) + k rope (1 box)
+constexpr uint32_t kOffV = 6 * kAtBox;     // v (2 boxes: 128 keys x 64 value columns)
+constexpr uint32_t kOffP = 8 * kAtBox;     // p (2 boxes: 128 queries x 64 keys)
+constexpr uint32_t kAtBar = 10 * kAtBox;
+constexpr uint32_t kAtSmem = kAtBar + 128 + 1024;
+constexpr int kAtThreads = 192;            // warps 0-3 softmax, 4 loads, 5 MMAs
+constexpr uint32_t kColS = 0, kColO = 128;
+
+__global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
+    const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qr,
+    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_kr,
+    const __grid_constant__ CUtensorMap tm_v, int L, int H, float scale_log2, float *out, float *lse, int *status) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char *gbase = smem_raw + (base - raw);
+    const uint32_t bars = base + kAtBar;
+    // barriers: q_full, k_full, k_empty, v_full, v_empty(= pv done), s_full, s_free, p_full
+    const uint32_t q_full = bars, k_full = bars + 8, k_empty = bars + 16, v_full = bars + 24,
+                   pv_done = bars + 32, s_full = bars + 40, s_free = bars + 48, p_full = bars + 56;
+    int *abort_flag = reinterpret_cast<int *>(gbase + kAtBar + 64);
+    volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(gbase + kAtBar + 72);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nqt = (L + kAtQ - 1) / kAtQ;
+    const int h = blockIdx.x % H;
+    const int qt = nqt - 1 - (int)(blockIdx.x / H);  // longest (most key tiles) first
+    const int q0 = qt * kAtQ;
+    const int ntiles = qt + 1;                       // causal: key tiles 0 .. qt
+
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_init(q_full, 1);
+            mbar_init(k_full, 1);
+            mbar_init(k_empty, 1);
+            mbar_init(v_full, 1);
+            mbar_init(pv_done, 1);
+            mbar_init(s_full, 1);
+            mbar_init(s_free, 4);
+            mbar_init(p_full, 4);
+            *abort_flag = 0;
+            fence_mbar_init();
+        }
+        __syncwarp();
+        tmem_alloc(smem_u32(const_cast<uint32_t *>(tslot)), 256);
+        tmem_relinquish();
+    }
+    grid_dep_wait();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    bool ok = true;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(q_full, 3 * kAtBox);
+            tma_load_3d(base + kOffQ, &tm_qn, 0, h, q0, q_full);
+            tma_load_3d(base + kOffQ + kAtBox, &tm_qn, 64, h, q0, q_full);
+            tma_load_3d(base + kOffQ + 2 * kAtBox, &tm_qr, 0, h, q0, q_full);
+            for (int g = 0; g < ntiles && ok; ++g) {
+                const int k0 = g * kAtK;
+                if (g > 0) ok = wait_bar_bounded(k_empty, (g - 1) & 1, abort_flag);
+                if (!ok) break;
+                mbar_arrive_expect_tx(k_full, 3 * kAtBox);
+                tma_load_3d(base + kOffK, &tm_k, 0, k0, h, k_full);
+                tma_load_3d(base + kOffK + kAtBox, &tm_k, 64, k0, h, k_full);
+                tma_load_2d(base + kOffK + 2 * kAtBox, &tm_kr, kDLatent, k0, k_full);
+                if (g > 0) ok = wait_bar_bounded(pv_done, (g - 1) & 1, abort_flag);
+                if (!ok) break;
+                mbar_arrive_expect_tx(v_full, 2 * kAtBox);
+                tma_load_3d(base + kOffV, &tm_v, 0, k0, h, v_full);
+                tma_load_3d(base + kOffV + kAtBox, &tm_v, 64, k0, h, v_full);
+            }
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_major(128, kAtK, false, false);
+            constexpr uint32_t idesc_o = idesc_bf16_major(128, kDh, false, true);
+            ok = wait_bar_bounded(q_full, 0, abort_flag);
+            for (int g = 0; g < ntiles && ok; ++g) {
+                ok = wait_bar_bounded(k_full, g & 1, abort_flag) &&
+                     (g == 0 || wait_bar_bounded(s_free, (g - 1) & 1, abort_flag));
+                if (!ok) break;
+                tc_fence_after();
+                for (int k = 0; k < 12; ++k) {  // 8 steps over the 128 nope columns, 4 over RoPE
+                    const uint32_t off = (k >> 2) * kAtBox + (k & 3) * 32u;
+                    mma_ss(tmem + kColS, smem_desc_sw128(base + kOffQ + off, 16u, 1024u),
+                           smem_desc_sw128(base + kOffK + off, 16u, 1024u), idesc_s, k > 0 ? 1u : 0u);
+                }
+                mma_commit(s_full);
+                mma_commit(k_empty);
+                ok = wait_bar_bounded(p_full, g & 1, abort_flag) && wait_bar_bounded(v_full, g & 1, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                for (int k = 0; k < kAtK / 16; ++k) {
+                    // A: P rows (queries) x 16 keys; B: 16 key rows of V, 128 value columns
+                    const uint64_t ad = smem_desc_sw128(base + kOffP + (k >> 2) * kAtBox + (k & 3) * 32u, 16u, 1024u);
+                    const uint64_t bd = smem_desc_sw128(base + kOffV + k * 2048u, kAtBox, 1024u);
+                    mma_ss(tmem + kColO, ad, bd, idesc_o, (g > 0 || k > 0) ? 1u : 0u);
+                }
+                mma_commit(pv_done);
+            }
+        }
+    } else {
+        // ---------------------------------------------------------------- softmax (row i)
+        const int row = 32 * warp + lane;  // TMEM lane = query row of the tile
+        const int qi = q0 + row;
+        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        float m = -INFINITY, l = 0.f;      // running maximum (log2 units) and sum
+        for (int g = 0; g < ntiles && ok; ++g) {
+            const int k0 = g * kAtK;
+            ok = wait_bar_bounded(s_full, g & 1, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            float s[kAtK];
+#pragma unroll
+            for (int c = 0; c < kAtK / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + kColS + 32u * c, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(r[i]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free);
+            // causal mask (and keys past the sequence) on the diagonal tile
+            const int lim = min(qi, L - 1) - k0;  // keys k0 + x with x <= lim are seen
+            float mx = m;
+#pragma unroll
+            for (int x = 0; x < kAtK; ++x) {
+                s[x] = x <= lim ? s[x] * scale_log2 : -INFINITY;
+                mx = fmaxf(mx, s[x]);
+            }
+            const float alpha = (m == -INFINITY) ? 0.f : exp2f(m - mx);
+            float sum = 0.f;
+#pragma unroll
+            for (int x = 0; x < kAtK; ++x) {
+                s[x] = (mx == -INFINITY) ? 0.f : exp2f(s[x] - mx);
+                sum += s[x];
+            }
+            l = l * alpha + sum;
+            m = mx;
+            // P and O are free once the previous tile's PV has finished
+            if (g > 0) {
+                ok = wait_bar_bounded(pv_done, (g - 1) & 1, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                    for (int c = 0; c < kDh / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(tmem + lane_base + kColO + 32u * c, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tmem_st32(tmem + lane_base + kColO + 32u * c, r);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            // P row as bf16: keys 64 b2 .. 64 b2 + 63 in box b2, 16-B unit u at u ^ (row % 8)
+#pragma unroll
+            for (int u = 0; u < kAtK / 8; ++u) {
+                const uint32_t addr = base + kOffP + (u >> 3) * kAtBox + row * 128 + ((((u & 7) ^ (row & 7))) << 4);
+                st_shared_v4(addr, bf16x2_bits(s[8 * u], s[8 * u + 1]), bf16x2_bits(s[8 * u + 2], s[8 * u + 3]),
+                             bf16x2_bits(s[8 * u + 4], s[8 * u + 5]), bf16x2_bits(s[8 * u + 6], s[8 * u + 7]));
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+        }
+        if (ok) {
+            ok = wait_bar_bounded(pv_done, (ntiles - 1) & 1, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok) {
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+            for (int c = 0; c < kDh / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + kColO + 32u * c, r);
+                tmem_wait_ld();
+                if (qi < L) {
+                    float4 *dst = reinterpret_cast<float4 *>(out + ((int64_t)qi * H + h) * kDh + 32 * c);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
+                                             __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+                }
+            }
+            if (qi < L) lse[(int64_t)qi * H + h] = (m + log2f(l)) * kLn2;
+        }
+    }
+    grid_dep_launch();
+    if (!__syncthreads_and(ok ? 1 : 0)) {
+        if (threadIdx.x == 0 && status) record_error(status, MLA_ERR_TIMEOUT);
+        drain_pause();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// bf16 tensor of rank 2 or 3 (d[0] innermost; byte strides s[0..rank-2]), boxes b, 128-B
+// swizzle; elements outside the tensor read as zero and are not written by stores.
+bool tmap_bf16(CUtensorMap *m, const void *p, int rank, const uint64_t *d, const uint64_t *s, const uint32_t *b) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3], estr[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        dims[i] = d[i];
+        box[i] = b[i];
+    }
+    for (int i = 0; i + 1 < rank; ++i) strides[i] = s[i];
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(p), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool set_prefill_attrs() {
+    static bool done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (done[dev]) return true;
+    if (cudaFuncSetAttribute(decompress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDcSmem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAtSmem) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    done[dev] = true;
+    return true;
+}
+
+template <typename K, typename... Args>
+cudaError_t launch_pdl(K kernel, int grid, int threads, uint32_t smem, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" mla_status mla_prefill_decompress(const void *entries, int L, const void *w_uk, const void *w_uv, int H,
+                                             void *k_nope, void *v, int32_t *device_status, void *stream) {
+    if (!entries || !w_uk || !w_uv || !k_nope || !v || L < 1 || H < 1) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(entries) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(k_nope) || !aligned16(v))
+        return MLA_ERR_INVALID_ARG;
+    const int64_t grid = (int64_t)H * ((L + kDcTok - 1) / kDcTok);
+    if (grid > 0x7FFFFFFF) return MLA_ERR_UNSUPPORTED;
+    if (!set_prefill_attrs()) return MLA_ERR_CUDA;
+    CUtensorMap tuk, tuv, tc, tk, tv;
+    const uint64_t dw[3] = {kDLatent, kDh, (uint64_t)H}, sw[2] = {kDLatent * 2, (uint64_t)kDh * kDLatent * 2};
+    const uint32_t bw[3] = {64, 128, 1};
+    const uint64_t dc[2] = {kDEntry, (uint64_t)L}, sc[1] = {kDEntry * 2};
+    const uint32_t bc[2] = {64, kDcTok};
+    const uint64_t dkv[3] = {kDh, (uint64_t)L, (uint64_t)H}, skv[2] = {kDh * 2, (uint64_t)kDh * 2 * L};
+    const uint32_t bkv[3] = {64, kDcTok, 1};
+    if (!tmap_bf16(&tuk, w_uk, 3, dw, sw, bw) || !tmap_bf16(&tuv, w_uv, 3, dw, sw, bw) ||
+        !tmap_bf16(&tc, entries, 2, dc, sc, bc) || !tmap_bf16(&tk, k_nope, 3, dkv, skv, bkv) ||
+        !tmap_bf16(&tv, v, 3, dkv, skv, bkv))
+        return MLA_ERR_CUDA;
+    return launch_pdl(decompress_kernel, (int)grid, kDcThreads, kDcSmem, (cudaStream_t)stream, tuk, tuv, tc, tk, tv,
+                      H, (int *)device_status) == cudaSuccess
+               ? MLA_OK
+               : MLA_ERR_CUDA;
+}
+
+extern "C" mla_status mla_prefill_attention(const void *q_nope, const void *q_rope, const void *entries,
+                                            const void *k_nope, const void *v, int L, int H, float softmax_scale,
+                                            float *out, float *lse, int32_t *device_status, void *stream) {
+    if (!q_nope || !q_rope || !entries || !k_nope || !v || !out || !lse || L < 1 || H < 1)
+        return MLA_ERR_INVALID_ARG;
+    if (!(softmax_scale > 0.f) || softmax_scale == INFINITY) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(entries) || !aligned16(k_nope) || !aligned16(v) ||
+        !aligned16(out))
+        return MLA_ERR_INVALID_ARG;
+    const int64_t grid = (int64_t)H * ((L + kAtQ - 1) / kAtQ);
+    if (grid > 0x7FFFFFFF) return MLA_ERR_UNSUPPORTED;
+    if (!set_prefill_attrs()) return MLA_ERR_CUDA;
+    CUtensorMap tqn, tqr, tk, tkr, tv;
+    // q nope [L][H][128], q rope [L][H][64]: (cols, h, query); boxes of 64 columns x 128 queries
+    const uint64_t dqn[3] = {kDh, (uint64_t)H, (uint64_t)L}, sqn[2] = {kDh * 2, (uint64_t)kDh * 2 * H};
+    const uint64_t dqr[3] = {kDRope, (uint64_t)H, (uint64_t)L}, sqr[2] = {kDRope * 2, (uint64_t)kDRope * 2 * H};
+    const uint32_t bq[3] = {64, 1, kAtQ};
+    // k nope, v [H][L][128]: (cols, key, h); boxes of 64 columns x 128 keys
+    const uint64_t dkv[3] = {kDh, (uint64_t)L, (uint64_t)H}, skv[2] = {kDh * 2, (uint64_t)kDh * 2 * L};
+    const uint32_t bkv[3] = {64, kAtK, 1};
+    // RoPE keys: columns 512 .. 575 of the [L][576] entries
+    const uint64_t de[2] = {kDEntry, (uint64_t)L}, se[1] = {kDEntry * 2};
+    const uint32_t be[2] = {64, kAtK};
+    if (!tmap_bf16(&tqn, q_nope, 3, dqn, sqn, bq) || !tmap_bf16(&tqr, q_rope, 3, dqr, sqr, bq) ||
+        !tmap_bf16(&tk, k_nope, 3, dkv, skv, bkv) || !tmap_bf16(&tkr, entries, 2, de, se, be) ||
+        !tmap_bf16(&tv, v, 3, dkv, skv, bkv))
+        return MLA_ERR_CUDA;
+    const float scale_log2 = softmax_scale * kLog2e;
+    return launch_pdl(attention_kernel, (int)grid, kAtThreads, kAtSmem, (cudaStream_t)stream, tqn, tqr, tk, tkr, tv, L,
+                      H, scale_log2, out, lse, (int *)device_status) == cudaSuccess
+               ? MLA_OK
+               : MLA_ERR_CUDA;
+}

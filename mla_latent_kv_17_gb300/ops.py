@@ -57,6 +57,10 @@ def lib():
             L.mla_decode_static.restype = I
             L.mla_cache_append.argtypes = [P, I, I64, P, I, P, P, P, I, P, P]
             L.mla_cache_append.restype = I
+            L.mla_prefill_decompress.argtypes = [P, I, P, P, I, P, P, P, P]
+            L.mla_prefill_decompress.restype = I
+            L.mla_prefill_attention.argtypes = [P, P, P, P, P, I, I, F, P, P, P, P]
+            L.mla_prefill_attention.restype = I
             L.mla_topk_select.argtypes = [P, I64, I, P, I, I, P, P, P]
             L.mla_topk_select.restype = I
             L.mla_absorb_query.argtypes = [P, P, I, I, P, P, P]
@@ -211,6 +215,60 @@ def topk_select(scores, seq_lens, k: int, indices=None, device_status=None, stre
                                _ptr(device_status), _stream(stream))
     _check("mla_topk_select", st)
     return indices
+
+
+def _bf16(t, shape, name):
+    if t.dtype != torch.bfloat16 or tuple(t.shape) != tuple(shape) or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError(f"{name} must be contiguous CUDA bf16 {list(shape)}")
+
+
+def prefill_decompress(entries, w_uk, w_uv, k_nope=None, v=None, device_status=None, stream=None):
+    """Per-head keys and values of a sequence: entries bf16 [L,576] (latent | RoPE key) ->
+    k_nope, v bf16 [H,L,128] with k_nope[h,t] = w_uk[h] @ c_t and v[h,t] = w_uv[h] @ c_t."""
+    if entries.dim() != 2:
+        raise ValueError("entries must be [L,576]")
+    L = entries.shape[0]
+    H = w_uk.shape[0]
+    _bf16(entries, (L, 576), "entries")
+    _weights(w_uk, H, "w_uk")
+    _weights(w_uv, H, "w_uv")
+    if k_nope is None:
+        k_nope = torch.empty((H, L, 128), dtype=torch.bfloat16, device=entries.device)
+    if v is None:
+        v = torch.empty((H, L, 128), dtype=torch.bfloat16, device=entries.device)
+    _bf16(k_nope, (H, L, 128), "k_nope")
+    _bf16(v, (H, L, 128), "v")
+    if device_status is not None:
+        _i32(device_status, "device_status")
+    st = lib().mla_prefill_decompress(_ptr(entries), L, _ptr(w_uk), _ptr(w_uv), H, _ptr(k_nope), _ptr(v),
+                                      _ptr(device_status), _stream(stream))
+    _check("mla_prefill_decompress", st)
+    return k_nope, v
+
+
+def prefill_attention(q_nope, q_rope, entries, k_nope, v, softmax_scale: float, out=None, lse=None,
+                      device_status=None, stream=None):
+    """Causal prefill attention (non-absorbed): q_nope bf16 [L,H,128], q_rope bf16 [L,H,64],
+    entries bf16 [L,576], k_nope / v bf16 [H,L,128] -> out fp32 [L,H,128], lse fp32 [L,H]."""
+    if q_nope.dim() != 3:
+        raise ValueError("q_nope must be [L,H,128]")
+    L, H = q_nope.shape[0], q_nope.shape[1]
+    _bf16(q_nope, (L, H, 128), "q_nope")
+    _bf16(q_rope, (L, H, 64), "q_rope")
+    _bf16(entries, (L, 576), "entries")
+    _bf16(k_nope, (H, L, 128), "k_nope")
+    _bf16(v, (H, L, 128), "v")
+    if out is None:
+        out = torch.empty((L, H, 128), dtype=torch.float32, device=q_nope.device)
+    if lse is None:
+        lse = torch.empty((L, H), dtype=torch.float32, device=q_nope.device)
+    if device_status is not None:
+        _i32(device_status, "device_status")
+    st = lib().mla_prefill_attention(_ptr(q_nope), _ptr(q_rope), _ptr(entries), _ptr(k_nope), _ptr(v), L, H,
+                                     float(softmax_scale), _ptr(out), _ptr(lse), _ptr(device_status),
+                                     _stream(stream))
+    _check("mla_prefill_attention", st)
+    return out, lse
 
 
 def _weights(w, H, name):

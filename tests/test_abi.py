@@ -32,7 +32,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for must in ("mla_decode_workspace_size", "mla_decode_plan", "mla_decode", "mla_decode_sparse",
                  "mla_decode_status", "mla_status_string", "mla_decode_plan_host",
-                 "mla_cache_append", "mla_absorb_query", "mla_project_output", "mla_topk_select"):
+                 "mla_cache_append", "mla_absorb_query", "mla_project_output", "mla_topk_select",
+                 "mla_prefill_decompress", "mla_prefill_attention"):
         assert must in names
 
 
@@ -119,6 +120,13 @@ def test_absorb_project_append_reject_bad_arguments_on_host(L):
     assert L.mla_project_output(f, None, 4, 16, f, None, None) == 1
     assert L.mla_project_output(f, f, -1, 16, f, None, None) == 1
     assert L.mla_project_output(odd, f, 4, 16, f, None, None) == 1
+    assert L.mla_prefill_decompress(None, 64, f, f, 4, f, f, None, None) == 1
+    assert L.mla_prefill_decompress(f, 0, f, f, 4, f, f, None, None) == 1
+    assert L.mla_prefill_decompress(f, 64, f, odd, 4, f, f, None, None) == 1
+    assert L.mla_prefill_attention(f, f, None, f, f, 64, 4, ctypes.c_float(0.07), f, f, None, None) == 1
+    assert L.mla_prefill_attention(f, f, f, f, f, 0, 4, ctypes.c_float(0.07), f, f, None, None) == 1
+    assert L.mla_prefill_attention(f, f, f, f, f, 64, 4, ctypes.c_float(0.0), f, f, None, None) == 1
+    assert L.mla_prefill_attention(f, odd, f, f, f, 64, 4, ctypes.c_float(0.07), f, f, None, None) == 1
     assert L.mla_topk_select(None, 64, 64, f, 2, 8, f, None, None) == 1
     assert L.mla_topk_select(f, 62, 62, f, 2, 8, f, None, None) == 1     # stride not a multiple of 4
     assert L.mla_topk_select(f, 64, 65, f, 2, 8, f, None, None) == 1     # stride < Lmax

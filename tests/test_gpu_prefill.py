@@ -1,0 +1,86 @@
+"""GPU parity of the non-absorbed prefill (through the C ABI) against the CPU oracle:
+decompressed keys and values elementwise (|x - ref| <= 1e-2 + 1e-2 |ref|), then the causal
+attention's out (same bound) and lse (1e-3) against the oracle's prefill with keys and
+values rounded to bf16 (the tensors the attention reads), over one query, ragged tiles,
+several key tiles, and the bench's 4096-token size on sampled heads."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mla_latent_kv_17_gb300 import inputs, ops
+
+pytestmark = pytest.mark.gpu
+
+SCALE = inputs.SOFTMAX_SCALE
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from mla_latent_kv_17_gb300 import build
+    build.build()
+    ops.lib()
+
+
+def _f64(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def _close(got, ref, what, atol=1e-2, rtol=1e-2):
+    err = np.abs(got - ref)
+    bad = ~(err <= atol + rtol * np.abs(ref))
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: mismatch at {i}: got {got[i]} ref {ref[i]} ({bad.sum()} of {bad.size})")
+
+
+def _inputs(L, H, seed):
+    g = torch.Generator().manual_seed(seed)
+    entries = torch.randn(L, 576, generator=g).to(torch.bfloat16)
+    q_nope = torch.randn(L, H, 128, generator=g).to(torch.bfloat16)
+    q_rope = torch.randn(L, H, 64, generator=g).to(torch.bfloat16)
+    _, w_uk, w_uv, _ = inputs.projection_inputs(1, H, seed=seed + 1)
+    return entries, q_nope, q_rope, w_uk, w_uv
+
+
+@pytest.mark.parametrize("L,H", [(1, 4), (300, 3), (1024, 8)])
+def test_decompress_matches_oracle(L, H):
+    entries, _, _, w_uk, w_uv = _inputs(L, H, 90 + L)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k, v = ops.prefill_decompress(entries.cuda(), w_uk.cuda(), w_uv.cuda(), device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    lat = np.broadcast_to(_f64(entries)[:, None, :512], (L, H, 512))
+    for name, got, w in (("k", k, w_uk), ("v", v, w_uv)):
+        ref = oracle.project(lat, _f64(w)).transpose(1, 0, 2)  # [H, L, 128]
+        _close(_f64(got), ref, f"decompress {name} L={L} H={H}")
+
+
+@pytest.mark.parametrize("L,H", [(1, 2), (129, 3), (300, 2), (700, 4)])
+def test_prefill_attention_matches_oracle(L, H):
+    entries, q_nope, q_rope, w_uk, w_uv = _inputs(L, H, 100 + L)
+    ref_out, ref_lse = oracle.prefill(_f64(entries), _f64(q_nope), _f64(q_rope), _f64(w_uk), _f64(w_uv), SCALE,
+                                      kv_bf16=True)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    e = entries.cuda()
+    k, v = ops.prefill_decompress(e, w_uk.cuda(), w_uv.cuda(), device_status=status)
+    out, lse = ops.prefill_attention(q_nope.cuda(), q_rope.cuda(), e, k, v, SCALE, device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    _close(_f64(out), ref_out, f"prefill out L={L} H={H}")
+    _close(_f64(lse), ref_lse, f"prefill lse L={L} H={H}", atol=1e-3, rtol=0.0)
+
+
+def test_prefill_bench_size_sampled_heads():
+    # the 4096-token, 128-head prefill the bench times; the oracle checks two heads
+    L, H = 4096, 128
+    entries, q_nope, q_rope, w_uk, w_uv = _inputs(L, H, 110)
+    e = entries.cuda()
+    k, v = ops.prefill_decompress(e, w_uk.cuda(), w_uv.cuda())
+    out, lse = ops.prefill_attention(q_nope.cuda(), q_rope.cuda(), e, k, v, SCALE)
+    torch.cuda.synchronize()
+    hs = [5, 127]
+    ref_out, ref_lse = oracle.prefill(_f64(entries), _f64(q_nope[:, hs]), _f64(q_rope[:, hs]), _f64(w_uk[hs]),
+                                      _f64(w_uv[hs]), SCALE, kv_bf16=True)
+    _close(_f64(out[:, hs]), ref_out, "prefill out, sampled heads")
+    _close(_f64(lse[:, hs]), ref_lse, "prefill lse, sampled heads", atol=1e-3, rtol=0.0)
