@@ -437,6 +437,8 @@ def main():
         ops.prefill_attention(pf_qn, pf_qr, pf_e, pf_k, pf_v, case.scale, out=pf_o, lse=pf_l, stream=stream)
 
     pf_ms = time_alone(prefill_call, args.steps, flush, stream)
+    pf_dc_ms = time_alone(lambda: ops.prefill_decompress(pf_e, w_uk, w_uv, k_nope=pf_k, v=pf_v, stream=stream),
+                          args.steps, flush, stream)
     pf_dc_flops = 2 * 2 * pf_L * 512 * 128 * case.H
     pf_at_flops = 2 * case.H * (pf_L * (pf_L + 1) // 2) * (192 + 128)
     BH = case.B * case.H
@@ -486,7 +488,8 @@ def main():
                  "bytes": tk_bytes, "gbs": tk_bytes / (tk_ms * 1e-3) / 1e9,
                  "frac_hbm": tk_bytes / (tk_ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
         "prefill": {"kernel": "non-absorbed prefill (mla_prefill_decompress + mla_prefill_attention), causal",
-                    "tokens": pf_L, "heads": case.H, "us": pf_ms * 1e3,
+                    "tokens": pf_L, "heads": case.H, "us": pf_ms * 1e3, "decompress_us": pf_dc_ms * 1e3,
+                    "decompress_tflops": pf_dc_flops / (pf_dc_ms * 1e-3) / 1e12,
                     "flops": pf_dc_flops + pf_at_flops,
                     "tflops": (pf_dc_flops + pf_at_flops) / (pf_ms * 1e-3) / 1e12,
                     "frac_bf16": (pf_dc_flops + pf_at_flops) / (pf_ms * 1e-3) / 1e12 / pk["bf16_tflops"]},

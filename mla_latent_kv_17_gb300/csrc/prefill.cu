@@ -12,8 +12,9 @@
 // attention_kernel: per (head, tile of 128 queries) a loop over the causal key tiles of 128:
 // S = Q K^T on tcgen05 (K = 128 nope + 64 RoPE) into TMEM, online softmax by four warps
 // (one query row per thread), P as bf16 in shared memory, O += P V on tcgen05 into TMEM
-// (rescaled in place when a row maximum grows).  The next key tile loads while the current
-// one is in softmax and PV; values load while the scores are computed.
+// (rescaled in place when a row maximum grows).  Keys (shared memory) and scores (TMEM) are
+// double-buffered, so the next tile's S = Q K^T runs under this tile's softmax; one warp
+// loads keys, another values (once the previous PV is done).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -205,13 +206,13 @@ constexpr int kAtQ = 128;                  // queries per CTA (MMA M)
 constexpr int kAtK = 128;                  // keys per tile (MMA N of the scores, K of PV)
 constexpr uint32_t kAtBox = 128 * 128;     // 128 rows x 64 bf16
 constexpr uint32_t kOffQ = 0;              // q nope (2 boxes) + q rope (1 box)
-constexpr uint32_t kOffK = 3 * kAtBox;     // k nope (2 boxes) + k rope (1 box)
-constexpr uint32_t kOffV = 6 * kAtBox;     // v (2 boxes: 128 keys x 64 value columns)
-constexpr uint32_t kOffP = 8 * kAtBox;     // p (2 boxes: 128 queries x 64 keys)
-constexpr uint32_t kAtBar = 10 * kAtBox;
-constexpr uint32_t kAtSmem = kAtBar + 128 + 1024;
-constexpr int kAtThreads = 192;            // warps 0-3 softmax, 4 loads, 5 MMAs
-constexpr uint32_t kColS = 0, kColO = 128;
+constexpr uint32_t kOffK = 3 * kAtBox;     // two key buffers: k nope (2 boxes) + k rope (1 box)
+constexpr uint32_t kOffV = 9 * kAtBox;     // v (2 boxes: 128 keys x 64 value columns)
+constexpr uint32_t kOffP = 11 * kAtBox;    // p (2 boxes: 128 queries x 64 keys)
+constexpr uint32_t kAtBar = 13 * kAtBox;
+constexpr uint32_t kAtSmem = kAtBar + 256 + 1024;
+constexpr int kAtThreads = 224;            // warps 0-3 softmax, 4 query/key loads, 5 MMAs, 6 value loads
+constexpr uint32_t kColS = 0, kColO = 256;  // S double-buffered at columns 0 and 128
 
 __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
     const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qr,
@@ -222,11 +223,15 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char *gbase = smem_raw + (base - raw);
     const uint32_t bars = base + kAtBar;
-    // barriers: q_full, k_full, k_empty, v_full, v_empty(= pv done), s_full, s_free, p_full
-    const uint32_t q_full = bars, k_full = bars + 8, k_empty = bars + 16, v_full = bars + 24,
-                   pv_done = bars + 32, s_full = bars + 40, s_free = bars + 48, p_full = bars + 56;
-    int *abort_flag = reinterpret_cast<int *>(gbase + kAtBar + 64);
-    volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(gbase + kAtBar + 72);
+    // barriers: q_full, v_full, pv_done (also frees V, P and O), p_full, and per key buffer
+    // b: k_full[b], k_empty[b], per score buffer b: s_full[b], s_free[b]
+    const uint32_t q_full = bars, v_full = bars + 8, pv_done = bars + 16, p_full = bars + 24;
+    auto k_full = [&](int b) { return bars + 32u + 8u * b; };
+    auto k_empty = [&](int b) { return bars + 48u + 8u * b; };
+    auto s_full = [&](int b) { return bars + 64u + 8u * b; };
+    auto s_free = [&](int b) { return bars + 80u + 8u * b; };
+    int *abort_flag = reinterpret_cast<int *>(gbase + kAtBar + 128);
+    volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(gbase + kAtBar + 136);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nqt = (L + kAtQ - 1) / kAtQ;
     const int h = blockIdx.x % H;
@@ -237,18 +242,20 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
     if (warp == 0) {
         if (lane == 0) {
             mbar_init(q_full, 1);
-            mbar_init(k_full, 1);
-            mbar_init(k_empty, 1);
             mbar_init(v_full, 1);
             mbar_init(pv_done, 1);
-            mbar_init(s_full, 1);
-            mbar_init(s_free, 4);
             mbar_init(p_full, 4);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(k_full(b), 1);
+                mbar_init(k_empty(b), 1);
+                mbar_init(s_full(b), 1);
+                mbar_init(s_free(b), 4);
+            }
             *abort_flag = 0;
             fence_mbar_init();
         }
         __syncwarp();
-        tmem_alloc(smem_u32(const_cast<uint32_t *>(tslot)), 256);
+        tmem_alloc(smem_u32(const_cast<uint32_t *>(tslot)), 512);
         tmem_relinquish();
     }
     grid_dep_wait();
@@ -259,43 +266,62 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
     bool ok = true;
 
     if (warp == 4) {
+        // queries once, then the keys of tile g into buffer g % 2 once QK(g - 2) has read it
         if (lane == 0) {
             mbar_arrive_expect_tx(q_full, 3 * kAtBox);
             tma_load_3d(base + kOffQ, &tm_qn, 0, h, q0, q_full);
             tma_load_3d(base + kOffQ + kAtBox, &tm_qn, 64, h, q0, q_full);
             tma_load_3d(base + kOffQ + 2 * kAtBox, &tm_qr, 0, h, q0, q_full);
             for (int g = 0; g < ntiles && ok; ++g) {
-                const int k0 = g * kAtK;
-                if (g > 0) ok = wait_bar_bounded(k_empty, (g - 1) & 1, abort_flag);
+                const int k0 = g * kAtK, kb = g & 1;
+                if (g >= 2) ok = wait_bar_bounded(k_empty(kb), ((g >> 1) - 1) & 1, abort_flag);
                 if (!ok) break;
-                mbar_arrive_expect_tx(k_full, 3 * kAtBox);
-                tma_load_3d(base + kOffK, &tm_k, 0, k0, h, k_full);
-                tma_load_3d(base + kOffK + kAtBox, &tm_k, 64, k0, h, k_full);
-                tma_load_2d(base + kOffK + 2 * kAtBox, &tm_kr, kDLatent, k0, k_full);
+                const uint32_t kd = base + kOffK + kb * 3 * kAtBox;
+                mbar_arrive_expect_tx(k_full(kb), 3 * kAtBox);
+                tma_load_3d(kd, &tm_k, 0, k0, h, k_full(kb));
+                tma_load_3d(kd + kAtBox, &tm_k, 64, k0, h, k_full(kb));
+                tma_load_2d(kd + 2 * kAtBox, &tm_kr, kDLatent, k0, k_full(kb));
+            }
+        }
+    } else if (warp == 6) {
+        // the values of tile g once PV(g - 1) is done
+        if (lane == 0) {
+            for (int g = 0; g < ntiles && ok; ++g) {
                 if (g > 0) ok = wait_bar_bounded(pv_done, (g - 1) & 1, abort_flag);
                 if (!ok) break;
                 mbar_arrive_expect_tx(v_full, 2 * kAtBox);
-                tma_load_3d(base + kOffV, &tm_v, 0, k0, h, v_full);
-                tma_load_3d(base + kOffV + kAtBox, &tm_v, 64, k0, h, v_full);
+                tma_load_3d(base + kOffV, &tm_v, 0, g * kAtK, h, v_full);
+                tma_load_3d(base + kOffV + kAtBox, &tm_v, 64, g * kAtK, h, v_full);
             }
         }
     } else if (warp == 5) {
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_major(128, kAtK, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_major(128, kDh, false, true);
-            ok = wait_bar_bounded(q_full, 0, abort_flag);
-            for (int g = 0; g < ntiles && ok; ++g) {
-                ok = wait_bar_bounded(k_full, g & 1, abort_flag) &&
-                     (g == 0 || wait_bar_bounded(s_free, (g - 1) & 1, abort_flag));
-                if (!ok) break;
+            // S(g) into buffer g % 2: 8 steps over the 128 nope columns, 4 over RoPE
+            // (key buffer and score buffer are both g % 2)
+            auto qk = [&](int g) -> bool {
+                const int b = g & 1;
+                if (!wait_bar_bounded(k_full(b), (g >> 1) & 1, abort_flag)) return false;
+                if (g >= 2 && !wait_bar_bounded(s_free(b), ((g >> 1) - 1) & 1, abort_flag)) return false;
                 tc_fence_after();
-                for (int k = 0; k < 12; ++k) {  // 8 steps over the 128 nope columns, 4 over RoPE
+                const uint32_t kd = base + kOffK + b * 3 * kAtBox;
+                for (int k = 0; k < 12; ++k) {
                     const uint32_t off = (k >> 2) * kAtBox + (k & 3) * 32u;
-                    mma_ss(tmem + kColS, smem_desc_sw128(base + kOffQ + off, 16u, 1024u),
-                           smem_desc_sw128(base + kOffK + off, 16u, 1024u), idesc_s, k > 0 ? 1u : 0u);
+                    mma_ss(tmem + kColS + 128u * b, smem_desc_sw128(base + kOffQ + off, 16u, 1024u),
+                           smem_desc_sw128(kd + off, 16u, 1024u), idesc_s, k > 0 ? 1u : 0u);
                 }
-                mma_commit(s_full);
-                mma_commit(k_empty);
+                mma_commit(s_full(b));
+                mma_commit(k_empty(b));
+                return true;
+            };
+            ok = wait_bar_bounded(q_full, 0, abort_flag) && qk(0);
+            for (int g = 0; g < ntiles && ok; ++g) {
+                // the next tile's scores go ahead of this tile's PV, under this tile's softmax
+                if (g + 1 < ntiles && !qk(g + 1)) {
+                    ok = false;
+                    break;
+                }
                 ok = wait_bar_bounded(p_full, g & 1, abort_flag) && wait_bar_bounded(v_full, g & 1, abort_flag);
                 if (!ok) break;
                 tc_fence_after();
@@ -316,7 +342,8 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
         float m = -INFINITY, l = 0.f;      // running maximum (log2 units) and sum
         for (int g = 0; g < ntiles && ok; ++g) {
             const int k0 = g * kAtK;
-            ok = wait_bar_bounded(s_full, g & 1, abort_flag);
+            const int sb = g & 1;
+            ok = wait_bar_bounded(s_full(sb), (g >> 1) & 1, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
@@ -324,14 +351,14 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
 #pragma unroll
             for (int c = 0; c < kAtK / 32; ++c) {
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_base + kColS + 32u * c, r);
+                tmem_ld32(tmem + lane_base + kColS + 128u * sb + 32u * c, r);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(r[i]);
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(s_free);
+            if (lane == 0) mbar_arrive(s_free(sb));
             // causal mask (and keys past the sequence) on the diagonal tile
             const int lim = min(qi, L - 1) - k0;  // keys k0 + x with x <= lim are seen
             float mx = m;
@@ -340,11 +367,11 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
                 s[x] = x <= lim ? s[x] * scale_log2 : -INFINITY;
                 mx = fmaxf(mx, s[x]);
             }
-            const float alpha = (m == -INFINITY) ? 0.f : exp2f(m - mx);
+            const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - mx);
             float sum = 0.f;
 #pragma unroll
             for (int x = 0; x < kAtK; ++x) {
-                s[x] = (mx == -INFINITY) ? 0.f : exp2f(s[x] - mx);
+                s[x] = ex2_approx(s[x] - mx);  // mx is finite: key 0 of the tile is always seen
                 sum += s[x];
             }
             l = l * alpha + sum;
@@ -412,7 +439,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, 512);
     }
 }
 
