@@ -10,11 +10,12 @@
 // shared memory and written by TMA tile stores as K_h, V_h [H][L][128] bf16.
 //
 // attention_kernel: per (head, tile of 128 queries) a loop over the causal key tiles of 128:
-// S = Q K^T on tcgen05 (K = 128 nope + 64 RoPE) into TMEM, online softmax by four warps
-// (one query row per thread), P as bf16 in shared memory, O += P V on tcgen05 into TMEM
-// (rescaled in place when a row maximum grows).  Keys (shared memory) and scores (TMEM) are
-// double-buffered, so the next tile's S = Q K^T runs under this tile's softmax; one warp
-// loads keys, another values (once the previous PV is done).
+// S = Q K^T on tcgen05 (K = 128 nope + 64 RoPE) into TMEM, online softmax by eight warps (two
+// threads per query row, 64 keys each; the halves exchange their maxima through shared
+// memory), P as bf16 in TMEM, O += P V on tcgen05 into TMEM (rescaled in place only when a
+// row's maximum exceeds its reference by 2^8).  Keys and values (shared memory) and scores
+// (TMEM) are double-buffered, so the next tile's S = Q K^T runs under this tile's softmax
+// and its values load under this tile's PV.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -61,9 +62,6 @@ __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bul
 __device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-}
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 __device__ __forceinline__ uint16_t bf16_bits(float f) {
     __nv_bfloat16 v = __float2bfloat16_rn(f);
@@ -207,12 +205,13 @@ constexpr int kAtK = 128;                  // keys per tile (MMA N of the scores
 constexpr uint32_t kAtBox = 128 * 128;     // 128 rows x 64 bf16
 constexpr uint32_t kOffQ = 0;              // q nope (2 boxes) + q rope (1 box)
 constexpr uint32_t kOffK = 3 * kAtBox;     // two key buffers: k nope (2 boxes) + k rope (1 box)
-constexpr uint32_t kOffV = 9 * kAtBox;     // v (2 boxes: 128 keys x 64 value columns)
-constexpr uint32_t kOffP = 11 * kAtBox;    // p (2 boxes: 128 queries x 64 keys)
+constexpr uint32_t kOffV = 9 * kAtBox;     // two value buffers (2 boxes each: 128 keys x 64 value columns)
 constexpr uint32_t kAtBar = 13 * kAtBox;
 constexpr uint32_t kAtSmem = kAtBar + 256 + 1024;
-constexpr int kAtThreads = 224;            // warps 0-3 softmax, 4 query/key loads, 5 MMAs, 6 value loads
-constexpr uint32_t kColS = 0, kColO = 256;  // S double-buffered at columns 0 and 128
+constexpr int kAtThreads = 352;            // warps 0-7 softmax, 8 query/key loads, 9 MMAs, 10 value loads
+constexpr float kRescaleLog2 = 8.0f;       // a row's reference maximum moves only when exceeded by 2^8
+// TMEM: S double-buffered at columns 0 and 128, O at 256, P (bf16 pairs, the A operand of PV) at 384
+constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
 
 __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
     const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qr,
@@ -223,15 +222,22 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char *gbase = smem_raw + (base - raw);
     const uint32_t bars = base + kAtBar;
-    // barriers: q_full, v_full, pv_done (also frees V, P and O), p_full, and per key buffer
-    // b: k_full[b], k_empty[b], per score buffer b: s_full[b], s_free[b]
-    const uint32_t q_full = bars, v_full = bars + 8, pv_done = bars + 16, p_full = bars + 24;
+    // barriers: q_full, pv_done (frees P and O), p_full, l_done, and per buffer b (tile g uses
+    // b = g % 2): k_full, k_empty, v_full, v_empty, s_full, s_free, red_full
+    const uint32_t q_full = bars, pv_done = bars + 8, p_full = bars + 16, l_done = bars + 24;
     auto k_full = [&](int b) { return bars + 32u + 8u * b; };
     auto k_empty = [&](int b) { return bars + 48u + 8u * b; };
     auto s_full = [&](int b) { return bars + 64u + 8u * b; };
     auto s_free = [&](int b) { return bars + 80u + 8u * b; };
+    auto red_full = [&](int b) { return bars + 96u + 8u * b; };
+    auto v_full = [&](int b) { return bars + 112u + 8u * b; };
+    auto v_empty = [&](int b) { return bars + 160u + 8u * b; };
     int *abort_flag = reinterpret_cast<int *>(gbase + kAtBar + 128);
     volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(gbase + kAtBar + 136);
+    // (v_empty sits past the flag and the TMEM address: bars + 160, + 168)
+    // the two halves of a row exchange their partial maxima (per score buffer) and sums
+    __shared__ float red[2][2][kAtQ];
+    __shared__ float lsum[2][kAtQ];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nqt = (L + kAtQ - 1) / kAtQ;
     const int h = blockIdx.x % H;
@@ -242,14 +248,17 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
     if (warp == 0) {
         if (lane == 0) {
             mbar_init(q_full, 1);
-            mbar_init(v_full, 1);
             mbar_init(pv_done, 1);
-            mbar_init(p_full, 4);
+            mbar_init(p_full, 8);
+            mbar_init(l_done, 8);
             for (int b = 0; b < 2; ++b) {
                 mbar_init(k_full(b), 1);
                 mbar_init(k_empty(b), 1);
                 mbar_init(s_full(b), 1);
-                mbar_init(s_free(b), 4);
+                mbar_init(s_free(b), 8);
+                mbar_init(red_full(b), 8);
+                mbar_init(v_full(b), 1);
+                mbar_init(v_empty(b), 1);
             }
             *abort_flag = 0;
             fence_mbar_init();
@@ -265,7 +274,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
     const uint32_t tmem = *tslot;
     bool ok = true;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // queries once, then the keys of tile g into buffer g % 2 once QK(g - 2) has read it
         if (lane == 0) {
             mbar_arrive_expect_tx(q_full, 3 * kAtBox);
@@ -283,18 +292,20 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
                 tma_load_2d(kd + 2 * kAtBox, &tm_kr, kDLatent, k0, k_full(kb));
             }
         }
-    } else if (warp == 6) {
-        // the values of tile g once PV(g - 1) is done
+    } else if (warp == 10) {
+        // the values of tile g into buffer g % 2 once PV(g - 2) has read it
         if (lane == 0) {
             for (int g = 0; g < ntiles && ok; ++g) {
-                if (g > 0) ok = wait_bar_bounded(pv_done, (g - 1) & 1, abort_flag);
+                const int vb = g & 1;
+                if (g >= 2) ok = wait_bar_bounded(v_empty(vb), ((g >> 1) - 1) & 1, abort_flag);
                 if (!ok) break;
-                mbar_arrive_expect_tx(v_full, 2 * kAtBox);
-                tma_load_3d(base + kOffV, &tm_v, 0, g * kAtK, h, v_full);
-                tma_load_3d(base + kOffV + kAtBox, &tm_v, 64, g * kAtK, h, v_full);
+                const uint32_t vd = base + kOffV + vb * 2 * kAtBox;
+                mbar_arrive_expect_tx(v_full(vb), 2 * kAtBox);
+                tma_load_3d(vd, &tm_v, 0, g * kAtK, h, v_full(vb));
+                tma_load_3d(vd + kAtBox, &tm_v, 64, g * kAtK, h, v_full(vb));
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_major(128, kAtK, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_major(128, kDh, false, true);
@@ -322,24 +333,29 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
                     ok = false;
                     break;
                 }
-                ok = wait_bar_bounded(p_full, g & 1, abort_flag) && wait_bar_bounded(v_full, g & 1, abort_flag);
+                const int vb = g & 1;
+                ok = wait_bar_bounded(p_full, g & 1, abort_flag) &&
+                     wait_bar_bounded(v_full(vb), (g >> 1) & 1, abort_flag);
                 if (!ok) break;
                 tc_fence_after();
+                const uint32_t vd = base + kOffV + vb * 2 * kAtBox;
                 for (int k = 0; k < kAtK / 16; ++k) {
-                    // A: P rows (queries) x 16 keys; B: 16 key rows of V, 128 value columns
-                    const uint64_t ad = smem_desc_sw128(base + kOffP + (k >> 2) * kAtBox + (k & 3) * 32u, 16u, 1024u);
-                    const uint64_t bd = smem_desc_sw128(base + kOffV + k * 2048u, kAtBox, 1024u);
-                    mma_ss(tmem + kColO, ad, bd, idesc_o, (g > 0 || k > 0) ? 1u : 0u);
+                    // A: P in TMEM, 16 keys = 8 columns of bf16 pairs; B: 16 key rows of V
+                    const uint64_t bd = smem_desc_sw128(vd + k * 2048u, kAtBox, 1024u);
+                    mma_ts(tmem + kColO, tmem + kColP + 8u * k, bd, idesc_o, (g > 0 || k > 0) ? 1u : 0u);
                 }
+                mma_commit(v_empty(vb));
                 mma_commit(pv_done);
             }
         }
     } else {
-        // ---------------------------------------------------------------- softmax (row i)
-        const int row = 32 * warp + lane;  // TMEM lane = query row of the tile
+        // ---------------------------------------------------------------- softmax
+        // warp w: query rows 32 (w % 4) .. (its TMEM lanes), key / value columns 64 (w / 4) ..
+        const int quad = warp & 3, hf = warp >> 2;
+        const int row = 32 * quad + lane;
         const int qi = q0 + row;
-        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-        float m = -INFINITY, l = 0.f;      // running maximum (log2 units) and sum
+        const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
+        float m = -INFINITY, l = 0.f;  // reference maximum (log2 units, shared by both halves), partial sum
         for (int g = 0; g < ntiles && ok; ++g) {
             const int k0 = g * kAtK;
             const int sb = g & 1;
@@ -347,11 +363,11 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            float s[kAtK];
+            float s[64];
 #pragma unroll
-            for (int c = 0; c < kAtK / 32; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_base + kColS + 128u * sb + 32u * c, r);
+                tmem_ld32(tmem + lane_base + kColS + 128u * sb + 64u * hf + 32u * c, r);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(r[i]);
@@ -360,22 +376,32 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free(sb));
             // causal mask (and keys past the sequence) on the diagonal tile
-            const int lim = min(qi, L - 1) - k0;  // keys k0 + x with x <= lim are seen
-            float mx = m;
+            const int lim = min(qi, L - 1) - k0 - 64 * hf;  // columns x <= lim are seen
+            float pm = m;
 #pragma unroll
-            for (int x = 0; x < kAtK; ++x) {
+            for (int x = 0; x < 64; ++x) {
                 s[x] = x <= lim ? s[x] * scale_log2 : -INFINITY;
-                mx = fmaxf(mx, s[x]);
+                pm = fmaxf(pm, s[x]);
             }
-            const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - mx);
+            red[sb][hf][row] = pm;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(red_full(sb));
+            ok = wait_bar_bounded(red_full(sb), (g >> 1) & 1, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            const float mx = fmaxf(red[sb][0][row], red[sb][1][row]);  // finite: key 0 is seen
+            // the reference maximum moves only when the row maximum exceeds it by 2^8, so most
+            // tiles keep it and leave O alone (probabilities stay <= 2^8)
+            const float mref = (m == -INFINITY || mx > m + kRescaleLog2) ? mx : m;
+            const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - mref);
             float sum = 0.f;
 #pragma unroll
-            for (int x = 0; x < kAtK; ++x) {
-                s[x] = ex2_approx(s[x] - mx);  // mx is finite: key 0 of the tile is always seen
+            for (int x = 0; x < 64; ++x) {
+                s[x] = ex2_approx(s[x] - mref);
                 sum += s[x];
             }
             l = l * alpha + sum;
-            m = mx;
+            m = mref;
             // P and O are free once the previous tile's PV has finished
             if (g > 0) {
                 ok = wait_bar_bounded(pv_done, (g - 1) & 1, abort_flag);
@@ -384,50 +410,55 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
                 tc_fence_after();
                 if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-                    for (int c = 0; c < kDh / 32; ++c) {
+                    for (int c = 0; c < 2; ++c) {
                         uint32_t r[32];
-                        tmem_ld32(tmem + lane_base + kColO + 32u * c, r);
+                        tmem_ld32(tmem + lane_base + kColO + 64u * hf + 32u * c, r);
                         tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(tmem + lane_base + kColO + 32u * c, r);
+                        tmem_st32(tmem + lane_base + kColO + 64u * hf + 32u * c, r);
                     }
                     tmem_wait_st();
                 }
             }
-            // P row as bf16: keys 64 b2 .. 64 b2 + 63 in box b2, 16-B unit u at u ^ (row % 8)
+            // this half of the P row as bf16 pairs (lower key in the low half) into TMEM columns
+            // kColP + 32 hf ..: the A operand of PV
+            {
+                uint32_t pv[32];
 #pragma unroll
-            for (int u = 0; u < kAtK / 8; ++u) {
-                const uint32_t addr = base + kOffP + (u >> 3) * kAtBox + row * 128 + ((((u & 7) ^ (row & 7))) << 4);
-                st_shared_v4(addr, bf16x2_bits(s[8 * u], s[8 * u + 1]), bf16x2_bits(s[8 * u + 2], s[8 * u + 3]),
-                             bf16x2_bits(s[8 * u + 4], s[8 * u + 5]), bf16x2_bits(s[8 * u + 6], s[8 * u + 7]));
+                for (int c = 0; c < 32; ++c) pv[c] = bf16x2_bits(s[2 * c], s[2 * c + 1]);
+                tmem_st32(tmem + lane_base + kColP + 32u * hf, pv);
+                tmem_wait_st();
             }
-            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
         }
         if (ok) {
-            ok = wait_bar_bounded(pv_done, (ntiles - 1) & 1, abort_flag);
+            lsum[hf][row] = l;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(l_done);
+            ok = wait_bar_bounded(l_done, 0, abort_flag) && wait_bar_bounded(pv_done, (ntiles - 1) & 1, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
         }
         if (ok) {
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float lt = lsum[0][row] + lsum[1][row];
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
 #pragma unroll 1
-            for (int c = 0; c < kDh / 32; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_base + kColO + 32u * c, r);
+                tmem_ld32(tmem + lane_base + kColO + 64u * hf + 32u * c, r);
                 tmem_wait_ld();
                 if (qi < L) {
-                    float4 *dst = reinterpret_cast<float4 *>(out + ((int64_t)qi * H + h) * kDh + 32 * c);
+                    float4 *dst = reinterpret_cast<float4 *>(out + ((int64_t)qi * H + h) * kDh + 64 * hf + 32 * c);
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
                                              __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
                 }
             }
-            if (qi < L) lse[(int64_t)qi * H + h] = (m + log2f(l)) * kLn2;
+            if (qi < L && hf == 0) lse[(int64_t)qi * H + h] = (m + log2f(lt)) * kLn2;
         }
     }
     grid_dep_launch();
