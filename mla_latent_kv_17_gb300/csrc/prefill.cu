@@ -240,8 +240,10 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
     __shared__ float lsum[2][kAtQ];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nqt = (L + kAtQ - 1) / kAtQ;
-    const int h = blockIdx.x % H;
-    const int qt = nqt - 1 - (int)(blockIdx.x / H);  // longest (most key tiles) first
+    // head-major order: the CTAs resident at once share a few heads' keys and values (2 MB
+    // a head at 4,096 tokens), which then stay in L2; within a head the longest rows first
+    const int h = (int)(blockIdx.x / nqt);
+    const int qt = nqt - 1 - (int)(blockIdx.x % nqt);
     const int q0 = qt * kAtQ;
     const int ntiles = qt + 1;                       // causal: key tiles 0 .. qt
 
