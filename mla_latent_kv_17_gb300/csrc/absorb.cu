@@ -9,7 +9,9 @@
 //   project: D[j][b] = sum_c W^UV[h][j][c] out[b][h][c]    M = d_h = 128, K = 512
 // so that one TMEM lane holds one output channel of every request in the tile.  The
 // projection's warps store y straight from TMEM (32 consecutive channels of one request per
-// store); the absorption transposes q~ through shared memory and stores it by the TMA.
+// store); the absorption transposes q~ through shared memory and stores it by the TMA.  The
+// projection streams K in 64-column chunks (weights and the fp32 output by the TMA, the
+// output rounded to bf16 in shared memory by eight warps).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -34,11 +36,15 @@ constexpr long long kSpinCycles = 4000000000LL;  // about two seconds
 // K-major boxes; then three mbarriers and the TMEM address
 constexpr uint32_t kAbsBar = 2 * kWBox + 2 * kRBox;
 constexpr uint32_t kAbsSmem = kAbsBar + 32 + 1024;
-// project: A = W^UV[h] as eight K-major boxes (512 latent columns), B = out of the tile
-// converted to bf16, eight K-major boxes
-constexpr uint32_t kPrjBar = 8 * kWBox + 8 * kRBox;
-constexpr uint32_t kPrjSmem = kPrjBar + 32 + 1024;
-constexpr int kPrjThreads = 512;  // sixteen warps: more of the latent output's loads in flight
+// project: a ring of four stages, each one 64-column chunk of K: the W^UV box (bf16, 16 KB),
+// the tile's fp32 output (two 32-column boxes, 16 KB) and its bf16 copy (the B operand, 8 KB)
+constexpr int kPrjStages = 4;
+constexpr uint32_t kPrjF = kNb * 64 * 4;                 // fp32 output chunk: 64 requests x 64 columns
+constexpr uint32_t kPrjStage = kWBox + kPrjF + kRBox;    // 40 KB
+constexpr uint32_t kPrjBar = kPrjStages * kPrjStage;
+constexpr uint32_t kPrjSmem = kPrjBar + 128 + 1024;
+constexpr int kPrjConvWarps = 8;                         // convert, then store y
+constexpr int kPrjThreads = 32 * (kPrjConvWarps + 2);    // + one loading warp, one MMA warp
 
 __device__ bool wait_bounded(uint32_t bar, uint32_t parity) {
     const long long t0 = (long long)clock64_now();
@@ -53,19 +59,6 @@ __device__ __forceinline__ void drain_pause() {
     const long long t0 = (long long)clock64_now();
     while ((long long)clock64_now() - t0 < 20000000LL) {
     }
-}
-
-// 16-B global load (read-only path) and 8-B shared store as volatile asm, so that all of a
-// thread's loads are issued before its first store.
-__device__ __forceinline__ float4 ld_nc_v4(const float *p) {
-    float4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "l"(p));
-    return v;
-}
-__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t a, uint32_t b) {
-    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
 }
 
 // Tile store shared -> global through a 3-D tensor map (bulk group), and the waits for it.
@@ -185,18 +178,24 @@ __global__ void __launch_bounds__(128) absorb_kernel(const __grid_constant__ CUt
     }
 }
 
-// One CTA per (head h, request tile bt): sixteen warps convert the tile's fp32 latent output
-// to bf16 while the weights arrive; one thread issues the MMAs; eight warps store.
-__global__ void __launch_bounds__(kPrjThreads) project_kernel(const __grid_constant__ CUtensorMap tm_v,
-                                                              const float *__restrict__ out, float *y, int B,
-                                                              int H, int *status) {
+// One CTA per (head h, request tile bt).  K = 512 latent columns in eight chunks of 64 through
+// a four-stage ring: one thread loads each chunk's W^UV box (bf16) and the tile's fp32 output
+// (two 32-column boxes, 128-B swizzle) by the TMA; eight warps round the fp32 values to the
+// swizzled bf16 B operand; one thread issues the chunk's four MMAs; the eight warps store y.
+__global__ void __launch_bounds__(kPrjThreads, 1) project_kernel(const __grid_constant__ CUtensorMap tm_v,
+                                                                 const __grid_constant__ CUtensorMap tm_f, float *y,
+                                                                 int B, int H, int *status) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char *gbase = smem_raw + (base - raw);
-    const uint32_t sA = base, sB = base + 8 * kWBox;
-    const uint32_t bar_a = base + kPrjBar, bar_b = bar_a + 8, bar_done = bar_a + 16;
-    volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(gbase + kPrjBar + 24);
+    const uint32_t bars = base + kPrjBar;  // full[4], conv[4], empty[4], done
+    auto full = [&](int st) { return bars + 8u * st; };
+    auto conv = [&](int st) { return bars + 32u + 8u * st; };
+    auto empty = [&](int st) { return bars + 64u + 8u * st; };
+    const uint32_t done = bars + 96u;
+    volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(gbase + kPrjBar + 104);
+    int *abort_flag = reinterpret_cast<int *>(gbase + kPrjBar + 112);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.x % H;
     const int bt = blockIdx.x / H;
@@ -204,9 +203,13 @@ __global__ void __launch_bounds__(kPrjThreads) project_kernel(const __grid_const
 
     if (warp == 0) {
         if (lane == 0) {
-            mbar_init(bar_a, 1);
-            mbar_init(bar_b, kPrjThreads / 32);
-            mbar_init(bar_done, 1);
+            for (int st = 0; st < kPrjStages; ++st) {
+                mbar_init(full(st), 1);
+                mbar_init(conv(st), kPrjConvWarps);
+                mbar_init(empty(st), 1);
+            }
+            mbar_init(done, 1);
+            *abort_flag = 0;
             fence_mbar_init();
         }
         __syncwarp();
@@ -217,72 +220,104 @@ __global__ void __launch_bounds__(kPrjThreads) project_kernel(const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    if (threadIdx.x == 0) {  // the weights do not depend on the previous kernel
-        mbar_arrive_expect_tx(bar_a, 8 * kWBox);
-        for (int i = 0; i < 8; ++i) tma_load_3d(sA + i * kWBox, &tm_v, 64 * i, 0, h, bar_a);
-    }
-    grid_dep_wait();  // the latent output comes from the previous kernel of the stream
-
-    // 64 requests x 128 chunks of four fp32: chunk id = thread + 256 i, request row id / 128,
-    // chunk c4 = id % 128 (columns 4 c4 .. 4 c4 + 3), so a warp reads 512 contiguous bytes.
-    constexpr int kIter = kNb * (kDLatent / 4) / kPrjThreads;
-    float4 v[kIter];
-    // every load is issued unconditionally (rows past B read row B - 1 and are zeroed after),
-    // so that none waits behind a branch
-#pragma unroll
-    for (int i = 0; i < kIter; ++i) {
-        const int id = threadIdx.x + kPrjThreads * i;
-        const int b = min(b0 + (id >> 7), B - 1);
-        v[i] = ld_nc_v4(out + ((int64_t)b * H + h) * kDLatent + 4 * (id & 127));
-    }
-#pragma unroll
-    for (int i = 0; i < kIter; ++i)
-        if (b0 + ((threadIdx.x + kPrjThreads * i) >> 7) >= B) v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < kIter; ++i) {
-        const int id = threadIdx.x + kPrjThreads * i;
-        const int row = id >> 7, c4 = id & 127;
-        // box c4 / 16 (64 columns); 16-B unit (c4 % 16) / 2 of the row, swizzled by row % 8
-        const uint32_t dst = sB + (c4 >> 4) * kRBox + row * 128 + ((((c4 & 15) >> 1) ^ (row & 7)) << 4) + (c4 & 1) * 8;
-        st_shared_v2(dst, bf16x2_bits(v[i].x, v[i].y), bf16x2_bits(v[i].z, v[i].w));
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar_b);
-
     bool ok = true;
-    if (threadIdx.x == 0) {
-        ok = wait_bounded(bar_a, 0) && wait_bounded(bar_b, 0);
+    auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
+        if (wait_bounded(bar, parity)) return true;
+        *reinterpret_cast<volatile int *>(abort_flag) = 1;
+        return false;
+    };
+    constexpr int kChunks = kDLatent / 64;
+    if (warp == kPrjConvWarps) {
+        // loads: the weights do not depend on the previous kernel, the output does
+        if (lane == 0) {
+            bool waited = false;
+            for (int c = 0; c < kChunks && ok; ++c) {
+                const int st = c % kPrjStages;
+                if (c >= kPrjStages) ok = wait(empty(st), ((c / kPrjStages) - 1) & 1);
+                if (!ok) break;
+                const uint32_t sd = base + st * kPrjStage;
+                mbar_arrive_expect_tx(full(st), kWBox + kPrjF);
+                tma_load_3d(sd, &tm_v, 64 * c, 0, h, full(st));
+                if (!waited) {
+                    grid_dep_wait();
+                    waited = true;
+                }
+                tma_load_3d(sd + kWBox, &tm_f, 64 * c, h, b0, full(st));
+                tma_load_3d(sd + kWBox + kPrjF / 2, &tm_f, 64 * c + 32, h, b0, full(st));
+            }
+        }
+    } else if (warp == kPrjConvWarps + 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_major(128, kNb, false, false);
+            for (int c = 0; c < kChunks && ok; ++c) {
+                const int st = c % kPrjStages;
+                ok = wait(conv(st), (c / kPrjStages) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t sd = base + st * kPrjStage;
+                for (int k = 0; k < 4; ++k)
+                    mma_ss(tmem, smem_desc_sw128(sd + k * 32u, 16u, 1024u),
+                           smem_desc_sw128(sd + kWBox + kPrjF + k * 32u, 16u, 1024u), idesc, (c | k) ? 1u : 0u);
+                mma_commit(empty(st));
+            }
+            if (ok) mma_commit(done);
+        }
+    } else {
+        // thread t: request row r = t / 4 of the tile, 16 columns (quarter qd) of each chunk
+        const int r = threadIdx.x >> 2, qd = threadIdx.x & 3;
+        for (int c = 0; c < kChunks && ok; ++c) {
+            const int st = c % kPrjStages;
+            ok = wait(full(st), (c / kPrjStages) & 1);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            const uint32_t sd = base + st * kPrjStage;
+            // fp32 box qd / 2 (32 columns, 128-B rows, 16-B unit u at u ^ (r % 8)); units
+            // 4 (qd % 2) .. + 3 hold this thread's 16 values
+            const uint32_t fbox = sd + kWBox + (qd >> 1) * (kPrjF / 2) + r * 128;
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int u = 4 * (qd & 1) + i;
+                float4 f;
+                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                             : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w)
+                             : "r"(fbox + ((u ^ (r & 7)) << 4)));
+                w[2 * i] = bf16x2_bits(f.x, f.y);
+                w[2 * i + 1] = bf16x2_bits(f.z, f.w);
+            }
+            // bf16 B operand row r: 16-B units 2 qd and 2 qd + 1, swizzled
+            const uint32_t brow = sd + kWBox + kPrjF + r * 128;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(brow + (((2 * qd) ^ (r & 7)) << 4)),
+                         "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                         : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(brow + (((2 * qd + 1) ^ (r & 7)) << 4)),
+                         "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                         : "memory");
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(conv(st));
+        }
+        if (ok) {
+            ok = wait(done, 0);
+            ok = __all_sync(0xffffffffu, ok);
+        }
         if (ok) {
             tc_fence_after();
-            constexpr uint32_t idesc = idesc_bf16_major(128, kNb, false, false);
-            for (int k = 0; k < kDLatent / 16; ++k) {
-                const uint64_t ad = smem_desc_sw128(sA + (k >> 2) * kWBox + (k & 3) * 32u, 16u, 1024u);
-                const uint64_t bd = smem_desc_sw128(sB + (k >> 2) * kRBox + (k & 3) * 32u, 16u, 1024u);
-                mma_ss(tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
-            }
-            mma_commit(bar_done);
-        }
-    }
-    grid_dep_launch();
-    if (__syncthreads_and(ok ? 1 : 0)) {
-        ok = wait_bounded(bar_done, 0);
-        tc_fence_after();
-        if (ok && warp < 8) {
-            // warp w < 8: TMEM lanes 32 (w % 4) .. (output channels j), requests 32 (w / 4) ..
+            // warp w: TMEM lanes 32 (w % 4) .. (output channels j), requests 32 (w / 4) ..
             const int j = 32 * (warp & 3) + lane;
             const int half = warp >> 2;
-            uint32_t r[32];
-            tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32u * half, r);
+            uint32_t rr[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32u * half, rr);
             tmem_wait_ld();
             const int bb = b0 + 32 * half;
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-                if (bb + i < B) y[((int64_t)(bb + i) * H + h) * kDh + j] = __uint_as_float(r[i]);
+                if (bb + i < B) y[((int64_t)(bb + i) * H + h) * kDh + j] = __uint_as_float(rr[i]);
         }
     }
-    if (!ok) {
-        if (status) record_error(status, MLA_ERR_TIMEOUT);
+    grid_dep_launch();
+    if (!__syncthreads_and(ok ? 1 : 0)) {
+        if (threadIdx.x == 0 && status) record_error(status, MLA_ERR_TIMEOUT);
         drain_pause();
     }
     tc_fence_before();
@@ -321,6 +356,20 @@ bool tmap_3d(CUtensorMap *m, const void *p, uint64_t d0, uint64_t d1, uint64_t d
     const cuuint32_t box[3] = {b0, b1, b2};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Same for an fp32 tensor (boxes of 32 columns = 128 B, 128-B swizzle).
+bool tmap_3d_f32(CUtensorMap *m, const void *p, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
+                 uint32_t b0, uint32_t b1, uint32_t b2) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {s1, s2};
+    const cuuint32_t box[3] = {b0, b1, b2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(p), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -389,11 +438,13 @@ extern "C" mla_status mla_project_output(const float *out, const void *w_uv, int
     const int64_t tiles = (int64_t)H * ((B + kNb - 1) / kNb);
     if (tiles > 0x7FFFFFFF) return MLA_ERR_UNSUPPORTED;
     if (!set_attrs()) return MLA_ERR_CUDA;
-    CUtensorMap tv;
-    // W^UV [H][128][512]: (c, j, h)
-    if (!tmap_3d(&tv, w_uv, kDLatent, kDh, H, kDLatent * 2, (uint64_t)kDh * kDLatent * 2, 64, 128, 1))
+    CUtensorMap tv, tf;
+    // W^UV [H][128][512]: (c, j, h); the latent output [B][H][512] fp32: (c, h, b), boxes of
+    // 32 columns x 64 requests
+    if (!tmap_3d(&tv, w_uv, kDLatent, kDh, H, kDLatent * 2, (uint64_t)kDh * kDLatent * 2, 64, 128, 1) ||
+        !tmap_3d_f32(&tf, out, kDLatent, H, B, kDLatent * 4, (uint64_t)kDLatent * 4 * H, 32, 1, kNb))
         return MLA_ERR_CUDA;
-    return launch_pdl(project_kernel, (int)tiles, kPrjThreads, kPrjSmem, (cudaStream_t)stream, tv, out, y, B, H,
+    return launch_pdl(project_kernel, (int)tiles, kPrjThreads, kPrjSmem, (cudaStream_t)stream, tv, tf, y, B, H,
                       (int *)device_status) == cudaSuccess
                ? MLA_OK
                : MLA_ERR_CUDA;
