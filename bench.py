@@ -12,6 +12,13 @@ before every timed step and each step is timed with CUDA events on the launching
 N > 1 runs under torch.distributed.run: every rank decodes its own full batch (requests are
 independent, no collective on the data path), value = all ranks' FLOPs / max rank time.
 --impl reference times the CPU oracle on a bounded sample of the same workload.
+
+Beside the step, the line reports the kernels around the decode, each timed alone with the
+same flush and events (outside the step's timed region): `append` (one new token per
+request into the cache), `absorb` (q~ = q^C W^UK) and `project` (y = W^UV out) for the
+workload's B and H, `topk` (DSA selection, k = 2048, over synthetic scores of the
+workload's lengths) and `prefill` (decompression + causal attention of one 4,096-token
+sequence with the workload's head count).
 """
 from __future__ import annotations
 
