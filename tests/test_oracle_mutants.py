@@ -204,3 +204,70 @@ def test_prefill_mutant_is_caught(tmp_path, name):
         return out, lse
 
     assert not all(ok for _, ok in _prefill_pins(prefill)), f"pins missed mutant {name}"
+
+
+# slips in the cache append and its FP8 quantiser, planted in copies of the C oracle
+APPEND_MUTANTS = {
+    "row_from_page_index": ("const int64_t row = (int64_t)page * PAGE_ROWS + pos % PAGE_ROWS;",
+                            "const int64_t row = (int64_t)page * PAGE_ROWS + (pos / PAGE_ROWS) % PAGE_ROWS;"),
+    "one_scale_for_all_blocks": ("for (int i = 0; i < 128; ++i) {\n                const float x = (float)bf16_bits_to_double(c[blk * 128 + i]);",
+                                 "for (int i = 0; i < 128; ++i) {\n                const float x = (float)bf16_bits_to_double(c[((blk + i) % 4) * 128 + i]);"),
+    "ties_away_from_even": ("if (d < bestd || (d == bestd && (c & 1) == 0 && (best & 1) == 1)) {",
+                            "if (d < bestd || (d == bestd && c > best)) {"),
+    "rope_not_copied": ("memcpy(dst + D_LATENT + 16, kr, D_ROPE * 2);", "(void)kr;"),
+}
+
+
+def _append_pins_hold(lib):
+    """The append pins of test_oracle.py that need no oracle internals: the record equals the
+    input generator's quantiser (a second implementation of reading 7), and only the mapped
+    row of each request changes."""
+    import torch
+    from mla_latent_kv_17_gb300 import inputs
+    P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    lib.mla_oracle_append.argtypes = [P, I, I64, P, I, P, P, P, I]
+    lib.mla_oracle_append.restype = I
+    ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    r = np.random.default_rng(11)
+    B, num_pages, max_pages = 5, 12, 2
+    for fp8 in (True, False):
+        rb = 656 if fp8 else 1152
+        cache = r.integers(0, 256, size=num_pages * 64 * rb, dtype=np.uint8)
+        bt = r.permutation(num_pages)[:B * max_pages].reshape(B, max_pages).astype(np.int32)
+        pos = np.array([0, 63, 64, 100, 127], dtype=np.int32)
+        mag = np.repeat([1.0, 1e-3, 300.0, 0.5], 128)
+        lat = torch.from_numpy(r.standard_normal((B, 512)) * mag).to(torch.bfloat16)
+        lat[0, :4] = torch.tensor([448.0, -448.0, 1.0625, -1.1875]).to(torch.bfloat16)  # exact ties
+        rope = torch.from_numpy(r.standard_normal((B, 64))).to(torch.bfloat16)
+        ck = np.ascontiguousarray(lat.view(torch.int16).numpy().view(np.uint16))
+        kr = np.ascontiguousarray(rope.view(torch.int16).numpy().view(np.uint16))
+        new = cache.copy()
+        if lib.mla_oracle_append(ptr(new), 1 if fp8 else 0, num_pages, ptr(bt), max_pages, ptr(pos), ptr(ck),
+                                 ptr(kr), B) != 0:
+            return False
+        rows, old = new.reshape(-1, rb), cache.reshape(-1, rb)
+        mapped = {int(bt[b, p // 64]) * 64 + p % 64: b for b, p in enumerate(pos)}
+        for i in range(rows.shape[0]):
+            if i not in mapped and not np.array_equal(rows[i], old[i]):
+                return False
+        if fp8:
+            ref = inputs.quantize_fp8_records(lat.float(), rope).numpy()
+            want = lambda b: ref[b]
+        else:
+            want = lambda b: np.concatenate([ck[b].view(np.uint8), kr[b].view(np.uint8)])
+        for i, b in mapped.items():
+            if not np.array_equal(rows[i], want(b)):
+                return False
+    return True
+
+
+def test_real_oracle_passes_append_pins(tmp_path):
+    lib = _build(tmp_path, "identity", "#include <math.h>", "#include <math.h>")
+    assert _append_pins_hold(lib)
+
+
+@pytest.mark.parametrize("name", sorted(APPEND_MUTANTS))
+def test_append_mutant_is_caught(tmp_path, name):
+    old, new = APPEND_MUTANTS[name]
+    lib = _build(tmp_path, name, old, new)
+    assert not _append_pins_hold(lib), f"pins missed mutant {name}"
