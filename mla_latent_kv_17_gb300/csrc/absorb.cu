@@ -20,6 +20,7 @@
 #include "common.cuh"
 #include "mla_decode.h"
 #include "sm103_ptx.cuh"
+#include "tc_util.cuh"
 
 namespace mla {
 namespace {
@@ -30,7 +31,6 @@ constexpr int kDh = 128;     // per-head nope / value width d_h
 constexpr int kNb = 64;      // requests per tile (MMA N, TMEM columns)
 constexpr uint32_t kWBox = 128 * 128;       // 128 rows x 64 bf16 of a weight matrix, 128-B swizzle
 constexpr uint32_t kRBox = kNb * 128;       // 64 requests x 64 bf16, 128-B swizzle
-constexpr long long kSpinCycles = 4000000000LL;  // about two seconds
 
 // absorb: A = W^UK[h][0:128][c0 : c0 + 128] as two MN-major boxes, B = q^C of the tile as two
 // K-major boxes; then three mbarriers and the TMEM address
@@ -45,44 +45,6 @@ constexpr uint32_t kPrjBar = kPrjStages * kPrjStage;
 constexpr uint32_t kPrjSmem = kPrjBar + 128 + 1024;
 constexpr int kPrjConvWarps = 8;                         // convert, then store y
 constexpr int kPrjThreads = 32 * (kPrjConvWarps + 2);    // + one loading warp, one MMA warp
-
-__device__ bool wait_bounded(uint32_t bar, uint32_t parity) {
-    const long long t0 = (long long)clock64_now();
-    for (uint32_t i = 0;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 63u && (long long)clock64_now() - t0 > kSpinCycles) return false;
-    }
-}
-
-// Gives copies or MMAs still in flight a bounded time to land before the CTA leaves.
-__device__ __forceinline__ void drain_pause() {
-    const long long t0 = (long long)clock64_now();
-    while ((long long)clock64_now() - t0 < 20000000LL) {
-    }
-}
-
-// Tile store shared -> global through a 3-D tensor map (bulk group), and the waits for it.
-__device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int32_t x, int32_t y, int32_t z) {
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
-                 ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(src), "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Waits until the committed bulk stores have completed (written to global memory).
-__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
-    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-}
-
-__device__ __forceinline__ uint16_t bf16_bits(float f) {
-    __nv_bfloat16 v = __float2bfloat16_rn(f);
-    return *reinterpret_cast<uint16_t *>(&v);
-}
-
-__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
 
 // One CTA per (latent tile ct of 128 columns, head h, request tile bt): four warps.
 __global__ void __launch_bounds__(128) absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
@@ -221,11 +183,7 @@ __global__ void __launch_bounds__(kPrjThreads, 1) project_kernel(const __grid_co
     tc_fence_after();
     const uint32_t tmem = *tslot;
     bool ok = true;
-    auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
-        if (wait_bounded(bar, parity)) return true;
-        *reinterpret_cast<volatile int *>(abort_flag) = 1;
-        return false;
-    };
+    auto wait = [&](uint32_t bar, uint32_t parity) { return wait_bounded(bar, parity, abort_flag); };
     constexpr int kChunks = kDLatent / 64;
     if (warp == kPrjConvWarps) {
         // loads: the weights do not depend on the previous kernel, the output does
@@ -328,53 +286,19 @@ __global__ void __launch_bounds__(kPrjThreads, 1) project_kernel(const __grid_co
     }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
-    return fn;
-}
-
-// 3-D bf16 tensor (d0 innermost, d1, d2) with byte strides s1, s2; boxes b0 x b1 x b2, 128-B
-// swizzle; elements outside the tensor read as zero.
+// 3-D bf16 / fp32 tensors (d0 innermost, d1, d2) with byte strides s1, s2 and boxes b0 x b1 x b2.
 bool tmap_3d(CUtensorMap *m, const void *p, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
              uint32_t b0, uint32_t b1, uint32_t b2) {
-    EncodeTiledFn enc = encode_tiled();
-    if (!enc) return false;
-    const cuuint64_t dims[3] = {d0, d1, d2};
-    const cuuint64_t strides[2] = {s1, s2};
-    const cuuint32_t box[3] = {b0, b1, b2};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const uint64_t d[3] = {d0, d1, d2}, st[2] = {s1, s2};
+    const uint32_t b[3] = {b0, b1, b2};
+    return tmap_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p, 3, d, st, b);
 }
-
-// Same for an fp32 tensor (boxes of 32 columns = 128 B, 128-B swizzle).
 bool tmap_3d_f32(CUtensorMap *m, const void *p, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
                  uint32_t b0, uint32_t b1, uint32_t b2) {
-    EncodeTiledFn enc = encode_tiled();
-    if (!enc) return false;
-    const cuuint64_t dims[3] = {d0, d1, d2};
-    const cuuint64_t strides[2] = {s1, s2};
-    const cuuint32_t box[3] = {b0, b1, b2};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(p), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const uint64_t d[3] = {d0, d1, d2}, st[2] = {s1, s2};
+    const uint32_t b[3] = {b0, b1, b2};
+    return tmap_tiled(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p, 3, d, st, b);
 }
-
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool set_attrs() {
     static bool done[64] = {};
@@ -390,21 +314,6 @@ bool set_attrs() {
     }
     done[dev] = true;
     return true;
-}
-
-template <typename K, typename... Args>
-cudaError_t launch_pdl(K kernel, int grid, int threads, uint32_t smem, cudaStream_t stream, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(threads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 }  // namespace

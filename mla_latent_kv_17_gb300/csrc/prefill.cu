@@ -24,6 +24,7 @@
 #include "common.cuh"
 #include "mla_decode.h"
 #include "sm103_ptx.cuh"
+#include "tc_util.cuh"
 
 namespace mla {
 namespace {
@@ -31,46 +32,6 @@ namespace {
 using namespace ptx;
 
 constexpr int kDh = 128;
-constexpr long long kSpinCycles = 4000000000LL;  // about two seconds
-
-__device__ bool wait_bar_bounded(uint32_t bar, uint32_t parity, int *abort_flag) {
-    const long long t0 = (long long)clock64_now();
-    for (uint32_t i = 0;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 63u) {
-            if (*reinterpret_cast<volatile int *>(abort_flag)) return false;
-            if ((long long)clock64_now() - t0 > kSpinCycles) {
-                *reinterpret_cast<volatile int *>(abort_flag) = 1;
-                return false;
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ void drain_pause() {
-    const long long t0 = (long long)clock64_now();
-    while ((long long)clock64_now() - t0 < 20000000LL) {
-    }
-}
-
-__device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int32_t x, int32_t y, int32_t z) {
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
-                 ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(src), "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
-    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-}
-__device__ __forceinline__ uint16_t bf16_bits(float f) {
-    __nv_bfloat16 v = __float2bfloat16_rn(f);
-    return *reinterpret_cast<uint16_t *>(&v);
-}
-__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
 
 // ------------------------------------------------------------------ decompression
 constexpr int kDcTok = 256;                       // tokens per CTA (MMA N)
@@ -126,7 +87,7 @@ __global__ void __launch_bounds__(kDcThreads, 1) decompress_kernel(const __grid_
     if (warp == 4 && lane == 0) {
         for (int c = 0; c < kChunks && ok; ++c) {
             const int s = c % kDcStages;
-            if (c >= kDcStages) ok = wait_bar_bounded(empty(s), ((c / kDcStages) - 1) & 1, abort_flag);
+            if (c >= kDcStages) ok = wait_bounded(empty(s), ((c / kDcStages) - 1) & 1, abort_flag);
             if (!ok) break;
             const uint32_t st = base + s * kDcStage;
             mbar_arrive_expect_tx(full(s), kDcStage);
@@ -138,7 +99,7 @@ __global__ void __launch_bounds__(kDcThreads, 1) decompress_kernel(const __grid_
         constexpr uint32_t idesc = idesc_bf16_major(128, kDcTok, false, false);
         for (int c = 0; c < kChunks && ok; ++c) {
             const int s = c % kDcStages;
-            ok = wait_bar_bounded(full(s), (c / kDcStages) & 1, abort_flag);
+            ok = wait_bounded(full(s), (c / kDcStages) & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
             const uint32_t st = base + s * kDcStage;
@@ -153,7 +114,7 @@ __global__ void __launch_bounds__(kDcThreads, 1) decompress_kernel(const __grid_
     }
     grid_dep_launch();
     if (warp < 4) {
-        ok = wait_bar_bounded(done, 0, abort_flag);
+        ok = wait_bounded(done, 0, abort_flag);
         tc_fence_after();
         if (ok) {
             // both results transposed into [256 tokens][64 bf16] boxes over the (finished)
@@ -285,7 +246,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
             tma_load_3d(base + kOffQ + 2 * kAtBox, &tm_qr, 0, h, q0, q_full);
             for (int g = 0; g < ntiles && ok; ++g) {
                 const int k0 = g * kAtK, kb = g & 1;
-                if (g >= 2) ok = wait_bar_bounded(k_empty(kb), ((g >> 1) - 1) & 1, abort_flag);
+                if (g >= 2) ok = wait_bounded(k_empty(kb), ((g >> 1) - 1) & 1, abort_flag);
                 if (!ok) break;
                 const uint32_t kd = base + kOffK + kb * 3 * kAtBox;
                 mbar_arrive_expect_tx(k_full(kb), 3 * kAtBox);
@@ -299,7 +260,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
         if (lane == 0) {
             for (int g = 0; g < ntiles && ok; ++g) {
                 const int vb = g & 1;
-                if (g >= 2) ok = wait_bar_bounded(v_empty(vb), ((g >> 1) - 1) & 1, abort_flag);
+                if (g >= 2) ok = wait_bounded(v_empty(vb), ((g >> 1) - 1) & 1, abort_flag);
                 if (!ok) break;
                 const uint32_t vd = base + kOffV + vb * 2 * kAtBox;
                 mbar_arrive_expect_tx(v_full(vb), 2 * kAtBox);
@@ -315,8 +276,8 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
             // (key buffer and score buffer are both g % 2)
             auto qk = [&](int g) -> bool {
                 const int b = g & 1;
-                if (!wait_bar_bounded(k_full(b), (g >> 1) & 1, abort_flag)) return false;
-                if (g >= 2 && !wait_bar_bounded(s_free(b), ((g >> 1) - 1) & 1, abort_flag)) return false;
+                if (!wait_bounded(k_full(b), (g >> 1) & 1, abort_flag)) return false;
+                if (g >= 2 && !wait_bounded(s_free(b), ((g >> 1) - 1) & 1, abort_flag)) return false;
                 tc_fence_after();
                 const uint32_t kd = base + kOffK + b * 3 * kAtBox;
                 for (int k = 0; k < 12; ++k) {
@@ -328,7 +289,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
                 mma_commit(k_empty(b));
                 return true;
             };
-            ok = wait_bar_bounded(q_full, 0, abort_flag) && qk(0);
+            ok = wait_bounded(q_full, 0, abort_flag) && qk(0);
             for (int g = 0; g < ntiles && ok; ++g) {
                 // the next tile's scores go ahead of this tile's PV, under this tile's softmax
                 if (g + 1 < ntiles && !qk(g + 1)) {
@@ -336,8 +297,8 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
                     break;
                 }
                 const int vb = g & 1;
-                ok = wait_bar_bounded(p_full, g & 1, abort_flag) &&
-                     wait_bar_bounded(v_full(vb), (g >> 1) & 1, abort_flag);
+                ok = wait_bounded(p_full, g & 1, abort_flag) &&
+                     wait_bounded(v_full(vb), (g >> 1) & 1, abort_flag);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t vd = base + kOffV + vb * 2 * kAtBox;
@@ -361,7 +322,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
         for (int g = 0; g < ntiles && ok; ++g) {
             const int k0 = g * kAtK;
             const int sb = g & 1;
-            ok = wait_bar_bounded(s_full(sb), (g >> 1) & 1, abort_flag);
+            ok = wait_bounded(s_full(sb), (g >> 1) & 1, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
@@ -388,7 +349,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
             red[sb][hf][row] = pm;
             __syncwarp();
             if (lane == 0) mbar_arrive(red_full(sb));
-            ok = wait_bar_bounded(red_full(sb), (g >> 1) & 1, abort_flag);
+            ok = wait_bounded(red_full(sb), (g >> 1) & 1, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             const float mx = fmaxf(red[sb][0][row], red[sb][1][row]);  // finite: key 0 is seen
@@ -406,7 +367,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
             m = mref;
             // P and O are free once the previous tile's PV has finished
             if (g > 0) {
-                ok = wait_bar_bounded(pv_done, (g - 1) & 1, abort_flag);
+                ok = wait_bounded(pv_done, (g - 1) & 1, abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
@@ -440,7 +401,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
             lsum[hf][row] = l;
             __syncwarp();
             if (lane == 0) mbar_arrive(l_done);
-            ok = wait_bar_bounded(l_done, 0, abort_flag) && wait_bar_bounded(pv_done, (ntiles - 1) & 1, abort_flag);
+            ok = wait_bounded(l_done, 0, abort_flag) && wait_bounded(pv_done, (ntiles - 1) & 1, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
         }
         if (ok) {
@@ -476,41 +437,9 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
     }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
-    return fn;
-}
-
-// bf16 tensor of rank 2 or 3 (d[0] innermost; byte strides s[0..rank-2]), boxes b, 128-B
-// swizzle; elements outside the tensor read as zero and are not written by stores.
 bool tmap_bf16(CUtensorMap *m, const void *p, int rank, const uint64_t *d, const uint64_t *s, const uint32_t *b) {
-    EncodeTiledFn enc = encode_tiled();
-    if (!enc) return false;
-    cuuint64_t dims[3], strides[2];
-    cuuint32_t box[3], estr[3] = {1, 1, 1};
-    for (int i = 0; i < rank; ++i) {
-        dims[i] = d[i];
-        box[i] = b[i];
-    }
-    for (int i = 0; i + 1 < rank; ++i) strides[i] = s[i];
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(p), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return tmap_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p, rank, d, s, b);
 }
-
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool set_prefill_attrs() {
     static bool done[64] = {};
@@ -526,21 +455,6 @@ bool set_prefill_attrs() {
     }
     done[dev] = true;
     return true;
-}
-
-template <typename K, typename... Args>
-cudaError_t launch_pdl(K kernel, int grid, int threads, uint32_t smem, cudaStream_t stream, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(threads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 }  // namespace
