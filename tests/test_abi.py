@@ -37,6 +37,20 @@ def test_header_declares_the_boundary():
         assert must in names
 
 
+def test_header_is_plain_c():
+    # the boundary carries no C++ or torch types: the header compiles as C99 on its own
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            r = subprocess.run([cc, "-fsyntax-only", "-std=c99", "-Wall", "-Werror", "-x", "c",
+                                os.path.join(ROOT, "include", h)], capture_output=True, text=True)
+            assert r.returncode == 0, r.stderr
+
+
 def test_library_exports_every_declared_symbol(L):
     for name in declared_functions():
         assert hasattr(L, name), f"{name} declared in include/ but not exported"
