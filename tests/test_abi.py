@@ -51,6 +51,24 @@ def test_header_is_plain_c():
             assert r.returncode == 0, r.stderr
 
 
+def test_c_program_uses_the_abi_without_python(L, tmp_path):
+    # a plain C program links the library and calls its host-side entry points
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(ops.LIB_PATH)
+    exe = str(tmp_path / "abi_host")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        os.path.join(ROOT, "tests", "c", "abi_host.c"), "-L", libdir, "-lmla_decode",
+                        f"-Wl,-rpath,{libdir}", "-o", exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    assert "c abi ok" in r.stdout
+
+
 def test_library_exports_every_declared_symbol(L):
     for name in declared_functions():
         assert hasattr(L, name), f"{name} declared in include/ but not exported"
