@@ -117,3 +117,19 @@ def test_plan_is_deterministic():
     a = ops.plan_host(sl, 64, 128, 0, 148)
     b = ops.plan_host(sl, 64, 128, 0, 148)
     assert np.array_equal(a, b)
+
+
+def test_random_plans_hold_every_invariant():
+    # mixtures of empty, single-token, page-edge, ordinary and very long requests, over
+    # request counts from 1 to 700 and several SM counts: coverage, slots, unit order and
+    # per-unit load bound all hold (check_plan)
+    r = np.random.default_rng(2024)
+    for trial in range(150):
+        B = int(r.choice([1, 2, 3, 7, 64, 128, 300, 700]))
+        kind = r.integers(0, 5, size=B)
+        lens = np.where(kind == 0, 0,
+               np.where(kind == 1, 1,
+               np.where(kind == 2, 64 * r.integers(1, 40, size=B),
+               np.where(kind == 3, r.integers(2, 9000, size=B), r.integers(30000, 140000, size=B)))))
+        num_sms = int(r.choice([2, 20, 132, 148, 152]))
+        check_plan(lens.astype(np.int32), H=int(r.choice([16, 64, 128])), num_sms=num_sms)
