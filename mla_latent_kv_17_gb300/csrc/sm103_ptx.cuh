@@ -149,16 +149,6 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int3
         :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
         : "memory");
 }
-// Same load, delivered to every CTA of the cluster named in cta_mask (same shared-memory
-// offset and mbarrier offset in each).
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void *tmap, int32_t x, int32_t y,
-                                                      uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;"
-        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
-        : "memory");
-}
 // Asks the memory system to bring `bytes` (a multiple of 16) at `src` into L2; nothing is
 // written to shared memory and nothing waits for it.
 __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
