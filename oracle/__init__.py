@@ -16,7 +16,9 @@ Functions follow these passages (page title, section):
 * ``decode_sparse``: same guide §1.2 / §4.2 (attend over the top-k selected tokens).
 * ``decode_fp8`` / ``e4m3_to_float``: same guide §5.3 (FP8 latent cache).  The format
   (e4m3 "fn", one fp32 scale per 128 channels) is this library's reading; the pages
-  name only "FP8".
+  name only "FP8".  The dequantized latent is code x scale, exact (the default); the
+  ``operand="bf16"`` mode rounds it to bf16 as a bf16 tensor-core operand would, a
+  tighter secondary check only.
 * ``append`` / ``e4m3_encode``: the cache append after a decode step (same guide §4,
   the decode figure: the output token is appended to the cache) and the FP8 record it
   writes (§5.3; per-128-channel scale max|x|/448, nearest e4m3 code, ties to even).
@@ -85,6 +87,8 @@ def _load():
             lib.mla_oracle_e4m3_to_double.restype = D
             lib.mla_oracle_fp8_latent.argtypes = [ctypes.c_uint8, ctypes.c_float]
             lib.mla_oracle_fp8_latent.restype = D
+            lib.mla_oracle_fp8_latent_exact.argtypes = [ctypes.c_uint8, ctypes.c_float]
+            lib.mla_oracle_fp8_latent_exact.restype = D
             lib.mla_oracle_e4m3_encode.argtypes = [ctypes.c_float]
             lib.mla_oracle_e4m3_encode.restype = ctypes.c_uint8
             lib.mla_oracle_append.argtypes = [P, I, I64, P, I, P, P, P, I]
@@ -100,7 +104,7 @@ def _load():
             common = [I, I, P, P, P, I64, P, I, P]
             lib.mla_oracle_decode_dense.argtypes = common + [D, P, P, I]
             lib.mla_oracle_decode_dense.restype = I
-            lib.mla_oracle_decode_fp8.argtypes = common + [D, P, P, I]
+            lib.mla_oracle_decode_fp8.argtypes = common + [I, D, P, P, I]
             lib.mla_oracle_decode_fp8.restype = I
             lib.mla_oracle_decode_sparse.argtypes = common + [P, I, D, P, P, I]
             lib.mla_oracle_decode_sparse.restype = I
@@ -122,9 +126,14 @@ def e4m3_to_float(code: int) -> float:
     return float(_load().mla_oracle_e4m3_to_double(int(code) & 0xFF))
 
 
-def fp8_latent(code: int, scale: float) -> float:
-    """One dequantized FP8 latent value: bf16_rne(fp32(e4m3(code)) * fp32(scale))."""
-    return float(_load().mla_oracle_fp8_latent(int(code) & 0xFF, float(scale)))
+def fp8_latent(code: int, scale: float, operand: str = "exact") -> float:
+    """One dequantized FP8 latent value: e4m3(code) * scale exactly, or with
+    operand="bf16" bf16_rne(fp32(e4m3(code)) * fp32(scale))."""
+    if operand == "exact":
+        return float(_load().mla_oracle_fp8_latent_exact(int(code) & 0xFF, float(scale)))
+    if operand == "bf16":
+        return float(_load().mla_oracle_fp8_latent(int(code) & 0xFF, float(scale)))
+    raise ValueError(operand)
 
 
 def e4m3_encode(v: float) -> int:
@@ -294,10 +303,13 @@ def decode_dense(q_nope, q_rope, cache, block_table, seq_lens, scale, nthreads=0
                 scale, nthreads)
 
 
-def decode_fp8(q_nope, q_rope, cache, block_table, seq_lens, scale, nthreads=0):
-    """Dense decode over the paged FP8 cache [num_pages,64,656] (bytes)."""
+def decode_fp8(q_nope, q_rope, cache, block_table, seq_lens, scale, nthreads=0, operand="exact"):
+    """Dense decode over the paged FP8 cache [num_pages,64,656] (bytes).  operand="exact":
+    latent = code x scale exactly (the definition); "bf16": that value rounded to bf16."""
+    if operand not in ("exact", "bf16"):
+        raise ValueError(operand)
     return _run("mla_oracle_decode_fp8", q_nope, q_rope, cache, block_table, seq_lens,
-                scale, nthreads, cache_kind="fp8")
+                scale, nthreads, extra=(1 if operand == "exact" else 0,), cache_kind="fp8")
 
 
 def decode_sparse(q_nope, q_rope, cache, block_table, seq_lens, indices, scale, nthreads=0):

@@ -30,10 +30,12 @@
  *    tokens only.
  *  - Same guide, §5.3: the FP8 latent cache.  The pages do not fix the FP8 format; this
  *    oracle reads e4m3 "fn" (bias 7, no infinities, S.1111.111 is NaN) with one fp32
- *    scale per 128 latent channels.  The dequantized latent is the bf16 operand of the
- *    bf16 contraction that follows (the guide's FP8 cache feeds bf16/FP8 compute; the
- *    pages fix no intermediate precision): x = bf16_rne(fp32(e4m3(code)) * scale), the
- *    product formed in fp32 (exact for the code; one rounding) and rounded once to bf16.
+ *    scale per 128 latent channels.  The dequantized latent is what the guide defines:
+ *    x = e4m3(code) * scale, exact in double (a 4-bit significand times a 24-bit one).
+ *    A second mode, used only as a tighter check of one GPU operand choice, rounds that
+ *    value the way a bf16 tensor-core operand would: x = bf16_rne(fp32(e4m3(code)) * scale),
+ *    the product formed in fp32 and rounded once to bf16.  The pages fix no intermediate
+ *    precision, so only the exact mode is the definition.
  *
  * Readings where the pages are silent: the scale multiplies the raw score before the
  * exponential; lse is the natural log of the normaliser of the scaled scores; an empty
@@ -89,8 +91,14 @@ double mla_oracle_e4m3_to_double(uint8_t code) {
     return sign ? -v : v;
 }
 
-/* One dequantized latent value of an FP8 record: code times its block scale, formed in
- * binary32 and rounded once to bfloat16 (see the header). */
+/* One dequantized latent value of an FP8 record: code times its block scale, exact in
+ * double (the definition). */
+double mla_oracle_fp8_latent_exact(uint8_t code, float scale) {
+    return mla_oracle_e4m3_to_double(code) * (double)scale;
+}
+
+/* The same value formed in binary32 and rounded once to bfloat16 (the bf16-operand mode
+ * described in the header). */
 double mla_oracle_fp8_latent(uint8_t code, float scale) {
     return f32_to_bf16_double((float)mla_oracle_e4m3_to_double(code) * scale);
 }
@@ -161,14 +169,25 @@ void mla_oracle_combine_f64(int S, int D, const double *outs, const double *lses
 }
 
 /* ---------------------------------------------------------------------------------
- * Paged front ends.  They gather the request's token rows into double arrays and call
- * mla_oracle_attend_f64.  Work is spread over requests with plain pthreads.
+ * Paged front ends.  They gather each request's token rows into double arrays and call
+ * mla_oracle_attend_f64 on slices of its heads.  Work is spread with plain pthreads in
+ * rounds: a round gathers up to `nthreads` requests (one thread per request), then every
+ * thread takes (request, head slice) tasks of that round, so that a batch of a few long
+ * requests still uses every core.  Parallelism only: each head's arithmetic is the
+ * definition above, unchanged.
  * -------------------------------------------------------------------------------*/
 
-enum { CACHE_BF16 = 0, CACHE_FP8 = 1 };
+enum { CACHE_BF16 = 0, CACHE_FP8 = 1, CACHE_FP8_EXACT = 2 };
 
 typedef struct {
-    int kind; /* CACHE_BF16 or CACHE_FP8 */
+    int64_t N;          /* attended tokens */
+    double *qn, *qr;    /* [H*512], [H*64] */
+    double *C, *Kr;     /* [N*512], [N*64] */
+    int rc;
+} gathered_t;
+
+typedef struct {
+    int kind; /* CACHE_BF16, CACHE_FP8 (bf16-operand latent) or CACHE_FP8_EXACT */
     int B, H;
     const uint16_t *q_nope, *q_rope;
     const void *cache;
@@ -180,7 +199,10 @@ typedef struct {
     int topk;
     double scale;
     double *out, *lse;
-    int next_b; /* shared work counter */
+    /* the current round: requests b0 .. b0 + nb - 1, heads cut into `slices` slices */
+    int b0, nb, slices;
+    gathered_t *g;
+    int next; /* shared task counter of the current phase */
     pthread_mutex_t mu;
     int error;
 } job_t;
@@ -201,7 +223,9 @@ static int load_token(const job_t *J, int b, int64_t t, double *c, double *kr) {
         const uint8_t *e = (const uint8_t *)J->cache + (size_t)row * FP8_RECORD_BYTES;
         float sc[4];
         for (int g = 0; g < 4; ++g) sc[g] = (float)f32_bits_to_double(e + 512 + 4 * g);
-        for (int i = 0; i < D_LATENT; ++i) c[i] = mla_oracle_fp8_latent(e[i], sc[i / 128]);
+        for (int i = 0; i < D_LATENT; ++i)
+            c[i] = J->kind == CACHE_FP8_EXACT ? mla_oracle_fp8_latent_exact(e[i], sc[i / 128])
+                                              : mla_oracle_fp8_latent(e[i], sc[i / 128]);
         const uint8_t *rp = e + 528;
         for (int i = 0; i < D_ROPE; ++i) {
             uint16_t bits = (uint16_t)(rp[2 * i] | (rp[2 * i + 1] << 8));
@@ -211,7 +235,8 @@ static int load_token(const job_t *J, int b, int64_t t, double *c, double *kr) {
     return 0;
 }
 
-static int do_request(job_t *J, int b) {
+/* Gathers request b's queries and attended token rows into *G. */
+static void gather_request(const job_t *J, int b, gathered_t *G) {
     int H = J->H;
     int64_t N = 0;
     if (J->indices) {
@@ -220,62 +245,94 @@ static int do_request(job_t *J, int b) {
     } else {
         N = J->seq_lens[b];
     }
-    double *qn = (double *)malloc(sizeof(double) * (size_t)H * D_LATENT);
-    double *qr = (double *)malloc(sizeof(double) * (size_t)H * D_ROPE);
-    double *C = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1) * D_LATENT);
-    double *Kr = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1) * D_ROPE);
+    G->N = N;
+    G->qn = (double *)malloc(sizeof(double) * (size_t)H * D_LATENT);
+    G->qr = (double *)malloc(sizeof(double) * (size_t)H * D_ROPE);
+    G->C = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1) * D_LATENT);
+    G->Kr = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1) * D_ROPE);
     int rc = 0;
     for (int i = 0; i < H * D_LATENT; ++i)
-        qn[i] = bf16_bits_to_double(J->q_nope[(size_t)b * H * D_LATENT + i]);
+        G->qn[i] = bf16_bits_to_double(J->q_nope[(size_t)b * H * D_LATENT + i]);
     for (int i = 0; i < H * D_ROPE; ++i)
-        qr[i] = bf16_bits_to_double(J->q_rope[(size_t)b * H * D_ROPE + i]);
+        G->qr[i] = bf16_bits_to_double(J->q_rope[(size_t)b * H * D_ROPE + i]);
     int64_t n = 0;
     if (J->indices) {
         for (int j = 0; j < J->topk && rc == 0; ++j) {
             int32_t t = J->indices[(size_t)b * J->topk + j];
             if (t == -1) continue;
             if (t < -1) { rc = -1; break; }
-            rc = load_token(J, b, t, C + (size_t)n * D_LATENT, Kr + (size_t)n * D_ROPE);
+            rc = load_token(J, b, t, G->C + (size_t)n * D_LATENT, G->Kr + (size_t)n * D_ROPE);
             ++n;
         }
     } else {
         for (int64_t t = 0; t < N && rc == 0; ++t, ++n)
-            rc = load_token(J, b, t, C + (size_t)t * D_LATENT, Kr + (size_t)t * D_ROPE);
+            rc = load_token(J, b, t, G->C + (size_t)t * D_LATENT, G->Kr + (size_t)t * D_ROPE);
     }
-    if (rc == 0)
-        mla_oracle_attend_f64(H, N, qn, qr, C, Kr, J->scale,
-                              J->out + (size_t)b * H * D_LATENT, J->lse + (size_t)b * H);
-    free(qn); free(qr); free(C); free(Kr);
-    return rc;
+    G->rc = rc;
 }
 
-static void *worker(void *arg) {
+static void free_gathered(gathered_t *G) {
+    free(G->qn); free(G->qr); free(G->C); free(G->Kr);
+}
+
+static int take_task(job_t *J) {
+    pthread_mutex_lock(&J->mu);
+    int k = J->next++;
+    pthread_mutex_unlock(&J->mu);
+    return k;
+}
+
+static void *gather_worker(void *arg) {
     job_t *J = (job_t *)arg;
-    for (;;) {
-        pthread_mutex_lock(&J->mu);
-        int b = J->next_b++;
-        pthread_mutex_unlock(&J->mu);
-        if (b >= J->B) break;
-        if (do_request(J, b) != 0) {
-            pthread_mutex_lock(&J->mu);
-            J->error = 1;
-            pthread_mutex_unlock(&J->mu);
-        }
+    for (int k; (k = take_task(J)) < J->nb;) gather_request(J, J->b0 + k, &J->g[k]);
+    return NULL;
+}
+
+/* Task k of the round: request b0 + k / slices, heads of slice k % slices. */
+static void *attend_worker(void *arg) {
+    job_t *J = (job_t *)arg;
+    const int H = J->H;
+    const int per = (H + J->slices - 1) / J->slices;
+    for (int k; (k = take_task(J)) < J->nb * J->slices;) {
+        const int r = k / J->slices, h0 = (k % J->slices) * per;
+        const int h1 = h0 + per < H ? h0 + per : H;
+        const gathered_t *G = &J->g[r];
+        if (G->rc != 0 || h0 >= h1) continue;
+        const int b = J->b0 + r;
+        mla_oracle_attend_f64(h1 - h0, G->N, G->qn + (size_t)h0 * D_LATENT, G->qr + (size_t)h0 * D_ROPE,
+                              G->C, G->Kr, J->scale, J->out + ((size_t)b * H + h0) * D_LATENT,
+                              J->lse + (size_t)b * H + h0);
     }
     return NULL;
+}
+
+static void run_phase(job_t *J, int nthreads, void *(*fn)(void *)) {
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    J->next = 0;
+    for (int i = 0; i < nthreads; ++i) pthread_create(&th[i], NULL, fn, J);
+    for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+    free(th);
 }
 
 static int run_jobs(job_t *J, int nthreads) {
     if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
     if (nthreads < 1) nthreads = 1;
-    if (nthreads > J->B) nthreads = J->B > 0 ? J->B : 1;
     pthread_mutex_init(&J->mu, NULL);
-    J->next_b = 0;
     J->error = 0;
-    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
-    for (int i = 0; i < nthreads; ++i) pthread_create(&th[i], NULL, worker, J);
-    for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
-    free(th);
+    J->g = (gathered_t *)calloc((size_t)nthreads, sizeof(gathered_t));
+    for (J->b0 = 0; J->b0 < J->B; J->b0 += nthreads) {
+        J->nb = J->B - J->b0 < nthreads ? J->B - J->b0 : nthreads;
+        /* enough head slices that every thread has work */
+        J->slices = (nthreads + J->nb - 1) / J->nb;
+        if (J->slices > J->H) J->slices = J->H;
+        run_phase(J, J->nb, gather_worker);
+        run_phase(J, nthreads, attend_worker);
+        for (int r = 0; r < J->nb; ++r) {
+            if (J->g[r].rc != 0) J->error = 1;
+            free_gathered(&J->g[r]);
+        }
+    }
+    free(J->g);
     pthread_mutex_destroy(&J->mu);
     return J->error ? -1 : 0;
 }
@@ -299,15 +356,17 @@ int mla_oracle_decode_dense(int B, int H, const uint16_t *q_nope, const uint16_t
 }
 
 /* Dense decode over a paged FP8 cache: page = 64 records of 656 bytes
- * (512 e4m3 latent codes | 4 little-endian fp32 scales | 64 bf16 RoPE values). */
+ * (512 e4m3 latent codes | 4 little-endian fp32 scales | 64 bf16 RoPE values).
+ * exact != 0: latent = code * scale exactly (the definition); exact == 0: the bf16-operand
+ * rounding of the header. */
 int mla_oracle_decode_fp8(int B, int H, const uint16_t *q_nope, const uint16_t *q_rope,
                           const uint8_t *cache, int64_t num_pages,
                           const int32_t *block_table, int max_pages,
-                          const int32_t *seq_lens, double scale, double *out, double *lse,
-                          int nthreads) {
+                          const int32_t *seq_lens, int exact, double scale, double *out,
+                          double *lse, int nthreads) {
     job_t J;
     memset(&J, 0, sizeof J);
-    J.kind = CACHE_FP8; J.B = B; J.H = H; J.q_nope = q_nope; J.q_rope = q_rope;
+    J.kind = exact ? CACHE_FP8_EXACT : CACHE_FP8; J.B = B; J.H = H; J.q_nope = q_nope; J.q_rope = q_rope;
     J.cache = cache; J.num_pages = num_pages; J.block_table = block_table;
     J.max_pages = max_pages; J.seq_lens = seq_lens; J.scale = scale; J.out = out; J.lse = lse;
     return run_jobs(&J, nthreads);

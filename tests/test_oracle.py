@@ -484,33 +484,57 @@ def test_e4m3_decoder_against_library_and_format_constants():
     assert math.isnan(oracle.e4m3_to_float(0x7F)) and math.isnan(oracle.e4m3_to_float(0xFF))
 
 
-def test_fp8_latent_is_fp32_product_rounded_once_to_bf16():
-    # every code against torch's own e4m3 decode, fp32 multiply and round-to-nearest-even
-    # bf16 conversion, for scales with full fp32 mantissas (so the bf16 rounding matters)
-    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
-    vals = codes.view(torch.float8_e4m3fn).float()
+def _fp8_scales():
     g = torch.Generator().manual_seed(3)
-    scales = torch.cat([torch.tensor([1.0, 1.0 / 448, 3.7e-3]), torch.rand(5, generator=g) * 0.05 + 1e-4])
-    for sc in scales.float():
-        ref = (vals * sc).to(torch.bfloat16).double()
+    return torch.cat([torch.tensor([1.0, 1.0 / 448, 3.7e-3]), torch.rand(5, generator=g) * 0.05 + 1e-4]).float()
+
+
+def test_fp8_latent_exact_is_code_times_scale():
+    # the definition (guide §5.3: an FP8 code and its block scale): every code against
+    # torch's own e4m3 decode times the fp32 scale, both widened to double, where the
+    # product of a 4-bit and a 24-bit significand is exact
+    vals = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double()
+    for sc in _fp8_scales():
         for code in range(256):
             v = oracle.fp8_latent(code, float(sc))
+            r = float(vals[code]) * float(sc)
+            assert (math.isnan(v) and math.isnan(r)) or v == r, (code, float(sc), v, r)
+    # a scale whose product is not a bf16 value stays unrounded: 1.125 * (1 + 2^-20)
+    assert oracle.fp8_latent(0x39, 1.0 + 2.0 ** -20) == 1.125 * (1.0 + 2.0 ** -20)
+
+
+def test_fp8_latent_bf16_operand_is_fp32_product_rounded_once_to_bf16():
+    # the secondary mode: every code against torch's own e4m3 decode, fp32 multiply and
+    # round-to-nearest-even bf16 conversion, for scales with full fp32 mantissas (so the
+    # bf16 rounding matters)
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    vals = codes.view(torch.float8_e4m3fn).float()
+    for sc in _fp8_scales():
+        ref = (vals * sc).to(torch.bfloat16).double()
+        for code in range(256):
+            v = oracle.fp8_latent(code, float(sc), operand="bf16")
             r = float(ref[code])
             assert (math.isnan(v) and math.isnan(r)) or v == r, (code, float(sc), v, r)
     # scale 1: e4m3 values are exact in bf16
-    assert oracle.fp8_latent(0x7E, 1.0) == 448.0 and oracle.fp8_latent(0x01, 1.0) == 2.0 ** -9
+    assert oracle.fp8_latent(0x7E, 1.0, operand="bf16") == 448.0
+    assert oracle.fp8_latent(0x01, 1.0, operand="bf16") == 2.0 ** -9
+    assert oracle.fp8_latent(0x39, 1.0 + 2.0 ** -20, operand="bf16") == 1.125
 
 
-def test_fp8_decode_equals_dense_on_dequantised_values():
+@pytest.mark.parametrize("operand", ["exact", "bf16"])
+def test_fp8_decode_equals_dense_on_dequantised_values(operand):
     B, H, lens = 2, 3, [97, 64]
     c = inputs.make_case(B, H, lens, seed=21, kv_dtype="fp8", extra_pages=1)
-    out, lse = oracle.decode_fp8(c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens, SCALE)
+    out, lse = oracle.decode_fp8(c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens, SCALE,
+                                 operand=operand)
     rec = c.cache
     codes = rec[..., :512].contiguous().view(torch.float8_e4m3fn).double()     # library decode
     scales = rec[..., 512:528].contiguous().view(torch.float32).double()       # [P,64,4]
     rope = rec[..., 528:656].contiguous().view(torch.bfloat16).double()
-    # dequantized latent: fp32 product of code and block scale, rounded once to bf16 (torch)
-    lat = (codes.float() * scales.float().repeat_interleave(128, dim=-1)).to(torch.bfloat16).double()
+    if operand == "exact":   # code x scale in double (exact)
+        lat = codes * scales.repeat_interleave(128, dim=-1)
+    else:                    # fp32 product of code and block scale, rounded once to bf16 (torch)
+        lat = (codes.float() * scales.float().repeat_interleave(128, dim=-1)).to(torch.bfloat16).double()
     for b in range(B):
         rows = [(int(c.block_table[b, t // 64]), t % 64) for t in range(lens[b])]
         C = np.stack([lat[p, r].numpy() for p, r in rows])
