@@ -13,12 +13,19 @@ N > 1 runs under torch.distributed.run: every rank decodes its own full batch (r
 independent, no collective on the data path), value = all ranks' FLOPs / max rank time.
 --impl reference times the CPU oracle on a bounded sample of the same workload.
 
+The top-level keys describe the headline workload (--workload, by default the
+DeepSeek-V3-shaped dense batch: B=64, H=128, lengths uniform in [1024, 8192]).  `workloads`
+holds the same measurements for the other four workloads (tiny, long-context 128K, FP8
+ragged, DSA sparse): step and decode-call times (mean, median, min), TFLOP/s, GB/s, the
+roofline fraction of the decode call, the end-to-end rate through the public API with host
+buffers, and the oracle's CPU baseline.
+
 Beside the step, the line reports the kernels around the decode, each timed alone with the
 same flush and events (outside the step's timed region): `append` (one new token per
 request into the cache), `absorb` (q~ = q^C W^UK) and `project` (y = W^UV out) for the
 workload's B and H, `topk` (DSA selection, k = 2048, over synthetic scores of the
 workload's lengths) and `prefill` (decompression + causal attention of one 4,096-token
-sequence with the workload's head count).
+sequence with the workload's head count).  --only skips the other workloads and these.
 """
 from __future__ import annotations
 
@@ -221,61 +228,60 @@ def run_reference(args, ws_n, rank):
             flops_tot += f
     secs = sum(per_step)
     val = flops_tot / secs / 1e12
+    from mla_latent_kv_17_gb300 import metrics
+    alg = metrics.algorithmic(case)
     line = {"metric": METRIC, "value": val, "unit": "TFLOP/s", "impl": "reference",
             "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload},
-            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                             "sample": desc},
+            "config": {"workload": args.workload, "B": case.B, "H": case.H,
+                       "tokens": alg["tokens"], "kv": case.kv_dtype,
+                       "l2": "flushed before every step (2x L2 write); step = plan + decode + merge",
+                       "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU"},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "cpu_model": cpu_model(),
+                             "kind": "oracle", "sample": desc},
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ref-budget", type=float, default=8.0,
-                    help="seconds of oracle work per reference step")
-    args = ap.parse_args()
-    args.warmup = max(3, args.warmup)
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for ln in r.stdout.splitlines():
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
 
-    ws_n, rank, local = dist_env()
+
+def stats(ms):
+    return {"mean": sum(ms) / len(ms), "median": statistics.median(ms), "min": min(ms)}
+
+
+def measure_workload(name, args, dev, stream, flush, pk, pk_kind, pg, ws_n, clocks=False):
+    """Times one workload: the step (plan + decode call, back to back), the decode call alone
+    (decode kernel + split merge, the roofline unit) and the end-to-end call through the
+    public API with host buffers; returns (summary dict, case, out) plus the clock sampler."""
     import torch
-    pg = None
-    if ws_n > 1:
-        import torch.distributed as dist
-        backend = "nccl" if args.impl == "ours" else "gloo"
-        if backend == "nccl":
-            torch.cuda.set_device(local)
-        dist.init_process_group(backend=backend)
-        pg = dist
-    if args.impl == "reference":
-        run_reference(args, ws_n, rank)
-        if pg:
-            pg.destroy_process_group()
-        return
-
-    from mla_latent_kv_17_gb300 import build as mbuild
-    mbuild.build()
     from mla_latent_kv_17_gb300 import inputs, metrics, ops
 
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    case = inputs.make_workload(args.workload, device=dev)
+    case = inputs.make_workload(name, device=dev)
     alg = metrics.algorithmic(case)
     sparse = case.indices is not None
     topk = case.indices.shape[1] if sparse else 0
     wsp = ops.Workspace(case.B, case.H, device=dev)
     out = torch.empty((case.B, case.H, 512), dtype=torch.float32, device=dev)
     lse = torch.empty((case.B, case.H), dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
 
     def decode_call():
         if sparse:
@@ -289,16 +295,13 @@ def main():
         ops.plan(wsp, None if sparse else case.seq_lens, topk=topk, stream=stream)
         decode_call()
 
-    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20)
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
-
     for _ in range(args.warmup):
         flush.fill_(1)
         step()
     torch.cuda.synchronize()
     st = ops.status(wsp, stream)
     if st != 0:
-        raise RuntimeError(f"device status {ops.STATUS_NAMES.get(st, st)} during warm-up")
+        raise RuntimeError(f"{name}: device status {ops.STATUS_NAMES.get(st, st)} during warm-up")
 
     # a step is plan + decode call, back to back on the stream (no event between them: the
     # decode launches while the plan finishes)
@@ -307,22 +310,25 @@ def main():
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
-    with Clocks(local) as clk:
-        t_wall = time.perf_counter()
-        for i in range(args.steps):
-            flush.fill_(i & 0xFF)
-            ev[i][0].record(stream)
-            ops.plan(wsp, None if sparse else case.seq_lens, topk=topk, stream=stream)
-            decode_call()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall
+    clk = Clocks(torch.cuda.current_device()) if clocks else None
+    if clk:
+        clk.__enter__()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if clk:
+        clk.__exit__(None, None, None)
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
     st = ops.status(wsp, stream)
     if st != 0:
-        raise RuntimeError(f"device status {ops.STATUS_NAMES.get(st, st)} in timed region")
+        raise RuntimeError(f"{name}: device status {ops.STATUS_NAMES.get(st, st)} in timed region")
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     # the decode call alone (decode kernel + split-KV merge) for the roofline, on the plan
     # of the last step, with the same L2 flush before every call
@@ -337,7 +343,7 @@ def main():
         dec_ms.append(a_.elapsed_time(b_))
     st = ops.status(wsp, stream)
     if st != 0:
-        raise RuntimeError(f"device status {ops.STATUS_NAMES.get(st, st)} in the call timing")
+        raise RuntimeError(f"{name}: device status {ops.STATUS_NAMES.get(st, st)} in the call timing")
     tot_ms = metrics.max_over_ranks(sum(step_ms), pg, dev)
     ms_per_step = tot_ms / args.steps
     dec_avg_ms = sum(dec_ms) / len(dec_ms)
@@ -388,6 +394,139 @@ def main():
         e_ms.append(a.elapsed_time(b))
     e2e_ms = metrics.max_over_ranks(sum(e_ms) / len(e_ms), pg, dev)
 
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    bound = "hbm" if alg["ai"] < ridge else "tensor"
+    dec_s = dec_avg_ms * 1e-3
+    if bound == "hbm":
+        achieved, peak, unit = alg["bytes"] / dec_s / 1e9, pk["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = alg["flops"] / dec_s / 1e12, pk["bf16_tflops"], "TFLOP/s"
+    roof_s = metrics.roofline_seconds(alg["flops"], alg["bytes"], pk["bf16_tflops"], pk["hbm_gbs"])
+    summary = {
+        "B": case.B, "H": case.H, "kv": case.kv_dtype, "tokens": alg["tokens"],
+        "value": metrics.whole_job_rate(alg["flops"], ws_n, ms_per_step * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "ms_per_step": ms_per_step, "step_ms": stats(step_ms), "call_ms": stats(dec_ms),
+        "hbm_gbs": alg["bytes"] / (ms_per_step * 1e-3) / 1e9,
+        "tflops_decode_call": alg["flops"] / dec_s / 1e12,
+        "pct_roofline": roof_s / (ms_per_step * 1e-3),
+        "roofline": {"kernel": "mla_decode call (decode kernel + split-KV merge)", "bound": bound,
+                     "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                     "traffic": dram_traffic(name), "peak_source": pk_kind,
+                     "ai_flop_per_byte": alg["ai"], "alg_bytes_per_call": alg["bytes"],
+                     "alg_flops_per_call": alg["flops"], "call_ms": dec_avg_ms},
+        "e2e": {"value": metrics.whole_job_rate(alg["flops"], ws_n, e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "wall_s_timed_region": t_wall,
+    }
+    return summary, case, clk
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--only", action="store_true",
+                    help="measure --workload alone (no other workloads, no side kernels)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=8.0,
+                    help="seconds of oracle work per reference step")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    ws_n, rank, local = dist_env()
+    import torch
+    pg = None
+    if ws_n > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        pg = dist
+    if args.impl == "reference":
+        run_reference(args, ws_n, rank)
+        if pg:
+            pg.destroy_process_group()
+        return
+
+    from mla_latent_kv_17_gb300 import build as mbuild
+    mbuild.build()
+    from mla_latent_kv_17_gb300 import inputs, ops
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20)
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    pk, pk_kind = peaks()
+
+    head, case, clk = measure_workload(args.workload, args, dev, stream, flush, pk, pk_kind, pg, ws_n,
+                                       clocks=True)
+    do_cpu = rank == 0 and ws_n == 1 and not args.no_cpu_baseline
+    threads = 0
+    if do_cpu:
+        f, s_, threads, desc = oracle_sample_time(case, budget_s=12.0)
+        head["cpu_baseline"] = {"value": f / s_ / 1e12, "unit": "TFLOP/s", "cores": threads,
+                                "cpu_model": cpu_model(), "kind": "oracle", "sample": desc, "seconds": s_}
+
+    # ---- the kernels around the decode, for the headline workload's B and H ------------
+    side = {} if args.only else side_kernels(case, args, dev, stream, flush, pk)
+    del case
+    torch.cuda.empty_cache()
+
+    # ---- the other workloads: same measurements, each its own line item ----------------
+    others = {}
+    if not args.only:
+        for name in inputs.WORKLOADS:
+            if name == args.workload:
+                continue
+            summ, c2, _ = measure_workload(name, args, dev, stream, flush, pk, pk_kind, pg, ws_n)
+            if do_cpu:
+                f, s_, th, desc = oracle_sample_time(c2, budget_s=8.0)
+                summ["cpu_baseline"] = {"value": f / s_ / 1e12, "unit": "TFLOP/s", "cores": th,
+                                        "cpu_model": cpu_model(), "kind": "oracle", "sample": desc,
+                                        "seconds": s_}
+            others[name] = summ
+            del c2
+            torch.cuda.empty_cache()
+
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": "TFLOP/s", "n_gpus": ws_n,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "B": head["B"], "H": head["H"],
+                   "tokens": head["tokens"], "kv": head["kv"],
+                   "l2": "flushed before every step (2x L2 write); step = plan + decode + merge",
+                   "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU"},
+        "step_ms": head["step_ms"], "call_ms": head["call_ms"],
+        "hbm_gbs": head["hbm_gbs"], "tflops_decode_call": head["tflops_decode_call"],
+        "pct_roofline": head["pct_roofline"], "roofline": head["roofline"], "e2e": head["e2e"],
+        "gpu_launches": 3 * args.steps,
+        **side,
+        "workloads": others,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": head["wall_s_timed_region"],
+    }
+    if "cpu_baseline" in head:
+        line["cpu_baseline"] = head["cpu_baseline"]
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+def side_kernels(case, args, dev, stream, flush, pk):
+    """Times the kernels around the decode for `case`'s B and H, each alone with the same
+    flush and events: the cache append, query absorption, value projection, top-k selection
+    and a 4,096-token prefill."""
+    import torch
+    from mla_latent_kv_17_gb300 import inputs, ops
+
     # ---- cache append (the step after decode): one token per request, timed alone -------
     # (written at each request's last position, inside its block table; after every decode
     # measurement, since it changes the cache)
@@ -395,19 +534,8 @@ def main():
     a_lat = torch.randn(case.B, 512, generator=g_app).to(torch.bfloat16).to(dev)
     a_rope = torch.randn(case.B, 64, generator=g_app).to(torch.bfloat16).to(dev)
     a_pos = (case.seq_lens - 1).clamp(min=-1).to(torch.int32).contiguous()
-    for _ in range(3):
-        ops.cache_append(case.cache, case.block_table, a_pos, a_lat, a_rope, stream=stream)
-    torch.cuda.synchronize()
-    a_ms = []
-    for i in range(args.steps):
-        flush.fill_(i & 0xFF)
-        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ea.record(stream)
-        ops.cache_append(case.cache, case.block_table, a_pos, a_lat, a_rope, stream=stream)
-        eb.record(stream)
-        eb.synchronize()
-        a_ms.append(ea.elapsed_time(eb))
-    app_ms = sum(a_ms) / len(a_ms)
+    app_ms = time_alone(lambda: ops.cache_append(case.cache, case.block_table, a_pos, a_lat, a_rope,
+                                                 stream=stream), args.steps, flush, stream)
     rec_bytes = 656 if case.kv_dtype == "fp8" else 1152
     n_app = int((a_pos >= 0).sum().item())
     app_bytes = n_app * (rec_bytes + 1024 + 128 + 4 + 4)  # record out; latent, rope, position, page id in
@@ -451,37 +579,7 @@ def main():
     BH = case.B * case.H
     ab_bytes = case.H * 128 * 512 * 2 + BH * 128 * 2 + BH * 512 * 2  # W^UK, q^C in; q~ out
     pj_bytes = case.H * 128 * 512 * 2 + BH * 512 * 4 + BH * 128 * 4  # W^UV, latent out in; y out
-
-    pk, pk_kind = peaks()
-    tf = metrics.whole_job_rate(alg["flops"], ws_n, ms_per_step * 1e-3) / 1e12
-    gbs = alg["bytes"] / (ms_per_step * 1e-3) / 1e9
-    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
-    bound = "hbm" if alg["ai"] < ridge else "tensor"
-    dec_s = dec_avg_ms * 1e-3
-    if bound == "hbm":
-        achieved, peak, unit = alg["bytes"] / dec_s / 1e9, pk["hbm_gbs"], "GB/s"
-    else:
-        achieved, peak, unit = alg["flops"] / dec_s / 1e12, pk["bf16_tflops"], "TFLOP/s"
-    roof_s = metrics.roofline_seconds(alg["flops"], alg["bytes"], pk["bf16_tflops"], pk["hbm_gbs"])
-    line = {
-        "metric": METRIC, "value": tf, "unit": "TFLOP/s", "n_gpus": ws_n, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "B": case.B, "H": case.H,
-                   "tokens": alg["tokens"], "kv": case.kv_dtype,
-                   "l2": "flushed before every step (2x L2 write); step = plan + decode + merge",
-                   "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU"},
-        "hbm_gbs": gbs, "tflops_decode_call": alg["flops"] / dec_s / 1e12,
-        "pct_roofline": roof_s / (ms_per_step * 1e-3),
-        "roofline": {"kernel": "mla_decode call (decode kernel + split-KV merge)", "bound": bound,
-                     "achieved": achieved, "peak": peak, "unit": unit,
-                     "frac": achieved / peak, "traffic": dram_traffic(args.workload),
-                     "peak_source": pk_kind, "ai_flop_per_byte": alg["ai"],
-                     "alg_bytes_per_call": alg["bytes"], "alg_flops_per_call": alg["flops"],
-                     "call_ms": dec_avg_ms},
-        "e2e": {"value": metrics.whole_job_rate(alg["flops"], ws_n, e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": 3 * args.steps,
+    return {
         "append": {"kernel": "cache append (mla_cache_append), one token per request", "requests": n_app,
                    "kv": case.kv_dtype, "us": app_ms * 1e3, "bytes": app_bytes,
                    "gbs": app_bytes / (app_ms * 1e-3) / 1e9},
@@ -500,18 +598,7 @@ def main():
                     "flops": pf_dc_flops + pf_at_flops,
                     "tflops": (pf_dc_flops + pf_at_flops) / (pf_ms * 1e-3) / 1e12,
                     "frac_bf16": (pf_dc_flops + pf_at_flops) / (pf_ms * 1e-3) / 1e12 / pk["bf16_tflops"]},
-        "clocks": clk.summary(),
-        "wall_s_timed_region": t_wall,
     }
-    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
-        f, s, threads, desc = oracle_sample_time(case, budget_s=12.0)
-        line["cpu_baseline"] = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": threads,
-                                "kind": "oracle", "sample": desc, "seconds": s}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if pg:
-        pg.barrier()
-        pg.destroy_process_group()
 
 
 if __name__ == "__main__":

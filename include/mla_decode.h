@@ -57,7 +57,9 @@ typedef enum {
     MLA_ERR_WORKSPACE = 3,   /* workspace too small, or it does not hold a matching plan */
     MLA_ERR_CUDA = 4,        /* a CUDA runtime call failed                               */
     MLA_ERR_INDEX = 5,       /* device: page id, token index or length out of range      */
-    MLA_ERR_TIMEOUT = 6      /* device: a pipeline wait exceeded its iteration limit     */
+    MLA_ERR_TIMEOUT = 6,     /* device: a pipeline wait exceeded its iteration limit     */
+    MLA_ERR_RANGE = 7        /* device: FP8-record decode met a value outside the fp16
+                                range of its operands (|query| or 448 x scale > 65504)   */
 } mla_status;
 
 typedef enum { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
@@ -104,6 +106,25 @@ mla_status mla_decode_status(void *workspace, size_t ws_bytes, void *stream);
 
 /* Static description of a status code. */
 const char *mla_status_string(mla_status status);
+
+/* Limit, in SM clock cycles, of every pipeline wait inside the decode kernel, for the
+ * mla_decode / mla_decode_sparse / mla_decode_static calls made after it in this process
+ * (0 restores the default, about two seconds).  A wait that runs out records
+ * MLA_ERR_TIMEOUT in the status word; the kernel then stops issuing work, gives copies and
+ * tensor-core operations already in flight a bounded time to land, releases its tensor
+ * memory and returns, so the device and the workspace stay usable (the call's out and lse
+ * are then undefined).  The default is far above any healthy wait; a tiny limit makes
+ * waits run out on purpose, which is how the timeout path is tested.  Returns
+ * MLA_ERR_INVALID_ARG for a negative limit. */
+mla_status mla_decode_set_wait_limit(int64_t cycles);
+
+/* Test hook for the timeout path: while enabled (enable != 0), every decode call made
+ * afterwards in this process has its tensor-core issuer wait, before it issues anything,
+ * on a barrier that nothing ever completes.  That wait runs out after the wait limit
+ * above, the call records MLA_ERR_TIMEOUT and winds down as described there, and the
+ * device stays usable.  It exists so that tests can make a wait run out on purpose without
+ * any fault; production code leaves it disabled (the default). */
+mla_status mla_decode_inject_stall(int enable);
 
 /* Dense decode (plan + decode + split merge) that allocates nothing and takes no
  * workspace.  It is for callers that cannot allocate device memory at decode time: all

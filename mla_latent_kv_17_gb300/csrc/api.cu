@@ -4,6 +4,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "launch.h"
 #include "mla_decode.h"
@@ -240,6 +242,11 @@ int device_sm_count() {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Limit of one pipeline wait in the decode kernel (SM clock cycles), for calls made from now on.
+std::atomic<long long> g_wait_cycles{kDefaultWaitCycles};
+// Injected stall for tests of the timeout path (mla_decode_inject_stall).
+std::atomic<int> g_stall_test{0};
+
 mla_status check_common(const void *ws, size_t ws_bytes, const void *q_nope, const void *q_rope,
                         const void *cache, int64_t num_pages, const int32_t *block_table,
                         int max_pages, const int32_t *seq_lens, int B, int H, float scale,
@@ -371,6 +378,8 @@ mla_status mla_decode(const void *workspace, size_t ws_bytes, const void *q_nope
     a.lse = lse;
     a.kv_fp8 = kv_dtype == MLA_KV_FP8_E4M3;
     a.ws_bytes = ws_bytes;
+    a.wait_cycles = g_wait_cycles.load();
+    a.stall_test = g_stall_test.load();
     return run_decode(a, (cudaStream_t)stream);
 }
 
@@ -404,6 +413,8 @@ mla_status mla_decode_sparse(const void *workspace, size_t ws_bytes, const void 
     a.lse = lse;
     a.kv_fp8 = 0;
     a.ws_bytes = ws_bytes;
+    a.wait_cycles = g_wait_cycles.load();
+    a.stall_test = g_stall_test.load();
     return run_decode(a, (cudaStream_t)stream);
 }
 
@@ -419,6 +430,17 @@ mla_status mla_decode_status(void *workspace, size_t ws_bytes, void *stream) {
     return (mla_status)host;
 }
 
+mla_status mla_decode_inject_stall(int enable) {
+    g_stall_test.store(enable ? 1 : 0);
+    return MLA_OK;
+}
+
+mla_status mla_decode_set_wait_limit(int64_t cycles) {
+    if (cycles < 0) return MLA_ERR_INVALID_ARG;
+    g_wait_cycles.store(cycles == 0 ? kDefaultWaitCycles : (long long)cycles);
+    return MLA_OK;
+}
+
 const char *mla_status_string(mla_status s) {
     switch (s) {
         case MLA_OK: return "ok";
@@ -428,6 +450,7 @@ const char *mla_status_string(mla_status s) {
         case MLA_ERR_CUDA: return "CUDA runtime error";
         case MLA_ERR_INDEX: return "page id, token index or length out of range";
         case MLA_ERR_TIMEOUT: return "pipeline wait exceeded its iteration limit";
+        case MLA_ERR_RANGE: return "value outside the fp16 operand range of the FP8-record decode";
     }
     return "unknown status";
 }

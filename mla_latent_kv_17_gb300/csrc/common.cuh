@@ -30,7 +30,14 @@ struct DecodeArgs {
     float *lse;                   // [B][H]
     int kv_fp8;
     size_t ws_bytes;
+    long long wait_cycles;        // iteration limit of every pipeline wait, in SM clock cycles
+    int stall_test;               // nonzero: the MMA issuer first waits on a barrier nothing completes
 };
+
+// Default limit of a pipeline wait: about two seconds of SM clock.  Nothing in a healthy run
+// waits anywhere near this long; a wait that does records MLA_ERR_TIMEOUT and the kernel
+// winds down instead of spinning forever.
+constexpr long long kDefaultWaitCycles = 4000000000LL;
 
 // True when the workspace holds a plan built for this call (same B, H, topk) that fits in
 // ws_bytes.  Otherwise the caller's kernel records MLA_ERR_WORKSPACE and does nothing.

@@ -66,7 +66,6 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 320;
 constexpr uint32_t kColQRope = kColQ + 128, kColQOther = kColQ + 160;
 constexpr float kRescaleLog2 = 8.0f;
-constexpr long long kSpinCycles = 4000000000LL;  // about two seconds
 
 constexpr uint32_t kOffDh = 0;
 constexpr uint32_t kOffOth = kOffDh + kDhSlots * kDhBytes;
@@ -94,7 +93,8 @@ enum {
     B_P_FULL,   // the probability tile holds the merged weights of its tile
     B_QLD,      // a round of query boxes has landed in the query area
     B_RAW,      // FP8: raw codes + scales of latent slot s (s < 3) or of the other-columns stage (3)
-    B_COUNT = B_RAW + 4
+    B_STALL = B_RAW + 4,  // never completed: the injected stall of the timeout test waits on it
+    B_COUNT
 };
 static_assert(B_COUNT <= 32, "barrier area");
 
@@ -102,6 +102,7 @@ struct Ctx {
     uint32_t base;
     int *status;
     volatile uint32_t *abort;
+    long long wait_cycles;  // limit of one wait (DecodeArgs::wait_cycles)
 };
 
 __device__ __forceinline__ uint32_t bar(uint32_t base, int i) { return base + kOffBar + 8u * i; }
@@ -115,7 +116,7 @@ __device__ bool wait_bar(const Ctx &c, uint32_t b, uint32_t parity, bool cluster
         if (ok) return true;
         if ((i & 63u) == 63u) {
             if (*c.abort) return false;
-            if ((long long)clock64_now() - t0 > kSpinCycles) {
+            if ((long long)clock64_now() - t0 > c.wait_cycles) {
                 *c.abort = 1u;
                 record_error(c.status, MLA_ERR_TIMEOUT);
                 return false;
@@ -145,18 +146,53 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
 }
-// Multiplies one 128-B row of bf16 weights by f (the chunk order inside the row does not
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ float2 unpack_f16(uint32_t w) {
+    return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+}
+// The 16-bit operand type of the MMAs: bf16 for a bf16 cache (its values are the operands
+// as stored), fp16 for FP8 records (code x scale keeps 3 more significand bits in fp16).
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack_op(float lo, float hi) {
+    if constexpr (kF16)
+        return pack_f16(lo, hi);
+    else
+        return pack_bf16(lo, hi);
+}
+template <bool kF16>
+__device__ __forceinline__ uint32_t scale_pair(uint32_t w, float f) {
+    if constexpr (kF16) {
+        const float2 v = unpack_f16(w);
+        return pack_f16(v.x * f, v.y * f);
+    } else {
+        return pack_bf16(bf16lo(w) * f, bf16hi(w) * f);
+    }
+}
+// Multiplies one 128-B row of 16-bit weights by f (the chunk order inside the row does not
 // matter).
+template <bool kF16>
 __device__ __forceinline__ void scale_row(uint4 *prow, float f) {
     for (int q = 0; q < 8; ++q) {
         uint4 v = prow[q];
-        v.x = pack_bf16(bf16lo(v.x) * f, bf16hi(v.x) * f);
-        v.y = pack_bf16(bf16lo(v.y) * f, bf16hi(v.y) * f);
-        v.z = pack_bf16(bf16lo(v.z) * f, bf16hi(v.z) * f);
-        v.w = pack_bf16(bf16lo(v.w) * f, bf16hi(v.w) * f);
+        v.x = scale_pair<kF16>(v.x, f);
+        v.y = scale_pair<kF16>(v.y, f);
+        v.z = scale_pair<kF16>(v.z, f);
+        v.w = scale_pair<kF16>(v.w, f);
         prow[q] = v;
     }
 }
+// A bf16 pair as an fp16 pair (exact for |x| in the fp16 normal range); *amax collects
+// the larger magnitude so that the caller can report values beyond the fp16 range.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, float *amax) {
+    const float lo = bf16lo(w), hi = bf16hi(w);
+    *amax = fmaxf(*amax, fmaxf(fabsf(lo), fabsf(hi)));
+    return pack_f16(lo, hi);
+}
+// Largest magnitude an fp16 operand holds (beyond it the conversion gives infinity).
+constexpr float kF16Max = 65504.0f;
 
 // Page p (0 or 1) of the tile starting at token t of item w: its valid rows (0 when the page
 // lies past the item's end) and its physical id (-1 when that id is out of range).
@@ -349,13 +385,13 @@ __device__ int next_request(const int32_t *ub, const WorkItem *items, int units,
     return -1;
 }
 
-// kSparse: tiles are 128 index slots (DSA top-k lists) gathered row by row; otherwise 128
-// consecutive tokens (two pages) loaded as 64-row boxes.
-// Two e4m3 codes (low byte first) times their block scale, as a packed bf16 pair.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two, float s) {
+// Two e4m3 codes (low byte first) times their block scale, as a packed fp16 pair: the code
+// is widened exactly (e4m3 -> fp16 -> fp32), the product formed in fp32 and rounded once to
+// fp16, the operand type of the FP8 path's MMAs.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two, float s) {
     const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
     const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
-    return pack_bf16(f.x * s, f.y * s);
+    return pack_f16(f.x * s, f.y * s);
 }
 
 // Expands 16 e4m3 codes (v) with block scale s into the 16-code chunk q (0..3) of row r of a
@@ -366,8 +402,8 @@ __device__ __forceinline__ void expand_chunk(uint4 v, float s, uint8_t *box, int
     uint32_t o[8];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        o[2 * k] = e4m3x2_to_bf16x2(w[k], s);
-        o[2 * k + 1] = e4m3x2_to_bf16x2(w[k] >> 16, s);
+        o[2 * k] = e4m3x2_to_f16x2(w[k], s);
+        o[2 * k + 1] = e4m3x2_to_f16x2(w[k] >> 16, s);
     }
     *reinterpret_cast<uint4 *>(box + (((2 * q) ^ (r & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
     *reinterpret_cast<uint4 *>(box + (((2 * q + 1) ^ (r & 7)) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
@@ -435,7 +471,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
     const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
     volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(gbase + kOffMisc);
     // misc[0]: TMEM base address, misc[1]: abort flag
-    Ctx c{base, a.status, misc + 1};
+    Ctx c{base, a.status, misc + 1, a.wait_cycles};
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kDhSlots; ++s) {
@@ -454,6 +490,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
         mbar_init(bar(base, B_PFREE), 2);  // one commit from each CTA's PV
         mbar_init(bar(base, B_P_FULL), 4);
         mbar_init(bar(base, B_QLD), 1);  // + the boxes' bytes
+        mbar_init(bar(base, B_STALL), 1);
         misc[1] = 0u;
         fence_mbar_init();
     }
@@ -519,6 +556,9 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
             if (!warp_wait(c, bar(base, raw_bar), raw_phase & 1u, false)) return false;
             if (pg.rows > 0 && pg.id >= 0) {
                 const float sc = reinterpret_cast<const float *>(gbase + scale_off + r * 16)[2 * half + p];
+                // code x scale must stay inside the fp16 range of the operand (|x| <= 65504);
+                // rows past the item's end may hold anything and are not checked
+                if (r < pg.rows && !(fabsf(sc) * 448.f <= kF16Max)) record_error(a.status, MLA_ERR_RANGE);
                 uint8_t *row = gbase + region + r * 128;                 // row r of box 0
                 const uint8_t *codes = row + 2 * p * kBox;               // its 8 chunks of 16 codes
                 uint8_t *first = row + 2 * p * kBox, *second = first + kBox;
@@ -723,9 +763,15 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
     } else if (warp == 5) {
         // ------------------------------------------------------------ QK^T issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16(128, 64, false);
+            // FP8 records: the latent columns in fp16, the RoPE columns (bf16 in the record and
+            // in the query) in bf16; every MMA accumulates into the same fp32 scores
+            constexpr uint32_t idesc_qk_rope = idesc_bf16(128, 64, false);
+            constexpr uint32_t idesc_qk = kFp8 ? idesc_f16(128, 64, false) : idesc_qk_rope;
             uint32_t g = 0, nitem = 0;
             bool ok = true;
+            // injected stall (test of the timeout path): a wait on a barrier nothing completes,
+            // before any MMA is issued; it runs out after the wait limit and the CTA winds down
+            if (a.stall_test && !wait_bar(c, bar(base, B_STALL), 0u, false)) ok = false;
             for (int u = cl; u < units && ok; u += ncl) {
                 for (int it = unit_begin[u]; it < unit_begin[u + 1] && ok; ++it) {
                     const WorkItem w = items[it];
@@ -756,7 +802,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                                 if (i == 0)
                                     mma_ts(tmem + kColS, tmem + kColQOther + 8u * k, bd, idesc_qk, k > 0 ? 1u : 0u);
                                 else if (i == 4)
-                                    mma_ts(tmem + kColS, tmem + kColQRope + 8u * k, bd, idesc_qk, 1u);
+                                    mma_ts(tmem + kColS, tmem + kColQRope + 8u * k, bd, idesc_qk_rope, 1u);
                                 else
                                     mma_ss(tmem + kColS,
                                            smem_desc_sw128(base + kOffQs + (i - 1) * kQsBox + k * 32u, 16u, 1024u),
@@ -786,7 +832,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
     } else if (warp == 6) {
         // ------------------------------------------------------------ PV issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_pv = idesc_bf16(128, 256, true);
+            constexpr uint32_t idesc_pv = kFp8 ? idesc_f16(128, 256, true) : idesc_bf16(128, 256, true);
             uint32_t g = 0;
             bool ok = true;
             for (int u = cl; u < units && ok; u += ncl) {
@@ -849,6 +895,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
         // shared-memory query area: rounds 0 and 1 go on to TMEM, each thread moving its own
         // head's row; round 2 stays.  Heads at or beyond H lie outside the tensor: zeros.
         uint32_t qphase = 0;
+        float qmax = 0.f;  // FP8 records: largest query magnitude converted to fp16
         // issues round `round` of request bq's query boxes (thread 0)
         auto q_round = [&](int bq, int round) {
             const uint32_t qb = bar(base, B_QLD);
@@ -866,15 +913,19 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
         };
         // round0_issued: round 0 was issued already (as soon as the previous item's last
         // scores were read, so that its latency hides behind that tile's merge)
+        // A warp whose wait fails still takes part in the named barriers of rounds 0 and 1
+        // (bar.sync has no time limit, so every one of the 128 threads must arrive); it only
+        // skips the work, and the load reports the failure at the end.
         auto load_q = [&](int bq, bool round0_issued) -> bool {
             const uint32_t qb = bar(base, B_QLD);
+            bool okq = true;
             for (int round = 0; round < 3; ++round) {
-                if (threadIdx.x == 0 && !(round == 0 && round0_issued)) q_round(bq, round);
-                if (!warp_wait(c, qb, qphase & 1u, false)) return false;
+                if (threadIdx.x == 0 && okq && !(round == 0 && round0_issued)) q_round(bq, round);
+                if (okq) okq = warp_wait(c, qb, qphase & 1u, false);
                 ++qphase;
                 if (round == 2) break;
 #pragma unroll 1
-                for (int i = 0; i < 3; ++i) {
+                for (int i = 0; i < 3 && okq; ++i) {
                     const uint8_t *row = gbase + kOffQs + i * kQsBox + h * 128;
                     uint32_t v[32];
 #pragma unroll
@@ -885,9 +936,36 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                         v[4 * q + 2] = x.z;
                         v[4 * q + 3] = x.w;
                     }
+                    // FP8 records: the latent part of the query becomes fp16 like the latent
+                    // operand it meets (block 4, the RoPE part, stays bf16)
+                    if (kFp8 && 3 * round + i != 4) {
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) v[q] = bf16x2_to_f16x2(v[q], &qmax);
+                    }
                     tmem_st32(trow + kColQ + 32u * (3 * round + i), v);
                 }
                 named_bar_sync(1, 128);  // every head's rows are read before the next round lands
+            }
+            if (!okq) return false;
+            if constexpr (kFp8) {
+                // the query's last 192 latent columns stay in shared memory: each thread
+                // converts its own head's rows in place (the conversion is per element, so the
+                // swizzle of the 16-B units does not matter)
+                for (int i = 0; i < 3; ++i) {
+                    uint4 *row = reinterpret_cast<uint4 *>(gbase + kOffQs + i * kQsBox + h * 128);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        uint4 x = row[q];
+                        x.x = bf16x2_to_f16x2(x.x, &qmax);
+                        x.y = bf16x2_to_f16x2(x.y, &qmax);
+                        x.z = bf16x2_to_f16x2(x.z, &qmax);
+                        x.w = bf16x2_to_f16x2(x.w, &qmax);
+                        row[q] = x;
+                    }
+                }
+                fence_proxy_async_smem();
+                if (qmax > kF16Max) record_error(a.status, MLA_ERR_RANGE);
+                qmax = 0.f;
             }
             tmem_wait_st();
             tc_fence_before();
@@ -980,7 +1058,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                         const float p0 = ex2_approx(fmaf(s[2 * i], sc, nr));
                         const float p1 = ex2_approx(fmaf(s[2 * i + 1], sc, nr));
                         lown += p0 + p1;
-                        pk[i] = pack_bf16(p0, p1);
+                        pk[i] = pack_op<kFp8>(p0, p1);
                     }
                     // cache rows that PV reads but must not contribute (rows of the last
                     // 16-row step past the end, a page whose id was out of range, sparse slots
@@ -1048,11 +1126,11 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                     if (__any_sync(0xffffffffu, fown < 1.f)) {
                         if (lane == 0) bulk_wait_read_all();
                         __syncwarp();
-                        if (fown < 1.f) scale_row(reinterpret_cast<uint4 *>(ps + rank * kPPage + h * 128), fown);
+                        if (fown < 1.f) scale_row<kFp8>(reinterpret_cast<uint4 *>(ps + rank * kPPage + h * 128), fown);
                         wrote = true;
                     }
                     if (fpeer < 1.f) {
-                        scale_row(reinterpret_cast<uint4 *>(ps + peer * kPPage + h * 128), fpeer);
+                        scale_row<kFp8>(reinterpret_cast<uint4 *>(ps + peer * kPPage + h * 128), fpeer);
                         wrote = true;
                     }
                     // zero the rows decided in part A

@@ -42,8 +42,10 @@ mla_status scratch_for_current_device(void **out) {
     std::lock_guard<std::mutex> lock(g_setup_mu);
     if (!g_scratch_ptr[dev]) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr)
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();  // leave no pending error behind for the caller's next CUDA call
             return MLA_ERR_CUDA;
+        }
         g_scratch_ptr[dev] = p;
     }
     *out = g_scratch_ptr[dev];

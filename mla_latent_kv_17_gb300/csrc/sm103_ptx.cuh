@@ -274,6 +274,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f16 with fp16 A and B (format code 0), fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) {
+    return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // Same, with the major order of each operand chosen (MN-major A: bit 15, MN-major B: bit 16).
 __host__ __device__ constexpr uint32_t idesc_bf16_major(int M, int N, bool a_mn_major, bool b_mn_major) {
     return idesc_bf16(M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libmla_decode.so")
 MLA_OK = 0
 STATUS_NAMES = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
                 3: "MLA_ERR_WORKSPACE", 4: "MLA_ERR_CUDA", 5: "MLA_ERR_INDEX",
-                6: "MLA_ERR_TIMEOUT"}
+                6: "MLA_ERR_TIMEOUT", 7: "MLA_ERR_RANGE"}
 KV_BF16, KV_FP8 = 0, 1
 
 _lock = threading.Lock()
@@ -69,6 +69,10 @@ def lib():
             L.mla_project_output.restype = I
             L.mla_decode_status.argtypes = [P, SZ, P]
             L.mla_decode_status.restype = I
+            L.mla_decode_inject_stall.argtypes = [I]
+            L.mla_decode_inject_stall.restype = I
+            L.mla_decode_set_wait_limit.argtypes = [I64]
+            L.mla_decode_set_wait_limit.restype = I
             L.mla_status_string.argtypes = [I]
             L.mla_status_string.restype = ctypes.c_char_p
             _lib = L
@@ -357,6 +361,18 @@ def decode_static(q_nope, q_rope, cache, block_table, seq_lens, softmax_scale: f
                                  _stream(stream))
     _check("mla_decode_static", st)
     return out, lse
+
+
+def set_wait_limit(cycles: int = 0) -> None:
+    """Limit of every pipeline wait of the decode kernel, in SM clock cycles, for later calls
+    (0 restores the default of about two seconds)."""
+    _check("mla_decode_set_wait_limit", lib().mla_decode_set_wait_limit(int(cycles)))
+
+
+def inject_stall(enable: bool) -> None:
+    """Test hook: while enabled, decode calls make their MMA issuer wait on a barrier that
+    nothing completes, so that the wait runs out (MLA_ERR_TIMEOUT) without any fault."""
+    _check("mla_decode_inject_stall", lib().mla_decode_inject_stall(1 if enable else 0))
 
 
 def status(ws: Workspace, stream=None) -> int:

@@ -35,6 +35,8 @@ int main(void) {
     CHECK(mla_topk_select(NULL, 64, 64, NULL, B, 8, NULL, NULL, NULL) == MLA_ERR_INVALID_ARG);
     CHECK(mla_prefill_attention(NULL, NULL, NULL, NULL, NULL, 16, H, 0.07f, NULL, NULL, NULL, NULL) ==
           MLA_ERR_INVALID_ARG);
+    CHECK(mla_decode_set_wait_limit(-1) == MLA_ERR_INVALID_ARG);
+    CHECK(mla_decode_set_wait_limit(0) == MLA_OK); /* the default */
     free(buf);
     printf("c abi ok: workspace %zu bytes\n", ws);
     return 0;

@@ -33,7 +33,8 @@ def test_header_declares_the_boundary():
     for must in ("mla_decode_workspace_size", "mla_decode_plan", "mla_decode", "mla_decode_sparse",
                  "mla_decode_status", "mla_status_string", "mla_decode_plan_host",
                  "mla_cache_append", "mla_absorb_query", "mla_project_output", "mla_topk_select",
-                 "mla_prefill_decompress", "mla_prefill_attention"):
+                 "mla_prefill_decompress", "mla_prefill_attention", "mla_decode_set_wait_limit",
+                 "mla_decode_inject_stall", "mla_decode_static"):
         assert must in names
 
 
@@ -75,7 +76,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings(L):
-    for code in range(7):
+    for code in range(8):
         s = L.mla_status_string(code).decode()
         assert s and s != "unknown status"
     assert L.mla_status_string(99).decode() == "unknown status"

@@ -54,6 +54,19 @@ def test_static_entry_split_requests():
         assert_close(out, lse, ref_out, ref_lse, "static split")
 
 
+def test_static_entry_fp8_records_twice():
+    # a ragged batch over an FP8-record cache, with one request long enough to be split
+    c = inputs.make_case(5, 128, [64, 700, 2500, 1, 9000], seed=33, kv_dtype="fp8").to("cuda")
+    ref_out, ref_lse = _with_workspace(c)
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        out, lse = ops.decode_static(c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens,
+                                     c.scale, device_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert_close(out, lse, ref_out, ref_lse, "static fp8")
+
+
 def test_static_entry_rejects_batches_beyond_the_fixed_array():
     c = inputs.make_case(400, 128, [64] * 400, seed=2).to("cuda")
     with pytest.raises(ops.MlaError) as e:
