@@ -94,6 +94,8 @@ enum {
     B_QLD,      // a round of query boxes has landed in the query area
     B_RAW,      // FP8: raw codes + scales of latent slot s (s < 3) or of the other-columns stage (3)
     B_STALL = B_RAW + 4,  // never completed: the injected stall of the timeout test waits on it
+    B_QCP,      // dense / sparse: the query boxes copied into TMEM (tcgen05.cp) have been read
+    B_QDONE,    // dense / sparse: every QK^T of the previous work item has completed
     B_COUNT
 };
 static_assert(B_COUNT <= 32, "barrier area");
@@ -310,7 +312,8 @@ __device__ __forceinline__ PageMask page_mask(const DecodeArgs &a, const WorkIte
 // in slot (g + 2) % 3; the loader issues own(0), own(1), then peer(g), own(g + 2) for
 // g = 0, 1, ...  PV of tile g hands back the peer page's slot first, and own(g + 2) — the
 // page the scores need soonest — takes exactly that slot, ahead of peer(g + 1), which takes
-// own(g)'s.  Each slot alternates own and peer pages.  `fill` counts the slot's loads before
+// own(g)'s.  (Reading the own page first and loading peer(g + 1) first was measured 10 %
+// slower per tile.)  Each slot alternates own and peer pages.  `fill` counts the slot's loads before
 // this one (the phase of its empty barrier).  Own-page and peer-page loads complete on
 // separate full barriers (`full`, phase `phase` = g / 3): the score issuer waits for own
 // pages only, and with one barrier per slot a parity wait for the next own page could be
@@ -491,6 +494,8 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
         mbar_init(bar(base, B_P_FULL), 4);
         mbar_init(bar(base, B_QLD), 1);  // + the boxes' bytes
         mbar_init(bar(base, B_STALL), 1);
+        mbar_init(bar(base, B_QCP), 1);
+        mbar_init(bar(base, B_QDONE), 1);
         misc[1] = 0u;
         fence_mbar_init();
     }
@@ -772,13 +777,69 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
             // injected stall (test of the timeout path): a wait on a barrier nothing completes,
             // before any MMA is issued; it runs out after the wait limit and the CTA winds down
             if (a.stall_test && !wait_bar(c, bar(base, B_STALL), 0u, false)) ok = false;
+            // Dense and sparse tiles: this thread loads each work item's query itself.  The TMA
+            // brings three rounds of three 64-column x 128-head boxes (128-B swizzle; heads at or
+            // past H read zeros) into the shared-memory query area; rounds 0 and 1 (own latent
+            // half, RoPE, the other half's first 64 columns) go on into TMEM by tcgen05.cp, which
+            // reads the swizzled boxes like an MMA operand and is ordered before the MMAs issued
+            // after it; round 2 (the other half's last 192 columns) stays in shared memory as
+            // an operand.  The next round reuses the area once the copies have read it
+            // (tcgen05.commit).  The area and the TMEM columns are refilled only after the
+            // previous item's last QK^T has completed (B_QDONE), and the softmax warps never
+            // wait for any of it.  FP8 records convert the query to fp16 on the way in, which
+            // the softmax warps do (B_Q_READY).
+            uint32_t qld_phase = 0, qcp_phase = 0;
+            auto load_query = [&](int bq) -> bool {
+                const uint32_t qb = bar(base, B_QLD);
+                for (int round = 0; round < 3; ++round) {
+                    mbar_arrive_expect_tx(qb, 3 * kQsBox);
+                    for (int i = 0; i < 3; ++i) {
+                        const int blk = 3 * round + i;  // 0-3 own half, 4 RoPE, 5-8 other half
+                        const uint32_t dst = base + kOffQs + i * kQsBox;
+                        if (blk == 4)
+                            tma_load_3d(dst, &tmap_qr, 0, 0, bq, qb);
+                        else
+                            tma_load_3d(dst, &tmap_qn, blk < 4 ? 256 * (int)rank + 64 * blk : 256 * (int)peer + 64 * (blk - 5),
+                                        0, bq, qb);
+                    }
+                    if (!wait_bar(c, qb, (qld_phase++) & 1u, false)) return false;
+                    if (round == 2) break;
+                    tc_fence_after();
+                    for (int i = 0; i < 3; ++i)
+                        for (int k = 0; k < 4; ++k)
+                            tmem_cp_128x256b(tmem + kColQ + 32u * (3 * round + i) + 8u * k,
+                                             smem_desc_sw128(base + kOffQs + i * kQsBox + k * 32u, 16u, 1024u));
+                    mma_commit(bar(base, B_QCP));
+                    if (!wait_bar(c, bar(base, B_QCP), (qcp_phase++) & 1u, false)) return false;
+                }
+                tc_fence_after();
+                return true;
+            };
             for (int u = cl; u < units && ok; u += ncl) {
                 for (int it = unit_begin[u]; it < unit_begin[u + 1] && ok; ++it) {
                     const WorkItem w = items[it];
                     if (w.t1 <= w.t0) continue;
-                    if (!wait_bar(c, bar(base, B_Q_READY), nitem & 1u, false)) {
-                        ok = false;
-                        break;
+                    if constexpr (kFp8) {
+                        if (!wait_bar(c, bar(base, B_Q_READY), nitem & 1u, false)) {
+                            ok = false;
+                            break;
+                        }
+                    } else {
+                        // the previous item's QK^T must be done with the query area and columns
+                        if (nitem > 0 && !wait_bar(c, bar(base, B_QDONE), (nitem - 1) & 1u, false)) {
+                            ok = false;
+                            break;
+                        }
+                        if (!load_query(w.b)) {
+                            ok = false;
+                            break;
+                        }
+                        // the next item's query is loaded after this one: bring it into L2 now
+                        const int bnext = next_request(unit_begin, items, units, ncl, u, it);
+                        if (bnext >= 0) {
+                            prefetch_l2(a.q_nope + (int64_t)bnext * a.H * kDLatent, (uint32_t)(a.H * kDLatent * 2));
+                            prefetch_l2(a.q_rope + (int64_t)bnext * a.H * kDRope, (uint32_t)(a.H * kDRope * 2));
+                        }
                     }
                     ++nitem;
                     tc_fence_after();
@@ -825,6 +886,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                         }
                         mma_commit(bar(base, B_S_FULL));
                     }
+                    if (!kFp8 && ok) mma_commit(bar(base, B_QDONE));  // this item's QK^T are issued
                 }
             }
             if (!ok) drain_pause();
@@ -996,16 +1058,21 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                     }
                     continue;
                 }
-                if (!q_ready && !load_q(b, false)) {
-                    ok = false;
-                    break;
-                }
-                q_ready = false;
-                // the next item's query is loaded at the end of this one: bring it into L2 now
-                const int bnext = next_request(unit_begin, items, units, ncl, u, it);
-                if (bnext >= 0 && threadIdx.x == 0) {
-                    prefetch_l2(a.q_nope + (int64_t)bnext * a.H * kDLatent, (uint32_t)(a.H * kDLatent * 2));
-                    prefetch_l2(a.q_rope + (int64_t)bnext * a.H * kDRope, (uint32_t)(a.H * kDRope * 2));
+                // FP8 records: this warp group loads and converts the query (dense and sparse
+                // tiles: the MMA issuer does, with tcgen05.cp)
+                int bnext = -1;
+                if constexpr (kFp8) {
+                    if (!q_ready && !load_q(b, false)) {
+                        ok = false;
+                        break;
+                    }
+                    q_ready = false;
+                    // the next item's query is loaded at the end of this one: bring it into L2 now
+                    bnext = next_request(unit_begin, items, units, ncl, u, it);
+                    if (bnext >= 0 && threadIdx.x == 0) {
+                        prefetch_l2(a.q_nope + (int64_t)bnext * a.H * kDLatent, (uint32_t)(a.H * kDLatent * 2));
+                        prefetch_l2(a.q_rope + (int64_t)bnext * a.H * kDRope, (uint32_t)(a.H * kDRope * 2));
+                    }
                 }
                 float m = -INFINITY, l = 0.f;
                 // which rows of each page attend (warp-collective), read one tile ahead
@@ -1037,7 +1104,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(base, B_S_FREE));
                     // the item's last scores are read: its query area is free for the next query
-                    if (t + kTile >= w.t1 && bnext >= 0 && threadIdx.x == 0) q_round(bnext, 0);
+                    if (kFp8 && t + kTile >= w.t1 && bnext >= 0 && threadIdx.x == 0) q_round(bnext, 0);
                     if (vown != ~0ull) {
 #pragma unroll
                         for (int i = 0; i < 64; ++i)
@@ -1179,7 +1246,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                 // ---- the next item's query: this item's QK^T is complete (its last S was
                 // read), so the query columns are free; loading now lets the next item's
                 // QK^T overlap this item's last PV and epilogue
-                if (bnext >= 0) {
+                if (kFp8 && bnext >= 0) {
                     if (!load_q(bnext, true)) {
                         ok = false;
                         break;

@@ -233,6 +233,12 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
         :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
+// Copies 128 rows x 32 bytes from shared memory (described like an MMA operand, so swizzled
+// tiles work) into 128 TMEM lanes x 8 columns at taddr.  Asynchronous like tcgen05.mma and
+// ordered with the MMAs the same thread issues after it; tcgen05.commit tracks it.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" :: "r"(taddr), "l"(sdesc) : "memory");
+}
 // Like mma_commit, but arrives on the barrier at the same shared-memory offset in every CTA
 // of the cluster named in cta_mask.
 __device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
