@@ -12,6 +12,7 @@
 // per-piece partial results (out_i normalised, lse_i), merged afterwards through their
 // log-sum-exp ("Fused Reduction" of weight-absorbed decode, "MLA 最佳算子全景调研" §3).
 #pragma once
+#include <limits.h>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -110,7 +111,10 @@ MLA_HD int64_t req_cost(int32_t tiles) { return tiles > 0 ? tiles + kPieceOverhe
 // comes first, so tile t sits at S_b + overhead + t.  Unit u owns positions
 // [u * per, (u + 1) * per); the last unit also takes anything beyond.
 MLA_HD int32_t unit_of(int64_t pos, int64_t per, int units) {
-    int64_t u = pos / per;
+    // the same quotient in 32-bit arithmetic when it fits (always, for realistic batches): a
+    // 64-bit division is a long instruction sequence on the GPU
+    const int64_t u = (pos >= 0 && pos <= INT32_MAX && per <= INT32_MAX) ? (int64_t)((uint32_t)pos / (uint32_t)per)
+                                                                          : pos / per;
     return u >= units ? units - 1 : (int32_t)u;
 }
 
@@ -167,7 +171,8 @@ MLA_HD void req_piece(const ReqSplit &r, int i, int64_t per, int units, int32_t 
 }
 
 MLA_HD int64_t plan_budget(int64_t total_cost, int units) {
-    int64_t per = (total_cost + units - 1) / units;
+    const int64_t num = total_cost + units - 1;
+    int64_t per = num <= INT32_MAX ? (int64_t)((uint32_t)num / (uint32_t)units) : num / units;
     const int64_t lo = kPieceOverheadTiles + kMinPieceTiles;
     return per < lo ? lo : per;
 }

@@ -107,7 +107,7 @@ class Workspace:
     def __init__(self, B: int, H: int, num_sms: int = 0, device=None):
         self.B, self.H = int(B), int(H)
         self.nbytes = workspace_size(B, H, num_sms)
-        self.buf = torch.empty(self.nbytes, dtype=torch.uint8,
+        self.buf = torch.zeros(self.nbytes, dtype=torch.uint8,
                                device=device or torch.device("cuda", torch.cuda.current_device()))
         self.topk = None
 

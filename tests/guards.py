@@ -15,7 +15,7 @@ HEAD, TAIL = 0xA5, 0x5A
 class Guarded:
     def __init__(self, nbytes, device="cuda"):
         self.nbytes = int(nbytes)
-        self.full = torch.empty(self.nbytes + 2 * GUARD, dtype=torch.uint8, device=device)
+        self.full = torch.zeros(self.nbytes + 2 * GUARD, dtype=torch.uint8, device=device)
         self.full[:GUARD] = HEAD
         self.full[GUARD + self.nbytes:] = TAIL
         self.inner = self.full[GUARD:GUARD + self.nbytes]

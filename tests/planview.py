@@ -24,6 +24,10 @@ def parse(buf, B, H):
     o = _up(o + 8 * B)
     iu = buf[o:o + 4 * max_items].view(np.int32)[:n_items].copy()
     o = _up(o + 4 * max_items)
+    n_split = int(hd[10])
+    sl = buf[o:o + 4 * B].view(np.int32)[:n_split].copy()
+    o = _up(o + 4 * B)
     return dict(req_start=rs, item_unit=iu, topk=topk, units=units, n_items=n_items, max_items=max_items,
                 max_partials=max_partials, per=per, n_partials=n_part, unit_begin=ub,
-                items=items, num_splits=ns, split_base=sb, plan_end=o)
+                items=items, num_splits=ns, split_base=sb, split_list=sl, n_split_reqs=n_split,
+                plan_end=o)

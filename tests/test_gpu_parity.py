@@ -16,7 +16,7 @@ import torch
 
 from mla_latent_kv_17_gb300 import inputs, ops
 from guards import Guarded, guarded_workspace
-from oracle_ref import assert_close, oracle_for
+from oracle_ref import assert_close, assert_close_fp8, oracle_for
 from planview import parse
 
 pytestmark = pytest.mark.gpu
@@ -29,16 +29,18 @@ def _lib():
     ops.lib()
 
 
-def run(case, num_sms=0, ws=None):
+def run(case, ws=None):
+    """Plan and decode through the C ABI into guarded buffers; checks the status word and
+    the guards."""
     c = case
     if ws is None:
-        ws = guarded_workspace(c.B, c.H, num_sms)
+        ws = guarded_workspace(c.B, c.H)
     out_g = Guarded(c.B * c.H * 512 * 4)
     lse_g = Guarded(c.B * c.H * 4)
     out = out_g.inner.view(torch.float32).view(c.B, c.H, 512)
     lse = lse_g.inner.view(torch.float32).view(c.B, c.H)
     topk = c.indices.shape[1] if c.indices is not None else 0
-    ops.plan(ws, c.seq_lens if topk == 0 else None, topk=topk, num_sms=num_sms)
+    ops.plan(ws, c.seq_lens if topk == 0 else None, topk=topk)
     if c.indices is not None:
         ops.decode_sparse(ws, c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens, c.indices,
                           c.scale, out=out, lse=lse)
@@ -54,8 +56,8 @@ def run(case, num_sms=0, ws=None):
     return out, lse, ws
 
 
-def check(case, num_sms=0, what=""):
-    out, lse, _ = run(case, num_sms)
+def check(case, what=""):
+    out, lse, _ = run(case)
     ref_out, ref_lse = oracle_for(case)
     assert_close(out, lse, ref_out, ref_lse, what)
     return out, lse
@@ -85,15 +87,28 @@ def test_dense_zero_length_request():
     assert_close(out, lse, ref_out, ref_lse, "zero-length")
 
 
-@pytest.mark.parametrize("num_sms", [6, 10, 16])
-def test_dense_split_kv_and_combine(num_sms):
-    # few SMs force long requests into several pieces merged by the combine step
-    c = small(3, 128, [3000, 1000, 4097], seed=num_sms)
-    out, lse, ws = run(c, num_sms=num_sms)
+@pytest.mark.parametrize("lens", [[3000, 1000, 4097], [20000, 3, 9000, 129], [70000]])
+def test_dense_split_kv_and_merge(lens):
+    # a few long requests over every SM's worker: each is cut into several pieces whose
+    # partial results the merge step combines
+    c = small(len(lens), 128, lens, seed=len(lens))
+    out, lse, ws = run(c)
     p = parse(ws.buf.cpu().numpy(), c.B, c.H)
     assert p["n_partials"] > 0
     ref_out, ref_lse = oracle_for(c)
-    assert_close(out, lse, ref_out, ref_lse, f"split num_sms={num_sms}")
+    assert_close(out, lse, ref_out, ref_lse, f"split {lens}")
+
+
+def test_repeated_calls_on_one_workspace():
+    # many calls on one workspace, plans of different shapes in between, all against the
+    # oracle
+    ws = guarded_workspace(3, 128)
+    for i, lens in enumerate(([3000, 1000, 4097], [100, 9000, 64], [3000, 1000, 4097])):
+        c = small(3, 128, lens, seed=40 + i)
+        ref_out, ref_lse = oracle_for(c)
+        for _ in range(3):
+            out, lse, _ = run(c, ws=ws)
+            assert_close(out, lse, ref_out, ref_lse, f"call on one workspace {lens}")
 
 
 def _plan_cases():
@@ -166,47 +181,23 @@ def test_one_hot_page_mapping_bit_exact():
 
 
 # ------------------------------------------------------------------------------ fp8
-F16_UNIT = 2.0 ** -11   # unit roundoff of an fp16 operand (11 significant bits)
-
-
-def _fp8_operand_bound(c, b):
-    """Largest score error the fp16 operands of the FP8 path can cause for request b, per
-    head: the dequantised latent x = code x scale reaches the tensor core rounded to fp16
-    (|fp16(x) - x| <= 2^-11 |x|, plus 2^-25 below the normal range); the query is exact in
-    fp16.  So |ds_t| <= scale * sum_c |q_c| (2^-11 |x_tc| + 2^-25), and the log-sum-exp of
-    the scores moves by at most max_t |ds_t|."""
-    L = int(c.seq_lens[b])
-    rec = c.cache.cpu()
-    rows = [(int(c.block_table[b, t // 64]), t % 64) for t in range(L)]
-    codes = torch.stack([rec[p, r, :512] for p, r in rows]).view(torch.float8_e4m3fn).double()
-    sc = torch.stack([rec[p, r, 512:528] for p, r in rows]).contiguous().view(torch.float32).double()
-    x = (codes * sc.repeat_interleave(128, dim=-1)).abs()                       # [L, 512]
-    q = c.q_nope.cpu()[b].double().abs()                                        # [H, 512]
-    return c.scale * (q @ (F16_UNIT * x + 2.0 ** -25).T).max(dim=1).values.numpy()   # [H]
+def check_fp8(case, what=""):
+    """FP8 records: out against the exact dequantisation within 1e-2 + 1e-2|ref|; lse within
+    1e-3, except where the fp16 rounding of the operands alone can move it further (a
+    handful of attended tokens: the L = 1 request of test_fp8_small measured 1.13e-3, one
+    of 76,800 64-token (request, head) pairs 1.01e-3 on a GB300), where the bound is 1e-3
+    plus that rounding's own bound, derived from the inputs (oracle_ref.fp8_operand_bound)."""
+    out, lse, _ = run(case)
+    ref_out, ref_lse = oracle_for(case)
+    return assert_close_fp8(out, lse, ref_out, ref_lse, case, what)
 
 
 def test_fp8_small():
-    """FP8 records against the exact dequantisation (code x scale).  out meets the 1e-2 +
-    1e-2|ref| bound everywhere and lse the 1e-3 bound for requests of 64 tokens or more.
-    With a handful of tokens the lse is (nearly) a single score, whose error is the fp16
-    rounding of the latent summed over 512 products: it can pass 1e-3 (the L = 1 request
-    of this case measured 1.13e-3 on a GB300), so there lse is held to 1e-3 plus the
-    operand-rounding bound derived from the inputs."""
-    c = small(4, 128, [1, 64, 65, 700], seed=8, kv_dtype="fp8")
-    out, lse, _ = run(c)
-    ref_out, ref_lse = oracle_for(c)
-    o = out.double().cpu().numpy()
-    l_ = lse.double().cpu().numpy()
-    assert np.all(np.abs(o - ref_out) <= 1e-2 + 1e-2 * np.abs(ref_out)), "fp8 out"
-    for b in range(c.B):
-        err = np.abs(l_[b] - ref_lse[b])
-        bound = 1e-3 if int(c.seq_lens[b]) >= 64 else 1e-3 + _fp8_operand_bound(c, b)
-        assert np.all(err <= bound), (b, err.max(), np.min(bound))
+    check_fp8(small(4, 128, [1, 64, 65, 700], seed=8, kv_dtype="fp8"), "fp8")
 
 
 def test_fp8_split():
-    c = small(2, 64, [2500, 3000], seed=9, kv_dtype="fp8")
-    check(c, num_sms=4, what="fp8 split")
+    check_fp8(small(2, 64, [2500, 3000], seed=9, kv_dtype="fp8"), "fp8 split")
 
 
 # ------------------------------------------------------------------------------ sparse
@@ -247,7 +238,7 @@ def test_sparse_all_indices_equals_dense():
 
 
 def test_sparse_split():
-    check(_sparse(2, 128, [9000, 5000], topk=2048, seed=5), num_sms=6, what="sparse split")
+    check(_sparse(2, 128, [9000, 5000], topk=2048, seed=5), what="sparse split")
 
 
 def test_sparse_page_runs_and_near_runs():
@@ -262,25 +253,30 @@ def test_sparse_page_runs_and_near_runs():
     check(c, what="sparse page runs")
 
 
-@pytest.mark.parametrize("L,num_sms", [(896, 2), (1024, 0), (2000, 6)])
-def test_sparse_contiguous_equals_dense_bitwise(L, num_sms):
+@pytest.mark.parametrize("L", [896, 1024, 2000, 30000])
+def test_sparse_contiguous_equals_dense_bitwise(L):
     # indices 0..L-1 make the sparse path gather exactly the rows the dense path loads as
     # page boxes, into the same layout, so the two results are bitwise equal; long items
     # also exercise every latent-buffer phase while the gathered loads run slowly
     c = small(1, 128, [L], seed=7)
-    d_out, d_lse, _ = run(c, num_sms=num_sms)
+    d_out, d_lse, _ = run(c)
     c.indices = torch.arange(L, dtype=torch.int32)[None].cuda()
-    s_out, s_lse, _ = run(c, num_sms=num_sms)
+    s_out, s_lse, _ = run(c)
     assert torch.equal(d_out, s_out) and torch.equal(d_lse, s_lse)
 
 
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
 @pytest.mark.parametrize("lens", [[130, 130, 130], [64, 64, 64, 64], [4262, 623, 662, 2157]])
-def test_odd_page_items_back_to_back_on_one_unit(kv, lens):
-    # one work unit takes every item in turn; odd page counts leave the second page of each
-    # item's last tile absent, so every buffer stage sees loads that carry no data
-    c = inputs.make_case(len(lens), 128, lens, seed=11, kv_dtype=kv).to("cuda")
-    check(c, num_sms=2, what=f"{kv} {lens}")
+def test_odd_page_items_back_to_back(kv, lens):
+    # many copies of the lengths, so that every worker takes several items in turn; odd page
+    # counts leave the second page of each item's last tile absent, so every buffer stage
+    # sees loads that carry no data
+    reps = max(1, 600 // sum((L + 127) // 128 for L in lens))
+    c = inputs.make_case(len(lens) * reps, 128, lens * reps, seed=11, kv_dtype=kv).to("cuda")
+    if kv == "fp8":
+        check_fp8(c, f"{kv} {lens}")
+    else:
+        check(c, what=f"{kv} {lens}")
 
 
 # ------------------------------------------------------------------------------ errors
@@ -296,6 +292,14 @@ def test_out_of_range_page_is_reported_not_faulted():
     assert ops.status(ws) == 0           # cleared after reading
 
 
+def test_plan_mismatch_is_reported():
+    c = small(2, 16, [100, 100], seed=8)
+    ws = ops.Workspace(2, 16)
+    ops.plan(ws, None, topk=64)          # a sparse plan used for dense decode
+    ops.decode(ws, c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens, c.scale)
+    assert ops.status(ws) == 3
+
+
 def test_out_of_range_sparse_index_is_reported():
     c = _sparse(1, 16, [100], topk=64, seed=7)
     idx = c.indices.clone()
@@ -307,14 +311,6 @@ def test_out_of_range_sparse_index_is_reported():
     assert ops.status(ws) == 5
 
 
-def test_plan_mismatch_is_reported():
-    c = small(2, 16, [100, 100], seed=8)
-    ws = ops.Workspace(2, 16)
-    ops.plan(ws, None, topk=64)          # a sparse plan used for dense decode
-    ops.decode(ws, c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens, c.scale)
-    assert ops.status(ws) == 3
-
-
 # ------------------------------------------------------------------------------ full size
 # Every (request, head, column) of each workload at its full size, in the launch
 # configuration the benchmark times, against the oracle.
@@ -322,7 +318,10 @@ def _full(name):
     c = inputs.make_workload(name, device="cuda")
     out, lse, _ = run(c)
     ref_out, ref_lse = oracle_for(c)
-    assert_close(out, lse, ref_out, ref_lse, name)
+    if c.kv_dtype == "fp8":
+        assert_close_fp8(out, lse, ref_out, ref_lse, c, name)
+    else:
+        assert_close(out, lse, ref_out, ref_lse, name)
 
 
 def test_full_tiny():
