@@ -331,6 +331,36 @@ __device__ __forceinline__ DhSlot dh_slot(uint32_t g, int e) {
     return DhSlot{slot, fill, B_DH_FULL + 2 * slot + e, q};
 }
 
+// Rare steps of the softmax warps, kept out of line: the per-tile loop then stays small
+// enough for the instruction cache, which the loaders and MMA issuers share.
+// O row of this thread (256 fp32 columns at taddr, warp-collective) times al.
+__device__ __noinline__ void rescale_o_row(uint32_t taddr, float al) {
+#pragma unroll 1
+    for (int cb = 0; cb < 256; cb += 32) {
+        uint32_t o[32];
+        tmem_ld32(taddr + cb, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * al);
+        tmem_st32(taddr + cb, o);
+    }
+    tmem_wait_st();
+}
+template <bool kF16>
+__device__ __noinline__ void scale_row_ool(uint4 *prow, float f) {
+    scale_row<kF16>(prow, f);
+}
+// Zeroes the rows of `zero` in a 64-row latent-half page (4 boxes); the 128 threads of the
+// softmax warps share its 16-B chunks (thread h takes chunks h, h + 128, ...).
+__device__ __noinline__ void zero_rows(uint8_t *dh, uint64_t zero, int h) {
+    const int z1 = 64 - __clzll((long long)zero);  // rows below the last one to zero
+    for (int i = h; i < z1 * 32; i += 128) {
+        const int row = i / 32, ch = i % 32;
+        if ((zero >> row) & 1ull)
+            *reinterpret_cast<uint4 *>(dh + (ch / 8) * kBox + row * 128 + (ch % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
 // Walks the tiles of this cluster's work in order: units cl, cl + ncl, ..., their items
 // (those with tokens), and each item's 128-token tiles.
 struct TileCursor {
@@ -1193,18 +1223,17 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                     if (__any_sync(0xffffffffu, fown < 1.f)) {
                         if (lane == 0) bulk_wait_read_all();
                         __syncwarp();
-                        if (fown < 1.f) scale_row<kFp8>(reinterpret_cast<uint4 *>(ps + rank * kPPage + h * 128), fown);
+                        if (fown < 1.f) scale_row_ool<kFp8>(reinterpret_cast<uint4 *>(ps + rank * kPPage + h * 128), fown);
                         wrote = true;
                     }
                     if (fpeer < 1.f) {
-                        scale_row<kFp8>(reinterpret_cast<uint4 *>(ps + peer * kPPage + h * 128), fpeer);
+                        scale_row_ool<kFp8>(reinterpret_cast<uint4 *>(ps + peer * kPPage + h * 128), fpeer);
                         wrote = true;
                     }
                     // zero the rows decided in part A
                     for (int p = 0; p < 2 && need_zero; ++p) {
                         const uint64_t zero = zmask[p];
                         if (zero == 0ull) continue;
-                        const int z1 = 64 - __clzll((long long)zero);  // rows below the last one to zero
                         const DhSlot d = dh_slot(g, p == (int)rank ? 0 : 1);
                         const int ds = d.slot;
                         // wait for the slot's load (or its empty arrival) to land first
@@ -1212,13 +1241,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                             ok = false;
                             break;
                         }
-                        uint8_t *dh = gbase + kOffDh + ds * kDhBytes;
-                        for (int i = h; i < z1 * 32; i += 128) {  // 16-B chunks over 4 boxes
-                            const int row = i / 32, ch = i % 32;
-                            if ((zero >> row) & 1ull)
-                                *reinterpret_cast<uint4 *>(dh + (ch / 8) * kBox + row * 128 + (ch % 8) * 16) =
-                                    make_uint4(0u, 0u, 0u, 0u);
-                        }
+                        zero_rows(gbase + kOffDh + ds * kDhBytes, zero, h);
                         wrote = true;
                     }
                     if (!ok) break;
@@ -1227,16 +1250,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                     // probability tile was rewritten)
                     if (__any_sync(0xffffffffu, resc_o)) {
                         tc_fence_after();
-                        const float al = resc_o ? alpha : 1.f;
-                        for (int cb = 0; cb < 256; cb += 32) {
-                            uint32_t o[32];
-                            tmem_ld32(trow + kColO + cb, o);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * al);
-                            tmem_st32(trow + kColO + cb, o);
-                        }
-                        tmem_wait_st();
+                        rescale_o_row(trow + kColO, resc_o ? alpha : 1.f);
                     }
                     tc_fence_before();
                     __syncwarp();
