@@ -110,8 +110,9 @@ struct Ctx {
 __device__ __forceinline__ uint32_t bar(uint32_t base, int i) { return base + kOffBar + 8u * i; }
 
 // Bounded wait by the calling thread.  False on timeout (recorded) or when another role
-// has already given up.
-__device__ bool wait_bar(const Ctx &c, uint32_t b, uint32_t parity, bool cluster_scope) {
+// has already given up.  The first test is inline; the polling loop is out of line, which
+// keeps every role's code small in the instruction cache.
+__device__ __noinline__ bool wait_bar_slow(const Ctx c, uint32_t b, uint32_t parity, bool cluster_scope) {
     const long long t0 = (long long)clock64_now();
     for (uint32_t i = 0;; ++i) {
         const bool ok = cluster_scope ? mbar_try_wait_cluster(b, parity) : mbar_try_wait(b, parity);
@@ -125,6 +126,11 @@ __device__ bool wait_bar(const Ctx &c, uint32_t b, uint32_t parity, bool cluster
             }
         }
     }
+}
+
+__device__ __forceinline__ bool wait_bar(const Ctx &c, uint32_t b, uint32_t parity, bool cluster_scope) {
+    const bool ok = cluster_scope ? mbar_try_wait_cluster(b, parity) : mbar_try_wait(b, parity);
+    return ok || wait_bar_slow(c, b, parity, cluster_scope);
 }
 
 // All lanes of a warp wait; the outcome is made warp-uniform.
@@ -358,6 +364,32 @@ __device__ __noinline__ void zero_rows(uint8_t *dh, uint64_t zero, int h) {
         const int row = i / 32, ch = i % 32;
         if ((zero >> row) & 1ull)
             *reinterpret_cast<uint4 *>(dh + (ch / 8) * kBox + row * 128 + (ch % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// Epilogue of a work item (out of line): this thread's O row (TMEM columns at tcol) times inv,
+// staged through its own 128-B row of stg so that each warp store covers whole lines; warp w
+// writes back rows 32w .. 32w + 31 of the item's output (row 0 at obase).
+__device__ __noinline__ void store_rows(uint32_t tcol, uint8_t *stg, float *obase, float inv, int h, int warp,
+                                        int lane, int H) {
+#pragma unroll 1
+    for (int cb = 0; cb < 256; cb += 32) {
+        uint32_t o[32];
+        tmem_ld32(tcol + cb, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4 *>(stg + h * 128 + ((q ^ (h & 7)) * 16)) =
+                make_float4(__uint_as_float(o[4 * q]) * inv, __uint_as_float(o[4 * q + 1]) * inv,
+                            __uint_as_float(o[4 * q + 2]) * inv, __uint_as_float(o[4 * q + 3]) * inv);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int row = warp * 32 + 4 * i + (lane >> 3), q = lane & 7;
+            const float4 v = *reinterpret_cast<const float4 *>(stg + row * 128 + ((q ^ (row & 7)) * 16));
+            if (row < H) *reinterpret_cast<float4 *>(obase + (int64_t)row * kDLatent + cb + 4 * q) = v;
+        }
+        __syncwarp();
     }
 }
 
@@ -1283,24 +1315,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                     float *obase = orow - (int64_t)h * kDLatent;  // row 0 of this item's output
                     if (lane == 0) bulk_wait_read_all();  // this warp's last message has left these rows
                     __syncwarp();
-                    for (int cb = 0; cb < 256; cb += 32) {
-                        uint32_t o[32];
-                        tmem_ld32(trow + kColO + cb, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            *reinterpret_cast<float4 *>(stg + h * 128 + ((q ^ (h & 7)) * 16)) =
-                                make_float4(__uint_as_float(o[4 * q]) * inv, __uint_as_float(o[4 * q + 1]) * inv,
-                                            __uint_as_float(o[4 * q + 2]) * inv, __uint_as_float(o[4 * q + 3]) * inv);
-                        __syncwarp();
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const int row = warp * 32 + 4 * i + (lane >> 3), q = lane & 7;
-                            const float4 v = *reinterpret_cast<const float4 *>(stg + row * 128 + ((q ^ (row & 7)) * 16));
-                            if (row < a.H) *reinterpret_cast<float4 *>(obase + (int64_t)row * kDLatent + cb + 4 * q) = v;
-                        }
-                        __syncwarp();
-                    }
+                    store_rows(trow + kColO, stg, obase, inv, h, warp, lane, a.H);
                 }
                 if (rank == 0 && h < a.H) *lrow = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
                 ++nitem;
