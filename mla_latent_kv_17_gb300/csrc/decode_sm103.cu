@@ -60,12 +60,16 @@ constexpr uint32_t kPPage = 128 * 128;           // 128 heads x 64 tokens bf16, 
 constexpr uint32_t kRlBytes = 1024;              // r[128] and sum[128], fp32
 constexpr uint32_t kPBytes = 2 * kPPage + 2 * kRlBytes;
 constexpr uint32_t kMsgBytes = kPPage + kRlBytes;
-constexpr int kThreads = 256;         // dense and sparse tiles
+constexpr int kThreads = 256;         // dense tiles
+constexpr int kThreadsSparse = 288;   // sparse tiles: + a loader warp for the peer pages
 constexpr int kThreadsFp8 = 384;      // FP8 records: + raw-load and expansion warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 320;
 constexpr uint32_t kColQRope = kColQ + 128, kColQOther = kColQ + 160;
 constexpr float kRescaleLog2 = 8.0f;
+// Sparse tiles: which stages copy their (non-contiguous) rows through the load/store path
+// instead of TMA gathers: the own page's latent half, the peer page's, the other columns.
+constexpr bool kSparseLsuOwn = true, kSparseLsuPeer = true, kSparseLsuOth = true;
 
 constexpr uint32_t kOffDh = 0;
 constexpr uint32_t kOffOth = kOffDh + kDhSlots * kDhBytes;
@@ -266,22 +270,28 @@ __device__ SparseRows sparse_rows(const DecodeArgs &a, const WorkItem &w, int t,
     return SparseRows{rows[0], rows[1], __ballot_sync(0xffffffffu, ok[0]), __ballot_sync(0xffffffffu, ok[1])};
 }
 
-// Gathers the 64 rows of `r` (columns x_of(i) .. + 63 for box i < nbox) into consecutive
-// 8-KB boxes at dst, four rows per tile::gather4; lanes 0-15 take row groups, the two
-// half-warps alternate boxes.  When the 64 rows are one whole cache page in order (a run of
-// consecutive positions, as the local window of a top-k list gives), 64-row boxes of the
-// page tensor map fetch them instead: a gather4 moves 512 B in ~70 cycles of an SM's TMA
-// unit, a box 8 KB in ~20.  Warp-collective.
-template <typename XOf>
-__device__ __forceinline__ void gather_rows(const SparseRows &r, int lane, uint32_t dst, const void *tmap,
-                                            const void *tmap_page, int nbox, XOf x_of, uint32_t bar) {
+// Sparse tiles move a page's 64 rows in one of three ways.  When they are one whole cache
+// page in order (a run of consecutive positions, as the local window of a top-k list gives),
+// 64-row boxes of the page tensor map fetch them (~20 cycles of the SM's TMA unit per 8 KB).
+// Otherwise either the TMA gathers them four rows at a time (tile::gather4: ~70 cycles of the
+// TMA unit per 512 B, the limit of a TMA-only sparse tile) or the loading warp copies them in
+// 16-B pieces through the load/store path (cp.async), which runs beside the TMA unit.
+__device__ __forceinline__ bool rows_whole(const SparseRows &r, int lane) {
     const int32_t r00 = __shfl_sync(0xffffffffu, r.row0, 0);
-    const bool whole = r.lo == 0xffffffffu && r.hi == 0xffffffffu && (r00 & (kPageRows - 1)) == 0 &&
-                       __all_sync(0xffffffffu, r.row0 == r00 + lane && r.row1 == r00 + 32 + lane);
-    if (whole) {
-        if (lane < nbox) tma_load_2d(dst + lane * kBox, tmap_page, x_of(lane), r00, bar);
-        return;
-    }
+    return r.lo == 0xffffffffu && r.hi == 0xffffffffu && (r00 & (kPageRows - 1)) == 0 &&
+           __all_sync(0xffffffffu, r.row0 == r00 + lane && r.row1 == r00 + 32 + lane);
+}
+// Whole page: box i (columns x_of(i) .. + 63) by lane i.
+template <typename XOf>
+__device__ __forceinline__ void page_boxes(const SparseRows &r, int lane, uint32_t dst, const void *tmap_page, int nbox,
+                                           XOf x_of, uint32_t bar) {
+    const int32_t r00 = __shfl_sync(0xffffffffu, r.row0, 0);
+    if (lane < nbox) tma_load_2d(dst + lane * kBox, tmap_page, x_of(lane), r00, bar);
+}
+// TMA gathers: lanes 0-15 take groups of four rows, the two half-warps alternate boxes.
+template <typename XOf>
+__device__ __forceinline__ void gather_rows(const SparseRows &r, int lane, uint32_t dst, const void *tmap, int nbox,
+                                            XOf x_of, uint32_t bar) {
     const int l = lane & 15;
     int32_t r4[4];
 #pragma unroll
@@ -292,6 +302,46 @@ __device__ __forceinline__ void gather_rows(const SparseRows &r, int lane, uint3
     }
     for (int i = lane >> 4; i < nbox; i += 2)
         tma_gather4(dst + i * kBox + 512u * l, tmap, x_of(i), r4[0], r4[1], r4[2], r4[3], bar);
+}
+// Load/store path: lane l copies the 16-B piece l % 8 of row 4 k + l / 8 of every box, into
+// its 128-B-swizzled place.  The caller waits for the copies (cp_async_wait_all) and fences
+// them for the tensor cores before it signals the stage.
+template <typename XOf>
+__device__ __forceinline__ void copy_rows_lsu(const SparseRows &r, int lane, uint32_t dst,
+                                              const unsigned char *cache, int nbox, XOf x_of) {
+    const int ch = lane & 7;
+#pragma unroll 1
+    for (int k = 0; k < 16; ++k) {
+        const int row = 4 * k + (lane >> 3);
+        const int32_t R = __shfl_sync(0xffffffffu, k < 8 ? r.row0 : r.row1, row & 31);
+        const unsigned char *src = cache + (int64_t)R * (kDEntry * 2) + ch * 16;
+        const uint32_t d = dst + row * 128 + ((ch ^ (row & 7)) << 4);
+#pragma unroll
+        for (int i = 0; i < nbox; ++i) cp_async16(d + i * kBox, src + x_of(i) * 2);
+    }
+}
+// Fills one stage of sparse rows (nbox boxes at dst) and completes its barrier `bar` (count
+// 1): whole pages and, unless `lsu`, the TMA gathers complete it by their bytes; the load/store
+// copies by an arrival once they have landed.  Warp-collective.
+template <typename XOf>
+__device__ __forceinline__ void sparse_stage(const SparseRows &r, int lane, uint32_t dst, const void *tmap,
+                                             const void *tmap_page, const unsigned char *cache, int nbox, XOf x_of,
+                                             uint32_t bar, bool lsu) {
+    const bool whole = rows_whole(r, lane);
+    if (whole || !lsu) {
+        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)nbox * kBox);
+        __syncwarp();
+        if (whole)
+            page_boxes(r, lane, dst, tmap_page, nbox, x_of, bar);
+        else
+            gather_rows(r, lane, dst, tmap, nbox, x_of, bar);
+        return;
+    }
+    copy_rows_lsu(r, lane, dst, cache, nbox, x_of);
+    cp_async_wait_all();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
 }
 
 // Which of page p's 64 rows attend (`valid`) and how many rows of the page lie inside the
@@ -324,13 +374,21 @@ __device__ __forceinline__ PageMask page_mask(const DecodeArgs &a, const WorkIte
 // separate full barriers (`full`, phase `phase` = g / 3): the score issuer waits for own
 // pages only, and with one barrier per slot a parity wait for the next own page could be
 // satisfied by an older phase while the peer page between them is still loading.
+// Sparse tiles load own and peer pages from two warps; there each slot has one of them as its
+// only user (own pages alternate slots 0 and 1, peer pages use slot 2), so that each warp's
+// parity waits on a slot follow its phases one by one.
 struct DhSlot {
     int slot;
     uint32_t fill;
     int full;        // barrier index
     uint32_t phase;
 };
+template <bool kSplitSlots>
 __device__ __forceinline__ DhSlot dh_slot(uint32_t g, int e) {
+    if constexpr (kSplitSlots) {
+        if (e == 0) return DhSlot{(int)(g & 1u), g >> 1, B_DH_FULL + 2 * (int)(g & 1u), g >> 1};
+        return DhSlot{2, g, B_DH_FULL + 2 * 2 + 1, g};
+    }
     const uint32_t q = g / 3u, r = g % 3u;
     const int slot = e == 0 ? (int)r : (int)((r + 2u) % 3u);
     const uint32_t fill = e == 0 ? 2u * q + (r == 2u ? 1u : 0u) : 2u * q + (r != 0u ? 1u : 0u);
@@ -517,7 +575,7 @@ __device__ bool fp8_jobs(const TileCursor &start, int which, F &&f) {
 // FP8 RoPE (bf16, 128-B swizzle); tmap_qn / tmap_qr:
 // the queries (64 columns x 128 heads of one request, 128-B swizzle).
 template <int kMode>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMode == 2 ? kThreadsFp8 : kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMode == 2 ? kThreadsFp8 : kMode == 1 ? kThreadsSparse : kThreads, 1)
 decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_sc,
                     const __grid_constant__ CUtensorMap tmap_rope, const __grid_constant__ CUtensorMap tmap_qn,
                     const __grid_constant__ CUtensorMap tmap_qr, DecodeArgs a) {
@@ -612,7 +670,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                 half = (int)peer;
                 full_bar = bar(base, B_OTH_FULL);
             } else {
-                const DhSlot d = dh_slot(g, kind);
+                const DhSlot d = dh_slot<kSparse>(g, kind);
                 raw_bar = B_RAW + d.slot;
                 raw_phase = d.fill;
                 region = kOffDh + d.slot * kDhBytes;
@@ -673,7 +731,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                     return true;
                 }
                 const PageRef pg = page_of(a, t.w, t.t, kind == 0 ? (int)rank : (int)peer);
-                const DhSlot d = dh_slot(g, kind);
+                const DhSlot d = dh_slot<kSparse>(g, kind);
                 if (d.fill > 0 && !wait_bar(c, bar(base, B_DH_EMPTY + d.slot), (d.fill - 1u) & 1u, false))
                     return false;
                 const uint32_t rb = bar(base, B_RAW + d.slot), dst = base + kOffDh + d.slot * kDhBytes;
@@ -691,29 +749,30 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
             });
             if (!ok) drain_pause();
         }
-    } else if (warp == 4 || warp == 7) {
-        // ------------------------------------------------------------ TMA loaders (whole warps)
+    } else if (warp == 4 || warp == 7 || (kSparse && warp == 8)) {
+        // ------------------------------------------------------------ loaders (whole warps)
         TileCursor cur, nx;
         cur.begin(unit_begin, items, units, cl, ncl);
         nx = cur;
         nx.next();
-        if (warp == 4) {
+        if (warp == 4 || warp == 8) {
             // own latent half of both pages, in the order own(0), own(1), peer(0), own(2),
-            // peer(1), own(3), ...
+            // peer(1), own(3), ...  Sparse tiles split the sequence over two warps (own pages:
+            // warp 4, peer pages: warp 8), since a load/store-path copy holds its warp until
+            // it has landed.
             const int xown = 256 * (int)rank;
             // loads page (rank if e == 0, else peer) of tile g at cursor position t
             // (sparse: the rows r were resolved one load ahead)
             auto load = [&](const TileCursor &t, uint32_t g, int e, const SparseRows &r) -> bool {
                 const int p = e == 0 ? (int)rank : (int)peer;
-                const DhSlot d = dh_slot(g, e);
+                const DhSlot d = dh_slot<kSparse>(g, e);
                 const uint32_t fb = bar(base, d.full), dst = base + kOffDh + d.slot * kDhBytes;
                 if constexpr (kSparse) {
                     if (d.fill > 0 && !warp_wait(c, bar(base, B_DH_EMPTY + d.slot), (d.fill - 1u) & 1u, false))
                         return false;
                     if (t.t + kPageRows * p < t.w.t1) {
-                        if (lane == 0) mbar_arrive_expect_tx(fb, kDhBytes);
-                        __syncwarp();
-                        gather_rows(r, lane, dst, &tmap, &tmap_sc, 4, [&](int i) { return xown + 64 * i; }, fb);
+                        sparse_stage(r, lane, dst, &tmap, &tmap_sc, a.cache, 4, [&](int i) { return xown + 64 * i; }, fb,
+                                     e == 0 ? kSparseLsuOwn : kSparseLsuPeer);
                     } else if (lane == 0) {
                         mbar_arrive(fb);
                     }
@@ -737,6 +796,12 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
             // the sequence of loads: own(0), own(1), then peer(g), own(g + 2) for g = 0, 1, ...
             TileCursor co = cur;  // next own page: tile go; cur: next peer page, tile gp
             uint32_t go = 0, gp = 0;
+            if (kSparse) {
+                if (warp == 4)
+                    cur.u = cur.units;  // own pages only
+                else
+                    co.u = co.units;  // peer pages only
+            }
             int step = 0;
             struct Ld {
                 int e;  // -1: none left
@@ -800,9 +865,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                         break;
                     }
                     if (cur.t + kPageRows * (int)rank < cur.w.t1) {
-                        if (lane == 0) mbar_arrive_expect_tx(fb, kOthBoxes * kBox);
-                        __syncwarp();
-                        gather_rows(r, lane, dst, &tmap, &tmap_sc, kOthBoxes, x_of, fb);
+                        sparse_stage(r, lane, dst, &tmap, &tmap_sc, a.cache, kOthBoxes, x_of, fb, kSparseLsuOth);
                     } else if (lane == 0) {
                         mbar_arrive(fb);
                     }
@@ -933,7 +996,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                             }
                         }
                         mma_commit(bar(base, B_OTH_EMPTY));
-                        const DhSlot dso = dh_slot(g, 0);
+                        const DhSlot dso = dh_slot<kSparse>(g, 0);
                         const int ds = dso.slot;
                         if (!wait_bar(c, bar(base, dso.full), dso.phase & 1u, false)) {
                             ok = false;
@@ -975,7 +1038,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                         const uint32_t ps = base + kOffP;
                         for (int e = 1; e >= 0; --e) {  // peer page, then own page
                             const int p = e == 0 ? (int)rank : (int)peer;
-                            const DhSlot d = dh_slot(g, e);
+                            const DhSlot d = dh_slot<kSparse>(g, e);
                             const int ds = d.slot;
                             const int ksteps = min(4, max(0, (nvalid - kPageRows * p + 15) / 16));
                             // wait even for a page that is absent (ksteps 0): the buffer is handed
@@ -1266,7 +1329,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                     for (int p = 0; p < 2 && need_zero; ++p) {
                         const uint64_t zero = zmask[p];
                         if (zero == 0ull) continue;
-                        const DhSlot d = dh_slot(g, p == (int)rank ? 0 : 1);
+                        const DhSlot d = dh_slot<kSparse>(g, p == (int)rank ? 0 : 1);
                         const int ds = d.slot;
                         // wait for the slot's load (or its empty arrival) to land first
                         if (!warp_wait(c, bar(base, d.full), d.phase & 1u, false)) {
@@ -1477,7 +1540,7 @@ cudaError_t launch_decode_sm103(const DecodeArgs &a, int num_clusters, cudaStrea
         if (!make_tmap(&tm_page, a.cache, a.num_pages, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)kDEntry * 2, 64,
                        kPageRows, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
-        return launch_pdl(decode_sm103_kernel<1>, grid, kThreads, stream, tm, tm_page, tm, tm_qn, tm_qr, a);
+        return launch_pdl(decode_sm103_kernel<1>, grid, kThreadsSparse, stream, tm, tm_page, tm, tm_qn, tm_qr, a);
     } else {
         // 64-row boxes: one page
         if (!make_tmap(&tm, a.cache, a.num_pages, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)kDEntry * 2, 64,

@@ -141,6 +141,12 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int3
 }
 // Four rows (tensor rows r0..r3, columns x .. x + box width) of a 2-D tensor whose box is
 // one row high, written to consecutive rows at dst with the tensor map's swizzle.
+// 16-B asynchronous copy global -> shared through the load/store path (cached in L2 only),
+// tracked per thread; cp_async_wait_all() waits for all of the thread's copies.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int32_t x, int32_t r0, int32_t r1,
                                             int32_t r2, int32_t r3, uint32_t bar) {
     asm volatile(
