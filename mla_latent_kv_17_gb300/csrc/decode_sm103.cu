@@ -61,15 +61,16 @@ constexpr uint32_t kRlBytes = 1024;              // r[128] and sum[128], fp32
 constexpr uint32_t kPBytes = 2 * kPPage + 2 * kRlBytes;
 constexpr uint32_t kMsgBytes = kPPage + kRlBytes;
 constexpr int kThreads = 256;         // dense tiles
-constexpr int kThreadsSparse = 288;   // sparse tiles: + a loader warp for the peer pages
+constexpr int kThreadsSparse = 384;   // sparse tiles: loader warps in pairs (see the loaders)
 constexpr int kThreadsFp8 = 384;      // FP8 records: + raw-load and expansion warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 320;
 constexpr uint32_t kColQRope = kColQ + 128, kColQOther = kColQ + 160;
 constexpr float kRescaleLog2 = 8.0f;
-// Sparse tiles: which stages copy their (non-contiguous) rows through the load/store path
-// instead of TMA gathers: the own page's latent half, the peer page's, the other columns.
-constexpr bool kSparseLsuOwn = true, kSparseLsuPeer = true, kSparseLsuOth = true;
+// Sparse tiles: how many boxes of each stage (own page's latent half: 4, peer page's: 4, other
+// columns: 5) copy their non-contiguous rows through the load/store path; the TMA gathers the
+// rest.
+constexpr int kSparseLsuOwn = 4, kSparseLsuPeer = 4, kSparseLsuOth = 5;
 
 constexpr uint32_t kOffDh = 0;
 constexpr uint32_t kOffOth = kOffDh + kDhSlots * kDhBytes;
@@ -288,10 +289,11 @@ __device__ __forceinline__ void page_boxes(const SparseRows &r, int lane, uint32
     const int32_t r00 = __shfl_sync(0xffffffffu, r.row0, 0);
     if (lane < nbox) tma_load_2d(dst + lane * kBox, tmap_page, x_of(lane), r00, bar);
 }
-// TMA gathers: lanes 0-15 take groups of four rows, the two half-warps alternate boxes.
+// TMA gathers of boxes i0 .. nbox - 1: lanes 0-15 take groups of four rows, the two
+// half-warps alternate boxes.
 template <typename XOf>
-__device__ __forceinline__ void gather_rows(const SparseRows &r, int lane, uint32_t dst, const void *tmap, int nbox,
-                                            XOf x_of, uint32_t bar) {
+__device__ __forceinline__ void gather_rows(const SparseRows &r, int lane, uint32_t dst, const void *tmap, int i0,
+                                            int nbox, XOf x_of, uint32_t bar) {
     const int l = lane & 15;
     int32_t r4[4];
 #pragma unroll
@@ -300,18 +302,18 @@ __device__ __forceinline__ void gather_rows(const SparseRows &r, int lane, uint3
         const int32_t a0 = __shfl_sync(0xffffffffu, r.row0, j & 31), a1 = __shfl_sync(0xffffffffu, r.row1, j & 31);
         r4[k] = j < 32 ? a0 : a1;
     }
-    for (int i = lane >> 4; i < nbox; i += 2)
+    for (int i = i0 + (lane >> 4); i < nbox; i += 2)
         tma_gather4(dst + i * kBox + 512u * l, tmap, x_of(i), r4[0], r4[1], r4[2], r4[3], bar);
 }
-// Load/store path: lane l copies the 16-B piece l % 8 of row 4 k + l / 8 of every box, into
-// its 128-B-swizzled place.  The caller waits for the copies (cp_async_wait_all) and fences
-// them for the tensor cores before it signals the stage.
+// Load/store path, rows 32 half .. 32 half + 31: lane l copies the 16-B piece l % 8 of row
+// 4 k + l / 8 of every box, into its 128-B-swizzled place.  The caller waits for the copies
+// (cp_async_wait_all) and fences them for the tensor cores before it signals the stage.
 template <typename XOf>
 __device__ __forceinline__ void copy_rows_lsu(const SparseRows &r, int lane, uint32_t dst,
-                                              const unsigned char *cache, int nbox, XOf x_of) {
+                                              const unsigned char *cache, int nbox, XOf x_of, int half) {
     const int ch = lane & 7;
 #pragma unroll 1
-    for (int k = 0; k < 16; ++k) {
+    for (int k = 8 * half; k < 8 * half + 8; ++k) {
         const int row = 4 * k + (lane >> 3);
         const int32_t R = __shfl_sync(0xffffffffu, k < 8 ? r.row0 : r.row1, row & 31);
         const unsigned char *src = cache + (int64_t)R * (kDEntry * 2) + ch * 16;
@@ -320,24 +322,35 @@ __device__ __forceinline__ void copy_rows_lsu(const SparseRows &r, int lane, uin
         for (int i = 0; i < nbox; ++i) cp_async16(d + i * kBox, src + x_of(i) * 2);
     }
 }
-// Fills one stage of sparse rows (nbox boxes at dst) and completes its barrier `bar` (count
-// 1): whole pages and, unless `lsu`, the TMA gathers complete it by their bytes; the load/store
-// copies by an arrival once they have landed.  Warp-collective.
+// Fills one stage of sparse rows (nbox boxes at dst), shared by a pair of warps (half 0 and
+// 1), each of which arrives once on the stage's barrier `bar` (count 2).  A whole page comes
+// in 64-row boxes, issued by half 0 with the bytes expected; otherwise boxes 0 .. nlsu - 1 are
+// copied through the load/store path (each warp its 32 rows; the arrival follows once they
+// have landed) and the rest gathered by the TMA (half 0), both at once.  Warp-collective.
 template <typename XOf>
 __device__ __forceinline__ void sparse_stage(const SparseRows &r, int lane, uint32_t dst, const void *tmap,
                                              const void *tmap_page, const unsigned char *cache, int nbox, XOf x_of,
-                                             uint32_t bar, bool lsu) {
+                                             uint32_t bar, int nlsu, int half) {
     const bool whole = rows_whole(r, lane);
-    if (whole || !lsu) {
+    if (whole || nlsu == 0) {
+        if (half != 0) {
+            if (lane == 0) mbar_arrive(bar);
+            return;
+        }
         if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)nbox * kBox);
         __syncwarp();
         if (whole)
             page_boxes(r, lane, dst, tmap_page, nbox, x_of, bar);
         else
-            gather_rows(r, lane, dst, tmap, nbox, x_of, bar);
+            gather_rows(r, lane, dst, tmap, 0, nbox, x_of, bar);
         return;
     }
-    copy_rows_lsu(r, lane, dst, cache, nbox, x_of);
+    if (nlsu < nbox && half == 0) {
+        if (lane == 0) mbar_expect_tx(bar, (uint32_t)(nbox - nlsu) * kBox);
+        __syncwarp();
+        gather_rows(r, lane, dst, tmap, nlsu, nbox, x_of, bar);
+    }
+    copy_rows_lsu(r, lane, dst, cache, nlsu, x_of, half);
     cp_async_wait_all();
     fence_proxy_async_smem();
     __syncwarp();
@@ -580,7 +593,8 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                     const __grid_constant__ CUtensorMap tmap_rope, const __grid_constant__ CUtensorMap tmap_qn,
                     const __grid_constant__ CUtensorMap tmap_qr, DecodeArgs a) {
     constexpr bool kSparse = kMode == 1, kFp8 = kMode == 2;
-    constexpr uint32_t kFullCount = kFp8 ? 4u : 1u;  // arrivals that complete a latent / other-columns stage
+    // arrivals that complete a latent / other-columns stage
+    constexpr uint32_t kFullCount = kFp8 ? 4u : kSparse ? 2u : 1u;
     extern __shared__ uint8_t smem_raw[];
     grid_dep_wait();  // the plan (or whatever ran before on the stream) is complete
     if (!plan_matches(a)) {
@@ -749,17 +763,19 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
             });
             if (!ok) drain_pause();
         }
-    } else if (warp == 4 || warp == 7 || (kSparse && warp == 8)) {
+    } else if (warp == 4 || warp == 7 || (kSparse && warp >= 8)) {
         // ------------------------------------------------------------ loaders (whole warps)
         TileCursor cur, nx;
         cur.begin(unit_begin, items, units, cl, ncl);
         nx = cur;
         nx.next();
-        if (warp == 4 || warp == 8) {
+        // Sparse tiles: a load/store-path copy holds its warp until it has landed, so each
+        // kind of stage has its own pair of warps, which split the rows: own pages 4 and 9,
+        // peer pages 8 and 10, other columns 7 and 11 (half 0 and 1).
+        const int half = (warp == 9 || warp == 10 || warp == 11) ? 1 : 0;
+        if (warp == 4 || (kSparse && warp >= 8 && warp <= 10)) {
             // own latent half of both pages, in the order own(0), own(1), peer(0), own(2),
-            // peer(1), own(3), ...  Sparse tiles split the sequence over two warps (own pages:
-            // warp 4, peer pages: warp 8), since a load/store-path copy holds its warp until
-            // it has landed.
+            // peer(1), own(3), ...
             const int xown = 256 * (int)rank;
             // loads page (rank if e == 0, else peer) of tile g at cursor position t
             // (sparse: the rows r were resolved one load ahead)
@@ -772,7 +788,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                         return false;
                     if (t.t + kPageRows * p < t.w.t1) {
                         sparse_stage(r, lane, dst, &tmap, &tmap_sc, a.cache, 4, [&](int i) { return xown + 64 * i; }, fb,
-                                     e == 0 ? kSparseLsuOwn : kSparseLsuPeer);
+                                     e == 0 ? kSparseLsuOwn : kSparseLsuPeer, half);
                     } else if (lane == 0) {
                         mbar_arrive(fb);
                     }
@@ -797,7 +813,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
             TileCursor co = cur;  // next own page: tile go; cur: next peer page, tile gp
             uint32_t go = 0, gp = 0;
             if (kSparse) {
-                if (warp == 4)
+                if (warp == 4 || warp == 9)
                     cur.u = cur.units;  // own pages only
                 else
                     co.u = co.units;  // peer pages only
@@ -830,7 +846,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
             auto rows_of = [&](const Ld &x) {
                 SparseRows r{0, 0, 0u, 0u};
                 if constexpr (kSparse) {
-                    if (x.e >= 0) r = sparse_rows(a, x.t.w, x.t.t, x.e == 0 ? (int)rank : (int)peer, lane, true);
+                    if (x.e >= 0) r = sparse_rows(a, x.t.w, x.t.t, x.e == 0 ? (int)rank : (int)peer, lane, half == 0);
                 }
                 return r;
             };
@@ -865,7 +881,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                         break;
                     }
                     if (cur.t + kPageRows * (int)rank < cur.w.t1) {
-                        sparse_stage(r, lane, dst, &tmap, &tmap_sc, a.cache, kOthBoxes, x_of, fb, kSparseLsuOth);
+                        sparse_stage(r, lane, dst, &tmap, &tmap_sc, a.cache, kOthBoxes, x_of, fb, kSparseLsuOth, half);
                     } else if (lane == 0) {
                         mbar_arrive(fb);
                     }
