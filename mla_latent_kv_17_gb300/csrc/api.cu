@@ -49,9 +49,48 @@ __device__ int64_t block_exclusive_scan(int64_t v, int64_t *total, int64_t *sh) 
     return r;
 }
 
+// The same for three values at once (one pass of barriers for the three).
+struct Sum3 {
+    int64_t v[3];
+};
+__device__ Sum3 block_exclusive_scan3(Sum3 v, Sum3 *total, Sum3 *sh) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    Sum3 x = v;
+    for (int off = 1; off < 32; off <<= 1) {
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, x.v[k], off);
+            if (lane >= off) x.v[k] += y;
+        }
+    }
+    if (lane == 31) sh[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        Sum3 t;
+#pragma unroll
+        for (int k = 0; k < 3; ++k) t.v[k] = lane < kPlanWarps ? sh[lane].v[k] : 0;
+        for (int off = 1; off < 32; off <<= 1) {
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+                const int64_t y = __shfl_up_sync(0xffffffffu, t.v[k], off);
+                if (lane >= off) t.v[k] += y;
+            }
+        }
+        if (lane < kPlanWarps) sh[lane] = t;
+    }
+    __syncthreads();
+    Sum3 r;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) r.v[k] = (wid > 0 ? sh[wid - 1].v[k] : 0) + x.v[k] - v.v[k];
+    *total = sh[kPlanWarps - 1];
+    __syncthreads();
+    return r;
+}
+
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int units, unsigned char *ws, int iu_in_smem) {
     __shared__ int64_t sh[kPlanWarps];
+    __shared__ Sum3 sh3[kPlanWarps];
     extern __shared__ int32_t s_iu[];  // items' units (when max_items of them fit)
     grid_dep_wait();    // seq_lens may come from the kernel before this one on the stream
     grid_dep_launch();  // the decode kernel may launch now; it waits for this plan to complete
@@ -86,10 +125,10 @@ plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int units, unsigned
             pos += req_cost(tiles);
         }
     }
-    int64_t n_total, s_total, r_total;
-    int64_t off = block_exclusive_scan(n_local, &n_total, sh);
-    int64_t slot = block_exclusive_scan(s_local, &s_total, sh);
-    int64_t rpos = block_exclusive_scan(r_local, &r_total, sh);
+    Sum3 tot;
+    const Sum3 ex = block_exclusive_scan3(Sum3{{n_local, s_local, r_local}}, &tot, sh3);
+    const int64_t n_total = tot.v[0], s_total = tot.v[1], r_total = tot.v[2];
+    int64_t off = ex.v[0], slot = ex.v[1], rpos = ex.v[2];
     int32_t *split_list = reinterpret_cast<int32_t *>(ws + L.split_list);
     {
         int64_t pos = pos0;

@@ -596,11 +596,6 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
     // arrivals that complete a latent / other-columns stage
     constexpr uint32_t kFullCount = kFp8 ? 4u : kSparse ? 2u : 1u;
     extern __shared__ uint8_t smem_raw[];
-    grid_dep_wait();  // the plan (or whatever ran before on the stream) is complete
-    if (!plan_matches(a)) {
-        if (threadIdx.x == 0 && blockIdx.x == 0) record_error(a.status, MLA_ERR_WORKSPACE);
-        return;
-    }
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
@@ -648,6 +643,14 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
     cluster_sync();
     tc_fence_after();
     const uint32_t tmem = misc[0];
+    // Everything above touches only this CTA's shared memory and TMEM, so it overlaps the
+    // kernel before this one on the stream (the plan); the plan is read from here on.
+    grid_dep_wait();
+    if (!plan_matches(a)) {  // the same outcome in every CTA
+        if (threadIdx.x == 0 && blockIdx.x == 0) record_error(a.status, MLA_ERR_WORKSPACE);
+        if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+        return;
+    }
 
     const PlanHeader *hd = reinterpret_cast<const PlanHeader *>(a.ws);
     const WsLayout L = ws_layout(hd->B, hd->H, hd->num_units);
