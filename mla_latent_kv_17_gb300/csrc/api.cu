@@ -108,7 +108,7 @@ plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int units, unsigned
     for (int b = b0; b < b1; ++b) local += req_cost(req_tiles(seq_lens, topk, b));
     int64_t total;
     const int64_t pos0 = block_exclusive_scan(local, &total, sh);
-    const int64_t per = plan_budget(total, units);
+    const int64_t per = plan_budget(total, units, topk > 0 ? req_cost(req_tiles(seq_lens, topk, 0)) : 0, B);
 
     int64_t n_local = 0, s_local = 0, r_local = 0;
     {

@@ -34,6 +34,7 @@ constexpr int kTileTokens = 128;
 constexpr int kSmsPerUnit = 2;
 constexpr int kPieceOverheadTiles = 2;
 constexpr int kMinPieceTiles = 2;
+constexpr int kMergeCostTiles = 3;  // the split-KV merge's cost on the critical path, in tiles
 constexpr uint32_t kPlanMagic = 0x4D4C4150u;  // "MLAP"
 
 struct PlanHeader {
@@ -170,11 +171,21 @@ MLA_HD void req_piece(const ReqSplit &r, int i, int64_t per, int units, int32_t 
     *unit = unit_of(r.p0 + (b + e - 1) / 2, per, units);
 }
 
-MLA_HD int64_t plan_budget(int64_t total_cost, int units) {
+// Per-unit budget: the total cost spread evenly, at least one minimal piece.  When every
+// request costs the same (top-k lists: uniform_cost > 0, nreq of them), a budget of k whole
+// requests per unit (k = ceil(nreq / units)) puts every request in one unit, with no partial
+// results and no merge; it is taken whenever it exceeds the even budget by no more than the
+// merge's cost (kMergeCostTiles).
+MLA_HD int64_t plan_budget(int64_t total_cost, int units, int64_t uniform_cost, int64_t nreq) {
     const int64_t num = total_cost + units - 1;
     int64_t per = num <= INT32_MAX ? (int64_t)((uint32_t)num / (uint32_t)units) : num / units;
     const int64_t lo = kPieceOverheadTiles + kMinPieceTiles;
-    return per < lo ? lo : per;
+    if (per < lo) per = lo;
+    if (uniform_cost > 0 && nreq > 0) {
+        const int64_t pack = (nreq + units - 1) / units * uniform_cost;
+        if (pack <= per + kMergeCostTiles) return pack;
+    }
+    return per;
 }
 
 // Writes the pieces of request b (its item offset `off`, its first partial slot `slot0`
@@ -248,7 +259,7 @@ inline void build_plan_serial(const int32_t *seq_lens, int B, int H, int topk, i
         req_start[b] = S;
         S += req_cost(req_tiles(seq_lens, topk, b));
     }
-    const int64_t per = plan_budget(S, units);
+    const int64_t per = plan_budget(S, units, topk > 0 ? req_cost(req_tiles(seq_lens, topk, 0)) : 0, B);
     int32_t off = 0, slots = 0, nsr = 0;
     for (int b = 0; b < B; ++b) {
         const ReqSplit r = req_split(req_start[b], req_tiles(seq_lens, topk, b), per, units);

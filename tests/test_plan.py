@@ -133,3 +133,13 @@ def test_random_plans_hold_every_invariant():
                np.where(kind == 3, r.integers(2, 9000, size=B), r.integers(30000, 140000, size=B)))))
         num_sms = int(r.choice([2, 20, 132, 148, 152]))
         check_plan(lens.astype(np.int32), H=int(r.choice([16, 64, 128])), num_sms=num_sms)
+
+
+def test_uniform_topk_batches_fit_one_unit_per_request():
+    # top-k lists cost the same for every request: with no more requests than units each
+    # request gets a unit of its own (no partials, no merge); with many more, they are split
+    p, _ = check_plan([65536] * 64, topk=2048)
+    assert p["n_partials"] == 0 and all(n == 1 for n in p["num_splits"])
+    assert p["per"] == 2048 // TILE + OVH
+    p, _ = check_plan([65536] * 4, topk=2048)
+    assert p["n_partials"] > 0
