@@ -10,9 +10,9 @@
 // shared memory and written by TMA tile stores as K_h, V_h [H][L][128] bf16.
 //
 // attention_kernel: per (head, tile of 128 queries) a loop over the causal key tiles of 128:
-// S = Q K^T on tcgen05 (K = 128 nope + 64 RoPE) into TMEM, online softmax by eight warps (two
-// threads per query row, 64 keys each; the halves exchange their maxima through shared
-// memory), P as bf16 in TMEM, O += P V on tcgen05 into TMEM (rescaled in place only when a
+// S = Q K^T on tcgen05 (K = 128 nope + 64 RoPE) into TMEM, online softmax by four warps (one
+// thread per query row, all 128 keys of the tile, so no row maximum is exchanged between
+// warps), P as bf16 in TMEM, O += P V on tcgen05 into TMEM (rescaled in place only when a
 // row's maximum exceeds its reference by 2^8).  Keys and values (shared memory) and scores
 // (TMEM) are double-buffered, so the next tile's S = Q K^T runs under this tile's softmax
 // and its values load under this tile's PV.
@@ -169,7 +169,11 @@ constexpr uint32_t kOffK = 3 * kAtBox;     // two key buffers: k nope (2 boxes) 
 constexpr uint32_t kOffV = 9 * kAtBox;     // two value buffers (2 boxes each: 128 keys x 64 value columns)
 constexpr uint32_t kAtBar = 13 * kAtBox;
 constexpr uint32_t kAtSmem = kAtBar + 256 + 1024;
-constexpr int kAtThreads = 352;            // warps 0-7 softmax, 8 query/key loads, 9 MMAs, 10 value loads
+constexpr int kAtGroups = 1;               // softmax warps per 32 query rows (the row's key columns split between them)
+constexpr int kAtCols = kAtK / kAtGroups;   // score columns per softmax thread
+constexpr int kAtSoftmaxWarps = 4 * kAtGroups;
+// softmax warps, then one query/key loader, one MMA issuer and one value loader
+constexpr int kAtThreads = 32 * (kAtSoftmaxWarps + 3);
 constexpr float kRescaleLog2 = 8.0f;       // a row's reference maximum moves only when exceeded by 2^8
 // TMEM: S double-buffered at columns 0 and 128, O at 256, P (bf16 pairs, the A operand of PV) at 384
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
@@ -196,9 +200,10 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
     int *abort_flag = reinterpret_cast<int *>(gbase + kAtBar + 128);
     volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(gbase + kAtBar + 136);
     // (v_empty sits past the flag and the TMEM address: bars + 160, + 168)
-    // the two halves of a row exchange their partial maxima (per score buffer) and sums
-    __shared__ float red[2][2][kAtQ];
-    __shared__ float lsum[2][kAtQ];
+    // with several warps per row (kAtGroups > 1) they exchange their partial maxima (per score
+    // buffer) and sums
+    __shared__ float red[2][kAtGroups][kAtQ];
+    __shared__ float lsum[kAtGroups][kAtQ];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nqt = (L + kAtQ - 1) / kAtQ;
     // head-major order: the CTAs resident at once share a few heads' keys and values (2 MB
@@ -212,14 +217,14 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
         if (lane == 0) {
             mbar_init(q_full, 1);
             mbar_init(pv_done, 1);
-            mbar_init(p_full, 8);
-            mbar_init(l_done, 8);
+            mbar_init(p_full, kAtSoftmaxWarps);
+            mbar_init(l_done, kAtSoftmaxWarps);
             for (int b = 0; b < 2; ++b) {
                 mbar_init(k_full(b), 1);
                 mbar_init(k_empty(b), 1);
                 mbar_init(s_full(b), 1);
-                mbar_init(s_free(b), 8);
-                mbar_init(red_full(b), 8);
+                mbar_init(s_free(b), kAtSoftmaxWarps);
+                mbar_init(red_full(b), kAtSoftmaxWarps);
                 mbar_init(v_full(b), 1);
                 mbar_init(v_empty(b), 1);
             }
@@ -237,7 +242,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
     const uint32_t tmem = *tslot;
     bool ok = true;
 
-    if (warp == 8) {
+    if (warp == kAtSoftmaxWarps) {
         // queries once, then the keys of tile g into buffer g % 2 once QK(g - 2) has read it
         if (lane == 0) {
             mbar_arrive_expect_tx(q_full, 3 * kAtBox);
@@ -255,7 +260,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
                 tma_load_2d(kd + 2 * kAtBox, &tm_kr, kDLatent, k0, k_full(kb));
             }
         }
-    } else if (warp == 10) {
+    } else if (warp == kAtSoftmaxWarps + 2) {
         // the values of tile g into buffer g % 2 once PV(g - 2) has read it
         if (lane == 0) {
             for (int g = 0; g < ntiles && ok; ++g) {
@@ -268,7 +273,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
                 tma_load_3d(vd + kAtBox, &tm_v, 64, g * kAtK, h, v_full(vb));
             }
         }
-    } else if (warp == 9) {
+    } else if (warp == kAtSoftmaxWarps + 1) {
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_major(128, kAtK, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_major(128, kDh, false, true);
@@ -313,12 +318,13 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
         }
     } else {
         // ---------------------------------------------------------------- softmax
-        // warp w: query rows 32 (w % 4) .. (its TMEM lanes), key / value columns 64 (w / 4) ..
+        // warp w: query rows 32 (w % 4) .. (its TMEM lanes), key / value columns kAtCols (w / 4) ..
+        constexpr int kCh = kAtCols / 32;  // 32-column TMEM chunks per thread
         const int quad = warp & 3, hf = warp >> 2;
         const int row = 32 * quad + lane;
         const int qi = q0 + row;
         const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
-        float m = -INFINITY, l = 0.f;  // reference maximum (log2 units, shared by both halves), partial sum
+        float m = -INFINITY, l = 0.f;  // reference maximum (log2 units, shared by the row's warps), partial sum
         for (int g = 0; g < ntiles && ok; ++g) {
             const int k0 = g * kAtK;
             const int sb = g & 1;
@@ -326,11 +332,11 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            float s[64];
+            float s[kAtCols];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < kCh; ++c) {
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_base + kColS + 128u * sb + 64u * hf + 32u * c, r);
+                tmem_ld32(tmem + lane_base + kColS + 128u * sb + kAtCols * hf + 32u * c, r);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(r[i]);
@@ -339,27 +345,32 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free(sb));
             // causal mask (and keys past the sequence) on the diagonal tile
-            const int lim = min(qi, L - 1) - k0 - 64 * hf;  // columns x <= lim are seen
+            const int lim = min(qi, L - 1) - k0 - kAtCols * hf;  // columns x <= lim are seen
             float pm = m;
 #pragma unroll
-            for (int x = 0; x < 64; ++x) {
+            for (int x = 0; x < kAtCols; ++x) {
                 s[x] = x <= lim ? s[x] * scale_log2 : -INFINITY;
                 pm = fmaxf(pm, s[x]);
             }
-            red[sb][hf][row] = pm;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(red_full(sb));
-            ok = wait_bounded(red_full(sb), (g >> 1) & 1, abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            const float mx = fmaxf(red[sb][0][row], red[sb][1][row]);  // finite: key 0 is seen
+            float mx = pm;  // finite: key 0 is seen
+            if constexpr (kAtGroups > 1) {
+                red[sb][hf][row] = pm;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(red_full(sb));
+                ok = wait_bounded(red_full(sb), (g >> 1) & 1, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                mx = red[sb][0][row];
+#pragma unroll
+                for (int q = 1; q < kAtGroups; ++q) mx = fmaxf(mx, red[sb][q][row]);
+            }
             // the reference maximum moves only when the row maximum exceeds it by 2^8, so most
             // tiles keep it and leave O alone (probabilities stay <= 2^8)
             const float mref = (m == -INFINITY || mx > m + kRescaleLog2) ? mx : m;
             const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - mref);
             float sum = 0.f;
 #pragma unroll
-            for (int x = 0; x < 64; ++x) {
+            for (int x = 0; x < kAtCols; ++x) {
                 s[x] = ex2_approx(s[x] - mref);
                 sum += s[x];
             }
@@ -373,26 +384,27 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
                 tc_fence_after();
                 if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-                    for (int c = 0; c < 2; ++c) {
+                    for (int c = 0; c < kCh; ++c) {
                         uint32_t r[32];
-                        tmem_ld32(tmem + lane_base + kColO + 64u * hf + 32u * c, r);
+                        tmem_ld32(tmem + lane_base + kColO + kAtCols * hf + 32u * c, r);
                         tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(tmem + lane_base + kColO + 64u * hf + 32u * c, r);
+                        tmem_st32(tmem + lane_base + kColO + kAtCols * hf + 32u * c, r);
                     }
                     tmem_wait_st();
                 }
             }
-            // this half of the P row as bf16 pairs (lower key in the low half) into TMEM columns
-            // kColP + 32 hf ..: the A operand of PV
-            {
+            // this warp's part of the P row as bf16 pairs (lower key in the low half) into TMEM
+            // columns kColP + (kAtCols / 2) hf ..: the A operand of PV
+#pragma unroll
+            for (int c = 0; c < kAtCols / 64; ++c) {
                 uint32_t pv[32];
 #pragma unroll
-                for (int c = 0; c < 32; ++c) pv[c] = bf16x2_bits(s[2 * c], s[2 * c + 1]);
-                tmem_st32(tmem + lane_base + kColP + 32u * hf, pv);
-                tmem_wait_st();
+                for (int i = 0; i < 32; ++i) pv[i] = bf16x2_bits(s[64 * c + 2 * i], s[64 * c + 2 * i + 1]);
+                tmem_st32(tmem + lane_base + kColP + (kAtCols / 2) * hf + 32u * c, pv);
             }
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
@@ -406,15 +418,17 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
         }
         if (ok) {
             tc_fence_after();
-            const float lt = lsum[0][row] + lsum[1][row];
+            float lt = 0.f;
+#pragma unroll
+            for (int q = 0; q < kAtGroups; ++q) lt += lsum[q][row];
             const float inv = lt > 0.f ? 1.f / lt : 0.f;
 #pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < kCh; ++c) {
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_base + kColO + 64u * hf + 32u * c, r);
+                tmem_ld32(tmem + lane_base + kColO + kAtCols * hf + 32u * c, r);
                 tmem_wait_ld();
                 if (qi < L) {
-                    float4 *dst = reinterpret_cast<float4 *>(out + ((int64_t)qi * H + h) * kDh + 64 * hf + 32 * c);
+                    float4 *dst = reinterpret_cast<float4 *>(out + ((int64_t)qi * H + h) * kDh + kAtCols * hf + 32 * c);
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
