@@ -9,13 +9,13 @@
 // 64-column chunks through a three-stage TMA ring; the results are transposed through
 // shared memory and written by TMA tile stores as K_h, V_h [H][L][128] bf16.
 //
-// attention_kernel: per (head, tile of 128 queries) a loop over the causal key tiles of 128:
-// S = Q K^T on tcgen05 (K = 128 nope + 64 RoPE) into TMEM, online softmax by four warps (one
-// thread per query row, all 128 keys of the tile, so no row maximum is exchanged between
-// warps), P as bf16 in TMEM, O += P V on tcgen05 into TMEM (rescaled in place only when a
-// row's maximum exceeds its reference by 2^8).  Keys and values (shared memory) and scores
-// (TMEM) are double-buffered, so the next tile's S = Q K^T runs under this tile's softmax
-// and its values load under this tile's PV.
+// attention_kernel: per (head, two adjacent tiles of 128 queries) a loop over the causal key
+// tiles of 128: S = Q K^T on tcgen05 (K = 128 nope + 64 RoPE) into TMEM, online softmax by
+// four warps per query tile (one thread per query row, all 128 keys of the tile), P as bf16
+// over the first half of that tile's S in TMEM, O += P V on tcgen05 into TMEM (rescaled in
+// place only when a row's maximum exceeds its reference by 2^8).  The two query tiles take
+// turns on the tensor pipe: while one tile's softmax runs, the other tile's PV and next
+// scores run.  Keys are double-buffered in shared memory and shared by both tiles' QK.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -161,22 +161,26 @@ __global__ void __launch_bounds__(kDcThreads, 1) decompress_kernel(const __grid_
 }
 
 // ------------------------------------------------------------------ attention
-constexpr int kAtQ = 128;                  // queries per CTA (MMA M)
+// Two query tiles per CTA (tiles 2p and 2p + 1 of a head, "A" and "B"): while one tile's
+// softmax runs, the tensor pipe works on the other tile's PV and next scores.  Each tile has
+// its scores S and its accumulator O in TMEM; P (bf16) overwrites the first 64 columns of its
+// S once the scores are read (the next S of that tile is issued after its PV, and the tensor
+// pipe runs them in order).  A key tile is read by both query tiles' QK; B, one tile further
+// down the diagonal, takes one key tile more.
+constexpr int kAtQ = 128;                  // queries per tile (MMA M)
 constexpr int kAtK = 128;                  // keys per tile (MMA N of the scores, K of PV)
 constexpr uint32_t kAtBox = 128 * 128;     // 128 rows x 64 bf16
-constexpr uint32_t kOffQ = 0;              // q nope (2 boxes) + q rope (1 box)
-constexpr uint32_t kOffK = 3 * kAtBox;     // two key buffers: k nope (2 boxes) + k rope (1 box)
-constexpr uint32_t kOffV = 9 * kAtBox;     // two value buffers (2 boxes each: 128 keys x 64 value columns)
-constexpr uint32_t kAtBar = 13 * kAtBox;
+constexpr uint32_t kOffQ = 0;              // per query tile: q nope (2 boxes) + q rope (1 box)
+constexpr uint32_t kOffK = 6 * kAtBox;     // two key buffers: k nope (2 boxes) + k rope (1 box)
+constexpr uint32_t kOffV = 12 * kAtBox;    // one value buffer (2 boxes: 128 keys x 64 value columns)
+constexpr uint32_t kAtBar = 14 * kAtBox;
 constexpr uint32_t kAtSmem = kAtBar + 256 + 1024;
-constexpr int kAtGroups = 1;               // softmax warps per 32 query rows (the row's key columns split between them)
-constexpr int kAtCols = kAtK / kAtGroups;   // score columns per softmax thread
-constexpr int kAtSoftmaxWarps = 4 * kAtGroups;
-// softmax warps, then one query/key loader, one MMA issuer and one value loader
-constexpr int kAtThreads = 32 * (kAtSoftmaxWarps + 3);
+// warps 0-3 softmax of tile A, 4-7 of tile B (one thread per query row), 8 query/key loads,
+// 9 MMAs, 10 value loads
+constexpr int kAtThreads = 32 * 11;
 constexpr float kRescaleLog2 = 8.0f;       // a row's reference maximum moves only when exceeded by 2^8
-// TMEM: S double-buffered at columns 0 and 128, O at 256, P (bf16 pairs, the A operand of PV) at 384
-constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+// TMEM: tile X (0 = A, 1 = B) has S at 256 X, O at 256 X + 128; P at 256 X (bf16 pairs)
+constexpr uint32_t kColS = 0, kColO = 128;
 
 __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
     const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qr,
@@ -187,47 +191,43 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char *gbase = smem_raw + (base - raw);
     const uint32_t bars = base + kAtBar;
-    // barriers: q_full, pv_done (frees P and O), p_full, l_done, and per buffer b (tile g uses
-    // b = g % 2): k_full, k_empty, v_full, v_empty, s_full, s_free, red_full
-    const uint32_t q_full = bars, pv_done = bars + 8, p_full = bars + 16, l_done = bars + 24;
-    auto k_full = [&](int b) { return bars + 32u + 8u * b; };
-    auto k_empty = [&](int b) { return bars + 48u + 8u * b; };
-    auto s_full = [&](int b) { return bars + 64u + 8u * b; };
-    auto s_free = [&](int b) { return bars + 80u + 8u * b; };
-    auto red_full = [&](int b) { return bars + 96u + 8u * b; };
-    auto v_full = [&](int b) { return bars + 112u + 8u * b; };
-    auto v_empty = [&](int b) { return bars + 160u + 8u * b; };
+    // barriers: q_full; per key buffer b: k_full, k_empty; the value buffer: v_full, v_empty;
+    // per query tile X: s_full (its scores are in TMEM), p_full (its P is, one arrival per
+    // softmax warp), pv_done (its PV has finished)
+    const uint32_t q_full = bars;
+    auto k_full = [&](int b) { return bars + 8u + 8u * b; };
+    auto k_empty = [&](int b) { return bars + 24u + 8u * b; };
+    const uint32_t v_full = bars + 40, v_empty = bars + 48;
+    auto s_full = [&](int x) { return bars + 56u + 8u * x; };
+    auto p_full = [&](int x) { return bars + 72u + 8u * x; };
+    auto pv_done = [&](int x) { return bars + 88u + 8u * x; };
     int *abort_flag = reinterpret_cast<int *>(gbase + kAtBar + 128);
     volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(gbase + kAtBar + 136);
-    // (v_empty sits past the flag and the TMEM address: bars + 160, + 168)
-    // with several warps per row (kAtGroups > 1) they exchange their partial maxima (per score
-    // buffer) and sums
-    __shared__ float red[2][kAtGroups][kAtQ];
-    __shared__ float lsum[kAtGroups][kAtQ];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nqt = (L + kAtQ - 1) / kAtQ;
+    const int npair = (nqt + 1) / 2;
     // head-major order: the CTAs resident at once share a few heads' keys and values (2 MB
     // a head at 4,096 tokens), which then stay in L2; within a head the longest rows first
-    const int h = (int)(blockIdx.x / nqt);
-    const int qt = nqt - 1 - (int)(blockIdx.x % nqt);
-    const int q0 = qt * kAtQ;
-    const int ntiles = qt + 1;                       // causal: key tiles 0 .. qt
+    const int h = (int)(blockIdx.x / npair);
+    const int pr = npair - 1 - (int)(blockIdx.x % npair);
+    const int qa = 2 * pr;                           // query tile A; B = qa + 1 if it exists
+    const bool has_b = qa + 1 < nqt;
+    const int nt_b = has_b ? qa + 2 : 0;             // causal: key tiles 0 .. q tile (A: qa + 1)
+    const int ntot = has_b ? qa + 2 : qa + 1;        // key tiles loaded
+    auto ntiles = [&](int x) { return x == 0 ? qa + 1 : nt_b; };
 
     if (warp == 0) {
         if (lane == 0) {
             mbar_init(q_full, 1);
-            mbar_init(pv_done, 1);
-            mbar_init(p_full, kAtSoftmaxWarps);
-            mbar_init(l_done, kAtSoftmaxWarps);
             for (int b = 0; b < 2; ++b) {
                 mbar_init(k_full(b), 1);
                 mbar_init(k_empty(b), 1);
                 mbar_init(s_full(b), 1);
-                mbar_init(s_free(b), kAtSoftmaxWarps);
-                mbar_init(red_full(b), kAtSoftmaxWarps);
-                mbar_init(v_full(b), 1);
-                mbar_init(v_empty(b), 1);
+                mbar_init(p_full(b), 4);
+                mbar_init(pv_done(b), 1);
             }
+            mbar_init(v_full, 1);
+            mbar_init(v_empty, 1);
             *abort_flag = 0;
             fence_mbar_init();
         }
@@ -242,14 +242,19 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
     const uint32_t tmem = *tslot;
     bool ok = true;
 
-    if (warp == kAtSoftmaxWarps) {
-        // queries once, then the keys of tile g into buffer g % 2 once QK(g - 2) has read it
+    if (warp == 8) {
+        // both query tiles once, then the keys of tile g into buffer g % 2 once the last QK of
+        // tile g - 2 has read it
         if (lane == 0) {
-            mbar_arrive_expect_tx(q_full, 3 * kAtBox);
-            tma_load_3d(base + kOffQ, &tm_qn, 0, h, q0, q_full);
-            tma_load_3d(base + kOffQ + kAtBox, &tm_qn, 64, h, q0, q_full);
-            tma_load_3d(base + kOffQ + 2 * kAtBox, &tm_qr, 0, h, q0, q_full);
-            for (int g = 0; g < ntiles && ok; ++g) {
+            mbar_arrive_expect_tx(q_full, (has_b ? 6 : 3) * kAtBox);
+            for (int x = 0; x < (has_b ? 2 : 1); ++x) {
+                const int q0 = (qa + x) * kAtQ;
+                const uint32_t qd = base + kOffQ + 3 * kAtBox * x;
+                tma_load_3d(qd, &tm_qn, 0, h, q0, q_full);
+                tma_load_3d(qd + kAtBox, &tm_qn, 64, h, q0, q_full);
+                tma_load_3d(qd + 2 * kAtBox, &tm_qr, 0, h, q0, q_full);
+            }
+            for (int g = 0; g < ntot && ok; ++g) {
                 const int k0 = g * kAtK, kb = g & 1;
                 if (g >= 2) ok = wait_bounded(k_empty(kb), ((g >> 1) - 1) & 1, abort_flag);
                 if (!ok) break;
@@ -260,182 +265,168 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
                 tma_load_2d(kd + 2 * kAtBox, &tm_kr, kDLatent, k0, k_full(kb));
             }
         }
-    } else if (warp == kAtSoftmaxWarps + 2) {
-        // the values of tile g into buffer g % 2 once PV(g - 2) has read it
+    } else if (warp == 10) {
+        // the values of tile g once the last PV of tile g - 1 has read the buffer
         if (lane == 0) {
-            for (int g = 0; g < ntiles && ok; ++g) {
-                const int vb = g & 1;
-                if (g >= 2) ok = wait_bounded(v_empty(vb), ((g >> 1) - 1) & 1, abort_flag);
+            for (int g = 0; g < ntot && ok; ++g) {
+                if (g >= 1) ok = wait_bounded(v_empty, (g - 1) & 1, abort_flag);
                 if (!ok) break;
-                const uint32_t vd = base + kOffV + vb * 2 * kAtBox;
-                mbar_arrive_expect_tx(v_full(vb), 2 * kAtBox);
-                tma_load_3d(vd, &tm_v, 0, g * kAtK, h, v_full(vb));
-                tma_load_3d(vd + kAtBox, &tm_v, 64, g * kAtK, h, v_full(vb));
+                mbar_arrive_expect_tx(v_full, 2 * kAtBox);
+                tma_load_3d(base + kOffV, &tm_v, 0, g * kAtK, h, v_full);
+                tma_load_3d(base + kOffV + kAtBox, &tm_v, 64, g * kAtK, h, v_full);
             }
         }
-    } else if (warp == kAtSoftmaxWarps + 1) {
+    } else if (warp == 9) {
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_major(128, kAtK, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_major(128, kDh, false, true);
-            // S(g) into buffer g % 2: 8 steps over the 128 nope columns, 4 over RoPE
-            // (key buffer and score buffer are both g % 2)
-            auto qk = [&](int g) -> bool {
+            // S_x(g): 8 steps over the 128 nope columns, 4 over RoPE; the key buffer goes back
+            // after the last query tile that reads it
+            auto qk = [&](int x, int g) -> bool {
                 const int b = g & 1;
-                if (!wait_bounded(k_full(b), (g >> 1) & 1, abort_flag)) return false;
-                if (g >= 2 && !wait_bounded(s_free(b), ((g >> 1) - 1) & 1, abort_flag)) return false;
+                if (!wait_quick(k_full(b), (g >> 1) & 1, abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t kd = base + kOffK + b * 3 * kAtBox;
+                const uint32_t kd = base + kOffK + b * 3 * kAtBox, qd = base + kOffQ + 3 * kAtBox * x;
                 for (int k = 0; k < 12; ++k) {
                     const uint32_t off = (k >> 2) * kAtBox + (k & 3) * 32u;
-                    mma_ss(tmem + kColS + 128u * b, smem_desc_sw128(base + kOffQ + off, 16u, 1024u),
+                    mma_ss(tmem + 256u * x + kColS, smem_desc_sw128(qd + off, 16u, 1024u),
                            smem_desc_sw128(kd + off, 16u, 1024u), idesc_s, k > 0 ? 1u : 0u);
                 }
-                mma_commit(s_full(b));
-                mma_commit(k_empty(b));
+                mma_commit(s_full(x));
+                if (x == 1 || g >= nt_b) mma_commit(k_empty(b));
                 return true;
             };
-            ok = wait_bounded(q_full, 0, abort_flag) && qk(0);
-            for (int g = 0; g < ntiles && ok; ++g) {
-                // the next tile's scores go ahead of this tile's PV, under this tile's softmax
-                if (g + 1 < ntiles && !qk(g + 1)) {
-                    ok = false;
-                    break;
-                }
-                const int vb = g & 1;
-                ok = wait_bounded(p_full, g & 1, abort_flag) &&
-                     wait_bounded(v_full(vb), (g >> 1) & 1, abort_flag);
-                if (!ok) break;
+            // O_x += P_x(g) V(g); the value buffer goes back after the last query tile's PV
+            auto pv = [&](int x, int g) -> bool {
+                if (!wait_quick(p_full(x), g & 1, abort_flag) || !wait_quick(v_full, g & 1, abort_flag))
+                    return false;
                 tc_fence_after();
-                const uint32_t vd = base + kOffV + vb * 2 * kAtBox;
                 for (int k = 0; k < kAtK / 16; ++k) {
                     // A: P in TMEM, 16 keys = 8 columns of bf16 pairs; B: 16 key rows of V
-                    const uint64_t bd = smem_desc_sw128(vd + k * 2048u, kAtBox, 1024u);
-                    mma_ts(tmem + kColO, tmem + kColP + 8u * k, bd, idesc_o, (g > 0 || k > 0) ? 1u : 0u);
+                    const uint64_t bd = smem_desc_sw128(base + kOffV + k * 2048u, kAtBox, 1024u);
+                    mma_ts(tmem + 256u * x + kColO, tmem + 256u * x + kColS + 8u * k, bd, idesc_o,
+                           (g > 0 || k > 0) ? 1u : 0u);
                 }
-                mma_commit(v_empty(vb));
-                mma_commit(pv_done);
+                mma_commit(pv_done(x));
+                if (x == 1 || g >= nt_b) mma_commit(v_empty);
+                return true;
+            };
+            ok = wait_quick(q_full, 0, abort_flag) && qk(0, 0) && (!has_b || qk(1, 0));
+            for (int g = 0; g < ntot && ok; ++g) {
+                for (int x = 0; x < 2 && ok; ++x) {
+                    if (g >= ntiles(x)) continue;
+                    ok = pv(x, g) && (g + 1 >= ntiles(x) || qk(x, g + 1));
+                }
             }
         }
     } else {
         // ---------------------------------------------------------------- softmax
-        // warp w: query rows 32 (w % 4) .. (its TMEM lanes), key / value columns kAtCols (w / 4) ..
-        constexpr int kCh = kAtCols / 32;  // 32-column TMEM chunks per thread
-        const int quad = warp & 3, hf = warp >> 2;
+        // warps 4x .. 4x + 3: query tile x, rows 32 (w % 4) .. (its TMEM lanes), one thread per
+        // row over the tile's 128 keys
+        const int x = warp >> 2, quad = warp & 3;
         const int row = 32 * quad + lane;
-        const int qi = q0 + row;
+        const int qi = (qa + x) * kAtQ + row;
         const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
-        float m = -INFINITY, l = 0.f;  // reference maximum (log2 units, shared by the row's warps), partial sum
-        for (int g = 0; g < ntiles && ok; ++g) {
+        const uint32_t cS = tmem + lane_base + 256u * x + kColS, cO = tmem + lane_base + 256u * x + kColO;
+        const int nt = ntiles(x);
+        float m = -INFINITY, l = 0.f;  // reference maximum (log2 units), running sum
+        for (int g = 0; g < nt && ok; ++g) {
             const int k0 = g * kAtK;
-            const int sb = g & 1;
-            ok = wait_bounded(s_full(sb), (g >> 1) & 1, abort_flag);
+            ok = wait_bounded(s_full(x), g & 1, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            float s[kAtCols];
+            float s[kAtK];
 #pragma unroll
-            for (int c = 0; c < kCh; ++c) {
+            for (int c = 0; c < kAtK / 32; ++c) {
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_base + kColS + 128u * sb + kAtCols * hf + 32u * c, r);
+                tmem_ld32(cS + 32u * c, r);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(r[i]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free(sb));
-            // causal mask (and keys past the sequence) on the diagonal tile
-            const int lim = min(qi, L - 1) - k0 - kAtCols * hf;  // columns x <= lim are seen
-            float pm = m;
+            // causal mask (and keys past the sequence) on the diagonal tiles
+            const int lim = min(qi, L - 1) - k0;  // columns c <= lim are seen
+            if (__any_sync(0xffffffffu, lim < kAtK - 1)) {
 #pragma unroll
-            for (int x = 0; x < kAtCols; ++x) {
-                s[x] = x <= lim ? s[x] * scale_log2 : -INFINITY;
-                pm = fmaxf(pm, s[x]);
+                for (int c = 0; c < kAtK; ++c) s[c] = c <= lim ? s[c] : -INFINITY;
             }
-            float mx = pm;  // finite: key 0 is seen
-            if constexpr (kAtGroups > 1) {
-                red[sb][hf][row] = pm;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(red_full(sb));
-                ok = wait_bounded(red_full(sb), (g >> 1) & 1, abort_flag);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                mx = red[sb][0][row];
+            // the row maximum over the raw scores (the scale is positive, so the order is
+            // theirs), in eight independent chains
+            float mxs[8];
 #pragma unroll
-                for (int q = 1; q < kAtGroups; ++q) mx = fmaxf(mx, red[sb][q][row]);
-            }
+            for (int j = 0; j < 8; ++j) mxs[j] = s[j];
+#pragma unroll
+            for (int c = 8; c < kAtK; ++c) mxs[c & 7] = fmaxf(mxs[c & 7], s[c]);
+            const float mx = fmaxf(m, scale_log2 * fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
+                                                         fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7]))));
             // the reference maximum moves only when the row maximum exceeds it by 2^8, so most
-            // tiles keep it and leave O alone (probabilities stay <= 2^8)
+            // tiles keep it and leave O alone (probabilities stay <= 2^8); key 0 is always seen,
+            // so mx is finite
             const float mref = (m == -INFINITY || mx > m + kRescaleLog2) ? mx : m;
             const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - mref);
-            float sum = 0.f;
+            // p = 2^(s scale_log2 - mref), the scale folded into the exponent's FMA; the P row as
+            // bf16 pairs (lower key in the low half) over the first 64 columns of this tile's S
+            // (read above): the A operand of PV
+            float sums[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int x = 0; x < kAtCols; ++x) {
-                s[x] = ex2_approx(s[x] - mref);
-                sum += s[x];
+            for (int c = 0; c < 2; ++c) {
+                uint32_t pv[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float p0 = ex2_approx(fmaf(s[64 * c + 2 * i], scale_log2, -mref));
+                    const float p1 = ex2_approx(fmaf(s[64 * c + 2 * i + 1], scale_log2, -mref));
+                    sums[i & 3] += p0 + p1;
+                    pv[i] = bf16x2_bits(p0, p1);
+                }
+                tmem_st32(cS + 32u * c, pv);
             }
+            const float sum = (sums[0] + sums[1]) + (sums[2] + sums[3]);
             l = l * alpha + sum;
             m = mref;
-            // P and O are free once the previous tile's PV has finished
-            if (g > 0) {
-                ok = wait_bounded(pv_done, (g - 1) & 1, abort_flag);
+            // O is rescaled (rarely) once the previous PV of this tile has finished; the next
+            // PV waits for this tile's P
+            if (g > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                ok = wait_bounded(pv_done(x), (g - 1) & 1, abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-                    for (int c = 0; c < kCh; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(tmem + lane_base + kColO + kAtCols * hf + 32u * c, r);
-                        tmem_wait_ld();
+                for (int c = 0; c < kDh / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(cO + 32u * c, r);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(tmem + lane_base + kColO + kAtCols * hf + 32u * c, r);
-                    }
-                    tmem_wait_st();
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                    tmem_st32(cO + 32u * c, r);
                 }
-            }
-            // this warp's part of the P row as bf16 pairs (lower key in the low half) into TMEM
-            // columns kColP + (kAtCols / 2) hf ..: the A operand of PV
-#pragma unroll
-            for (int c = 0; c < kAtCols / 64; ++c) {
-                uint32_t pv[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) pv[i] = bf16x2_bits(s[64 * c + 2 * i], s[64 * c + 2 * i + 1]);
-                tmem_st32(tmem + lane_base + kColP + (kAtCols / 2) * hf + 32u * c, pv);
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(p_full(x));
         }
-        if (ok) {
-            lsum[hf][row] = l;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(l_done);
-            ok = wait_bounded(l_done, 0, abort_flag) && wait_bounded(pv_done, (ntiles - 1) & 1, abort_flag);
+        if (ok && nt > 0) {
+            ok = wait_bounded(pv_done(x), (nt - 1) & 1, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
         }
-        if (ok) {
+        if (ok && nt > 0) {
             tc_fence_after();
-            float lt = 0.f;
-#pragma unroll
-            for (int q = 0; q < kAtGroups; ++q) lt += lsum[q][row];
-            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-            for (int c = 0; c < kCh; ++c) {
+            for (int c = 0; c < kDh / 32; ++c) {
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_base + kColO + kAtCols * hf + 32u * c, r);
+                tmem_ld32(cO + 32u * c, r);
                 tmem_wait_ld();
                 if (qi < L) {
-                    float4 *dst = reinterpret_cast<float4 *>(out + ((int64_t)qi * H + h) * kDh + kAtCols * hf + 32 * c);
+                    float4 *dst = reinterpret_cast<float4 *>(out + ((int64_t)qi * H + h) * kDh + 32 * c);
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
                                              __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
                 }
             }
-            if (qi < L && hf == 0) lse[(int64_t)qi * H + h] = (m + log2f(lt)) * kLn2;
+            if (qi < L) lse[(int64_t)qi * H + h] = (m + log2f(l)) * kLn2;
         }
     }
     grid_dep_launch();
@@ -510,7 +501,7 @@ extern "C" mla_status mla_prefill_attention(const void *q_nope, const void *q_ro
     if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(entries) || !aligned16(k_nope) || !aligned16(v) ||
         !aligned16(out))
         return MLA_ERR_INVALID_ARG;
-    const int64_t grid = (int64_t)H * ((L + kAtQ - 1) / kAtQ);
+    const int64_t grid = (int64_t)H * (((L + kAtQ - 1) / kAtQ + 1) / 2);
     if (grid > 0x7FFFFFFF) return MLA_ERR_UNSUPPORTED;
     if (!set_prefill_attrs()) return MLA_ERR_CUDA;
     CUtensorMap tqn, tqr, tk, tkr, tv;

@@ -17,7 +17,7 @@ constexpr long long kWaitCycles = 4000000000LL;  // about two seconds
 // Waits for phase `parity` of an mbarrier for at most kWaitCycles.  With an abort flag (a
 // shared-memory int of the CTA) a wait also gives up once another wait of the CTA has, and
 // a wait that runs out sets it.
-__device__ bool wait_bounded(uint32_t bar, uint32_t parity, int *abort_flag = nullptr) {
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, int *abort_flag = nullptr) {
     const long long t0 = (long long)ptx::clock64_now();
     for (uint32_t i = 0;; ++i) {
         if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -29,6 +29,11 @@ __device__ bool wait_bounded(uint32_t bar, uint32_t parity, int *abort_flag = nu
             }
         }
     }
+}
+// The same with the first probe inline, for an issuing thread whose barriers have mostly
+// completed already (one try_wait then, no call and no clock read).
+__device__ __forceinline__ bool wait_quick(uint32_t bar, uint32_t parity, int *abort_flag) {
+    return ptx::mbar_try_wait(bar, parity) || wait_bounded(bar, parity, abort_flag);
 }
 
 // Gives copies or MMAs still in flight a bounded time to land before the CTA leaves.
