@@ -277,41 +277,46 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
             }
         }
     } else if (warp == 9) {
-        if (lane == 0) {
+        // the whole warp runs the issue loop (its waits made warp-uniform); one elected lane
+        // issues each MMA and commit
+        auto wait_w = [&](uint32_t bar, uint32_t parity) {
+            return __all_sync(0xffffffffu, wait_quick(bar, parity, abort_flag));
+        };
+        {
             constexpr uint32_t idesc_s = idesc_bf16_major(128, kAtK, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_major(128, kDh, false, true);
             // S_x(g): 8 steps over the 128 nope columns, 4 over RoPE; the key buffer goes back
             // after the last query tile that reads it
             auto qk = [&](int x, int g) -> bool {
                 const int b = g & 1;
-                if (!wait_quick(k_full(b), (g >> 1) & 1, abort_flag)) return false;
+                if (!wait_w(k_full(b), (g >> 1) & 1)) return false;
                 tc_fence_after();
                 const uint32_t kd = base + kOffK + b * 3 * kAtBox, qd = base + kOffQ + 3 * kAtBox * x;
                 for (int k = 0; k < 12; ++k) {
                     const uint32_t off = (k >> 2) * kAtBox + (k & 3) * 32u;
-                    mma_ss(tmem + 256u * x + kColS, smem_desc_sw128(qd + off, 16u, 1024u),
-                           smem_desc_sw128(kd + off, 16u, 1024u), idesc_s, k > 0 ? 1u : 0u);
+                    mma_ss_warp(tmem + 256u * x + kColS, smem_desc_sw128(qd + off, 16u, 1024u),
+                                smem_desc_sw128(kd + off, 16u, 1024u), idesc_s, k > 0 ? 1u : 0u);
                 }
-                mma_commit(s_full(x));
-                if (x == 1 || g >= nt_b) mma_commit(k_empty(b));
+                mma_commit_warp(s_full(x));
+                if (x == 1 || g >= nt_b) mma_commit_warp(k_empty(b));
                 return true;
             };
             // O_x += P_x(g) V(g); the value buffer goes back after the last query tile's PV
             auto pv = [&](int x, int g) -> bool {
-                if (!wait_quick(p_full(x), g & 1, abort_flag) || !wait_quick(v_full, g & 1, abort_flag))
+                if (!wait_w(p_full(x), g & 1) || !wait_w(v_full, g & 1))
                     return false;
                 tc_fence_after();
                 for (int k = 0; k < kAtK / 16; ++k) {
                     // A: P in TMEM, 16 keys = 8 columns of bf16 pairs; B: 16 key rows of V
                     const uint64_t bd = smem_desc_sw128(base + kOffV + k * 2048u, kAtBox, 1024u);
-                    mma_ts(tmem + 256u * x + kColO, tmem + 256u * x + kColS + 8u * k, bd, idesc_o,
-                           (g > 0 || k > 0) ? 1u : 0u);
+                    mma_ts_warp(tmem + 256u * x + kColO, tmem + 256u * x + kColS + 8u * k, bd, idesc_o,
+                                (g > 0 || k > 0) ? 1u : 0u);
                 }
-                mma_commit(pv_done(x));
-                if (x == 1 || g >= nt_b) mma_commit(v_empty);
+                mma_commit_warp(pv_done(x));
+                if (x == 1 || g >= nt_b) mma_commit_warp(v_empty);
                 return true;
             };
-            ok = wait_quick(q_full, 0, abort_flag) && qk(0, 0) && (!has_b || qk(1, 0));
+            ok = wait_w(q_full, 0) && qk(0, 0) && (!has_b || qk(1, 0));
             for (int g = 0; g < ntot && ok; ++g) {
                 for (int x = 0; x < 2 && ok; ++x) {
                     if (g >= ntiles(x)) continue;
