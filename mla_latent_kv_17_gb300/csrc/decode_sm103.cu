@@ -911,7 +911,9 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
         }
     } else if (warp == 5) {
         // ------------------------------------------------------------ QK^T issuer
-        if (lane == 0) {
+        // The whole warp runs the loop (warp-uniform waits); one elected lane issues each
+        // tcgen05 operation, and lane 0 the TMA loads.
+        {
             // FP8 records: the latent columns in fp16, the RoPE columns (bf16 in the record and
             // in the query) in bf16; every MMA accumulates into the same fp32 scores
             constexpr uint32_t idesc_qk_rope = idesc_bf16(128, 64, false);
@@ -920,7 +922,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
             bool ok = true;
             // injected stall (test of the timeout path): a wait on a barrier nothing completes,
             // before any MMA is issued; it runs out after the wait limit and the CTA winds down
-            if (a.stall_test && !wait_bar(c, bar(base, B_STALL), 0u, false)) ok = false;
+            if (a.stall_test && !warp_wait(c, bar(base, B_STALL), 0u, false)) ok = false;
             // Dense and sparse tiles: this thread loads each work item's query itself.  The TMA
             // brings three rounds of three 64-column x 128-head boxes (128-B swizzle; heads at or
             // past H read zeros) into the shared-memory query area; rounds 0 and 1 (own latent
@@ -936,25 +938,28 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
             auto load_query = [&](int bq) -> bool {
                 const uint32_t qb = bar(base, B_QLD);
                 for (int round = 0; round < 3; ++round) {
-                    mbar_arrive_expect_tx(qb, 3 * kQsBox);
-                    for (int i = 0; i < 3; ++i) {
-                        const int blk = 3 * round + i;  // 0-3 own half, 4 RoPE, 5-8 other half
-                        const uint32_t dst = base + kOffQs + i * kQsBox;
-                        if (blk == 4)
-                            tma_load_3d(dst, &tmap_qr, 0, 0, bq, qb);
-                        else
-                            tma_load_3d(dst, &tmap_qn, blk < 4 ? 256 * (int)rank + 64 * blk : 256 * (int)peer + 64 * (blk - 5),
-                                        0, bq, qb);
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(qb, 3 * kQsBox);
+                        for (int i = 0; i < 3; ++i) {
+                            const int blk = 3 * round + i;  // 0-3 own half, 4 RoPE, 5-8 other half
+                            const uint32_t dst = base + kOffQs + i * kQsBox;
+                            if (blk == 4)
+                                tma_load_3d(dst, &tmap_qr, 0, 0, bq, qb);
+                            else
+                                tma_load_3d(dst, &tmap_qn,
+                                            blk < 4 ? 256 * (int)rank + 64 * blk : 256 * (int)peer + 64 * (blk - 5), 0,
+                                            bq, qb);
+                        }
                     }
-                    if (!wait_bar(c, qb, (qld_phase++) & 1u, false)) return false;
+                    if (!warp_wait(c, qb, (qld_phase++) & 1u, false)) return false;
                     if (round == 2) break;
                     tc_fence_after();
                     for (int i = 0; i < 3; ++i)
                         for (int k = 0; k < 4; ++k)
-                            tmem_cp_128x256b(tmem + kColQ + 32u * (3 * round + i) + 8u * k,
-                                             smem_desc_sw128(base + kOffQs + i * kQsBox + k * 32u, 16u, 1024u));
-                    mma_commit(bar(base, B_QCP));
-                    if (!wait_bar(c, bar(base, B_QCP), (qcp_phase++) & 1u, false)) return false;
+                            tmem_cp_128x256b_warp(tmem + kColQ + 32u * (3 * round + i) + 8u * k,
+                                                  smem_desc_sw128(base + kOffQs + i * kQsBox + k * 32u, 16u, 1024u));
+                    mma_commit_warp(bar(base, B_QCP));
+                    if (!warp_wait(c, bar(base, B_QCP), (qcp_phase++) & 1u, false)) return false;
                 }
                 tc_fence_after();
                 return true;
@@ -964,13 +969,13 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                     const WorkItem w = items[it];
                     if (w.t1 <= w.t0) continue;
                     if constexpr (kFp8) {
-                        if (!wait_bar(c, bar(base, B_Q_READY), nitem & 1u, false)) {
+                        if (!warp_wait(c, bar(base, B_Q_READY), nitem & 1u, false)) {
                             ok = false;
                             break;
                         }
                     } else {
                         // the previous item's QK^T must be done with the query area and columns
-                        if (nitem > 0 && !wait_bar(c, bar(base, B_QDONE), (nitem - 1) & 1u, false)) {
+                        if (nitem > 0 && !warp_wait(c, bar(base, B_QDONE), (nitem - 1) & 1u, false)) {
                             ok = false;
                             break;
                         }
@@ -980,7 +985,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                         }
                         // the next item's query is loaded after this one: bring it into L2 now
                         const int bnext = next_request(unit_begin, items, units, ncl, u, it);
-                        if (bnext >= 0) {
+                        if (bnext >= 0 && lane == 0) {
                             prefetch_l2(a.q_nope + (int64_t)bnext * a.H * kDLatent, (uint32_t)(a.H * kDLatent * 2));
                             prefetch_l2(a.q_rope + (int64_t)bnext * a.H * kDRope, (uint32_t)(a.H * kDRope * 2));
                         }
@@ -988,14 +993,14 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                     ++nitem;
                     tc_fence_after();
                     for (int t = w.t0; t < w.t1 && ok; t += kTile, ++g) {
-                        if (g > 0 && !wait_bar(c, bar(base, B_S_FREE), (g - 1) & 1u, false)) {
+                        if (g > 0 && !warp_wait(c, bar(base, B_S_FREE), (g - 1) & 1u, false)) {
                             ok = false;
                             break;
                         }
                         const bool have = t + kPageRows * (int)rank < w.t1;  // own page exists
                         // other latent half and RoPE first: their stage goes back to the loader
                         // while the own-half rows may still wait for the previous tile's PV
-                        if (!wait_bar(c, bar(base, B_OTH_FULL), g & 1u, false)) {
+                        if (!warp_wait(c, bar(base, B_OTH_FULL), g & 1u, false)) {
                             ok = false;
                             break;
                         }
@@ -1005,19 +1010,19 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                             for (int k = 0; k < 4; ++k) {
                                 const uint64_t bd = smem_desc_sw128(ot + k * 32u, 16u, 1024u);
                                 if (i == 0)
-                                    mma_ts(tmem + kColS, tmem + kColQOther + 8u * k, bd, idesc_qk, k > 0 ? 1u : 0u);
+                                    mma_ts_warp(tmem + kColS, tmem + kColQOther + 8u * k, bd, idesc_qk, k > 0 ? 1u : 0u);
                                 else if (i == 4)
-                                    mma_ts(tmem + kColS, tmem + kColQRope + 8u * k, bd, idesc_qk_rope, 1u);
+                                    mma_ts_warp(tmem + kColS, tmem + kColQRope + 8u * k, bd, idesc_qk_rope, 1u);
                                 else
-                                    mma_ss(tmem + kColS,
-                                           smem_desc_sw128(base + kOffQs + (i - 1) * kQsBox + k * 32u, 16u, 1024u),
-                                           bd, idesc_qk, 1u);
+                                    mma_ss_warp(tmem + kColS,
+                                                smem_desc_sw128(base + kOffQs + (i - 1) * kQsBox + k * 32u, 16u, 1024u),
+                                                bd, idesc_qk, 1u);
                             }
                         }
-                        mma_commit(bar(base, B_OTH_EMPTY));
+                        mma_commit_warp(bar(base, B_OTH_EMPTY));
                         const DhSlot dso = dh_slot<kSparse>(g, 0);
                         const int ds = dso.slot;
-                        if (!wait_bar(c, bar(base, dso.full), dso.phase & 1u, false)) {
+                        if (!warp_wait(c, bar(base, dso.full), dso.phase & 1u, false)) {
                             ok = false;
                             break;
                         }
@@ -1025,19 +1030,21 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                         if (have) {
                             const uint32_t dh = base + kOffDh + ds * kDhBytes;
                             for (int k = 0; k < 16; ++k)
-                                mma_ts(tmem + kColS, tmem + kColQ + 8u * k,
-                                       smem_desc_sw128(dh + (k >> 2) * kBox + (k & 3) * 32u, 16u, 1024u), idesc_qk, 1u);
+                                mma_ts_warp(tmem + kColS, tmem + kColQ + 8u * k,
+                                            smem_desc_sw128(dh + (k >> 2) * kBox + (k & 3) * 32u, 16u, 1024u), idesc_qk,
+                                            1u);
                         }
-                        mma_commit(bar(base, B_S_FULL));
+                        mma_commit_warp(bar(base, B_S_FULL));
                     }
-                    if (!kFp8 && ok) mma_commit(bar(base, B_QDONE));  // this item's QK^T are issued
+                    if (!kFp8 && ok) mma_commit_warp(bar(base, B_QDONE));  // this item's QK^T are issued
                 }
             }
             if (!ok) drain_pause();
         }
     } else if (warp == 6) {
         // ------------------------------------------------------------ PV issuer
-        if (lane == 0) {
+        // warp-wide like the QK^T issuer
+        {
             constexpr uint32_t idesc_pv = kFp8 ? idesc_f16(128, 256, true) : idesc_bf16(128, 256, true);
             uint32_t g = 0;
             bool ok = true;
@@ -1048,7 +1055,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                     for (int t = w.t0; t < w.t1; t += kTile, ++g) {
                         // the probability tile is reused only after both CTAs' PV of the
                         // previous tile, so P_FULL never runs two phases ahead
-                        if (!wait_bar(c, bar(base, B_P_FULL), g & 1u, false)) {
+                        if (!warp_wait(c, bar(base, B_P_FULL), g & 1u, false)) {
                             ok = false;
                             break;
                         }
@@ -1064,7 +1071,7 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                             // back below, and for FP8 records its expansion (a stage between the raw
                             // load and this barrier) must have passed first, or the raw loader could
                             // run two phases ahead of it
-                            if (!wait_bar(c, bar(base, d.full), d.phase & 1u, false)) {
+                            if (!warp_wait(c, bar(base, d.full), d.phase & 1u, false)) {
                                 ok = false;
                                 break;
                             }
@@ -1073,14 +1080,14 @@ decode_sm103_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_const
                             for (int kk = 0; kk < ksteps; ++kk) {
                                 const uint64_t ad = smem_desc_sw128(ps + p * kPPage + kk * 32u, 16u, 1024u);
                                 const uint64_t bd = smem_desc_sw128(dh + kk * 2048u, kBox, 1024u);
-                                mma_ss(tmem + kColO, ad, bd, idesc_pv, first ? 0u : 1u);
+                                mma_ss_warp(tmem + kColO, ad, bd, idesc_pv, first ? 0u : 1u);
                                 first = false;
                             }
-                            mma_commit(bar(base, B_DH_EMPTY + ds));
+                            mma_commit_warp(bar(base, B_DH_EMPTY + ds));
                         }
                         if (!ok) break;
-                        mma_commit_multicast(bar(base, B_PFREE), (uint16_t)3);
-                        if (t + kTile >= w.t1) mma_commit(bar(base, B_O_FINAL));
+                        mma_commit_multicast_warp(bar(base, B_PFREE), (uint16_t)3);
+                        if (t + kTile >= w.t1) mma_commit_warp(bar(base, B_O_FINAL));
                     }
                 }
             }

@@ -232,6 +232,21 @@ __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
         :: "r"(bar) : "memory");
 }
+__device__ __forceinline__ void tmem_cp_128x256b_warp(uint32_t taddr, uint64_t sdesc) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.cp.cta_group::1.128x256b [%0], %1;\n\t}"
+        :: "r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void mma_commit_multicast_warp(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;\n\t}"
+        :: "r"(bar), "h"(cta_mask) : "memory");
+}
 // The mbarrier completes once all tcgen05 operations issued so far by this thread finish.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
