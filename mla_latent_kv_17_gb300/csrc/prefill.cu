@@ -181,6 +181,7 @@ constexpr int kAtThreads = 32 * 11;
 constexpr float kRescaleLog2 = 8.0f;       // a row's reference maximum moves only when exceeded by 2^8
 // TMEM: tile X (0 = A, 1 = B) has S at 256 X, O at 256 X + 128; P at 256 X (bf16 pairs)
 constexpr uint32_t kColS = 0, kColO = 128;
+constexpr int kAtHeadGroup = 8;         // heads whose pairs are ordered together
 
 __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
     const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qr,
@@ -206,10 +207,15 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nqt = (L + kAtQ - 1) / kAtQ;
     const int npair = (nqt + 1) / 2;
-    // head-major order: the CTAs resident at once share a few heads' keys and values (2 MB
-    // a head at 4,096 tokens), which then stay in L2; within a head the longest rows first
-    const int h = (int)(blockIdx.x / npair);
-    const int pr = npair - 1 - (int)(blockIdx.x % npair);
+    // Groups of kAtHeadGroup heads in turn: the CTAs resident at once share a few heads' keys
+    // and values (2 MB a head at 4,096 tokens), which then stay in L2; within a group the
+    // longest pairs of all its heads first, so that every group, the last one too, ends on
+    // its shortest pairs.
+    const int g0 = (int)(blockIdx.x / (kAtHeadGroup * npair)) * kAtHeadGroup;
+    const int hg = min(kAtHeadGroup, H - g0);        // heads in this group
+    const int r = (int)blockIdx.x - g0 * npair;
+    const int h = g0 + r % hg;
+    const int pr = npair - 1 - r / hg;
     const int qa = 2 * pr;                           // query tile A; B = qa + 1 if it exists
     const bool has_b = qa + 1 < nqt;
     const int nt_b = has_b ? qa + 2 : 0;             // causal: key tiles 0 .. q tile (A: qa + 1)
