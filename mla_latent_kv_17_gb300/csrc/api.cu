@@ -110,12 +110,20 @@ plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int units, unsigned
     const int64_t pos0 = block_exclusive_scan(local, &total, sh);
     const int64_t per = plan_budget(total, units, topk > 0 ? req_cost(req_tiles(seq_lens, topk, 0)) : 0, B);
 
+    // With at most one request per thread, its cut stays in a register and every thread then
+    // emits one work item at a time (a request cut into many pieces is not left to one thread);
+    // otherwise each thread emits its requests' items itself.
+    const bool one_each = B <= kPlanThreads;
+    __shared__ int32_t s_off[kPlanThreads + 1], s_len[kPlanThreads], s_slot[kPlanThreads];
+    __shared__ ReqSplit s_rs[kPlanThreads];
+    ReqSplit r_one{};
     int64_t n_local = 0, s_local = 0, r_local = 0;
     {
         int64_t pos = pos0;
         for (int b = b0; b < b1; ++b) {
             const int32_t tiles = req_tiles(seq_lens, topk, b);
             const ReqSplit r = req_split(pos, tiles, per, units);
+            r_one = r;
             req_start[b] = pos;
             n_local += r.n;
             if (r.n > 1) {
@@ -130,21 +138,42 @@ plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int units, unsigned
     const int64_t n_total = tot.v[0], s_total = tot.v[1], r_total = tot.v[2];
     int64_t off = ex.v[0], slot = ex.v[1], rpos = ex.v[2];
     int32_t *split_list = reinterpret_cast<int32_t *>(ws + L.split_list);
+    int32_t *iu_copy = iu_in_smem ? s_iu : nullptr;
     {
         int64_t pos = pos0;
         for (int b = b0; b < b1; ++b) {
             const int32_t tiles = req_tiles(seq_lens, topk, b);
-            const ReqSplit r = req_split(pos, tiles, per, units);
+            const ReqSplit r = one_each ? r_one : req_split(pos, tiles, per, units);
+            const int32_t sb = r.n > 1 ? (int32_t)slot : -1;
             num_splits[b] = r.n;
-            split_base[b] = r.n > 1 ? (int32_t)slot : -1;
-            emit_request(ws, L, seq_lens, topk, b, pos, per, units, (int32_t)off, split_base[b],
-                         iu_in_smem ? s_iu : nullptr);
+            split_base[b] = sb;
+            if (one_each) {
+                s_off[b] = (int32_t)off;
+                s_rs[b] = r;
+                s_len[b] = req_len(seq_lens, topk, b);
+                s_slot[b] = sb;
+            } else {
+                emit_request(ws, L, seq_lens, topk, b, pos, per, units, (int32_t)off, sb, iu_copy);
+            }
             off += r.n;
             if (r.n > 1) {
                 slot += r.n;
                 split_list[rpos++] = b;
             }
             pos += req_cost(tiles);
+        }
+    }
+    if (one_each) {
+        __syncthreads();  // s_off, s_rs, s_len, s_slot are complete
+        for (int32_t i = threadIdx.x; i < (int32_t)n_total; i += kPlanThreads) {
+            // the request holding item i: the last b with s_off[b] <= i (every request has an item)
+            int lo = 0, hi = B - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_off[mid] <= i) lo = mid;
+                else hi = mid - 1;
+            }
+            emit_piece(ws, L, lo, s_len[lo], s_rs[lo], i - s_off[lo], per, units, i, s_slot[lo], iu_copy);
         }
     }
     __syncthreads();  // item_unit is complete (shared, or global writes of this block)
@@ -358,7 +387,7 @@ mla_status mla_decode_plan(const int32_t *seq_lens, int B, int H, int topk, int 
     // a programmatic dependent of whatever ran before on the stream (it waits for it before
     // reading seq_lens); the items' units stay in shared memory when they fit
     const size_t iu_bytes = sizeof(int32_t) * (size_t)ws_layout(B, H, units).max_items;
-    const int iu_in_smem = iu_bytes <= 48 * 1024 ? 1 : 0;
+    const int iu_in_smem = iu_bytes <= 32 * 1024 ? 1 : 0;  // beside the kernel's ~12 KB of static shared memory
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, 1);
     cfg.blockDim = dim3(kPlanThreads, 1, 1);

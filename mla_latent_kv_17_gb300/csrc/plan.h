@@ -190,27 +190,31 @@ MLA_HD int64_t plan_budget(int64_t total_cost, int units, int64_t uniform_cost, 
 
 // Writes the pieces of request b (its item offset `off`, its first partial slot `slot0`
 // or -1) into the workspace; unit_copy, when given, receives the items' units as well.
+// Piece i of request b (len tokens, cut as r) as work item `item`.
+MLA_HD void emit_piece(unsigned char *ws, const WsLayout &L, int b, int32_t len, const ReqSplit &r, int i,
+                       int64_t per, int units, int32_t item, int32_t slot0, int32_t *unit_copy) {
+    WorkItem *items = reinterpret_cast<WorkItem *>(ws + L.items);
+    int32_t *item_unit = reinterpret_cast<int32_t *>(ws + L.item_unit);
+    int32_t tb, te, u;
+    req_piece(r, i, per, units, &tb, &te, &u);
+    WorkItem w;
+    w.b = b;
+    w.t0 = tb * kTileTokens;
+    const int32_t e = te * kTileTokens;
+    w.t1 = e < len ? e : len;
+    w.slot = r.n > 1 ? slot0 + i : -1;
+    items[item] = w;
+    item_unit[item] = u;
+    if (unit_copy) unit_copy[item] = u;
+}
+
 MLA_HD void emit_request(unsigned char *ws, const WsLayout &L, const int32_t *seq_lens, int topk,
                          int b, int64_t S, int64_t per, int units, int32_t off, int32_t slot0,
                          int32_t *unit_copy = nullptr) {
-    WorkItem *items = reinterpret_cast<WorkItem *>(ws + L.items);
-    int32_t *item_unit = reinterpret_cast<int32_t *>(ws + L.item_unit);
     const int32_t len = req_len(seq_lens, topk, b);
     const int32_t tiles = (len + kTileTokens - 1) / kTileTokens;
     const ReqSplit r = req_split(S, tiles, per, units);
-    for (int i = 0; i < r.n; ++i) {
-        int32_t tb, te, u;
-        req_piece(r, i, per, units, &tb, &te, &u);
-        WorkItem w;
-        w.b = b;
-        w.t0 = tb * kTileTokens;
-        const int32_t e = te * kTileTokens;
-        w.t1 = e < len ? e : len;
-        w.slot = r.n > 1 ? slot0 + i : -1;
-        items[off + i] = w;
-        item_unit[off + i] = u;
-        if (unit_copy) unit_copy[off + i] = u;
-    }
+    for (int i = 0; i < r.n; ++i) emit_piece(ws, L, b, len, r, i, per, units, off + i, slot0, unit_copy);
 }
 
 MLA_HD void write_header(unsigned char *ws, const WsLayout &L, int B, int H, int topk, int units,
