@@ -58,7 +58,9 @@ def test_decompress_matches_oracle(L, H):
         _close(_f64(got), ref, f"decompress {name} L={L} H={H}")
 
 
-@pytest.mark.parametrize("L,H", [(1, 2), (129, 3), (300, 2), (700, 4)])
+# (384, 10): three query tiles (a pair and a tile alone) over a group of eight heads and a
+# remainder group of two, in the CTA order the kernel uses
+@pytest.mark.parametrize("L,H", [(1, 2), (129, 3), (300, 2), (700, 4), (384, 10)])
 def test_prefill_attention_matches_oracle(L, H):
     entries, q_nope, q_rope, w_uk, w_uv = _inputs(L, H, 100 + L)
     ref_out, ref_lse = oracle.prefill(_f64(entries), _f64(q_nope), _f64(q_rope), _f64(w_uk), _f64(w_uv), SCALE,
