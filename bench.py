@@ -292,7 +292,7 @@ def measure_workload(name, args, dev, stream, flush, pk, pk_kind, pg, ws_n, cloc
                        case.seq_lens, case.scale, out, lse, stream)
 
     def step():
-        ops.plan(wsp, None if sparse else case.seq_lens, topk=topk, stream=stream)
+        ops.plan(wsp, None if sparse else case.seq_lens, topk=topk, stream=stream, kv_dtype=case.kv_dtype)
         decode_call()
 
     for _ in range(args.warmup):
@@ -369,7 +369,7 @@ def measure_workload(name, args, dev, stream, flush, pk, pk_kind, pg, ws_n, cloc
         d_sl.copy_(h_sl, non_blocking=True)
         if sparse:
             d_idx.copy_(h_idx, non_blocking=True)
-        ops.plan(wsp, None if sparse else d_sl, topk=topk, stream=stream)
+        ops.plan(wsp, None if sparse else d_sl, topk=topk, stream=stream, kv_dtype=case.kv_dtype)
         if sparse:
             ops.decode_sparse(wsp, d_q_nope, d_q_rope, case.cache, d_bt, d_sl, d_idx, case.scale,
                               out, lse, stream)

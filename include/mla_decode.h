@@ -76,9 +76,11 @@ size_t mla_decode_workspace_size(int B, int H, int num_sms);
  * decode workers, the number of splits of each request and where its partial results go.
  * With topk > 0 the plan is for mla_decode_sparse: every request is planned over its
  * topk index slots and seq_lens may be NULL.  The plan stays valid until seq_lens changes.
+ * kv_dtype: the cache layout the decode will read (it sets the cost the planner charges per
+ * piece; a plan of either layout is correct for both); top-k plans take MLA_KV_BF16.
  * num_sms: SMs the decode may use (0 = all SMs of the current device). */
-mla_status mla_decode_plan(const int32_t *seq_lens, int B, int H, int topk, int num_sms,
-                           void *workspace, size_t ws_bytes, void *stream);
+mla_status mla_decode_plan(const int32_t *seq_lens, int B, int H, int topk, mla_kv_dtype kv_dtype,
+                           int num_sms, void *workspace, size_t ws_bytes, void *stream);
 
 /* Dense decode over the paged cache with the plan in `workspace` (built by
  * mla_decode_plan with topk = 0 for the same B, H and seq_lens).  Writes out and lse.
@@ -234,7 +236,7 @@ mla_status mla_prefill_attention(const void *q_nope, const void *q_rope, const v
  * seq_lens[B] (NULL with topk > 0) into a HOST buffer of mla_decode_workspace_size()
  * bytes, producing exactly the bytes the device planner writes into the plan region.
  * num_sms must be > 0. */
-mla_status mla_decode_plan_host(const int32_t *seq_lens, int B, int H, int topk,
+mla_status mla_decode_plan_host(const int32_t *seq_lens, int B, int H, int topk, mla_kv_dtype kv_dtype,
                                 int num_sms, void *workspace_host, size_t ws_bytes);
 
 #ifdef __cplusplus

@@ -88,7 +88,7 @@ __device__ Sum3 block_exclusive_scan3(Sum3 v, Sum3 *total, Sum3 *sh) {
 }
 
 __global__ void __launch_bounds__(kPlanThreads)
-plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int units, unsigned char *ws, int iu_in_smem) {
+plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int units, int ovh, unsigned char *ws, int iu_in_smem) {
     __shared__ int64_t sh[kPlanWarps];
     __shared__ Sum3 sh3[kPlanWarps];
     extern __shared__ int32_t s_iu[];  // items' units (when max_items of them fit)
@@ -105,10 +105,10 @@ plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int units, unsigned
 
     // budget positions: the running position stays in a register (req_start is only written)
     int64_t local = 0;
-    for (int b = b0; b < b1; ++b) local += req_cost(req_tiles(seq_lens, topk, b));
+    for (int b = b0; b < b1; ++b) local += req_cost(req_tiles(seq_lens, topk, b), ovh);
     int64_t total;
     const int64_t pos0 = block_exclusive_scan(local, &total, sh);
-    const int64_t per = plan_budget(total, units, topk > 0 ? req_cost(req_tiles(seq_lens, topk, 0)) : 0, B);
+    const int64_t per = plan_budget(total, units, topk > 0 ? req_cost(req_tiles(seq_lens, topk, 0), ovh) : 0, B, ovh);
 
     // With at most one request per thread, its cut stays in a register and every thread then
     // emits one work item at a time (a request cut into many pieces is not left to one thread);
@@ -122,7 +122,7 @@ plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int units, unsigned
         int64_t pos = pos0;
         for (int b = b0; b < b1; ++b) {
             const int32_t tiles = req_tiles(seq_lens, topk, b);
-            const ReqSplit r = req_split(pos, tiles, per, units);
+            const ReqSplit r = req_split(pos, tiles, per, units, ovh);
             r_one = r;
             req_start[b] = pos;
             n_local += r.n;
@@ -130,7 +130,7 @@ plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int units, unsigned
                 s_local += r.n;
                 ++r_local;
             }
-            pos += req_cost(tiles);
+            pos += req_cost(tiles, ovh);
         }
     }
     Sum3 tot;
@@ -143,7 +143,7 @@ plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int units, unsigned
         int64_t pos = pos0;
         for (int b = b0; b < b1; ++b) {
             const int32_t tiles = req_tiles(seq_lens, topk, b);
-            const ReqSplit r = one_each ? r_one : req_split(pos, tiles, per, units);
+            const ReqSplit r = one_each ? r_one : req_split(pos, tiles, per, units, ovh);
             const int32_t sb = r.n > 1 ? (int32_t)slot : -1;
             num_splits[b] = r.n;
             split_base[b] = sb;
@@ -153,14 +153,14 @@ plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int units, unsigned
                 s_len[b] = req_len(seq_lens, topk, b);
                 s_slot[b] = sb;
             } else {
-                emit_request(ws, L, seq_lens, topk, b, pos, per, units, (int32_t)off, sb, iu_copy);
+                emit_request(ws, L, seq_lens, topk, b, pos, per, units, ovh, (int32_t)off, sb, iu_copy);
             }
             off += r.n;
             if (r.n > 1) {
                 slot += r.n;
                 split_list[rpos++] = b;
             }
-            pos += req_cost(tiles);
+            pos += req_cost(tiles, ovh);
         }
     }
     if (one_each) {
@@ -188,7 +188,7 @@ plan_kernel(const int32_t *seq_lens, int B, int H, int topk, int units, unsigned
     for (int u = threadIdx.x; u <= units; u += kPlanThreads)
         if (u > last) unit_begin[u] = n;
     if (threadIdx.x == 0) {
-        write_header(ws, L, B, H, topk, units, n, per, (int32_t)s_total, (int32_t)r_total);
+        write_header(ws, L, B, H, topk, units, n, per, (int32_t)s_total, (int32_t)r_total, ovh);
         *reinterpret_cast<int *>(ws + L.status) = 0;
     }
 }
@@ -375,9 +375,11 @@ size_t mla_decode_workspace_size(int B, int H, int num_sms) {
     return ws_layout(B, H, units_for(num_sms)).total;
 }
 
-mla_status mla_decode_plan(const int32_t *seq_lens, int B, int H, int topk, int num_sms,
-                           void *workspace, size_t ws_bytes, void *stream) {
+mla_status mla_decode_plan(const int32_t *seq_lens, int B, int H, int topk, mla_kv_dtype kv_dtype,
+                           int num_sms, void *workspace, size_t ws_bytes, void *stream) {
     if (!workspace || B < 1 || H < 1 || topk < 0 || num_sms < 0) return MLA_ERR_INVALID_ARG;
+    if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+    if (topk > 0 && kv_dtype != MLA_KV_BF16) return MLA_ERR_UNSUPPORTED;
     if (H > kMaxHeads) return MLA_ERR_UNSUPPORTED;
     if (topk == 0 && !seq_lens) return MLA_ERR_INVALID_ARG;
     if (num_sms == 0) num_sms = device_sm_count();
@@ -398,21 +400,25 @@ mla_status mla_decode_plan(const int32_t *seq_lens, int B, int H, int topk, int 
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, plan_kernel, seq_lens, B, H, topk, units, (unsigned char *)workspace,
+    const int ovh = piece_overhead(kv_dtype == MLA_KV_FP8_E4M3);
+    return cudaLaunchKernelEx(&cfg, plan_kernel, seq_lens, B, H, topk, units, ovh, (unsigned char *)workspace,
                               iu_in_smem) == cudaSuccess
                ? MLA_OK
                : MLA_ERR_CUDA;
 }
 
-mla_status mla_decode_plan_host(const int32_t *seq_lens, int B, int H, int topk, int num_sms,
-                                void *workspace_host, size_t ws_bytes) {
+mla_status mla_decode_plan_host(const int32_t *seq_lens, int B, int H, int topk, mla_kv_dtype kv_dtype,
+                                int num_sms, void *workspace_host, size_t ws_bytes) {
     if (!workspace_host || B < 1 || H < 1 || topk < 0 || num_sms < 1) return MLA_ERR_INVALID_ARG;
+    if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+    if (topk > 0 && kv_dtype != MLA_KV_BF16) return MLA_ERR_UNSUPPORTED;
     if (H > kMaxHeads) return MLA_ERR_UNSUPPORTED;
     if (topk == 0 && !seq_lens) return MLA_ERR_INVALID_ARG;
     const int units = num_units_for(num_sms);
     const WsLayout L = ws_layout(B, H, units);
     if (ws_bytes < L.plan_end) return MLA_ERR_WORKSPACE;
-    build_plan_serial(seq_lens, B, H, topk, units, (unsigned char *)workspace_host);
+    build_plan_serial(seq_lens, B, H, topk, units, piece_overhead(kv_dtype == MLA_KV_FP8_E4M3),
+                      (unsigned char *)workspace_host);
     *reinterpret_cast<int *>((unsigned char *)workspace_host + L.status) = 0;
     return MLA_OK;
 }

@@ -68,7 +68,7 @@ extern "C" mla_status mla_decode_static(const void *q_nope, const void *q_rope, 
     void *ws = nullptr;
     mla_status st = scratch_for_current_device(&ws);
     if (st != MLA_OK) return st;
-    st = mla_decode_plan(seq_lens, B, H, 0, 0, ws, kStaticScratchBytes, stream);
+    st = mla_decode_plan(seq_lens, B, H, 0, kv_dtype, 0, ws, kStaticScratchBytes, stream);
     if (st != MLA_OK) return st;
     st = mla_decode(ws, kStaticScratchBytes, q_nope, q_rope, cache, kv_dtype, num_pages,
                     block_table, max_pages, seq_lens, B, H, softmax_scale, out, lse, stream);

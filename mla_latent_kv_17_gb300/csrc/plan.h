@@ -7,8 +7,8 @@
 // workers ("units", one per pair of SMs) each get an equal budget of tiles; the
 // planner walks the requests in order and fills units one after another, so a request
 // that straddles a unit boundary is cut into pieces (split-KV).  Each piece costs its
-// tiles plus a fixed overhead (query load, epilogue), and no piece is made smaller than
-// kMinPieceTiles unless it is the request's last.  Requests cut into several pieces write
+// tiles plus a fixed overhead (query load, epilogue; piece_overhead), and no piece is made
+// smaller than kMinPieceTiles unless it is the request's last.  Requests cut into several pieces write
 // per-piece partial results (out_i normalised, lse_i), merged afterwards through their
 // log-sum-exp ("Fused Reduction" of weight-absorbed decode, "MLA 最佳算子全景调研" §3).
 #pragma once
@@ -32,7 +32,6 @@ constexpr int kFp8RecordBytes = 656;
 constexpr int kMaxHeads = 128;
 constexpr int kTileTokens = 128;
 constexpr int kSmsPerUnit = 2;
-constexpr int kPieceOverheadTiles = 2;
 constexpr int kMinPieceTiles = 2;
 constexpr int kMergeCostTiles = 3;  // the split-KV merge's cost on the critical path, in tiles
 constexpr uint32_t kPlanMagic = 0x4D4C4150u;  // "MLAP"
@@ -40,7 +39,7 @@ constexpr uint32_t kPlanMagic = 0x4D4C4150u;  // "MLAP"
 struct PlanHeader {
     uint32_t magic;
     int32_t B, H, topk, num_units, num_items, max_items, max_partials;
-    int32_t tiles_per_unit, num_partials, num_split_reqs, reserved[5];
+    int32_t tiles_per_unit, num_partials, num_split_reqs, piece_overhead, reserved[4];
 };
 static_assert(sizeof(PlanHeader) == 64, "plan header is 64 bytes");
 
@@ -106,7 +105,12 @@ MLA_HD int32_t req_len(const int32_t *seq_lens, int topk, int b) {
 MLA_HD int32_t req_tiles(const int32_t *seq_lens, int topk, int b) {
     return (req_len(seq_lens, topk, b) + kTileTokens - 1) / kTileTokens;
 }
-MLA_HD int64_t req_cost(int32_t tiles) { return tiles > 0 ? tiles + kPieceOverheadTiles : 0; }
+// What a piece costs beyond its tiles, in tiles: its query load, pipeline refill and
+// epilogue.  Clock traces of the decode put an item at ~3 tiles of its own mode in both
+// layouts; planned at 2 the bf16 cache runs fastest, and FP8 records (whose softmax warps
+// also convert each item's query) at 3.
+MLA_HD int piece_overhead(int fp8_records) { return fp8_records ? 3 : 2; }
+MLA_HD int64_t req_cost(int32_t tiles, int ovh) { return tiles > 0 ? tiles + ovh : 0; }
 
 // The budget axis: request b occupies cost positions [S_b, S_b + cost_b); its overhead
 // comes first, so tile t sits at S_b + overhead + t.  Unit u owns positions
@@ -129,9 +133,9 @@ struct ReqSplit {
     int32_t uf, kfirst, klast, tiles, n;
 };
 
-MLA_HD ReqSplit req_split(int64_t S, int32_t tiles, int64_t per, int units) {
+MLA_HD ReqSplit req_split(int64_t S, int32_t tiles, int64_t per, int units, int ovh) {
     ReqSplit r;
-    r.p0 = S + kPieceOverheadTiles;
+    r.p0 = S + ovh;
     r.tiles = tiles;
     if (tiles <= 0) {
         r.uf = unit_of(S, per, units);
@@ -176,10 +180,10 @@ MLA_HD void req_piece(const ReqSplit &r, int i, int64_t per, int units, int32_t 
 // requests per unit (k = ceil(nreq / units)) puts every request in one unit, with no partial
 // results and no merge; it is taken whenever it exceeds the even budget by no more than the
 // merge's cost (kMergeCostTiles).
-MLA_HD int64_t plan_budget(int64_t total_cost, int units, int64_t uniform_cost, int64_t nreq) {
+MLA_HD int64_t plan_budget(int64_t total_cost, int units, int64_t uniform_cost, int64_t nreq, int ovh) {
     const int64_t num = total_cost + units - 1;
     int64_t per = num <= INT32_MAX ? (int64_t)((uint32_t)num / (uint32_t)units) : num / units;
-    const int64_t lo = kPieceOverheadTiles + kMinPieceTiles;
+    const int64_t lo = ovh + kMinPieceTiles;
     if (per < lo) per = lo;
     if (uniform_cost > 0 && nreq > 0) {
         const int64_t pack = (nreq + units - 1) / units * uniform_cost;
@@ -188,9 +192,8 @@ MLA_HD int64_t plan_budget(int64_t total_cost, int units, int64_t uniform_cost, 
     return per;
 }
 
-// Writes the pieces of request b (its item offset `off`, its first partial slot `slot0`
-// or -1) into the workspace; unit_copy, when given, receives the items' units as well.
-// Piece i of request b (len tokens, cut as r) as work item `item`.
+// Piece i of request b (len tokens, cut as r) as work item `item`; unit_copy, when given,
+// receives the item's unit as well.
 MLA_HD void emit_piece(unsigned char *ws, const WsLayout &L, int b, int32_t len, const ReqSplit &r, int i,
                        int64_t per, int units, int32_t item, int32_t slot0, int32_t *unit_copy) {
     WorkItem *items = reinterpret_cast<WorkItem *>(ws + L.items);
@@ -208,17 +211,19 @@ MLA_HD void emit_piece(unsigned char *ws, const WsLayout &L, int b, int32_t len,
     if (unit_copy) unit_copy[item] = u;
 }
 
+// Writes the pieces of request b (its item offset `off`, its first partial slot `slot0`
+// or -1) into the workspace.
 MLA_HD void emit_request(unsigned char *ws, const WsLayout &L, const int32_t *seq_lens, int topk,
-                         int b, int64_t S, int64_t per, int units, int32_t off, int32_t slot0,
+                         int b, int64_t S, int64_t per, int units, int ovh, int32_t off, int32_t slot0,
                          int32_t *unit_copy = nullptr) {
     const int32_t len = req_len(seq_lens, topk, b);
     const int32_t tiles = (len + kTileTokens - 1) / kTileTokens;
-    const ReqSplit r = req_split(S, tiles, per, units);
+    const ReqSplit r = req_split(S, tiles, per, units, ovh);
     for (int i = 0; i < r.n; ++i) emit_piece(ws, L, b, len, r, i, per, units, off + i, slot0, unit_copy);
 }
 
 MLA_HD void write_header(unsigned char *ws, const WsLayout &L, int B, int H, int topk, int units,
-                         int n_items, int64_t per, int n_partials, int n_split_reqs) {
+                         int n_items, int64_t per, int n_partials, int n_split_reqs, int ovh) {
     PlanHeader *hd = reinterpret_cast<PlanHeader *>(ws + L.header);
     hd->magic = kPlanMagic;
     hd->B = B;
@@ -231,7 +236,8 @@ MLA_HD void write_header(unsigned char *ws, const WsLayout &L, int B, int H, int
     hd->tiles_per_unit = (int32_t)per;
     hd->num_partials = n_partials;
     hd->num_split_reqs = n_split_reqs;
-    for (int i = 0; i < 5; ++i) hd->reserved[i] = 0;
+    hd->piece_overhead = ovh;
+    for (int i = 0; i < 4; ++i) hd->reserved[i] = 0;
 }
 
 // First item index whose unit is >= u (items are ordered by unit).
@@ -249,7 +255,7 @@ MLA_HD int32_t lower_bound_unit(const int32_t *item_unit, int32_t n, int32_t u) 
 
 // Host planner: the same per-request functions in serial loops.  The device planner
 // (plan kernel) computes the same prefix sums in parallel and writes identical bytes.
-inline void build_plan_serial(const int32_t *seq_lens, int B, int H, int topk, int units,
+inline void build_plan_serial(const int32_t *seq_lens, int B, int H, int topk, int units, int ovh,
                               unsigned char *ws) {
     const WsLayout L = ws_layout(B, H, units);
     int32_t *num_splits = reinterpret_cast<int32_t *>(ws + L.num_splits);
@@ -261,15 +267,15 @@ inline void build_plan_serial(const int32_t *seq_lens, int B, int H, int topk, i
     int64_t S = 0;
     for (int b = 0; b < B; ++b) {
         req_start[b] = S;
-        S += req_cost(req_tiles(seq_lens, topk, b));
+        S += req_cost(req_tiles(seq_lens, topk, b), ovh);
     }
-    const int64_t per = plan_budget(S, units, topk > 0 ? req_cost(req_tiles(seq_lens, topk, 0)) : 0, B);
+    const int64_t per = plan_budget(S, units, topk > 0 ? req_cost(req_tiles(seq_lens, topk, 0), ovh) : 0, B, ovh);
     int32_t off = 0, slots = 0, nsr = 0;
     for (int b = 0; b < B; ++b) {
-        const ReqSplit r = req_split(req_start[b], req_tiles(seq_lens, topk, b), per, units);
+        const ReqSplit r = req_split(req_start[b], req_tiles(seq_lens, topk, b), per, units, ovh);
         num_splits[b] = r.n;
         split_base[b] = r.n > 1 ? slots : -1;
-        emit_request(ws, L, seq_lens, topk, b, req_start[b], per, units, off, split_base[b]);
+        emit_request(ws, L, seq_lens, topk, b, req_start[b], per, units, ovh, off, split_base[b]);
         off += r.n;
         if (r.n > 1) {
             slots += r.n;
@@ -278,7 +284,7 @@ inline void build_plan_serial(const int32_t *seq_lens, int B, int H, int topk, i
     }
     for (int u = 0; u <= units; ++u)
         unit_begin[u] = u == units ? off : lower_bound_unit(item_unit, off, u);
-    write_header(ws, L, B, H, topk, units, off, per, slots, nsr);
+    write_header(ws, L, B, H, topk, units, off, per, slots, nsr, ovh);
 }
 
 }  // namespace mla

@@ -45,9 +45,9 @@ def lib():
                                 ctypes.c_size_t)
             L.mla_decode_workspace_size.argtypes = [I, I, I]
             L.mla_decode_workspace_size.restype = SZ
-            L.mla_decode_plan.argtypes = [P, I, I, I, I, P, SZ, P]
+            L.mla_decode_plan.argtypes = [P, I, I, I, I, I, P, SZ, P]
             L.mla_decode_plan.restype = I
-            L.mla_decode_plan_host.argtypes = [P, I, I, I, I, P, SZ]
+            L.mla_decode_plan_host.argtypes = [P, I, I, I, I, I, P, SZ]
             L.mla_decode_plan_host.restype = I
             L.mla_decode.argtypes = [P, SZ, P, P, P, I, I64, P, I, P, I, I, F, P, P, P]
             L.mla_decode.restype = I
@@ -121,12 +121,22 @@ def _i32(t, name):
     return t
 
 
-def plan(ws: Workspace, seq_lens=None, topk: int = 0, num_sms: int = 0, stream=None) -> Workspace:
-    """Build the split-KV plan for seq_lens (device int32 [B]) or for topk index slots."""
+def _kv_code(kv_dtype) -> int:
+    if kv_dtype in ("bf16", KV_BF16):
+        return KV_BF16
+    if kv_dtype in ("fp8", KV_FP8):
+        return KV_FP8
+    raise ValueError(f"kv_dtype must be 'bf16' or 'fp8', not {kv_dtype!r}")
+
+
+def plan(ws: Workspace, seq_lens=None, topk: int = 0, num_sms: int = 0, stream=None,
+         kv_dtype="bf16") -> Workspace:
+    """Build the split-KV plan for seq_lens (device int32 [B]) or for topk index slots;
+    kv_dtype ('bf16' or 'fp8') is the cache layout the decode will read."""
     if seq_lens is not None:
         _i32(seq_lens, "seq_lens")
-    st = lib().mla_decode_plan(_ptr(seq_lens), ws.B, ws.H, int(topk), int(num_sms), ws.ptr(),
-                               ws.nbytes, _stream(stream))
+    st = lib().mla_decode_plan(_ptr(seq_lens), ws.B, ws.H, int(topk), _kv_code(kv_dtype), int(num_sms),
+                               ws.ptr(), ws.nbytes, _stream(stream))
     _check("mla_decode_plan", st)
     ws.topk = int(topk)
     return ws
@@ -380,7 +390,7 @@ def status(ws: Workspace, stream=None) -> int:
     return int(lib().mla_decode_status(ws.ptr(), ws.nbytes, _stream(stream)))
 
 
-def plan_host(seq_lens, B: int, H: int, topk: int = 0, num_sms: int = 148):
+def plan_host(seq_lens, B: int, H: int, topk: int = 0, num_sms: int = 148, kv_dtype="bf16"):
     """Host twin of the planner: returns the plan bytes (numpy uint8) for host seq_lens."""
     import numpy as np
     n = lib().mla_decode_workspace_size(int(B), int(H), int(num_sms))
@@ -390,6 +400,6 @@ def plan_host(seq_lens, B: int, H: int, topk: int = 0, num_sms: int = 148):
         sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
     st = lib().mla_decode_plan_host(
         sl.ctypes.data_as(ctypes.c_void_p) if sl is not None else None, int(B), int(H),
-        int(topk), int(num_sms), buf.ctypes.data_as(ctypes.c_void_p), n)
+        int(topk), _kv_code(kv_dtype), int(num_sms), buf.ctypes.data_as(ctypes.c_void_p), n)
     _check("mla_decode_plan_host", st)
     return buf

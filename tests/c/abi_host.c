@@ -25,9 +25,10 @@ int main(void) {
     CHECK(mla_decode_workspace_size(0, H, sms) == 0);
     void *buf = calloc(1, ws);
     CHECK(buf != NULL);
-    CHECK(mla_decode_plan_host(seq_lens, B, H, 0, sms, buf, ws) == MLA_OK);
-    CHECK(mla_decode_plan_host(seq_lens, B, H, 0, sms, buf, 16) == MLA_ERR_WORKSPACE);
-    CHECK(mla_decode_plan_host(NULL, B, H, 0, sms, buf, ws) == MLA_ERR_INVALID_ARG);
+    CHECK(mla_decode_plan_host(seq_lens, B, H, 0, MLA_KV_BF16, sms, buf, ws) == MLA_OK);
+    CHECK(mla_decode_plan_host(seq_lens, B, H, 0, MLA_KV_FP8_E4M3, sms, buf, ws) == MLA_OK);
+    CHECK(mla_decode_plan_host(seq_lens, B, H, 0, MLA_KV_BF16, sms, buf, 16) == MLA_ERR_WORKSPACE);
+    CHECK(mla_decode_plan_host(NULL, B, H, 0, MLA_KV_BF16, sms, buf, ws) == MLA_ERR_INVALID_ARG);
     CHECK(strcmp(mla_status_string(MLA_OK), "unknown status") != 0);
     CHECK(strcmp(mla_status_string((mla_status)99), "unknown status") == 0);
     /* host-side rejections happen before any device work */

@@ -135,11 +135,13 @@ def test_sparse_rejects_bad_arguments_on_host(L):
 
 def test_plan_rejects_bad_arguments_on_host(L):
     P = ctypes.c_void_p
-    assert L.mla_decode_plan(None, 2, 16, 0, 148, None, 1 << 20, None) == 1
-    assert L.mla_decode_plan(None, 2, 16, 0, 148, P(4096), 1 << 20, None) == 1  # no seq_lens, no topk
-    assert L.mla_decode_plan(P(4096), 2, 200, 0, 148, P(4096), 1 << 20, None) == 2
-    assert L.mla_decode_plan(P(4096), 2, 16, 0, 148, P(4096), 64, None) == 3
-    assert L.mla_decode_plan_host(None, 2, 16, 0, 0, P(4096), 1 << 20) == 1
+    assert L.mla_decode_plan(None, 2, 16, 0, 0, 148, None, 1 << 20, None) == 1
+    assert L.mla_decode_plan(None, 2, 16, 0, 0, 148, P(4096), 1 << 20, None) == 1  # no seq_lens, no topk
+    assert L.mla_decode_plan(P(4096), 2, 200, 0, 0, 148, P(4096), 1 << 20, None) == 2
+    assert L.mla_decode_plan(P(4096), 2, 16, 0, 0, 148, P(4096), 64, None) == 3
+    assert L.mla_decode_plan(P(4096), 2, 16, 0, 7, 148, P(4096), 1 << 20, None) == 1   # unknown cache layout
+    assert L.mla_decode_plan(None, 2, 16, 64, 1, 148, P(4096), 1 << 20, None) == 2     # top-k over FP8 records
+    assert L.mla_decode_plan_host(None, 2, 16, 0, 0, 0, P(4096), 1 << 20) == 1
 
 
 def test_absorb_project_append_reject_bad_arguments_on_host(L):

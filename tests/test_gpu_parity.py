@@ -40,7 +40,7 @@ def run(case, ws=None):
     out = out_g.inner.view(torch.float32).view(c.B, c.H, 512)
     lse = lse_g.inner.view(torch.float32).view(c.B, c.H)
     topk = c.indices.shape[1] if c.indices is not None else 0
-    ops.plan(ws, c.seq_lens if topk == 0 else None, topk=topk)
+    ops.plan(ws, c.seq_lens if topk == 0 else None, topk=topk, kv_dtype=c.kv_dtype)
     if c.indices is not None:
         ops.decode_sparse(ws, c.q_nope, c.q_rope, c.cache, c.block_table, c.seq_lens, c.indices,
                           c.scale, out=out, lse=lse)
@@ -113,25 +113,29 @@ def test_repeated_calls_on_one_workspace():
 
 def _plan_cases():
     rng = np.random.default_rng(5)
-    cases = [(name, inputs.workload_seq_lens(name).numpy(), 2048 if "sparse" in name else 0)
+    cases = [(name, inputs.workload_seq_lens(name).numpy(), 2048 if "sparse" in name else 0, "bf16")
              for name in inputs.WORKLOADS]
-    cases += [("zeros", np.zeros(3, np.int32), 0), ("edges", np.array([1, 63, 64, 65, 0, 128, 129], np.int32), 0),
-              ("many_short", np.full(300, 5, np.int32), 0),
-              ("b700", rng.integers(0, 9000, size=700).astype(np.int32), 0)]
+    cases += [(name + "_fp8", inputs.workload_seq_lens(name).numpy(), 0, "fp8")
+              for name in inputs.WORKLOADS if "sparse" not in name]
+    cases += [("zeros", np.zeros(3, np.int32), 0, "bf16"),
+              ("edges", np.array([1, 63, 64, 65, 0, 128, 129], np.int32), 0, "bf16"),
+              ("many_short", np.full(300, 5, np.int32), 0, "bf16"),
+              ("b700", rng.integers(0, 9000, size=700).astype(np.int32), 0, "bf16"),
+              ("b700_fp8", rng.integers(0, 9000, size=700).astype(np.int32), 0, "fp8")]
     return cases
 
 
 @pytest.mark.parametrize("num_sms", [None, 16])
 @pytest.mark.parametrize("case", _plan_cases(), ids=lambda c: c[0])
 def test_device_plan_equals_host_plan(case, num_sms):
-    _, sl, topk = case
+    _, sl, topk, kv = case
     B = len(sl)
     sms = num_sms or torch.cuda.get_device_properties(0).multi_processor_count
     ws = ops.Workspace(B, 128)
-    ops.plan(ws, None if topk else torch.from_numpy(sl).cuda(), topk=topk, num_sms=sms)
+    ops.plan(ws, None if topk else torch.from_numpy(sl).cuda(), topk=topk, num_sms=sms, kv_dtype=kv)
     torch.cuda.synchronize()
     dev = ws.buf.cpu().numpy()
-    host = ops.plan_host(None if topk else sl, B, 128, topk, sms)
+    host = ops.plan_host(None if topk else sl, B, 128, topk, sms, kv_dtype=kv)
     assert np.array_equal(dev[:64], host[:64])  # header
     d, h = parse(dev, B, 128), parse(host, B, 128)
     for key in ("unit_begin", "items", "num_splits", "split_base", "req_start", "item_unit"):

@@ -52,7 +52,7 @@ def test_wait_that_runs_out_is_reported_and_the_next_call_is_clean(kind):
     c = _case(kind)
     ws = guarded_workspace(c.B, c.H)
     topk = c.indices.shape[1] if c.indices is not None else 0
-    ops.plan(ws, c.seq_lens if topk == 0 else None, topk=topk)
+    ops.plan(ws, c.seq_lens if topk == 0 else None, topk=topk, kv_dtype=c.kv_dtype)
     out_g, lse_g = Guarded(c.B * c.H * 512 * 4), Guarded(c.B * c.H * 4)
     out = out_g.inner.view(torch.float32).view(c.B, c.H, 512)
     lse = lse_g.inner.view(torch.float32).view(c.B, c.H)

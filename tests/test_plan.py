@@ -6,7 +6,7 @@ from mla_latent_kv_17_gb300 import build as mbuild
 from mla_latent_kv_17_gb300 import inputs, ops
 from planview import parse
 
-OVH = 2  # per-piece overhead in tiles, as the planner charges it
+OVH = {"bf16": 2, "fp8": 3}  # per-piece overhead in tiles, as the planner charges it per cache layout
 MIN = 2  # shortest piece the planner makes
 TILE = 128  # tokens per planner tile
 
@@ -16,9 +16,10 @@ def _built():
     mbuild.build()
 
 
-def check_plan(seq_lens, H=128, topk=0, num_sms=148):
+def check_plan(seq_lens, H=128, topk=0, num_sms=148, kv="bf16"):
     B = len(seq_lens)
-    p = parse(ops.plan_host(seq_lens if topk == 0 else None, B, H, topk, num_sms), B, H)
+    ovh = OVH[kv]
+    p = parse(ops.plan_host(seq_lens if topk == 0 else None, B, H, topk, num_sms, kv_dtype=kv), B, H)
     lens = [topk if topk else max(0, int(x)) for x in seq_lens]
     units = p["units"]
     assert units == max(1, num_sms // 2)
@@ -60,8 +61,8 @@ def check_plan(seq_lens, H=128, topk=0, num_sms=148):
         for i in range(ub[u], ub[u + 1]):
             b, t0, t1, _ = items[i]
             if t1 > t0:
-                cost[u] += (t1 - t0 + TILE - 1) // TILE + OVH
-    assert np.all(cost <= p["per"] + MIN + 2 * OVH), (cost.max(), p["per"])
+                cost[u] += (t1 - t0 + TILE - 1) // TILE + ovh
+    assert np.all(cost <= p["per"] + MIN + 2 * ovh), (cost.max(), p["per"])
     # pieces are never shorter than MIN tiles unless the whole request is
     for b in range(B):
         pcs = per_req[b]
@@ -82,6 +83,16 @@ def test_workload_plans(name):
     # the busiest unit carries at most its share plus two folded short runs
     assert max(load) <= p["per"] + 2 * (MIN - 1), (max(load), p["per"])
     assert sum(load) == tiles
+
+
+@pytest.mark.parametrize("name", ["dsv3_dense_b64_h128_l1k_8k", "fp8_ragged_b128_h128_lognormal", "long_dense_b4_h128_l128k"])
+def test_fp8_plans_charge_more_per_piece(name):
+    # the same invariants with the FP8 records' piece overhead; the budget grows with it
+    sl = inputs.workload_seq_lens(name).tolist()
+    p2, _ = check_plan(sl)
+    p3, _ = check_plan(sl, kv="fp8")
+    assert p3["per"] >= p2["per"]
+    assert p3["n_items"] <= p2["n_items"]
 
 
 def test_edge_lengths():
@@ -140,6 +151,6 @@ def test_uniform_topk_batches_fit_one_unit_per_request():
     # request gets a unit of its own (no partials, no merge); with many more, they are split
     p, _ = check_plan([65536] * 64, topk=2048)
     assert p["n_partials"] == 0 and all(n == 1 for n in p["num_splits"])
-    assert p["per"] == 2048 // TILE + OVH
+    assert p["per"] == 2048 // TILE + OVH["bf16"]
     p, _ = check_plan([65536] * 4, topk=2048)
     assert p["n_partials"] > 0
