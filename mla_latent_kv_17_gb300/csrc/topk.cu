@@ -9,7 +9,9 @@
 // (radix select), then one ordered pass writes every position above that key and the
 // first `need` positions equal to it, in position order, through block-wide prefix sums.
 // Loads are batched (several 16-B loads per thread in flight) so that one CTA streams its
-// request's scores at more than one load per thread per memory latency.
+// request's scores at more than one load per thread per memory latency.  Requests of up to
+// kCacheKeys positions keep their keys in shared memory after the first pass, so the later
+// passes read shared memory instead of the scores again.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -23,7 +25,8 @@ constexpr int kTkThreads = 1024;
 constexpr int kTkWarps = kTkThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kHistCopies = 8;  // warp w adds into copy w % 8 (fewer collisions on hot bins)
-constexpr uint32_t kTkSmem = kHistCopies * kBins * 4;
+constexpr uint32_t kTkHistBytes = kHistCopies * kBins * 4;
+constexpr int kCacheKeys = 32768;  // keys of a request kept in shared memory (128 KB)
 constexpr int kLoadsInFlight = 8;  // float4 loads per thread per histogram iteration
 constexpr int kPerThread = 16;     // consecutive positions per thread per ordered-write round
 
@@ -65,8 +68,8 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t *warp_sums, 
 
 __global__ void __launch_bounds__(kTkThreads) topk_kernel(const float *__restrict__ scores, int64_t stride, int Lmax,
                                                           const int32_t *__restrict__ seq_lens, int k,
-                                                          int32_t *indices, int *status) {
-    extern __shared__ uint32_t hist[];  // [kHistCopies][kBins]
+                                                          int32_t *indices, int cache_keys, int *status) {
+    extern __shared__ uint32_t hist[];  // [kHistCopies][kBins], then cache_keys keys
     __shared__ uint32_t warp_sums[kTkWarps];
     __shared__ uint32_t sel_bin, sel_above;
     const int b = blockIdx.x;
@@ -84,6 +87,9 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const float *__restric
     }
     const float *s = scores + (int64_t)b * stride;
     const int n4 = (L + 3) >> 2;
+    // keys of positions [0, L) after the first pass (when they fit; cache_keys is a multiple of 4)
+    uint32_t *cache = hist + kHistCopies * kBins;
+    const bool cached = L <= cache_keys;
 
     // ---- radix select: key of the K-th best position, and how many of its ties to keep
     uint32_t prefix = 0u, pmask = 0u, need = (uint32_t)K;
@@ -94,20 +100,33 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const float *__restric
         const uint32_t bmask = pass == 2 ? 1023u : 2047u;
         for (int i = threadIdx.x; i < kHistCopies * kBins; i += kTkThreads) hist[i] = 0u;
         __syncthreads();
-        // kLoadsInFlight float4 loads per thread are issued before any of them is used
-        for (int i0 = threadIdx.x; i0 < n4; i0 += kLoadsInFlight * kTkThreads) {
-            float4 v[kLoadsInFlight];
+        if (pass > 0 && cached) {
+            // the keys from shared memory, four per thread and step
+            for (int i = threadIdx.x; i < n4; i += kTkThreads) {
+                const uint4 kv = reinterpret_cast<const uint4 *>(cache)[i];
+                const uint32_t kk[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
-            for (int u = 0; u < kLoadsInFlight; ++u) v[u] = ld4(s + 4 * min(i0 + u * kTkThreads, n4 - 1));
+                for (int j = 0; j < 4; ++j)
+                    if (4 * i + j < L && (kk[j] & pmask) == prefix) atomicAdd(&hmine[(kk[j] >> shift) & bmask], 1u);
+            }
+        } else {
+            // kLoadsInFlight float4 loads per thread are issued before any of them is used
+            for (int i0 = threadIdx.x; i0 < n4; i0 += kLoadsInFlight * kTkThreads) {
+                float4 v[kLoadsInFlight];
 #pragma unroll
-            for (int u = 0; u < kLoadsInFlight; ++u) {
-                const int i = i0 + u * kTkThreads;
-                const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                for (int u = 0; u < kLoadsInFlight; ++u) v[u] = ld4(s + 4 * min(i0 + u * kTkThreads, n4 - 1));
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t key = order_key(f[j]);
-                    if (i < n4 && 4 * i + j < L && (key & pmask) == prefix)
-                        atomicAdd(&hmine[(key >> shift) & bmask], 1u);
+                for (int u = 0; u < kLoadsInFlight; ++u) {
+                    const int i = i0 + u * kTkThreads;
+                    const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                    uint32_t kk[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        kk[j] = order_key(f[j]);
+                        if (i < n4 && 4 * i + j < L && (kk[j] & pmask) == prefix)
+                            atomicAdd(&hmine[(kk[j] >> shift) & bmask], 1u);
+                    }
+                    if (cached && i < n4) reinterpret_cast<uint4 *>(cache)[i] = make_uint4(kk[0], kk[1], kk[2], kk[3]);
                 }
             }
         }
@@ -144,20 +163,34 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const float *__restric
 #pragma unroll 1
     for (int r0 = 0; r0 < L; r0 += kPerThread * kTkThreads) {
         const int p0 = r0 + kPerThread * (int)threadIdx.x;
-        float4 v[kPerThread / 4];
+        uint32_t keys[kPerThread];
+        if (cached) {
 #pragma unroll
-        for (int u = 0; u < kPerThread / 4; ++u) v[u] = ld4(s + min(p0 + 4 * u, 4 * (n4 - 1)));
+            for (int u = 0; u < kPerThread / 4; ++u) {
+                const uint4 kv = reinterpret_cast<const uint4 *>(cache)[min(p0 / 4 + u, n4 - 1)];
+                keys[4 * u] = kv.x;
+                keys[4 * u + 1] = kv.y;
+                keys[4 * u + 2] = kv.z;
+                keys[4 * u + 3] = kv.w;
+            }
+        } else {
+            float4 v[kPerThread / 4];
+#pragma unroll
+            for (int u = 0; u < kPerThread / 4; ++u) v[u] = ld4(s + min(p0 + 4 * u, 4 * (n4 - 1)));
+#pragma unroll
+            for (int u = 0; u < kPerThread / 4; ++u) {
+                keys[4 * u] = order_key(v[u].x);
+                keys[4 * u + 1] = order_key(v[u].y);
+                keys[4 * u + 2] = order_key(v[u].z);
+                keys[4 * u + 3] = order_key(v[u].w);
+            }
+        }
         uint32_t gt = 0u, eq = 0u;  // bit j: position p0 + j
 #pragma unroll
-        for (int u = 0; u < kPerThread / 4; ++u) {
-            const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t key = order_key(f[j]);
-                const bool ok = p0 + 4 * u + j < L;
-                if (ok && key > kstar) gt |= 1u << (4 * u + j);
-                if (ok && key == kstar) eq |= 1u << (4 * u + j);
-            }
+        for (int j = 0; j < kPerThread; ++j) {
+            const bool ok = p0 + j < L;
+            if (ok && keys[j] > kstar) gt |= 1u << j;
+            if (ok && keys[j] == kstar) eq |= 1u << j;
         }
         uint32_t total;
         const uint32_t mine = ((uint32_t)__popc(gt) << 16) | (uint32_t)__popc(eq);  // < 2^16 of each per round
@@ -189,7 +222,8 @@ bool set_topk_attr() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
     if (done[dev]) return true;
-    if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTkSmem) !=
+    if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(kTkHistBytes + 4u * kCacheKeys)) !=
         cudaSuccess) {
         cudaGetLastError();
         return false;
@@ -209,7 +243,10 @@ extern "C" mla_status mla_topk_select(const float *scores, int64_t row_stride, i
         (row_stride & 3) != 0 || (reinterpret_cast<uintptr_t>(scores) & 15u) != 0)
         return MLA_ERR_INVALID_ARG;
     if (!set_topk_attr()) return MLA_ERR_CUDA;
-    topk_kernel<<<B, kTkThreads, kTkSmem, (cudaStream_t)stream>>>(scores, row_stride, Lmax, seq_lens, k, indices,
-                                                                 (int *)device_status);
+    // the key cache holds the longest request when it fits (positions rounded up to 4)
+    const int cache_keys = Lmax <= kCacheKeys ? ((Lmax + 3) & ~3) : 0;
+    const size_t smem = kTkHistBytes + 4u * (size_t)cache_keys;
+    topk_kernel<<<B, kTkThreads, smem, (cudaStream_t)stream>>>(scores, row_stride, Lmax, seq_lens, k, indices,
+                                                              cache_keys, (int *)device_status);
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
