@@ -72,7 +72,9 @@ def test_topk_dsa_size_equals_oracle():
 
 
 def test_topk_long_requests_reread_scores():
-    # quarters longer than the shared-memory key cache (36,864 keys per CTA) re-read scores
+    # longer than the shared-memory key cache (32,768 keys): the candidates at or above the
+    # first pass's bin go to a list in shared memory (a block of ties above everything else
+    # in the second request)
     g = torch.Generator().manual_seed(76)
     s = torch.randn(2, 150000, generator=g)
     s[1, 1000:3000] = 5.0  # a block of ties above everything else
@@ -80,6 +82,33 @@ def test_topk_long_requests_reread_scores():
     got, st = _run(s, lens, 2048)
     assert st == 0
     assert np.array_equal(got, oracle.topk_select(s.numpy(), lens, 2048))
+
+
+def test_topk_long_requests_with_too_many_candidates():
+    # past the key cache, and more positions in the selected bin than the candidate list holds
+    # (16,384): all equal, or a wide block of equal scores at the k-th best value, so the later
+    # passes read the scores again
+    g = torch.Generator().manual_seed(77)
+    s = torch.randn(3, 40000, generator=g)
+    s[0, :] = 1.0
+    s[1, 5000:30000] = 4.0        # 25,000 ties above everything else
+    s[2, :] = -0.0
+    s[2, 39000:] = 0.0            # signed zeros share a key
+    lens = [40000, 40000, 33000]
+    got, st = _run(s, lens, 2048)
+    assert st == 0
+    assert np.array_equal(got, oracle.topk_select(s.numpy(), lens, 2048))
+
+
+@pytest.mark.parametrize("width", [32768, 32772])
+def test_topk_cache_boundary_lengths(width):
+    # rows of 32,768 positions fit the key cache, rows of 32,772 do not (candidate list)
+    g = torch.Generator().manual_seed(78)
+    s = torch.randn(4, width, generator=g)
+    lens = [width, width - 1, 32767, 20000]
+    got, st = _run(s, lens, 1000)
+    assert st == 0
+    assert np.array_equal(got, oracle.topk_select(s.numpy(), lens, 1000))
 
 
 def test_topk_bad_length_is_reported():
